@@ -1,0 +1,88 @@
+"""Brute-force tile classification and the per-block index lists (oracle).
+
+"How Does Flash-MSA Sparse Attention Work" (section "How Flash-MSA Sparse
+Attention Works") applies the mask inside the tiling loop through a per-block
+mask or "a precomputed index list", so that dead key/value tiles are never
+loaded.  Here every tile (qb, kb) of `tile` x `tile` entries is classified by
+evaluating the element predicate on ALL of its entries (rows and columns past
+the end of the sequence count as dead entries):
+
+    dead    -- no live entry;  full -- every entry live;  partial -- otherwise
+
+and the lists are built from that classification:
+
+    CSR  by query block: row_ptr, col_idx (ascending kb), kind (0 full, 1 partial)
+    CSC  by key block:   col_ptr, row_idx (ascending qb), kind_t
+    q_order / k_order:   query / key blocks sorted by descending live-tile
+                         count, ties by ascending index (longest work first)
+
+For masks with a local window and no strided part, key blocks farther than
+the window from the query block are skipped without evaluation: by the window
+definition none of their entries is live.  Tests check this shortcut against
+the full evaluation.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .mask import MaskSpec, live_matrix
+
+DEAD, FULL, PARTIAL = -1, 0, 1
+
+
+def classify(n: int, spec: MaskSpec, tile: int = 128, prune: bool = True) -> np.ndarray:
+    """kinds[qb, kb] in {DEAD, FULL, PARTIAL}."""
+    nb = (n + tile - 1) // tile
+    kinds = np.full((nb, nb), DEAD, dtype=np.int8)
+    span = None
+    if prune and spec.window is not None and spec.stride is None:
+        span = spec.window // tile + 2
+    for qb in range(nb):
+        rows = np.arange(qb * tile, qb * tile + tile)
+        if span is None:
+            kbs = range(nb)
+        else:
+            kbs = range(max(0, qb - span), min(nb, qb + span + 1))
+        for kb in kbs:
+            cols = np.arange(kb * tile, kb * tile + tile)
+            live = live_matrix(rows, cols, n, spec)
+            cnt = int(live.sum())
+            if cnt == 0:
+                continue
+            kinds[qb, kb] = FULL if cnt == tile * tile else PARTIAL
+    return kinds
+
+
+def build(n: int, spec: MaskSpec, tile: int = 128, prune: bool = True) -> dict:
+    kinds = classify(n, spec, tile, prune)
+    nb = kinds.shape[0]
+    row_ptr = np.zeros(nb + 1, dtype=np.int32)
+    col_idx, kind = [], []
+    for qb in range(nb):
+        kbs = np.nonzero(kinds[qb] != DEAD)[0]
+        col_idx.extend(kbs.tolist())
+        kind.extend(kinds[qb, kbs].tolist())
+        row_ptr[qb + 1] = row_ptr[qb] + len(kbs)
+    col_ptr = np.zeros(nb + 1, dtype=np.int32)
+    row_idx, kind_t = [], []
+    for kb in range(nb):
+        qbs = np.nonzero(kinds[:, kb] != DEAD)[0]
+        row_idx.extend(qbs.tolist())
+        kind_t.extend(kinds[qbs, kb].tolist())
+        col_ptr[kb + 1] = col_ptr[kb] + len(qbs)
+    row_len = np.diff(row_ptr)
+    col_len = np.diff(col_ptr)
+    q_order = np.array(sorted(range(nb), key=lambda b: (-row_len[b], b)), dtype=np.int32)
+    k_order = np.array(sorted(range(nb), key=lambda b: (-col_len[b], b)), dtype=np.int32)
+    return {
+        "n_blocks": nb,
+        "nnz": int(row_ptr[-1]),
+        "row_ptr": row_ptr,
+        "col_idx": np.array(col_idx, dtype=np.int32),
+        "kind": np.array(kind, dtype=np.uint8),
+        "col_ptr": col_ptr,
+        "row_idx": np.array(row_idx, dtype=np.int32),
+        "kind_t": np.array(kind_t, dtype=np.uint8),
+        "q_order": q_order,
+        "k_order": k_order,
+    }

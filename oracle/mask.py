@@ -1,0 +1,86 @@
+"""Element-level attention mask predicate (oracle; test infrastructure only).
+
+Definitions, one per mask kind named on the pages:
+
+* causal -- key j is visible to query i iff j <= i.  Masked scores are -inf,
+  never multiplied by zero ("Flash MSA Attention Kernel Implementation",
+  section "Optimization Tricks That Actually Matter", paragraph "Masking and
+  causal attention"; FAQ "How do I debug a flash attention kernel that
+  produces NaN?").
+* local window -- |i - j| <= W, inclusive ("How Does Flash-MSA Sparse
+  Attention Work", section "How Flash-MSA Sparse Attention Works", mask kind
+  "Local window").
+* dilated -- read at block level: with Delta = |i // blk - j // blk|, keep the
+  pair iff Delta < near or Delta % dilation == 0 (same section, mask kind
+  "Dilated").
+* strided -- fixed pattern in the style of Child et al.: every key in key
+  block kb with kb % stride == phase (same section, mask kind "Fixed
+  pattern").
+
+Combination: live = in_range AND causal_part AND pattern, where pattern is
+true when no window/dilation/stride is set, and otherwise
+(window AND dilation part) OR (strided part).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Optional
+
+import numpy as np
+
+
+@dataclass(frozen=True)
+class MaskSpec:
+    causal: bool = False
+    window: Optional[int] = None     # W, inclusive: |i - j| <= W
+    dilation: Optional[int] = None   # block dilation factor
+    dilation_near: int = 0           # block distances below this are always kept
+    stride: Optional[int] = None     # key block kb live iff kb % stride == stride_phase
+    stride_phase: int = 0
+    block: int = 128                 # pattern block, in tokens
+
+    @property
+    def has_pattern(self) -> bool:
+        return self.window is not None or self.dilation is not None or self.stride is not None
+
+
+DENSE = MaskSpec()
+CAUSAL = MaskSpec(causal=True)
+
+
+def live_matrix(rows, cols, n: int, spec: MaskSpec) -> np.ndarray:
+    """Boolean matrix live[a, b] = live(rows[a], cols[b]) for a length-n sequence."""
+    i = np.asarray(rows, dtype=np.int64)[:, None]
+    j = np.asarray(cols, dtype=np.int64)[None, :]
+    ok = (i >= 0) & (i < n) & (j >= 0) & (j < n)
+    if spec.causal:
+        ok = ok & (j <= i)
+    if spec.has_pattern:
+        part = np.zeros(ok.shape, dtype=bool)
+        if spec.window is not None or spec.dilation is not None:
+            near_part = np.ones(ok.shape, dtype=bool)
+            if spec.window is not None:
+                near_part &= np.abs(i - j) <= spec.window
+            if spec.dilation is not None:
+                delta = np.abs(i // spec.block - j // spec.block)
+                near_part &= (delta < spec.dilation_near) | (delta % spec.dilation == 0)
+            part |= near_part
+        if spec.stride is not None:
+            part |= (j // spec.block) % spec.stride == spec.stride_phase
+        ok = ok & part
+    return ok
+
+
+def candidate_cols(r0: int, r1: int, n: int, spec: MaskSpec) -> tuple[int, int]:
+    """Half-open key range [c0, c1) outside of which rows r0..r1-1 have no live key.
+
+    Pure bound from the definitions above (causal: j <= i; window without a
+    strided part: |i - j| <= W); it only skips keys that the predicate kills.
+    """
+    c0, c1 = 0, n
+    if spec.causal:
+        c1 = min(c1, r1)
+    if spec.window is not None and spec.stride is None:
+        c0 = max(c0, r0 - spec.window)
+        c1 = min(c1, r1 + spec.window)
+    return c0, max(c0, c1)

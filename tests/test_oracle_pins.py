@@ -1,0 +1,354 @@
+"""The oracle pinned to facts that do not come from the oracle itself (CPU only)."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+from oracle import attention, block_index, loops
+from oracle.mask import MaskSpec, candidate_cols, live_matrix
+from tests import oracle_pins as pins
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+# small-N mask family: block 4 so dilation / stride patterns appear at N <= 64
+SMALL_SPECS = {
+    "dense": MaskSpec(),
+    "causal": MaskSpec(causal=True),
+    "window": MaskSpec(window=5),
+    "causal_window": MaskSpec(causal=True, window=6),
+    "causal_window_strided": MaskSpec(causal=True, window=3, stride=3, stride_phase=1, block=4),
+    "causal_window_dilated": MaskSpec(causal=True, window=14, dilation=2, dilation_near=2, block=4),
+    "dilated_only": MaskSpec(dilation=3, dilation_near=1, block=4),
+    "strided_only": MaskSpec(causal=True, stride=2, stride_phase=0, block=4),
+}
+
+fwd_full = attention.forward_head
+bwd_full = attention.backward_head
+
+
+def rng(seed=0):
+    return np.random.default_rng(seed)
+
+
+# ---------------------------------------------------------------- mask predicate
+def test_mask_hand_examples():
+    n = 20
+    # causal: diagonal included
+    live = live_matrix([5], [4, 5, 6], n, MaskSpec(causal=True))
+    assert live.tolist() == [[True, True, False]]
+    # window inclusive at W, dead at W + 1, both sides when not causal
+    live = live_matrix([10], [6, 7, 13, 14], n, MaskSpec(window=3))
+    assert live.tolist() == [[False, True, True, False]]
+    # block dilation: block 4, near 2, dilation 2 -> block distance 0,1,2,4 live; 3 dead
+    live = live_matrix([19], [19, 15, 11, 7, 3], n, MaskSpec(dilation=2, dilation_near=2, block=4))
+    assert live.tolist() == [[True, True, True, False, True]]
+    # strided: key blocks with kb % 3 == 1 (block 4): keys 4..7 and 16..19
+    live = live_matrix([19], [0, 4, 7, 8, 16], n, MaskSpec(stride=3, stride_phase=1, block=4))
+    assert live.tolist() == [[False, True, True, False, True]]
+    # union: window OR strided, intersected with causal
+    spec = MaskSpec(causal=True, window=2, stride=3, stride_phase=1, block=4)
+    live = live_matrix([19], [17, 16, 5, 12, 20], 21, spec)
+    assert live.tolist() == [[True, True, True, False, False]]
+    # out of range entries are dead
+    assert not live_matrix([3], [7], 5, MaskSpec()).any()
+
+
+@pytest.mark.parametrize("name", sorted(SMALL_SPECS))
+def test_vector_predicate_matches_scalar(name):
+    spec = SMALL_SPECS[name]
+    n = 37
+    idx = np.arange(-2, n + 3)
+    m = live_matrix(idx, idx, n, spec)
+    ref = np.array([[loops.live_scalar(int(i), int(j), n, spec) for j in idx] for i in idx])
+    assert (m == ref).all()
+
+
+@pytest.mark.parametrize("name", sorted(SMALL_SPECS))
+def test_candidate_span_only_drops_dead_keys(name):
+    spec = SMALL_SPECS[name]
+    n = 60
+    for r0 in range(0, n, 7):
+        r1 = min(n, r0 + 7)
+        c0, c1 = candidate_cols(r0, r1, n, spec)
+        live = live_matrix(np.arange(r0, r1), np.arange(n), n, spec)
+        outside = np.ones(n, dtype=bool)
+        outside[c0:c1] = False
+        assert not live[:, outside].any()
+
+
+# ---------------------------------------------------------------- closed forms
+@pytest.mark.parametrize("name", sorted(SMALL_SPECS))
+def test_uniform_attention_when_q_is_zero(name):
+    assert pins.uniform_q_zero(fwd_full, 29, 6, SMALL_SPECS[name], rng(1)) < 1e-12
+
+
+def test_causal_row_zero():
+    assert pins.causal_row0(fwd_full, 17, 8, rng(2)) < 1e-12
+
+
+def test_one_hot_dominant_row():
+    assert pins.one_hot_dominant(fwd_full, 8, 16, rng(3)) < 1e-15
+
+
+@pytest.mark.parametrize("name", sorted(SMALL_SPECS))
+def test_constant_v(name):
+    assert pins.constant_v(fwd_full, bwd_full, 23, 5, SMALL_SPECS[name], rng(4)) < 1e-12
+
+
+@pytest.mark.parametrize("name", sorted(SMALL_SPECS))
+def test_probability_rows_sum_to_one(name):
+    spec = SMALL_SPECS[name]
+    r = rng(5)
+    q, k = r.standard_normal((31, 4)), r.standard_normal((31, 4))
+    p = attention.probabilities(q, k, 0.5, spec)
+    has = live_matrix(np.arange(31), np.arange(31), 31, spec).any(axis=1)
+    assert np.abs(p[has].sum(axis=1) - 1).max() < 1e-13
+    assert (p[~has] == 0).all()
+    assert (p >= 0).all()
+
+
+@pytest.mark.parametrize("name", sorted(SMALL_SPECS))
+def test_gradient_sum_invariants(name):
+    assert pins.gradient_invariants(fwd_full, bwd_full, 26, 5, SMALL_SPECS[name], rng(6)) < 1e-11
+
+
+def test_permutation_invariance_dense():
+    assert pins.permutation_invariance(fwd_full, 40, 8, rng(7)) < 1e-12
+
+
+@pytest.mark.parametrize("name", sorted(SMALL_SPECS))
+def test_finite_differences(name):
+    # N <= 8 rows with block 4 would hide the patterns; use N = 8, d = 3
+    assert pins.finite_differences(fwd_full, bwd_full, 8, 3, SMALL_SPECS[name], rng(8)) < 1e-6
+
+
+# ---------------------------------------------------------------- restatements
+@pytest.mark.parametrize("name", sorted(SMALL_SPECS))
+def test_scalar_loops_agree(name):
+    spec = SMALL_SPECS[name]
+    r = rng(9)
+    n, d = 16, 3
+    q, k, v, do = (r.standard_normal((n, d)) for _ in range(4))
+    o, lse = fwd_full(q, k, v, 0.6, spec)
+    o2, lse2 = loops.forward_loops(q.tolist(), k.tolist(), v.tolist(), 0.6, spec)
+    assert np.abs(o - o2).max() < 1e-12
+    fin = np.isfinite(lse)
+    assert (np.isfinite(lse2) == fin).all() and np.abs(lse[fin] - lse2[fin]).max(initial=0) < 1e-12
+    g = bwd_full(q, k, v, do, 0.6, spec)
+    g2 = loops.backward_loops(q.tolist(), k.tolist(), v.tolist(), do.tolist(), 0.6, spec)
+    for a, b in zip(g, g2):
+        assert np.abs(a - b).max() < 1e-12
+
+
+@pytest.mark.parametrize("name", sorted(SMALL_SPECS))
+@pytest.mark.parametrize("n,blk", [(50, 8), (61, 16), (130, 128)])
+def test_tiled_online_softmax_agrees(name, n, blk):
+    spec = SMALL_SPECS[name]
+    r = rng(10)
+    q, k, v = (r.standard_normal((n, 8)) for _ in range(3))
+    o, lse = fwd_full(q, k, v, 0.35, spec)
+    o2, lse2 = loops.forward_tiled(q, k, v, 0.35, spec, block=blk)
+    assert np.abs(o - o2).max() < 1e-12
+    fin = np.isfinite(lse)
+    assert (np.isfinite(lse2) == fin).all()
+    assert np.abs(lse[fin] - lse2[fin]).max(initial=0) < 1e-12
+
+
+@pytest.mark.parametrize("spec", [
+    MaskSpec(causal=True),
+    MaskSpec(causal=True, window=100, stride=4, stride_phase=0, block=32),
+    MaskSpec(causal=True, window=150, dilation=2, dilation_near=2, block=32),
+    MaskSpec(window=90),
+])
+def test_chunked_evaluation_matches_full(spec):
+    r = rng(11)
+    n, d = 333, 8
+    q, k, v, do = (r.standard_normal((n, d)) for _ in range(4))
+    o, lse = fwd_full(q, k, v, 0.3, spec)
+    o2, lse2 = attention.forward_rows(q, k, v, 0.3, spec, chunk=50)
+    assert np.abs(o - o2).max() < 1e-12 and np.abs(lse - lse2).max() < 1e-12
+    dq, dk, dv = bwd_full(q, k, v, do, 0.3, spec)
+    rows = np.array([0, 1, 77, 200, 332])
+    cols = np.array([0, 5, 128, 331, 332])
+    dq2, dk2, dv2 = attention.backward_sampled(q, k, v, do, 0.3, spec, rows, cols, chunk=64)
+    assert np.abs(dq[rows] - dq2).max() < 1e-12
+    assert np.abs(dk[cols] - dk2).max() < 1e-12
+    assert np.abs(dv[cols] - dv2).max() < 1e-12
+
+
+def test_empty_rows_are_zero_not_nan():
+    # strided-only causal mask at block 4 with phase 1: rows 0..3 have no live key
+    spec = MaskSpec(causal=True, stride=2, stride_phase=1, block=4)
+    r = rng(12)
+    q, k, v, do = (r.standard_normal((12, 3)) for _ in range(4))
+    o, lse = fwd_full(q, k, v, 0.5, spec)
+    assert (o[:4] == 0).all() and (lse[:4] == -np.inf).all() and np.isfinite(o).all()
+    g = bwd_full(q, k, v, do, 0.5, spec)
+    assert all(np.isfinite(x).all() for x in g)
+
+
+# ---------------------------------------------------------------- block index
+def _counts(idx):
+    kind = idx["kind"]
+    return idx["nnz"], int((kind == 0).sum()), int((kind == 1).sum())
+
+
+def test_golden_tile_counts():
+    gold = json.load(open(os.path.join(GOLDEN, "tile_counts.json")))
+    cases = {
+        "causal_n4096": (4096, MaskSpec(causal=True)),
+        "causal_n16384": (16384, MaskSpec(causal=True)),
+        "window1024_strided8_n32768": (32768, MaskSpec(causal=True, window=1024, stride=8)),
+        "window4096_dilation2_n131072": (131072, MaskSpec(causal=True, window=4096, dilation=2, dilation_near=2)),
+    }
+    for key, (n, spec) in cases.items():
+        idx = block_index.build(n, spec)
+        g = gold[key]
+        assert _counts(idx) == (g["nnz"], g["full"], g["partial"]), key
+
+
+def test_closed_form_counts_formulas():
+    # the same numbers, recomputed from the closed forms in the fixture
+    assert sum(range(1, 33)) == 528 and sum(range(1, 129)) == 8256
+    win = sum(qb + 1 for qb in range(8)) + 248 * 9
+    strided = sum((qb - 9) // 8 + 1 for qb in range(9, 256))
+    assert (win, strided, win + strided) == (2268, 3937, 6205)
+    dil = 992 * 18 + sum(1 + min(qb, 1) + qb // 2 for qb in range(32))
+    assert dil == 18159
+
+
+@pytest.mark.parametrize("n,spec", [
+    (1000, MaskSpec(causal=True, window=200)),
+    (1500, MaskSpec(window=300, dilation=2, dilation_near=1)),
+    (2100, MaskSpec(causal=True, window=129, dilation=3, dilation_near=2)),
+])
+def test_window_shortcut_matches_full_scan(n, spec):
+    a = block_index.classify(n, spec, prune=True)
+    b = block_index.classify(n, spec, prune=False)
+    assert (a == b).all()
+
+
+@pytest.mark.parametrize("n", [1, 127, 128, 129, 300, 1000])
+def test_tail_tiles_are_partial_and_structure_consistent(n):
+    spec = MaskSpec(causal=True, window=200, stride=3, stride_phase=2)
+    idx = block_index.build(n, spec)
+    nb = idx["n_blocks"]
+    assert nb == (n + 127) // 128
+    kinds = block_index.classify(n, spec)
+    if n % 128:
+        assert not (kinds[-1] == block_index.FULL).any()
+        assert not (kinds[:, -1] == block_index.FULL).any()
+    # CSR and CSC describe the same set of tiles with the same kinds
+    csr = {(qb, int(kb)): int(t) for qb in range(nb)
+           for kb, t in zip(idx["col_idx"][idx["row_ptr"][qb]:idx["row_ptr"][qb + 1]],
+                            idx["kind"][idx["row_ptr"][qb]:idx["row_ptr"][qb + 1]])}
+    csc = {(int(qb), kb): int(t) for kb in range(nb)
+           for qb, t in zip(idx["row_idx"][idx["col_ptr"][kb]:idx["col_ptr"][kb + 1]],
+                            idx["kind_t"][idx["col_ptr"][kb]:idx["col_ptr"][kb + 1]])}
+    assert csr == csc
+    lens = np.diff(idx["row_ptr"])
+    assert sorted(idx["q_order"].tolist()) == list(range(nb))
+    assert all(lens[a] >= lens[b] for a, b in zip(idx["q_order"], idx["q_order"][1:]))
+
+
+def test_smoke_golden_shape():
+    g = json.load(open(os.path.join(GOLDEN, "smoke_shape.json")))
+    B, N, H, d = g["input_shape"]
+    r = rng(13)
+    q, k, v = (r.standard_normal((N, d)) for _ in range(3))
+    o, _ = fwd_full(q, k, v, d ** -0.5, MaskSpec(causal=g["causal"]))
+    assert [B, o.shape[0], H, o.shape[1]] == g["output_shape"]
+
+
+# ---------------------------------------------------------------- negative controls
+def _mutant_zero_mask(q, k, v, scale, spec):
+    """Masking by multiplying scores by zero instead of -inf (a page's sketch does this)."""
+    n = q.shape[0]
+    live = live_matrix(np.arange(n), np.arange(n), n, spec)
+    s = scale * (q @ k.T) * live
+    m = s.max(axis=1, keepdims=True)
+    e = np.exp(s - m)
+    return (e / e.sum(axis=1, keepdims=True)) @ v, m[:, 0] + np.log(e.sum(axis=1))
+
+
+def _mutant_lse_sum(q, k, v, scale, spec, block=4):
+    """Online recurrence that adds log-sums and divides without the running-max rescale."""
+    n = q.shape[0]
+    o = np.zeros_like(v)
+    lse_out = np.zeros(n)
+    for r0 in range(0, n, block):
+        rows = np.arange(r0, min(n, r0 + block))
+        acc = np.zeros((len(rows), v.shape[1]))
+        lse = np.zeros(len(rows))
+        for c0 in range(0, n, block):
+            cols = np.arange(c0, min(n, c0 + block))
+            s = np.where(live_matrix(rows, cols, n, spec), scale * q[rows] @ k[cols].T, -np.inf)
+            mx = np.where(np.isfinite(s.max(axis=1)), s.max(axis=1), 0)
+            p = np.exp(s - mx[:, None])
+            lse = lse + np.log(p.sum(axis=1) + 1e-10)
+            acc = acc + (p @ v[cols]) / np.exp(lse)[:, None]
+        o[rows] = acc
+        lse_out[rows] = lse
+    return o, lse_out
+
+
+def _mutant_no_scale(q, k, v, scale, spec):
+    return fwd_full(q, k, v, 1.0, spec)
+
+
+def _mutant_strict_causal(q, k, v, scale, spec):
+    n = q.shape[0]
+    s = np.where(np.tril(np.ones((n, n), bool), -1) | ~np.array(spec.causal), scale * q @ k.T, -np.inf)
+    m = s.max(axis=1)
+    m = np.where(np.isfinite(m), m, 0)
+    e = np.exp(s - m[:, None])
+    l = e.sum(axis=1)
+    return (e / np.where(l > 0, l, 1)[:, None]) @ v, m + np.log(np.where(l > 0, l, 1))
+
+
+def _mutant_bwd_sign(q, k, v, do, scale, spec):
+    p = attention.probabilities(q, k, scale, spec)
+    dp = do @ v.T
+    ds = p * (dp + (p * dp).sum(axis=1)[:, None])
+    return scale * ds @ k, scale * ds.T @ q, p.T @ do
+
+
+def _mutant_bwd_transposed(q, k, v, do, scale, spec):
+    p = attention.probabilities(q, k, scale, spec)
+    dp = do @ v.T
+    ds = p * (dp - (p * dp).sum(axis=1)[:, None])
+    return scale * ds @ k, scale * ds.T @ q, p @ do
+
+
+def _mutant_bwd_no_scale(q, k, v, do, scale, spec):
+    dq, dk, dv = bwd_full(q, k, v, do, scale, spec)
+    return dq / scale, dk / scale, dv
+
+
+@pytest.mark.parametrize("mutant", [_mutant_zero_mask, _mutant_lse_sum, _mutant_no_scale,
+                                    _mutant_strict_causal])
+def test_forward_mistakes_fail_a_pin(mutant):
+    r = rng(20)
+    errs = [
+        max(pins.uniform_q_zero(mutant, 29, 6, s, r) for s in SMALL_SPECS.values()),
+        pins.causal_row0(mutant, 17, 8, r),
+        pins.permutation_invariance(mutant, 40, 8, r),
+    ]
+    # the mutant must also disagree with the scalar loops on random inputs
+    q, k, v = (r.standard_normal((12, 3)) for _ in range(3))
+    o_m, _ = mutant(q, k, v, 0.6, MaskSpec(causal=True))
+    o_l, _ = loops.forward_loops(q.tolist(), k.tolist(), v.tolist(), 0.6, MaskSpec(causal=True))
+    errs.append(np.abs(o_m - o_l).max())
+    assert max(errs) > 1e-3, errs
+
+
+@pytest.mark.parametrize("mutant", [_mutant_bwd_sign, _mutant_bwd_transposed, _mutant_bwd_no_scale])
+def test_backward_mistakes_fail_a_pin(mutant):
+    r = rng(21)
+    spec = MaskSpec(causal=True, window=6)
+    errs = [
+        pins.gradient_invariants(fwd_full, mutant, 26, 5, spec, r),
+        pins.finite_differences(fwd_full, mutant, 6, 2, spec, r),
+    ]
+    assert max(errs) > 1e-3, errs

@@ -1,0 +1,68 @@
+"""Seeded synthetic inputs and workload descriptions (no attention arithmetic here).
+
+Shared by the tests, ``bench.py`` and ``__graft_entry__``: every tensor is
+``numpy.random.default_rng(seed).standard_normal(shape, dtype=float32)`` in
+(B, N, H, d) layout, rounded once to bf16 (round-to-nearest-even via
+``torch.Tensor.to(torch.bfloat16)``).  The CUDA path consumes the bf16 tensor;
+the oracle consumes the same values promoted exactly to float64.
+
+Workloads: the five attention configurations the pages' discussion motivates
+(7B-style layer, d = 128, long context; causal, local window + strided, and
+local window with block dilation).  Seeds: Q, K, V, dO of workload c use
+1000*c + 1 .. 1000*c + 4.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    cid: int
+    name: str
+    B: int
+    H: int
+    N: int
+    d: int
+    # mask description: plain fields, converted by each side into its own type
+    mask: dict = field(default_factory=dict)
+
+    @property
+    def shape(self):
+        return (self.B, self.N, self.H, self.d)
+
+
+WORKLOADS = {
+    1: Workload(1, "dense B1 H1 N256 d64", 1, 1, 256, 64, {}),
+    2: Workload(2, "causal B4 H16 N4096 d128", 4, 16, 4096, 128, {"causal": True}),
+    3: Workload(3, "causal B1 H32 N16384 d128", 1, 32, 16384, 128, {"causal": True}),
+    4: Workload(4, "causal window1024 + strided8 B1 H32 N32768 d128", 1, 32, 32768, 128,
+                {"causal": True, "window": 1024, "stride": 8, "stride_phase": 0}),
+    5: Workload(5, "causal window4096 dilation2 B1 H8 N131072 d128", 1, 8, 131072, 128,
+                {"causal": True, "window": 4096, "dilation": 2, "dilation_near": 2}),
+}
+
+
+def normal_bf16(shape, seed: int) -> torch.Tensor:
+    """float32 N(0, 1) from a seeded generator, rounded to bf16 (CPU tensor)."""
+    x = np.random.default_rng(seed).standard_normal(shape, dtype=np.float32)
+    return torch.from_numpy(x).to(torch.bfloat16)
+
+
+def workload_inputs(w: Workload, names=("q", "k", "v", "do")) -> dict:
+    seeds = {"q": 1, "k": 2, "v": 3, "do": 4}
+    return {n: normal_bf16(w.shape, 1000 * w.cid + seeds[n]) for n in names}
+
+
+def small_inputs(B, N, H, d, seed: int, names=("q", "k", "v", "do")) -> dict:
+    """Inputs for extra test cases (ragged N, tiny shapes): seeds seed*10 + 1..4."""
+    seeds = {"q": 1, "k": 2, "v": 3, "do": 4}
+    return {n: normal_bf16((B, N, H, d), 10 * seed + seeds[n]) for n in names}
+
+
+def as_f64(t: torch.Tensor) -> np.ndarray:
+    """Exact promotion of a (bf16) tensor to a float64 numpy array."""
+    return t.detach().to("cpu").to(torch.float64).numpy()
