@@ -96,11 +96,18 @@ def _chunks(rows, chunk):
 
 
 def _row_block(q, k, scale, spec, rows):
-    """Masked scores for `rows` over their candidate key span; returns (cols, S)."""
+    """Masked scores for `rows` over their candidate key span; returns (cols, S).
+
+    Key columns that are dead for every row of the chunk are dropped before
+    the product (they would only contribute exp(-inf) = 0)."""
     n = q.shape[0]
     c0, c1 = candidate_cols(int(rows.min()), int(rows.max()) + 1, n, spec)
     cols = np.arange(c0, c1)
-    s = _masked_scores(q[rows], k[cols], scale, live_matrix(rows, cols, n, spec))
+    live = live_matrix(rows, cols, n, spec)
+    keep = live.any(axis=0)
+    if keep.size and keep.mean() < 0.75:
+        cols, live = cols[keep], live[:, keep]
+    s = _masked_scores(q[rows], k[cols], scale, live)
     return cols, s
 
 
