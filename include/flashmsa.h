@@ -1,0 +1,197 @@
+/*
+ * libflashmsa -- exact tiled ("Flash MSA") scaled-dot-product attention on
+ * GB300 (sm_103a), forward and recompute backward, dense / causal /
+ * block-sparse masks.
+ *
+ * Operation (page "Flash MSA Attention Kernel Implementation: A Practical
+ * Guide for Production AI", section "Why Standard Attention Broke"; page "How
+ * to Use Flash MSA Kernels for Long Context", section "What Flash MSA
+ * Actually Does"):
+ *
+ *     O = softmax(mask(Q K^T * scale)) V,   scale = d^-1/2 unless given,
+ *
+ * computed tile by tile with an online softmax (running row max and sum, the
+ * partial output rescaled per key tile; same page 1, section "The Flash Core:
+ * Tiling Over the Memory Hierarchy"), never materialising the N x N matrix.
+ * Masked scores are -inf and take no part in the max or the sum (page 1,
+ * section "Optimization Tricks That Actually Matter", paragraph "Masking and
+ * causal attention").  The forward stores O and the per-row natural-log
+ * logsumexp LSE; the backward recomputes the scores from Q, K, V, O, LSE
+ * (page 1, section "The Backward Pass: The Real Beast").  Sparse masks are
+ * applied inside the tiling loop through a precomputed per-query-block list
+ * of live key blocks (page "How Does Flash-MSA Sparse Attention Work",
+ * section "How Flash-MSA Sparse Attention Works"), so dead tiles are never
+ * loaded.
+ *
+ * Conventions shared by every entry point:
+ *   - q, k, v, o, dO, dq, dk, dv: DEVICE pointers to bf16, contiguous
+ *     (B, N, H, d) (token stride H*d elements), 16-byte aligned, owned by the
+ *     caller.  lse: DEVICE fp32 (B, H, N).
+ *   - d must be 64 or 128 (else FLASH_MSA_ERR_UNSUPPORTED); 1 <= N < 2^31 - 256;
+ *     B, H >= 1.
+ *   - scale <= 0 or NaN selects the default d^-1/2.
+ *   - stream is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     asynchronous on that stream.  The return value covers argument
+ *     validation and launch errors only; a kernel that gives up waiting (see
+ *     FLASH_MSA_ERR_TIMEOUT) or meets a corrupt index records that in a device
+ *     status word read by flash_msa_get_status().
+ *   - No entry point aborts, throws, or falls back to a CPU implementation.
+ *     On error the last message is available from flash_msa_last_error_string().
+ */
+#ifndef FLASHMSA_H
+#define FLASHMSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FLASH_MSA_OK = 0,
+  FLASH_MSA_ERR_INVALID_ARG = 1, /* null / misaligned pointer, bad size, bad mask field */
+  FLASH_MSA_ERR_UNSUPPORTED = 2, /* head dimension other than 64 or 128, pattern block != 128 */
+  FLASH_MSA_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed */
+  FLASH_MSA_ERR_TIMEOUT = 4,     /* device: a bounded wait inside a kernel ran out */
+  FLASH_MSA_ERR_WORKSPACE = 5,   /* workspace missing or smaller than required */
+  FLASH_MSA_ERR_INDEX = 6        /* block index missing, built for another N, or corrupt */
+} flash_msa_status;
+
+/* Mask flags.  Element predicate for query i, key j of a length-N sequence:
+ *   live(i,j) = (i < N) && (j < N) && (!CAUSAL || j <= i) && pattern(i,j)
+ *   pattern   = true                                   if no WINDOW/DILATED/STRIDED flag
+ *             = near(i,j) || strided(j)                otherwise
+ *   near      = (WINDOW or DILATED set) && (!WINDOW || |i-j| <= window)
+ *               && (!DILATED || D < dilation_near || D % dilation == 0),
+ *               D = | floor(i/block) - floor(j/block) |
+ *   strided   = STRIDED && floor(j/block) % stride == stride_phase
+ * Window: "Local window -- attend only to +-W tokens"; dilated: "skip every
+ * few tokens", read at block level; strided: the fixed pattern of Child et
+ * al. (page "How Does Flash-MSA Sparse Attention Work", section "How
+ * Flash-MSA Sparse Attention Works", list of masks). */
+enum {
+  FLASH_MSA_CAUSAL = 1,
+  FLASH_MSA_WINDOW = 2,
+  FLASH_MSA_DILATED = 4,
+  FLASH_MSA_STRIDED = 8
+};
+
+/* Per-query-block list of live key blocks ("a precomputed index list", page
+ * "How Does Flash-MSA Sparse Attention Work", section "How Flash-MSA Sparse
+ * Attention Works").  Tiles are block x block = 128 x 128.  A tile is dead
+ * (no live entry; not listed), full (every entry live; kind 0) or partial
+ * (kind 1: the kernel evaluates the element predicate).  Rows/columns past N
+ * count as dead entries, so tail tiles are never full.
+ *   CSR by query block: row_ptr[n_q_blocks+1], col_idx[nnz] (ascending), kind[nnz]
+ *   CSC by key block:   col_ptr[n_k_blocks+1], row_idx[nnz] (ascending), kind_t[nnz]
+ *   q_order[n_q_blocks] / k_order[n_k_blocks]: blocks by descending live-tile
+ *   count, ties by ascending index (longest work is scheduled first).
+ * The struct itself always lives in HOST memory.  Its array pointers are host
+ * pointers when filled by flash_msa_build_block_index() and DEVICE pointers
+ * when passed to flash_msa_fwd()/flash_msa_bwd() (copy the arrays over and
+ * point a second struct at the copies).  The caller owns every array. */
+typedef struct flash_msa_block_index {
+  int64_t seq_len; /* N the index was built for */
+  int32_t n_q_blocks, n_k_blocks, block;
+  int64_t nnz;
+  int32_t* row_ptr;
+  int32_t* col_idx;
+  uint8_t* kind;
+  int32_t* col_ptr;
+  int32_t* row_idx;
+  uint8_t* kind_t;
+  int32_t* q_order;
+  int32_t* k_order;
+} flash_msa_block_index;
+
+/* Mask description (host memory).  A NULL mask, or flags == 0, is dense
+ * attention.  flags == CAUSAL may pass index = NULL (tiles are derived
+ * arithmetically); any WINDOW/DILATED/STRIDED flag requires an index built for
+ * the same N and mask, else FLASH_MSA_ERR_INDEX.  block must be 128.
+ * window >= 0 (tokens, inclusive); dilation >= 1; dilation_near >= 0;
+ * stride >= 1 and 0 <= stride_phase < stride when the flag is set. */
+typedef struct {
+  uint32_t flags;
+  int32_t block;
+  int64_t window;
+  int32_t dilation, dilation_near;
+  int32_t stride, stride_phase;
+  const flash_msa_block_index* index;
+} flash_msa_mask_desc;
+
+/* Build the block index for `mask` and sequence length N on the HOST (no GPU
+ * work).  Two phases: call with out->row_ptr == NULL to fill only the counts
+ * (seq_len, n_q_blocks, n_k_blocks, block, nnz); allocate every array with
+ * those sizes (row_ptr/col_ptr n+1 int32, col_idx/row_idx nnz int32,
+ * kind/kind_t nnz uint8, q_order/k_order n int32) and call again to fill
+ * them.  mask->index is ignored.  Errors: INVALID_ARG (null, N < 1, bad
+ * field), UNSUPPORTED (block != 128). */
+flash_msa_status flash_msa_build_block_index(const flash_msa_mask_desc* mask, int64_t N,
+                                             flash_msa_block_index* out);
+
+/* Check a HOST copy of an index for internal consistency against N: sizes,
+ * monotone pointers, ascending in-range block ids, kinds in {0,1}, CSC equal
+ * to the transpose of CSR, orders being permutations.  Returns OK or
+ * ERR_INDEX.  The kernels additionally skip (and report ERR_INDEX for) any
+ * out-of-range block id they meet, so a corrupt device index cannot make
+ * them read outside the tensors. */
+flash_msa_status flash_msa_check_block_index(const flash_msa_block_index* host_index, int64_t N);
+
+/* Forward: o = attention(q, k, v), lse[b,h,i] = log sum_j exp(scale q_i.k_j)
+ * over live j (natural log; -inf and o_i = 0 for a row with no live key).
+ * One persistent kernel launch on `stream`. */
+flash_msa_status flash_msa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                               int B, int H, int64_t N, int d, float scale,
+                               const flash_msa_mask_desc* mask, void* stream);
+
+/* Bytes of device workspace flash_msa_bwd() needs: two fp32 vectors per
+ * (b, h), each padded to whole 128-row tiles -- LSE_i * log2(e) and
+ * D_i = sum_c dO_ic * O_ic -- rounded up to 256 bytes.  0 for invalid sizes. */
+size_t flash_msa_bwd_workspace_bytes(int B, int H, int64_t N, int d);
+
+/* Backward: given the forward's o and lse and the upstream gradient dO,
+ * write dq, dk, dv (bf16, (B, N, H, d)):
+ *   P = exp(scale Q K^T - LSE) on live entries, dV = P^T dO, dP = dO V^T,
+ *   D = rowsum(dO o O), dS = P o (dP - D), dQ = scale dS K, dK = scale dS^T Q
+ * (page 1, section "The Backward Pass: The Real Beast"; the scale enters dQ
+ * and dK by the chain rule).  `workspace` is a DEVICE buffer of at least
+ * flash_msa_bwd_workspace_bytes() bytes owned by the caller (contents are
+ * overwritten); else FLASH_MSA_ERR_WORKSPACE.  Three kernel launches on
+ * `stream` (D, then dK/dV, then dQ); no atomics, results are deterministic. */
+flash_msa_status flash_msa_bwd(const void* q, const void* k, const void* v, const void* o,
+                               const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                               int B, int H, int64_t N, int d, float scale,
+                               const flash_msa_mask_desc* mask, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+/* The three launches of flash_msa_bwd() one at a time (same arguments plus a
+ * bit set): bit 0 = D and scaled LSE into the workspace (must run first),
+ * bit 1 = dK and dV, bit 2 = dQ.  flash_msa_bwd() is stages = 7.  Bits 1 and
+ * 2 read the workspace written by bit 0 and may run in either order. */
+#define FLASH_MSA_BWD_PREPROCESS 1u
+#define FLASH_MSA_BWD_DKDV 2u
+#define FLASH_MSA_BWD_DQ 4u
+flash_msa_status flash_msa_bwd_stages(const void* q, const void* k, const void* v, const void* o,
+                                      const float* lse, const void* dO, void* dq, void* dk,
+                                      void* dv, int B, int H, int64_t N, int d, float scale,
+                                      const flash_msa_mask_desc* mask, void* workspace,
+                                      size_t workspace_bytes, unsigned stages, void* stream);
+
+/* Synchronise `stream`, then read and clear the device status word shared by
+ * every kernel of this library on the current device.  Returns OK, or the
+ * first device-side error recorded since the last call (TIMEOUT, INDEX), or
+ * ERR_CUDA if the synchronisation itself failed. */
+flash_msa_status flash_msa_get_status(void* stream);
+
+/* Message for the last error returned on this host thread ("" if none). */
+const char* flash_msa_last_error_string(void);
+
+/* Library version string. */
+const char* flash_msa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLASHMSA_H */

@@ -1,0 +1,86 @@
+"""The C++ block-index builder is bit-exact with the oracle's brute-force build."""
+import numpy as np
+import pytest
+
+from tests.oracle_cache import oracle_index
+from tiled_exact_attention_flash_gb300 import api
+from tiled_exact_attention_flash_gb300.inputs import WORKLOADS
+
+ARRAYS = ("row_ptr", "col_idx", "kind", "col_ptr", "row_idx", "kind_t", "q_order", "k_order")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from tests.libbuild import ensure_built
+    ensure_built()
+
+
+def compare(n, fields):
+    ref = oracle_index(n, tuple(sorted(fields.items())))
+    got = api.build_block_index(api.Mask(**fields), n)
+    assert got.nnz == ref["nnz"]
+    assert got.header.n_q_blocks == ref["n_blocks"] == got.header.n_k_blocks
+    for name in ARRAYS:
+        a, b = got.host[name], ref[name]
+        assert a.dtype == b.dtype, name
+        assert np.array_equal(a, b), name
+    assert api.check_block_index(got) == api.OK
+    return got
+
+
+@pytest.mark.parametrize("cid", [1, 2, 3, 4, 5])
+def test_workload_indices_bit_exact(cid):
+    w = WORKLOADS[cid]
+    fields = dict(w.mask)
+    if not fields:
+        fields = {}
+    compare(w.N, fields)
+
+
+MASKS = [
+    {},
+    {"causal": True},
+    {"window": 300},
+    {"causal": True, "window": 1},
+    {"causal": True, "window": 129, "stride": 3, "stride_phase": 1},
+    {"causal": True, "window": 700, "dilation": 2, "dilation_near": 2},
+    {"window": 513, "dilation": 3, "dilation_near": 1},
+    {"dilation": 2, "dilation_near": 0},
+    {"causal": True, "stride": 4, "stride_phase": 3},
+    {"stride": 2, "stride_phase": 0, "window": 64},
+]
+
+
+@pytest.mark.parametrize("n", [1, 5, 127, 128, 129, 255, 256, 1000, 2047])
+@pytest.mark.parametrize("mi", range(len(MASKS)))
+def test_small_indices_bit_exact(n, mi):
+    compare(n, MASKS[mi])
+
+
+def test_random_indices_bit_exact():
+    rng = np.random.default_rng(7)
+    for _ in range(25):
+        n = int(rng.integers(1, 2049))
+        f = {"causal": bool(rng.integers(0, 2))}
+        if rng.integers(0, 2):
+            f["window"] = int(rng.integers(0, 1500))
+        if rng.integers(0, 2):
+            f["dilation"] = int(rng.integers(1, 5))
+            f["dilation_near"] = int(rng.integers(0, 4))
+        if rng.integers(0, 2):
+            s = int(rng.integers(1, 9))
+            f["stride"] = s
+            f["stride_phase"] = int(rng.integers(0, s))
+        compare(n, f)
+
+
+def test_checker_rejects_corruption():
+    idx = api.build_block_index(api.Mask(causal=True, window=500, stride=2), 2000)
+    assert api.check_block_index(idx) == api.OK
+    for name, pos, val in [("col_idx", 3, 99), ("kind", 0, 7), ("row_idx", 1, -1),
+                           ("q_order", 0, 1), ("row_ptr", 2, 0)]:
+        saved = idx.host[name][pos]
+        idx.host[name][pos] = val
+        assert api.check_block_index(idx) == api.ERR_INDEX, name
+        idx.host[name][pos] = saved
+    assert api.check_block_index(idx) == api.OK

@@ -1,0 +1,319 @@
+"""ctypes binding over libflashmsa (argument marshalling only).
+
+Every step of the computation runs in the CUDA library; this module checks
+tensor dtypes / devices / shapes, allocates outputs with PyTorch (which is
+used here only for device memory and streams), passes raw pointers and the
+current CUDA stream, and turns non-zero status codes into exceptions.  There
+is no fallback: if ``libflashmsa.so`` is missing, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libflashmsa.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE, ERR_INDEX = range(7)
+STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "TIMEOUT",
+                5: "WORKSPACE", 6: "INDEX"}
+CAUSAL, WINDOW, DILATED, STRIDED = 1, 2, 4, 8
+
+# exported symbols, in the order include/flashmsa.h declares them
+SYMBOLS = (
+    "flash_msa_build_block_index",
+    "flash_msa_check_block_index",
+    "flash_msa_fwd",
+    "flash_msa_bwd_workspace_bytes",
+    "flash_msa_bwd",
+    "flash_msa_bwd_stages",
+    "flash_msa_get_status",
+    "flash_msa_last_error_string",
+    "flash_msa_version",
+)
+
+
+class BlockIndexStruct(ctypes.Structure):
+    _fields_ = [
+        ("seq_len", ctypes.c_int64),
+        ("n_q_blocks", ctypes.c_int32),
+        ("n_k_blocks", ctypes.c_int32),
+        ("block", ctypes.c_int32),
+        ("nnz", ctypes.c_int64),
+        ("row_ptr", ctypes.c_void_p),
+        ("col_idx", ctypes.c_void_p),
+        ("kind", ctypes.c_void_p),
+        ("col_ptr", ctypes.c_void_p),
+        ("row_idx", ctypes.c_void_p),
+        ("kind_t", ctypes.c_void_p),
+        ("q_order", ctypes.c_void_p),
+        ("k_order", ctypes.c_void_p),
+    ]
+
+
+class MaskDescStruct(ctypes.Structure):
+    _fields_ = [
+        ("flags", ctypes.c_uint32),
+        ("block", ctypes.c_int32),
+        ("window", ctypes.c_int64),
+        ("dilation", ctypes.c_int32),
+        ("dilation_near", ctypes.c_int32),
+        ("stride", ctypes.c_int32),
+        ("stride_phase", ctypes.c_int32),
+        ("index", ctypes.c_void_p),
+    ]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libflashmsa.so (once); raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                           "(there is no CPU fallback)")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+    L.flash_msa_build_block_index.argtypes = [ctypes.POINTER(MaskDescStruct), i64,
+                                              ctypes.POINTER(BlockIndexStruct)]
+    L.flash_msa_check_block_index.argtypes = [ctypes.POINTER(BlockIndexStruct), i64]
+    L.flash_msa_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i64, i32, f32,
+                                ctypes.POINTER(MaskDescStruct), vp]
+    L.flash_msa_bwd_workspace_bytes.argtypes = [i32, i32, i64, i32]
+    L.flash_msa_bwd_workspace_bytes.restype = ctypes.c_size_t
+    L.flash_msa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i64, i32, f32,
+                                ctypes.POINTER(MaskDescStruct), vp, ctypes.c_size_t, vp]
+    L.flash_msa_bwd_stages.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i64, i32,
+                                       f32, ctypes.POINTER(MaskDescStruct), vp, ctypes.c_size_t,
+                                       ctypes.c_uint, vp]
+    L.flash_msa_get_status.argtypes = [vp]
+    L.flash_msa_last_error_string.restype = ctypes.c_char_p
+    L.flash_msa_version.restype = ctypes.c_char_p
+    for name in ("flash_msa_build_block_index", "flash_msa_check_block_index", "flash_msa_fwd",
+                 "flash_msa_bwd", "flash_msa_bwd_stages", "flash_msa_get_status"):
+        getattr(L, name).restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+class FlashMSAError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        msg = lib().flash_msa_last_error_string().decode()
+        super().__init__(f"{where}: {STATUS_NAMES.get(code, code)} ({msg})")
+        self.code = code
+
+
+def _check(code: int, where: str):
+    if code != OK:
+        raise FlashMSAError(code, where)
+
+
+# ---------------------------------------------------------------------------
+# masks and block indices
+# ---------------------------------------------------------------------------
+@dataclass(frozen=True)
+class Mask:
+    """Attention mask description (semantics in include/flashmsa.h)."""
+    causal: bool = False
+    window: Optional[int] = None
+    dilation: Optional[int] = None
+    dilation_near: int = 0
+    stride: Optional[int] = None
+    stride_phase: int = 0
+    block: int = 128
+
+    @classmethod
+    def from_fields(cls, fields: dict) -> "Mask":
+        return cls(**fields)
+
+    @property
+    def flags(self) -> int:
+        f = CAUSAL if self.causal else 0
+        f |= WINDOW if self.window is not None else 0
+        f |= DILATED if self.dilation is not None else 0
+        f |= STRIDED if self.stride is not None else 0
+        return f
+
+    @property
+    def needs_index(self) -> bool:
+        return bool(self.flags & (WINDOW | DILATED | STRIDED))
+
+    def desc(self, index_ptr=None) -> MaskDescStruct:
+        return MaskDescStruct(self.flags, self.block, self.window or 0, self.dilation or 1,
+                              self.dilation_near, self.stride or 1, self.stride_phase,
+                              index_ptr)
+
+
+_INDEX_ARRAYS = (("row_ptr", np.int32, "nq1"), ("col_idx", np.int32, "nnz"),
+                 ("kind", np.uint8, "nnz"), ("col_ptr", np.int32, "nk1"),
+                 ("row_idx", np.int32, "nnz"), ("kind_t", np.uint8, "nnz"),
+                 ("q_order", np.int32, "nq"), ("k_order", np.int32, "nk"))
+
+
+class BlockIndex:
+    """Host arrays of a block index and (after ``to``) their device copies."""
+
+    def __init__(self, mask: Mask, n: int, host: dict, header: BlockIndexStruct):
+        self.mask, self.n, self.host, self.header = mask, n, host, header
+        self.device: dict = {}
+        self.device_struct: Optional[BlockIndexStruct] = None
+
+    @property
+    def nnz(self) -> int:
+        return int(self.header.nnz)
+
+    def host_struct(self) -> BlockIndexStruct:
+        s = BlockIndexStruct(self.header.seq_len, self.header.n_q_blocks, self.header.n_k_blocks,
+                             self.header.block, self.header.nnz)
+        for name, _, _ in _INDEX_ARRAYS:
+            setattr(s, name, self.host[name].ctypes.data)
+        return s
+
+    def to(self, device) -> "BlockIndex":
+        # at least one element per array, so every device pointer is non-null
+        self.device = {name: torch.from_numpy(arr.copy() if arr.size else np.zeros(1, arr.dtype)).to(device)
+                       for name, arr in self.host.items()}
+        s = BlockIndexStruct(self.header.seq_len, self.header.n_q_blocks, self.header.n_k_blocks,
+                             self.header.block, self.header.nnz)
+        for name, _, _ in _INDEX_ARRAYS:
+            t = self.device[name]
+            setattr(s, name, t.data_ptr())
+        self.device_struct = s
+        return self
+
+
+def build_block_index(mask: Mask, n: int) -> BlockIndex:
+    """Host-side build (two-phase C call); returns host numpy arrays."""
+    L = lib()
+    desc = mask.desc()
+    hdr = BlockIndexStruct()
+    _check(L.flash_msa_build_block_index(ctypes.byref(desc), n, ctypes.byref(hdr)),
+           "build_block_index(count)")
+    sizes = {"nq1": hdr.n_q_blocks + 1, "nk1": hdr.n_k_blocks + 1, "nnz": hdr.nnz,
+             "nq": hdr.n_q_blocks, "nk": hdr.n_k_blocks}
+    host = {name: np.zeros(max(1, sizes[kind]), dtype=dt) for name, dt, kind in _INDEX_ARRAYS}
+    out = BlockIndexStruct(hdr.seq_len, hdr.n_q_blocks, hdr.n_k_blocks, hdr.block, hdr.nnz)
+    for name, _, _ in _INDEX_ARRAYS:
+        setattr(out, name, host[name].ctypes.data)
+    _check(L.flash_msa_build_block_index(ctypes.byref(desc), n, ctypes.byref(out)),
+           "build_block_index(fill)")
+    host = {name: host[name][:sizes[kind]] for name, _, kind in _INDEX_ARRAYS}
+    return BlockIndex(mask, n, host, out)
+
+
+def check_block_index(index: BlockIndex) -> int:
+    s = index.host_struct()
+    return lib().flash_msa_check_block_index(ctypes.byref(s), index.n)
+
+
+# ---------------------------------------------------------------------------
+# attention calls
+# ---------------------------------------------------------------------------
+def _stream_ptr(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _check_qkv(name, t, shape=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (B, N, H, d)")
+    if t.dim() != 4:
+        raise ValueError(f"{name} must have shape (B, N, H, d)")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _mask_desc(mask: Optional[Mask], index: Optional[BlockIndex], n: int):
+    if mask is None:
+        return None, None
+    if index is not None:
+        if index.device_struct is None:
+            raise ValueError("block index has no device copy: call index.to(device)")
+        if index.n != n:
+            raise ValueError(f"block index built for N={index.n}, tensors have N={n}")
+        holder = index.device_struct
+        return mask.desc(ctypes.addressof(holder)), holder
+    return mask.desc(), None
+
+
+def fwd(q, k, v, mask: Optional[Mask] = None, index: Optional[BlockIndex] = None,
+        scale: Optional[float] = None, out=None, lse=None, stream=None):
+    """O (bf16, like q) and LSE (fp32, (B, H, N))."""
+    _check_qkv("q", q)
+    B, N, H, d = q.shape
+    _check_qkv("k", k, q.shape)
+    _check_qkv("v", v, q.shape)
+    o = torch.empty_like(q) if out is None else out
+    _check_qkv("out", o, q.shape)
+    l = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    if l.dtype != torch.float32 or not l.is_contiguous() or tuple(l.shape) != (B, H, N):
+        raise ValueError("lse must be contiguous float32 (B, H, N)")
+    desc, _keep = _mask_desc(mask, index, N)
+    code = lib().flash_msa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                               l.data_ptr(), B, H, N, d, float(scale or 0.0),
+                               ctypes.byref(desc) if desc is not None else None,
+                               _stream_ptr(stream))
+    _check(code, "flash_msa_fwd")
+    return o, l
+
+
+def bwd_workspace_bytes(B, H, N, d) -> int:
+    return int(lib().flash_msa_bwd_workspace_bytes(B, H, N, d))
+
+
+BWD_PREPROCESS, BWD_DKDV, BWD_DQ = 1, 2, 4
+
+
+def bwd(q, k, v, o, lse, do, mask: Optional[Mask] = None, index: Optional[BlockIndex] = None,
+        scale: Optional[float] = None, dq=None, dk=None, dv=None, workspace=None, stream=None,
+        stages: Optional[int] = None):
+    """dQ, dK, dV (bf16, like q).  ``stages`` (bits BWD_*) runs a subset of the
+    three launches through flash_msa_bwd_stages; default: all of them."""
+    _check_qkv("q", q)
+    B, N, H, d = q.shape
+    for name, t in (("k", k), ("v", v), ("o", o), ("do", do)):
+        _check_qkv(name, t, q.shape)
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (B, H, N):
+        raise ValueError("lse must be contiguous float32 (B, H, N)")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    ws_bytes = bwd_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    desc, _keep = _mask_desc(mask, index, N)
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+            do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d,
+            float(scale or 0.0), ctypes.byref(desc) if desc is not None else None,
+            workspace.data_ptr(), workspace.numel() * workspace.element_size())
+    if stages is None:
+        code = lib().flash_msa_bwd(*args, _stream_ptr(stream))
+    else:
+        code = lib().flash_msa_bwd_stages(*args, stages, _stream_ptr(stream))
+    _check(code, "flash_msa_bwd")
+    return dq, dk, dv
+
+
+def get_status(stream=None) -> int:
+    """Synchronise the stream and read + clear the device status word."""
+    return lib().flash_msa_get_status(_stream_ptr(stream))
+
+
+def check_status(stream=None):
+    _check(get_status(stream), "device status")
+
+
+def version() -> str:
+    return lib().flash_msa_version().decode()

@@ -1,0 +1,420 @@
+// C-ABI entry points of libflashmsa (declared in include/flashmsa.h):
+// argument validation, the host-side block-index builder and checker, TMA
+// descriptor creation, kernel launch and the device status word.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <vector>
+
+#include "internal.h"
+
+namespace fmsa {
+
+static thread_local char g_last_error[512] = "";
+
+flash_msa_status set_error(flash_msa_status code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+flash_msa_status set_cuda_error(const char* what) {
+  const cudaError_t e = cudaGetLastError();
+  return set_error(FLASH_MSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+flash_msa_status make_tile_map(CUtensorMap* m, const void* base, int B, int64_t N, int H, int d) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return set_error(FLASH_MSA_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  const cuuint64_t dims[4] = {cuuint64_t(d), cuuint64_t(N), cuuint64_t(H), cuuint64_t(B)};
+  const cuuint64_t strides[3] = {cuuint64_t(H) * d * 2, cuuint64_t(d) * 2,
+                                 cuuint64_t(N) * H * d * 2};
+  const cuuint32_t box[4] = {64, 128, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return set_error(FLASH_MSA_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", int(r));
+  return FLASH_MSA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// validation helpers
+// ---------------------------------------------------------------------------
+static constexpr int64_t kMaxN = (int64_t(1) << 31) - 256;
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static int64_t n_blocks_of(int64_t N) { return (N + kTile - 1) / kTile; }
+
+// Converts the mask into kernel form; `need_index` is set for pattern masks.
+static flash_msa_status check_mask(const flash_msa_mask_desc* m, MaskParams& mp,
+                                   bool& need_index) {
+  memset(&mp, 0, sizeof(mp));
+  mp.window = kUnbounded;
+  mp.dilation = 1;
+  mp.stride = 1;
+  need_index = false;
+  if (!m) return FLASH_MSA_OK;
+  if (m->flags & ~uint32_t(FLASH_MSA_CAUSAL | FLASH_MSA_WINDOW | FLASH_MSA_DILATED |
+                           FLASH_MSA_STRIDED))
+    return set_error(FLASH_MSA_ERR_INVALID_ARG, "mask: unknown flag bits 0x%x", m->flags);
+  const uint32_t pat = m->flags & (FLASH_MSA_WINDOW | FLASH_MSA_DILATED | FLASH_MSA_STRIDED);
+  if (m->block != kTile && !(m->block == 0 && pat == 0))
+    return set_error(FLASH_MSA_ERR_UNSUPPORTED, "mask: pattern block %d (only 128 is supported)",
+                     m->block);
+  mp.flags = m->flags;
+  if (m->flags & FLASH_MSA_WINDOW) {
+    if (m->window < 0) return set_error(FLASH_MSA_ERR_INVALID_ARG, "mask: window < 0");
+    mp.window = m->window < kUnbounded ? m->window : kUnbounded;
+  }
+  if (m->flags & FLASH_MSA_DILATED) {
+    if (m->dilation < 1 || m->dilation_near < 0)
+      return set_error(FLASH_MSA_ERR_INVALID_ARG, "mask: dilation must be >= 1, near >= 0");
+    mp.dilation = m->dilation;
+    mp.near = m->dilation_near;
+  }
+  if (m->flags & FLASH_MSA_STRIDED) {
+    if (m->stride < 1 || m->stride_phase < 0 || m->stride_phase >= m->stride)
+      return set_error(FLASH_MSA_ERR_INVALID_ARG, "mask: stride must be >= 1, 0 <= phase < stride");
+    mp.stride = m->stride;
+    mp.phase = m->stride_phase;
+  }
+  need_index = pat != 0;
+  return FLASH_MSA_OK;
+}
+
+static flash_msa_status check_dims(int B, int H, int64_t N, int d) {
+  if (B < 1 || H < 1) return set_error(FLASH_MSA_ERR_INVALID_ARG, "B and H must be >= 1");
+  if (N < 1 || N > kMaxN)
+    return set_error(FLASH_MSA_ERR_INVALID_ARG, "N must be in [1, 2^31 - 256], got %lld",
+                     static_cast<long long>(N));
+  if (d != 64 && d != 128)
+    return set_error(FLASH_MSA_ERR_UNSUPPORTED, "head dimension %d (supported: 64, 128)", d);
+  const int64_t units = int64_t(B) * H * n_blocks_of(N);
+  if (units > int64_t(1) << 30)
+    return set_error(FLASH_MSA_ERR_INVALID_ARG, "B * H * ceil(N/128) too large");
+  return FLASH_MSA_OK;
+}
+
+// Lists for the kernels: from a device index, or arithmetic for dense / causal.
+static flash_msa_status make_lists(const flash_msa_mask_desc* m, int64_t N, bool need_index,
+                                   bool want_csc, ListParams& rows, ListParams& cols) {
+  memset(&rows, 0, sizeof(rows));
+  memset(&cols, 0, sizeof(cols));
+  const int nb = int(n_blocks_of(N));
+  rows.n_blocks = cols.n_blocks = nb;
+  rows.causal = cols.causal = (m && (m->flags & FLASH_MSA_CAUSAL)) ? 1 : 0;
+  rows.tail = cols.tail = (N % kTile) != 0;
+  cols.transposed = 1;
+  const flash_msa_block_index* ix = m ? m->index : nullptr;
+  if (!ix) {
+    if (need_index)
+      return set_error(FLASH_MSA_ERR_INDEX, "mask has window/dilation/stride flags but no index");
+    return FLASH_MSA_OK;
+  }
+  if (ix->seq_len != N || ix->block != kTile || ix->n_q_blocks != nb || ix->n_k_blocks != nb ||
+      ix->nnz < 0)
+    return set_error(FLASH_MSA_ERR_INDEX,
+                     "index built for N=%lld block=%d blocks=%dx%d, call has N=%lld",
+                     static_cast<long long>(ix->seq_len), ix->block, ix->n_q_blocks,
+                     ix->n_k_blocks, static_cast<long long>(N));
+  if (!ix->row_ptr || !ix->col_idx || !ix->kind || !ix->q_order)
+    return set_error(FLASH_MSA_ERR_INDEX, "index: CSR arrays or q_order missing");
+  rows.ptr = ix->row_ptr;
+  rows.idx = ix->col_idx;
+  rows.kind = ix->kind;
+  rows.order = ix->q_order;
+  rows.nnz = ix->nnz;
+  if (want_csc) {
+    if (!ix->col_ptr || !ix->row_idx || !ix->kind_t || !ix->k_order)
+      return set_error(FLASH_MSA_ERR_INDEX, "index: CSC arrays or k_order missing");
+    cols.ptr = ix->col_ptr;
+    cols.idx = ix->row_idx;
+    cols.kind = ix->kind_t;
+    cols.order = ix->k_order;
+    cols.nnz = ix->nnz;
+  }
+  return FLASH_MSA_OK;
+}
+
+static float resolve_scale(float scale, int d) {
+  if (!(scale > 0.f) || std::isinf(scale)) return 1.0f / std::sqrt(float(d));
+  return scale;
+}
+
+}  // namespace fmsa
+
+using namespace fmsa;
+
+extern "C" {
+
+const char* flash_msa_last_error_string(void) { return g_last_error; }
+
+const char* flash_msa_version(void) { return "libflashmsa 0.1 (sm_103a, tcgen05)"; }
+
+flash_msa_status flash_msa_build_block_index(const flash_msa_mask_desc* mask, int64_t N,
+                                             flash_msa_block_index* out) {
+  g_last_error[0] = 0;
+  if (!mask || !out) return set_error(FLASH_MSA_ERR_INVALID_ARG, "build_block_index: null argument");
+  if (N < 1 || N > kMaxN) return set_error(FLASH_MSA_ERR_INVALID_ARG, "build_block_index: bad N");
+  if (mask->block != kTile)
+    return set_error(FLASH_MSA_ERR_UNSUPPORTED, "build_block_index: block must be 128");
+  MaskParams mp;
+  bool need = false;
+  flash_msa_status st = check_mask(mask, mp, need);
+  if (st != FLASH_MSA_OK) return st;
+  const int64_t nb = n_blocks_of(N);
+  // candidate key blocks per query block: causal and a plain window bound the span
+  const bool window_bound = (mp.flags & FLASH_MSA_WINDOW) && !(mp.flags & FLASH_MSA_STRIDED);
+  const int64_t span = window_bound ? mp.window / kTile + 2 : nb;
+  auto for_each_tile = [&](auto&& fn) {
+    for (int64_t qb = 0; qb < nb; ++qb) {
+      int64_t k0 = window_bound ? std::max<int64_t>(0, qb - span) : 0;
+      int64_t k1 = window_bound ? std::min<int64_t>(nb - 1, qb + span) : nb - 1;
+      if (mp.flags & FLASH_MSA_CAUSAL) k1 = std::min(k1, qb);
+      for (int64_t kb = k0; kb <= k1; ++kb) {
+        const int c = classify_tile(int(qb), int(kb), N, mp);
+        if (c >= 0) fn(int(qb), int(kb), c);
+      }
+    }
+  };
+  out->seq_len = N;
+  out->block = kTile;
+  out->n_q_blocks = out->n_k_blocks = int32_t(nb);
+  if (!out->row_ptr) {
+    int64_t nnz = 0;
+    for_each_tile([&](int, int, int) { ++nnz; });
+    if (nnz > INT32_MAX)
+      return set_error(FLASH_MSA_ERR_INVALID_ARG, "build_block_index: more than 2^31 live tiles");
+    out->nnz = nnz;
+    return FLASH_MSA_OK;
+  }
+  if (!out->col_idx || !out->kind || !out->col_ptr || !out->row_idx || !out->kind_t ||
+      !out->q_order || !out->k_order)
+    return set_error(FLASH_MSA_ERR_INVALID_ARG, "build_block_index: some output arrays are null");
+  // CSR
+  std::vector<int32_t> col_count(size_t(nb), 0);
+  int64_t pos = 0;
+  int64_t cur = 0;
+  out->row_ptr[0] = 0;
+  for_each_tile([&](int qb, int kb, int c) {
+    while (cur < qb) out->row_ptr[++cur] = int32_t(pos);
+    if (pos < out->nnz) {
+      out->col_idx[pos] = kb;
+      out->kind[pos] = uint8_t(c);
+    }
+    ++pos;
+    ++col_count[size_t(kb)];
+  });
+  while (cur < nb) out->row_ptr[++cur] = int32_t(pos);
+  if (pos != out->nnz)
+    return set_error(FLASH_MSA_ERR_INVALID_ARG,
+                     "build_block_index: nnz %lld does not match the counting pass (%lld)",
+                     static_cast<long long>(out->nnz), static_cast<long long>(pos));
+  // CSC by counting sort: query blocks come out ascending within each column
+  out->col_ptr[0] = 0;
+  for (int64_t kb = 0; kb < nb; ++kb) out->col_ptr[kb + 1] = out->col_ptr[kb] + col_count[size_t(kb)];
+  std::vector<int32_t> fill(out->col_ptr, out->col_ptr + nb);
+  for (int64_t qb = 0; qb < nb; ++qb)
+    for (int32_t e = out->row_ptr[qb]; e < out->row_ptr[qb + 1]; ++e) {
+      const int32_t kb = out->col_idx[e];
+      const int32_t dst = fill[size_t(kb)]++;
+      out->row_idx[dst] = int32_t(qb);
+      out->kind_t[dst] = out->kind[e];
+    }
+  // longest-first orders (stable)
+  for (int64_t b = 0; b < nb; ++b) out->q_order[b] = out->k_order[b] = int32_t(b);
+  std::stable_sort(out->q_order, out->q_order + nb, [&](int32_t a, int32_t b) {
+    return out->row_ptr[a + 1] - out->row_ptr[a] > out->row_ptr[b + 1] - out->row_ptr[b];
+  });
+  std::stable_sort(out->k_order, out->k_order + nb, [&](int32_t a, int32_t b) {
+    return out->col_ptr[a + 1] - out->col_ptr[a] > out->col_ptr[b + 1] - out->col_ptr[b];
+  });
+  return FLASH_MSA_OK;
+}
+
+flash_msa_status flash_msa_check_block_index(const flash_msa_block_index* ix, int64_t N) {
+  g_last_error[0] = 0;
+  if (!ix) return set_error(FLASH_MSA_ERR_INVALID_ARG, "check_block_index: null index");
+  const int64_t nb = n_blocks_of(N);
+  if (ix->seq_len != N || ix->block != kTile || ix->n_q_blocks != nb || ix->n_k_blocks != nb)
+    return set_error(FLASH_MSA_ERR_INDEX, "index: header does not match N=%lld",
+                     static_cast<long long>(N));
+  if (!ix->row_ptr || !ix->col_idx || !ix->kind || !ix->col_ptr || !ix->row_idx || !ix->kind_t ||
+      !ix->q_order || !ix->k_order)
+    return set_error(FLASH_MSA_ERR_INDEX, "index: missing array");
+  auto check_lists = [&](const int32_t* ptr, const int32_t* idx, const uint8_t* kind,
+                         const char* what) -> bool {
+    if (ptr[0] != 0 || ptr[nb] != ix->nnz) return false;
+    for (int64_t b = 0; b < nb; ++b) {
+      if (ptr[b + 1] < ptr[b]) return false;
+      for (int32_t e = ptr[b]; e < ptr[b + 1]; ++e) {
+        if (idx[e] < 0 || idx[e] >= nb || kind[e] > 1) return false;
+        if (e > ptr[b] && idx[e] <= idx[e - 1]) return false;
+      }
+    }
+    (void)what;
+    return true;
+  };
+  if (!check_lists(ix->row_ptr, ix->col_idx, ix->kind, "CSR"))
+    return set_error(FLASH_MSA_ERR_INDEX, "index: CSR arrays are inconsistent");
+  if (!check_lists(ix->col_ptr, ix->row_idx, ix->kind_t, "CSC"))
+    return set_error(FLASH_MSA_ERR_INDEX, "index: CSC arrays are inconsistent");
+  // CSC must be the transpose of CSR
+  std::vector<int32_t> fill(ix->col_ptr, ix->col_ptr + nb);
+  for (int64_t qb = 0; qb < nb; ++qb)
+    for (int32_t e = ix->row_ptr[qb]; e < ix->row_ptr[qb + 1]; ++e) {
+      const int32_t kb = ix->col_idx[e];
+      const int32_t at = fill[size_t(kb)]++;
+      if (at >= ix->col_ptr[kb + 1] || ix->row_idx[at] != qb || ix->kind_t[at] != ix->kind[e])
+        return set_error(FLASH_MSA_ERR_INDEX, "index: CSC is not the transpose of CSR");
+    }
+  for (const int32_t* ord : {ix->q_order, ix->k_order}) {
+    std::vector<char> seen(size_t(nb), 0);
+    for (int64_t b = 0; b < nb; ++b) {
+      if (ord[b] < 0 || ord[b] >= nb || seen[size_t(ord[b])])
+        return set_error(FLASH_MSA_ERR_INDEX, "index: order array is not a permutation");
+      seen[size_t(ord[b])] = 1;
+    }
+  }
+  return FLASH_MSA_OK;
+}
+
+flash_msa_status flash_msa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                               int B, int H, int64_t N, int d, float scale,
+                               const flash_msa_mask_desc* mask, void* stream) {
+  g_last_error[0] = 0;
+  flash_msa_status st = check_dims(B, H, N, d);
+  if (st != FLASH_MSA_OK) return st;
+  if (!q || !k || !v || !o || !lse)
+    return set_error(FLASH_MSA_ERR_INVALID_ARG, "fwd: null tensor pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return set_error(FLASH_MSA_ERR_INVALID_ARG, "fwd: tensors must be 16-byte aligned");
+  FwdLaunch a;
+  memset(&a, 0, sizeof(a));
+  bool need = false;
+  if ((st = check_mask(mask, a.mask, need)) != FLASH_MSA_OK) return st;
+  ListParams unused;
+  if ((st = make_lists(mask, N, need, false, a.list, unused)) != FLASH_MSA_OK) return st;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.B = B;
+  a.H = H;
+  a.d = d;
+  a.N = N;
+  a.scale = resolve_scale(scale, d);
+  a.status = status_word_ptr();
+  if (!a.status) return set_cuda_error("status word");
+  return launch_fwd(a, static_cast<cudaStream_t>(stream));
+}
+
+size_t flash_msa_bwd_workspace_bytes(int B, int H, int64_t N, int d) {
+  (void)d;
+  if (B < 1 || H < 1 || N < 1 || N > kMaxN) return 0;
+  // two fp32 vectors per (b, h) padded to whole 128-row tiles: LSE * log2(e) and D
+  const size_t padded = size_t(n_blocks_of(N)) * kTile;
+  const size_t bytes = 2 * size_t(B) * size_t(H) * padded * sizeof(float);
+  return (bytes + 255) & ~size_t(255);
+}
+
+flash_msa_status flash_msa_bwd(const void* q, const void* k, const void* v, const void* o,
+                               const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                               int B, int H, int64_t N, int d, float scale,
+                               const flash_msa_mask_desc* mask, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  return flash_msa_bwd_stages(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, mask,
+                              workspace, workspace_bytes,
+                              FLASH_MSA_BWD_PREPROCESS | FLASH_MSA_BWD_DKDV | FLASH_MSA_BWD_DQ,
+                              stream);
+}
+
+flash_msa_status flash_msa_bwd_stages(const void* q, const void* k, const void* v, const void* o,
+                                      const float* lse, const void* dO, void* dq, void* dk,
+                                      void* dv, int B, int H, int64_t N, int d, float scale,
+                                      const flash_msa_mask_desc* mask, void* workspace,
+                                      size_t workspace_bytes, unsigned stages, void* stream) {
+  g_last_error[0] = 0;
+  if (stages == 0 || (stages & ~7u))
+    return set_error(FLASH_MSA_ERR_INVALID_ARG, "bwd: stages must be a non-empty subset of 1|2|4");
+  flash_msa_status st = check_dims(B, H, N, d);
+  if (st != FLASH_MSA_OK) return st;
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv)
+    return set_error(FLASH_MSA_ERR_INVALID_ARG, "bwd: null tensor pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return set_error(FLASH_MSA_ERR_INVALID_ARG, "bwd: tensors must be 16-byte aligned");
+  const size_t need_ws = flash_msa_bwd_workspace_bytes(B, H, N, d);
+  if (!workspace || workspace_bytes < need_ws || !aligned16(workspace))
+    return set_error(FLASH_MSA_ERR_WORKSPACE, "bwd: workspace of %zu bytes required (got %zu)",
+                     need_ws, workspace_bytes);
+  BwdLaunch a;
+  memset(&a, 0, sizeof(a));
+  bool need = false;
+  if ((st = check_mask(mask, a.mask, need)) != FLASH_MSA_OK) return st;
+  if ((st = make_lists(mask, N, need, true, a.rows, a.cols)) != FLASH_MSA_OK) return st;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.dout = dO;
+  a.lse = lse;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.dsum = static_cast<float*>(workspace);
+  a.B = B;
+  a.H = H;
+  a.d = d;
+  a.N = N;
+  a.scale = resolve_scale(scale, d);
+  a.status = status_word_ptr();
+  a.stages = stages;
+  if (!a.status) return set_cuda_error("status word");
+  return launch_bwd(a, static_cast<cudaStream_t>(stream));
+}
+
+flash_msa_status flash_msa_get_status(void* stream) {
+  g_last_error[0] = 0;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return set_cuda_error("get_status: stream synchronize");
+  unsigned* ptr = status_word_ptr();
+  if (!ptr) return set_cuda_error("get_status: status word");
+  unsigned word = 0;
+  if (cudaMemcpy(&word, ptr, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return set_cuda_error("get_status: read");
+  if (word == 0) return FLASH_MSA_OK;
+  const unsigned zero = 0;
+  if (cudaMemcpy(ptr, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+    return set_cuda_error("get_status: clear");
+  const unsigned code = word & 0xFFu;
+  return set_error(static_cast<flash_msa_status>(code),
+                   "device status %u (site %u, block %u)", code, (word >> 8) & 0xFFu, word >> 16);
+}
+
+}  // extern "C"

@@ -1,0 +1,259 @@
+// Device-side pieces shared by the attention kernels: mask evaluation per
+// tile and per row, bounded mbarrier waits with an abort path, and decoding
+// of work units and their key-tile (or query-tile) lists.
+#pragma once
+#include <cstdint>
+
+#include "flashmsa.h"
+#include "ptx.cuh"
+
+namespace fmsa {
+
+constexpr int kTile = 128;                 // query / key tile edge (tokens)
+constexpr uint64_t kWaitLimitNs = 500ull * 1000ull * 1000ull;  // any single wait: 0.5 s
+constexpr uint64_t kDrainLimitNs = 50ull * 1000ull * 1000ull;  // draining copies after an abort
+constexpr int64_t kUnbounded = int64_t(1) << 40;
+
+// Mask fields in kernel-friendly form (window clamped, absent fields neutral).
+struct MaskParams {
+  uint32_t flags;
+  int32_t dilation, near;
+  int32_t stride, phase;
+  int64_t window;
+};
+
+// ---------------------------------------------------------------------------
+// Mask semantics (see flashmsa.h).  With a 128-token pattern block equal to
+// the 128-token tile, the dilation and stride parts are constant over a tile,
+// and the causal / window parts depend only on delta = i - j.  So over one
+// tile the live entries are exactly those whose delta lies in one interval
+// [dlo, dhi] (or none at all).
+// ---------------------------------------------------------------------------
+struct DeltaRange {
+  bool none;  // no entry of the tile can be live
+  int64_t lo, hi;
+};
+
+__host__ __device__ inline DeltaRange tile_delta_range(int qb, int kb, const MaskParams& m) {
+  DeltaRange r{false, -kUnbounded, kUnbounded};
+  const uint32_t pat = m.flags & (FLASH_MSA_WINDOW | FLASH_MSA_DILATED | FLASH_MSA_STRIDED);
+  bool window_applies = false;
+  if (pat) {
+    const bool strided_ok = (m.flags & FLASH_MSA_STRIDED) && (kb % m.stride == m.phase);
+    if (!strided_ok) {
+      if (!(m.flags & (FLASH_MSA_WINDOW | FLASH_MSA_DILATED))) {
+        r.none = true;
+        return r;
+      }
+      if (m.flags & FLASH_MSA_DILATED) {
+        const int dd = qb > kb ? qb - kb : kb - qb;
+        if (!(dd < m.near || dd % m.dilation == 0)) {
+          r.none = true;
+          return r;
+        }
+      }
+      window_applies = (m.flags & FLASH_MSA_WINDOW) != 0;
+    }
+  }
+  if (m.flags & FLASH_MSA_CAUSAL) r.lo = 0;
+  if (window_applies) {
+    r.lo = r.lo > -m.window ? r.lo : -m.window;
+    r.hi = m.window;
+  }
+  return r;
+}
+
+// Tile classification: 0 full, 1 partial, -1 dead.  Rows / columns at or past
+// n are dead entries, so a tile that crosses n is never full.
+__host__ __device__ inline int classify_tile(int qb, int kb, int64_t n, const MaskParams& m) {
+  const DeltaRange r = tile_delta_range(qb, kb, m);
+  if (r.none) return -1;
+  const int64_t i0 = int64_t(qb) * kTile, j0 = int64_t(kb) * kTile;
+  const int64_t i1 = (i0 + kTile < n ? i0 + kTile : n) - 1;
+  const int64_t j1 = (j0 + kTile < n ? j0 + kTile : n) - 1;
+  if (i1 < i0 || j1 < j0) return -1;
+  const int64_t dmin = i0 - j1, dmax = i1 - j0;
+  if (dmax < r.lo || dmin > r.hi) return -1;
+  const bool clipped = (i1 - i0 + 1 < kTile) || (j1 - j0 + 1 < kTile);
+  if (!clipped && dmin >= r.lo && dmax <= r.hi) return 0;
+  return 1;
+}
+
+// Live tile-local key columns [lo, hi] of query row i in the key tile kb.
+__device__ __forceinline__ void row_live_range(int64_t i, int qb, int kb, int64_t n,
+                                               const MaskParams& m, int& lo, int& hi) {
+  const DeltaRange r = tile_delta_range(qb, kb, m);
+  const int64_t j0 = int64_t(kb) * kTile;
+  if (r.none || i >= n) {
+    lo = 0;
+    hi = -1;
+    return;
+  }
+  int64_t clo = i - r.hi - j0;                      // j >= i - hi
+  int64_t chi = i - r.lo - j0;                      // j <= i - lo
+  const int64_t last = (n - 1 - j0) < (kTile - 1) ? (n - 1 - j0) : (kTile - 1);
+  if (clo < 0) clo = 0;
+  if (chi > last) chi = last;
+  if (chi < -1) chi = -1;
+  if (clo > kTile) clo = kTile;
+  lo = int(clo);
+  hi = int(chi);
+}
+
+// Query-side version for the key-stationary backward: live tile-local query
+// rows [lo, hi] of key column j in the query tile qb.
+__device__ __forceinline__ void col_live_range(int64_t j, int qb, int kb, int64_t n,
+                                               const MaskParams& m, int& lo, int& hi) {
+  const DeltaRange r = tile_delta_range(qb, kb, m);
+  const int64_t i0 = int64_t(qb) * kTile;
+  if (r.none || j >= n) {
+    lo = 0;
+    hi = -1;
+    return;
+  }
+  int64_t rlo = j + r.lo - i0;                      // i >= j + lo
+  int64_t rhi = j + r.hi - i0;                      // i <= j + hi
+  const int64_t last = (n - 1 - i0) < (kTile - 1) ? (n - 1 - i0) : (kTile - 1);
+  if (rlo < 0) rlo = 0;
+  if (rhi > last) rhi = last;
+  if (rhi < -1) rhi = -1;
+  if (rlo > kTile) rlo = kTile;
+  lo = int(rlo);
+  hi = int(rhi);
+}
+
+// ---------------------------------------------------------------------------
+// Status word and bounded waits
+// ---------------------------------------------------------------------------
+// Status encoding: bits 0..7 = flash_msa_status code, bits 8..15 = where
+// (kernel-specific wait site), bits 16..31 = block index (low 16 bits).
+__device__ __forceinline__ void record_status(unsigned* status, unsigned code, unsigned where) {
+  const unsigned word = code | ((where & 0xFFu) << 8) | ((blockIdx.x & 0xFFFFu) << 16);
+  atomicCAS(status, 0u, word);
+}
+
+// Wait for the phase with the given parity; gives up (returns false) when the
+// CTA-wide abort flag is raised or after kWaitLimitNs, raising the flag and
+// recording FLASH_MSA_ERR_TIMEOUT.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         unsigned* status, unsigned where) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int k = 0; k < 16; ++k)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      record_status(status, FLASH_MSA_ERR_TIMEOUT, where);
+      return false;
+    }
+  }
+}
+
+// Used only on the abort path: wait for copies already in flight, ignoring
+// the abort flag, with a short limit.
+__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > kDrainLimitNs) return;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Work units and tile lists
+// ---------------------------------------------------------------------------
+// A list of blocks for one outer block (key tiles of a query block in the
+// forward / dQ pass, query tiles of a key block in the dK/dV pass).  With an
+// index it is a CSR (or CSC) row; without one it is derived arithmetically
+// for dense or causal masks.
+struct ListParams {
+  const int32_t* ptr;    // row_ptr / col_ptr (null: arithmetic mode)
+  const int32_t* idx;    // col_idx / row_idx
+  const uint8_t* kind;   // kind / kind_t
+  const int32_t* order;  // q_order / k_order
+  int64_t nnz;
+  int n_blocks;          // blocks along both axes (square tiling)
+  int causal;            // arithmetic mode: causal mask
+  int tail;              // N % 128 != 0
+  int transposed;        // 0: outer = query block (CSR); 1: outer = key block (CSC)
+};
+
+struct Unit {
+  int b, h, ob;  // batch, head, outer block
+  int begin, n;  // position in idx[] and number of inner blocks
+};
+
+__device__ __forceinline__ Unit decode_unit(int u, int H, const ListParams& L, unsigned* status) {
+  Unit un;
+  const int bh = u / L.n_blocks;
+  const int rank = u - bh * L.n_blocks;
+  un.b = bh / H;
+  un.h = bh - un.b * H;
+  if (L.order) {
+    int ob = __ldg(L.order + rank);
+    if (ob < 0 || ob >= L.n_blocks) {
+      record_status(status, FLASH_MSA_ERR_INDEX, 0xF0);
+      ob = rank;
+    }
+    un.ob = ob;
+  } else {
+    // arithmetic order, longest list first: causal query blocks descend, key blocks ascend
+    un.ob = (L.causal && !L.transposed) ? (L.n_blocks - 1 - rank) : rank;
+  }
+  if (L.ptr) {
+    const int a = __ldg(L.ptr + un.ob), e = __ldg(L.ptr + un.ob + 1);
+    if (a < 0 || e < a || int64_t(e) > L.nnz) {
+      record_status(status, FLASH_MSA_ERR_INDEX, 0xF1);
+      un.begin = 0;
+      un.n = 0;
+    } else {
+      un.begin = a;
+      un.n = e - a;
+    }
+  } else if (L.causal) {
+    un.begin = 0;
+    un.n = L.transposed ? (L.n_blocks - un.ob) : (un.ob + 1);
+  } else {
+    un.begin = 0;
+    un.n = L.n_blocks;
+  }
+  return un;
+}
+
+// Inner block t of a unit: block id, whether the element mask must be
+// evaluated (partial), and whether the entry was unusable (dead: every entry
+// masked; reported as FLASH_MSA_ERR_INDEX, block id replaced by 0).
+struct InnerTile {
+  int blk;
+  bool partial;
+  bool dead;
+};
+
+__device__ __forceinline__ InnerTile inner_tile(const Unit& un, int t, const ListParams& L,
+                                                unsigned* status) {
+  InnerTile it;
+  it.dead = false;
+  if (L.ptr) {
+    it.blk = __ldg(L.idx + un.begin + t);
+    it.partial = __ldg(L.kind + un.begin + t) != 0;
+    if (it.blk < 0 || it.blk >= L.n_blocks) {
+      record_status(status, FLASH_MSA_ERR_INDEX, 0xF2);
+      it.blk = 0;
+      it.dead = true;
+    }
+  } else {
+    it.blk = L.transposed ? (L.causal ? un.ob + t : t) : t;
+    const int last = L.n_blocks - 1;
+    it.partial = (L.causal && it.blk == un.ob) ||
+                 (L.tail && (it.blk == last || un.ob == last));
+  }
+  return it;
+}
+
+__device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+}  // namespace fmsa

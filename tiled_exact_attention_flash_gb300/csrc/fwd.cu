@@ -1,0 +1,474 @@
+// Forward attention kernel for sm_103a: O = softmax(mask(Q K^T * scale)) V
+// and LSE, one 128-row query tile per work unit, tile by tile over the unit's
+// live key tiles with an online softmax ("Flash MSA Attention Kernel
+// Implementation", sections "The Flash Core: Tiling Over the Memory
+// Hierarchy" and "Optimization Tricks That Actually Matter"; sparse lists
+// from "How Does Flash-MSA Sparse Attention Work", section "How Flash-MSA
+// Sparse Attention Works").
+//
+// CTA layout (384 threads, one CTA per SM):
+//   warp 0      TMA producer: Q tiles and the K/V ring, one elected lane
+//   warp 1      MMA issuer: tcgen05.mma for S = Q K^T and O += P V, one lane
+//   warp 2      TMEM allocator
+//   warps 4-7   softmax + epilogue for query slot 0 (thread = query row)
+//   warps 8-11  softmax + epilogue for query slot 1
+// Two independent query slots per CTA keep the tensor core busy with one
+// slot's MMAs while the other slot's softmax runs.  TMEM (512 columns):
+//   slot s: S at columns [256 s, 256 s + 128), P (bf16, two per column)
+//   aliased onto the first 64 of them, O at [256 s + 128, 256 s + 128 + d).
+// Shared memory: one Q tile per slot, a ring of K/V tiles, all 128-byte
+// swizzled by TMA and read by the tensor core through matrix descriptors.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace fmsa {
+
+struct FwdParams {
+  CUtensorMap tm_q, tm_k, tm_v;
+  __nv_bfloat16* o;
+  float* lse;
+  int B, H, N;
+  int n_units;
+  float scale_log2;  // scale * log2(e)
+  MaskParams mask;
+  ListParams list;
+  unsigned* status;
+};
+
+template <int HD>
+struct FwdLayout {
+  static constexpr int kTileBytes = kTile * HD * 2;
+  static constexpr int kStages = HD == 128 ? 4 : 8;
+  static constexpr int kQOff = 0;
+  static constexpr int kRingOff = 2 * kTileBytes;
+  static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
+  // barrier slots
+  static constexpr int kQFull = 0, kQEmpty = 2, kSFull = 4, kPFull = 6, kOFull = 8, kOEmpty = 10,
+                       kMmaDone = 12, kKvFull = 13, kKvEmpty = 13 + kStages;
+  static constexpr int kNumBars = 13 + 2 * kStages;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack for 1024-byte alignment
+};
+
+constexpr int kFwdThreads = 384;
+constexpr uint32_t kNegInfBits = 0xFF800000u;
+
+// Per-slot progress through the sequence of units of one CTA.  Unit k of
+// slot s is u = 2 * (blockIdx.x + k * gridDim.x) + s.  Units without any live
+// tile are skipped by the producer and the MMA issuer.
+struct SlotRun {
+  int k;
+  int t;
+  bool active;
+  Unit un;
+};
+
+__device__ __forceinline__ bool next_nonempty_unit(SlotRun& r, int slot, const FwdParams& p) {
+  while (true) {
+    const int u = 2 * (int(blockIdx.x) + r.k * int(gridDim.x)) + slot;
+    if (u >= p.n_units) return false;
+    ++r.k;
+    r.un = decode_unit(u, p.H, p.list, p.status);
+    if (r.un.n > 0) {
+      r.t = 0;
+      return true;
+    }
+  }
+}
+
+template <int HD>
+__device__ __forceinline__ void fwd_producer(const FwdParams& p, uint8_t* smem, uint64_t* bars,
+                                             volatile int* abort_flag) {
+  using L = FwdLayout<HD>;
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+  SlotRun st[2];
+  for (int s = 0; s < 2; ++s) {
+    st[s].k = 0;
+    st[s].active = next_nonempty_unit(st[s], s, p);
+  }
+  uint32_t kv_cnt = 0, qe_cnt[2] = {0, 0};
+  int last_kv[L::kStages];
+  for (int i = 0; i < L::kStages; ++i) last_kv[i] = -1;
+  int last_q[2] = {-1, -1};
+  bool ok = true;
+  auto load_tile = [&](const CUtensorMap* m, uint32_t dst, uint32_t b, int row, const Unit& un) {
+#pragma unroll
+    for (int c = 0; c < HD / 64; ++c)
+      tma_load_4d(dst + c * (kTile * 128), m, b, c * 64, row, un.h, un.b);
+  };
+  while (ok && (st[0].active || st[1].active)) {
+    for (int s = 0; s < 2 && ok; ++s) {
+      SlotRun& r = st[s];
+      if (!r.active) continue;
+      if (r.t > 0) {  // V of tile t-1
+        const int stage = kv_cnt % L::kStages;
+        if (!wait_bar(bar(L::kKvEmpty + stage), ((kv_cnt / L::kStages) & 1) ^ 1, abort_flag,
+                      p.status, 1)) {
+          ok = false;
+          break;
+        }
+        const InnerTile it = inner_tile(r.un, r.t - 1, p.list, p.status);
+        mbar_arrive_expect_tx(bar(L::kKvFull + stage), L::kTileBytes);
+        load_tile(&p.tm_v, smem_u32(smem + L::kRingOff + stage * L::kTileBytes),
+                  bar(L::kKvFull + stage), it.blk * kTile, r.un);
+        last_kv[stage] = int(kv_cnt);
+        ++kv_cnt;
+        if (r.t == r.un.n) {
+          r.active = next_nonempty_unit(r, s, p);
+          continue;
+        }
+      }
+      if (r.t == 0) {  // Q tile of a new unit
+        if (!wait_bar(bar(L::kQEmpty + s), (qe_cnt[s] & 1) ^ 1, abort_flag, p.status, 2)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(bar(L::kQFull + s), L::kTileBytes);
+        load_tile(&p.tm_q, smem_u32(smem + L::kQOff + s * L::kTileBytes), bar(L::kQFull + s),
+                  r.un.ob * kTile, r.un);
+        last_q[s] = int(qe_cnt[s]);
+        ++qe_cnt[s];
+      }
+      {  // K of tile t
+        const int stage = kv_cnt % L::kStages;
+        if (!wait_bar(bar(L::kKvEmpty + stage), ((kv_cnt / L::kStages) & 1) ^ 1, abort_flag,
+                      p.status, 3)) {
+          ok = false;
+          break;
+        }
+        const InnerTile it = inner_tile(r.un, r.t, p.list, p.status);
+        mbar_arrive_expect_tx(bar(L::kKvFull + stage), L::kTileBytes);
+        load_tile(&p.tm_k, smem_u32(smem + L::kRingOff + stage * L::kTileBytes),
+                  bar(L::kKvFull + stage), it.blk * kTile, r.un);
+        last_kv[stage] = int(kv_cnt);
+        ++kv_cnt;
+      }
+      ++r.t;
+    }
+  }
+  if (!ok) {  // let copies already issued land before the CTA exits
+    for (int i = 0; i < L::kStages; ++i)
+      if (last_kv[i] >= 0) drain_bar(bar(L::kKvFull + i), (last_kv[i] / L::kStages) & 1);
+    for (int s = 0; s < 2; ++s)
+      if (last_q[s] >= 0) drain_bar(bar(L::kQFull + s), last_q[s] & 1);
+  }
+}
+
+template <int HD>
+__device__ __forceinline__ void fwd_mma(const FwdParams& p, uint8_t* smem, uint64_t* bars,
+                                        uint32_t tmem, volatile int* abort_flag) {
+  using L = FwdLayout<HD>;
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+  constexpr uint32_t kIdQK = idesc_bf16_f32(128, 128, false, false);
+  constexpr uint32_t kIdPV = idesc_bf16_f32(128, HD, false, true);
+  SlotRun st[2];
+  for (int s = 0; s < 2; ++s) {
+    st[s].k = 0;
+    st[s].active = next_nonempty_unit(st[s], s, p);
+  }
+  uint32_t kv_cnt = 0, qf_cnt[2] = {0, 0}, pf_cnt[2] = {0, 0}, oe_cnt[2] = {0, 0};
+  const uint32_t ring = smem_u32(smem + L::kRingOff);
+  bool ok = true;
+  while (ok && (st[0].active || st[1].active)) {
+    for (int s = 0; s < 2 && ok; ++s) {
+      SlotRun& r = st[s];
+      if (!r.active) continue;
+      const uint32_t tS = tmem + uint32_t(s * 256);
+      const uint32_t tO = tS + 128;
+      if (r.t > 0) {  // O (+)= P(t-1) V(t-1)
+        if (!wait_bar(bar(L::kPFull + s), pf_cnt[s] & 1, abort_flag, p.status, 10)) {
+          ok = false;
+          break;
+        }
+        ++pf_cnt[s];
+        if (r.t == 1) {
+          if (!wait_bar(bar(L::kOEmpty + s), (oe_cnt[s] & 1) ^ 1, abort_flag, p.status, 11)) {
+            ok = false;
+            break;
+          }
+          ++oe_cnt[s];
+        }
+        const int stage = kv_cnt % L::kStages;
+        if (!wait_bar(bar(L::kKvFull + stage), (kv_cnt / L::kStages) & 1, abort_flag, p.status,
+                      12)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t vb = ring + stage * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          // B = V tile, MN-major: 64-column chunks 16 KB apart, 8-row groups 1 KB apart
+          const uint64_t bd = sdesc_sw128(vb + kk * 2048, kTile * 128, 1024);
+          mma_ts(tO, tS + kk * 8, bd, kIdPV, (r.t > 1 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(L::kKvEmpty + stage));
+        ++kv_cnt;
+        if (r.t == r.un.n) {
+          mma_commit(bar(L::kOFull + s));
+          r.active = next_nonempty_unit(r, s, p);
+          continue;
+        }
+      }
+      if (r.t == 0) {
+        if (!wait_bar(bar(L::kQFull + s), qf_cnt[s] & 1, abort_flag, p.status, 13)) {
+          ok = false;
+          break;
+        }
+        ++qf_cnt[s];
+      }
+      const int stage = kv_cnt % L::kStages;
+      if (!wait_bar(bar(L::kKvFull + stage), (kv_cnt / L::kStages) & 1, abort_flag, p.status,
+                    14)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t qb = smem_u32(smem + L::kQOff + s * L::kTileBytes);
+      const uint32_t kb = ring + stage * L::kTileBytes;
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk) {
+        // A = Q, B = K, both K-major: 16-element k-steps are 32 bytes apart
+        // inside a 128-byte swizzle row, 64-element chunks 16 KB apart
+        const uint32_t off = (kk / 4) * (kTile * 128) + (kk % 4) * 32;
+        mma_ss(tS, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), kIdQK,
+               kk > 0 ? 1u : 0u);
+      }
+      mma_commit(bar(L::kSFull + s));
+      mma_commit(bar(L::kKvEmpty + stage));
+      ++kv_cnt;
+      if (r.t == r.un.n - 1) mma_commit(bar(L::kQEmpty + s));
+      ++r.t;
+    }
+  }
+  // every MMA issued so far has finished before TMEM is released
+  mma_commit(bar(L::kMmaDone));
+  drain_bar(bar(L::kMmaDone), 0);
+}
+
+template <int HD>
+__device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint64_t* bars, uint32_t tmem,
+                                            int slot, volatile int* abort_flag) {
+  using L = FwdLayout<HD>;
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+  const int wq = int(warp_id()) & 3;
+  const int row = wq * 32 + int(lane_id());
+  const uint32_t lane_off = uint32_t(wq * 32) << 16;
+  const uint32_t tS = tmem + lane_off + uint32_t(slot * 256);
+  const uint32_t tO = tS + 128;
+  const float sl2 = p.scale_log2;
+  uint32_t sf_cnt = 0, of_cnt = 0;
+  for (int k = 0;; ++k) {
+    const int u = 2 * (int(blockIdx.x) + k * int(gridDim.x)) + slot;
+    if (u >= p.n_units) break;
+    const Unit un = decode_unit(u, p.H, p.list, p.status);
+    const int64_t i = int64_t(un.ob) * kTile + row;
+    float m_run = -INFINITY, l_run = 0.f;
+    for (int t = 0; t < un.n; ++t) {
+      const InnerTile it = inner_tile(un, t, p.list, p.status);
+      int lo = 0, hi = kTile - 1;
+      if (it.dead) {
+        hi = -1;
+      } else if (it.partial) {
+        row_live_range(i, un.ob, it.blk, p.N, p.mask, lo, hi);
+      }
+      const bool ok = wait_bar(bar(L::kSFull + slot), sf_cnt & 1, abort_flag, p.status, 20);
+      if (!__all_sync(0xFFFFFFFFu, ok)) return;  // tcgen05.ld below needs the whole warp
+      ++sf_cnt;
+      tc_fence_after();
+      uint32_t sr[128];
+      {
+        uint32_t* h0 = sr;
+        uint32_t* h1 = sr + 64;
+        tmem_ld_x64(tS, *reinterpret_cast<uint32_t(*)[64]>(h0));
+        tmem_ld_x64(tS + 64, *reinterpret_cast<uint32_t(*)[64]>(h1));
+      }
+      if (it.partial || it.dead) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c < lo || c > hi) sr[c] = kNegInfBits;
+      }
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 128; c += 4) {
+        mx0 = fmaxf(mx0, __uint_as_float(sr[c]));
+        mx1 = fmaxf(mx1, __uint_as_float(sr[c + 1]));
+        mx2 = fmaxf(mx2, __uint_as_float(sr[c + 2]));
+        mx3 = fmaxf(mx3, __uint_as_float(sr[c + 3]));
+      }
+      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+      const float m_new = fmaxf(m_run, mx * sl2);
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = ex2_approx(m_run - m_use);
+      float sum0 = 0.f, sum1 = 0.f;
+      uint32_t pk[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), sl2, -m_use));
+        const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), sl2, -m_use));
+        sum0 += p0;
+        sum1 += p1;
+        pk[c] = pack_bf16x2(p0, p1);
+      }
+      tmem_st_x32(tS, *reinterpret_cast<uint32_t(*)[32]>(pk));
+      tmem_st_x32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
+      l_run = l_run * alpha + (sum0 + sum1);
+      if (t > 0 && __any_sync(0xFFFFFFFFu, alpha < 1.f)) {
+        // the previous P V has completed: it was issued before this tile's Q K^T
+#pragma unroll
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld_x32(tO + c * 32, o);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+          tmem_st_x32(tO + c * 32, o);
+        }
+      }
+      m_run = m_new;
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(L::kPFull + slot));
+    }
+    // epilogue: O / l -> bf16, LSE = ln 2 * (m + log2 l)
+    if (un.n > 0) {
+      const bool ok = wait_bar(bar(L::kOFull + slot), of_cnt & 1, abort_flag, p.status, 21);
+      if (!__all_sync(0xFFFFFFFFu, ok)) return;
+      ++of_cnt;
+      tc_fence_after();
+    }
+    const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+    __nv_bfloat16* orow =
+        p.o + ((int64_t(un.b) * p.N + i) * p.H + un.h) * int64_t(HD);
+#pragma unroll
+    for (int c = 0; c < HD / 32; ++c) {
+      uint32_t o[32];
+      if (un.n > 0) {
+        tmem_ld_x32(tO + c * 32, o);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) o[j] = 0u;
+      }
+      uint32_t w[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        w[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv_l, __uint_as_float(o[2 * j + 1]) * inv_l);
+      if (i < p.N) {
+        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+      }
+    }
+    if (un.n > 0) {
+      tc_fence_before();
+      mbar_arrive(bar(L::kOEmpty + slot));
+    }
+    if (i < p.N) {
+      p.lse[(int64_t(un.b) * p.H + un.h) * p.N + i] =
+          l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+    }
+  }
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_constant__ FwdParams p) {
+  using L = FwdLayout<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align_1024(smem_raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+  const int warp = int(warp_id());
+  const int lane = int(lane_id());
+
+  if (warp == 2) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(bars + L::kQFull + s), 1);
+      mbar_init(smem_u32(bars + L::kQEmpty + s), 1);
+      mbar_init(smem_u32(bars + L::kSFull + s), 1);
+      mbar_init(smem_u32(bars + L::kPFull + s), 128);
+      mbar_init(smem_u32(bars + L::kOFull + s), 1);
+      mbar_init(smem_u32(bars + L::kOEmpty + s), 128);
+    }
+    mbar_init(smem_u32(bars + L::kMmaDone), 1);
+    for (int i = 0; i < L::kStages; ++i) {
+      mbar_init(smem_u32(bars + L::kKvFull + i), 1);
+      mbar_init(smem_u32(bars + L::kKvEmpty + i), 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tm_q);
+    tma_prefetch_desc(&p.tm_k);
+    tma_prefetch_desc(&p.tm_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) fwd_producer<HD>(p, smem, bars, abort_flag);
+  } else if (warp == 1) {
+    if (lane == 0) fwd_mma<HD>(p, smem, bars, tmem, abort_flag);
+  } else if (warp >= 4) {
+    fwd_softmax<HD>(p, bars, tmem, (warp - 4) >> 2, abort_flag);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host launcher
+// ---------------------------------------------------------------------------
+template <int HD>
+static flash_msa_status launch_fwd_hd(const FwdLaunch& a, cudaStream_t stream) {
+  using L = FwdLayout<HD>;
+  FwdParams p;
+  memset(&p, 0, sizeof(p));
+  flash_msa_status st;
+  if ((st = make_tile_map(&p.tm_q, a.q, a.B, a.N, a.H, HD)) != FLASH_MSA_OK) return st;
+  if ((st = make_tile_map(&p.tm_k, a.k, a.B, a.N, a.H, HD)) != FLASH_MSA_OK) return st;
+  if ((st = make_tile_map(&p.tm_v, a.v, a.B, a.N, a.H, HD)) != FLASH_MSA_OK) return st;
+  p.o = reinterpret_cast<__nv_bfloat16*>(a.o);
+  p.lse = a.lse;
+  p.B = a.B;
+  p.H = a.H;
+  p.N = int(a.N);
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.mask = a.mask;
+  p.list = a.list;
+  p.n_units = a.B * a.H * a.list.n_blocks;
+  p.status = a.status;
+  static bool attr_set[2] = {false, false};
+  if (!attr_set[HD == 128]) {
+    if (cudaFuncSetAttribute(fwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L::kSmemBytes) != cudaSuccess)
+      return set_cuda_error("cudaFuncSetAttribute(fwd)");
+    attr_set[HD == 128] = true;
+  }
+  const int pairs = (p.n_units + 1) / 2;
+  int grid = pairs;
+  if (a.max_ctas > 0 && grid > a.max_ctas) grid = a.max_ctas;
+  fwd_kernel<HD><<<grid, kFwdThreads, L::kSmemBytes, stream>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return set_cuda_error("fwd kernel launch");
+  return FLASH_MSA_OK;
+}
+
+flash_msa_status launch_fwd(const FwdLaunch& a, cudaStream_t stream) {
+  if (a.d == 128) return launch_fwd_hd<128>(a, stream);
+  return launch_fwd_hd<64>(a, stream);
+}
+
+}  // namespace fmsa

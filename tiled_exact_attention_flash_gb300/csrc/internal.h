@@ -1,0 +1,56 @@
+// Host-side declarations shared by the library's translation units (not part
+// of the public C ABI, which is include/flashmsa.h).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "common.cuh"
+#include "flashmsa.h"
+
+namespace fmsa {
+
+// error reporting (api.cpp): store a message for flash_msa_last_error_string
+flash_msa_status set_error(flash_msa_status code, const char* fmt, ...);
+flash_msa_status set_cuda_error(const char* what);
+
+// 4-D TMA map over a bf16 (B, N, H, d) tensor: dims (d, N, H, B), box
+// (64, 128, 1, 1), 128-byte swizzle, zero fill past N.  Encoded on the host.
+flash_msa_status make_tile_map(CUtensorMap* m, const void* base, int B, int64_t N, int H, int d);
+
+// device status word (status.cu)
+unsigned* status_word_ptr();  // device address for the current device, or null on error
+
+struct FwdLaunch {
+  const void *q, *k, *v;
+  void* o;
+  float* lse;
+  int B, H, d;
+  int64_t N;
+  float scale;
+  MaskParams mask;
+  ListParams list;  // CSR by query block (or arithmetic)
+  unsigned* status;
+  int max_ctas;     // 0: one CTA per pair of work units
+};
+flash_msa_status launch_fwd(const FwdLaunch& a, cudaStream_t stream);
+
+struct BwdLaunch {
+  const void *q, *k, *v, *o, *dout;
+  const float* lse;
+  void *dq, *dk, *dv;
+  float* dsum;  // workspace: D = rowsum(dO o O), fp32 (B, H, N)
+  int B, H, d;
+  int64_t N;
+  float scale;
+  MaskParams mask;
+  ListParams rows;  // CSR by query block (dQ pass)
+  ListParams cols;  // CSC by key block (dK/dV pass)
+  unsigned* status;
+  unsigned stages;  // FLASH_MSA_BWD_* bits
+};
+flash_msa_status launch_bwd(const BwdLaunch& a, cudaStream_t stream);
+
+}  // namespace fmsa
