@@ -178,6 +178,26 @@ flash_msa_status flash_msa_bwd_stages(const void* q, const void* k, const void* 
                                       const flash_msa_mask_desc* mask, void* workspace,
                                       size_t workspace_bytes, unsigned stages, void* stream);
 
+/* Backward for callers that may not allocate device memory at call time (a
+ * host framework that owns the whole device memory pool, or a latency-bound
+ * loop where cudaMalloc/cudaFree are banned because they can synchronise the
+ * device).  No counterpart on the pages: it exists only because such callers
+ * cannot hand flash_msa_bwd() a workspace.  Same arguments, kernels and
+ * results as flash_msa_bwd() minus the workspace: the scratch is a fixed
+ * 16 MiB array inside the library, held on every device that loads the
+ * library until the process exits.  Limit: B * H * ceil(N/128) * 128 <= 2^21
+ * (flash_msa_bwd_workspace_bytes() <= 16 MiB); larger calls return
+ * FLASH_MSA_ERR_WORKSPACE without launching anything.  Allocates nothing and
+ * calls no allocating routine.  The first call on a device looks the array's
+ * device address up (cudaGetSymbolAddress); make that first call before any
+ * stream capture.  All calls on a device share the array: calls whose kernels
+ * overlap on the GPU (e.g. on unordered streams) race and must be avoided;
+ * sequential calls are fine (each rewrites every scratch element it reads). */
+flash_msa_status flash_msa_bwd_noalloc(const void* q, const void* k, const void* v,
+                                       const void* o, const float* lse, const void* dO, void* dq,
+                                       void* dk, void* dv, int B, int H, int64_t N, int d,
+                                       float scale, const flash_msa_mask_desc* mask, void* stream);
+
 /* Synchronise `stream`, then read and clear the device status word shared by
  * every kernel of this library on the current device.  Returns OK, or the
  * first device-side error recorded since the last call (TIMEOUT, INDEX), or

@@ -32,6 +32,7 @@ SYMBOLS = (
     "flash_msa_bwd_workspace_bytes",
     "flash_msa_bwd",
     "flash_msa_bwd_stages",
+    "flash_msa_bwd_noalloc",
     "flash_msa_get_status",
     "flash_msa_last_error_string",
     "flash_msa_version",
@@ -94,11 +95,14 @@ def lib() -> ctypes.CDLL:
     L.flash_msa_bwd_stages.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i64, i32,
                                        f32, ctypes.POINTER(MaskDescStruct), vp, ctypes.c_size_t,
                                        ctypes.c_uint, vp]
+    L.flash_msa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i64, i32,
+                                        f32, ctypes.POINTER(MaskDescStruct), vp]
     L.flash_msa_get_status.argtypes = [vp]
     L.flash_msa_last_error_string.restype = ctypes.c_char_p
     L.flash_msa_version.restype = ctypes.c_char_p
     for name in ("flash_msa_build_block_index", "flash_msa_check_block_index", "flash_msa_fwd",
-                 "flash_msa_bwd", "flash_msa_bwd_stages", "flash_msa_get_status"):
+                 "flash_msa_bwd", "flash_msa_bwd_stages", "flash_msa_bwd_noalloc",
+                 "flash_msa_get_status"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -303,6 +307,33 @@ def bwd(q, k, v, o, lse, do, mask: Optional[Mask] = None, index: Optional[BlockI
     else:
         code = lib().flash_msa_bwd_stages(*args, stages, _stream_ptr(stream))
     _check(code, "flash_msa_bwd")
+    return dq, dk, dv
+
+
+def bwd_noalloc(q, k, v, o, lse, do, mask: Optional[Mask] = None,
+                index: Optional[BlockIndex] = None, scale: Optional[float] = None,
+                dq=None, dk=None, dv=None, stream=None):
+    """dQ, dK, dV through flash_msa_bwd_noalloc: the library's fixed 16 MiB
+    device scratch replaces the workspace (for callers that may not allocate
+    device memory per call; the outputs here still come from torch unless
+    passed in).  Calls overlapping on the GPU share that scratch and race."""
+    _check_qkv("q", q)
+    B, N, H, d = q.shape
+    for name, t in (("k", k), ("v", v), ("o", o), ("do", do)):
+        _check_qkv(name, t, q.shape)
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (B, H, N):
+        raise ValueError("lse must be contiguous float32 (B, H, N)")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    desc, _keep = _mask_desc(mask, index, N)
+    code = lib().flash_msa_bwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                       lse.data_ptr(), do.data_ptr(), dq.data_ptr(),
+                                       dk.data_ptr(), dv.data_ptr(), B, H, N, d,
+                                       float(scale or 0.0),
+                                       ctypes.byref(desc) if desc is not None else None,
+                                       _stream_ptr(stream))
+    _check(code, "flash_msa_bwd_noalloc")
     return dq, dk, dv
 
 

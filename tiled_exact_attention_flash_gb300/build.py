@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libflashmsa.so")
-SOURCES = ["api.cu", "status.cu", "fwd.cu", "bwd.cu"]
+SOURCES = ["api.cu", "status.cu", "fwd.cu", "bwd.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
