@@ -18,10 +18,11 @@
 // Each tile pair costs 4 + 3 tensor-core products; no atomics, so all three
 // outputs are deterministic.
 //
-// CTA layout of the two main kernels (256 threads, one CTA per SM):
+// CTA layout of the two main kernels (384 threads, one CTA per SM):
 //   warp 0 TMA producer (one lane), warp 1 MMA issuer (one lane), warp 2
-//   TMEM allocator, warps 4-7 elementwise work, thread = row of the
-//   stationary tile (key row in bwd_dkdv, query row in bwd_dq).
+//   TMEM allocator, warps 4-11 elementwise work in two warpgroups: thread =
+//   row of the stationary tile (key row in bwd_dkdv, query row in bwd_dq),
+//   warpgroup g = columns [64 g, 64 g + 64) of the moving tile.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -29,7 +30,8 @@
 
 namespace fmsa {
 
-constexpr int kBwdThreads = 256;
+constexpr int kBwdThreads = 384;
+constexpr int kEwWarps = 8;  // elementwise warps: two warpgroups, 64 columns each
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------------------
@@ -105,9 +107,11 @@ struct BwdLayout {
   static constexpr int kRingOff = 2 * kTileBytes;
   static constexpr int kVecOff = kRingOff + kStages * kTileBytes;  // (stages/2) x 1 KB
   static constexpr int kBarOff = kVecOff + (kStages / 2) * 1024;
-  static constexpr int kFixFull = 0, kFixEmpty = 1, kSFull = 2, kPFull = 3, kAccFull = 4,
-                       kAccEmpty = 5, kMmaDone = 6, kRingFull = 7, kRingEmpty = 7 + kStages;
-  static constexpr int kNumBars = 7 + 2 * kStages;
+  // kSFull / kPFull: two each (dK/dV: one per half-tile buffer; dQ: only [0])
+  static constexpr int kFixFull = 0, kFixEmpty = 1, kSFull = 2, kPFull = 4, kDpFree = 6,
+                       kAccFull = 7, kAccEmpty = 8, kMmaDone = 9, kRingFull = 10,
+                       kRingEmpty = 10 + kStages;
+  static constexpr int kNumBars = 10 + 2 * kStages;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
 };
@@ -134,10 +138,13 @@ __device__ __forceinline__ void init_bwd_barriers(uint64_t* bars) {
   using L = BwdLayout<HD>;
   mbar_init(smem_u32(bars + L::kFixFull), 1);
   mbar_init(smem_u32(bars + L::kFixEmpty), 1);
-  mbar_init(smem_u32(bars + L::kSFull), 1);
-  mbar_init(smem_u32(bars + L::kPFull), 128);
+  for (int i = 0; i < 2; ++i) {
+    mbar_init(smem_u32(bars + L::kSFull + i), 1);
+    mbar_init(smem_u32(bars + L::kPFull + i), kEwWarps);
+  }
+  mbar_init(smem_u32(bars + L::kDpFree), kEwWarps);
   mbar_init(smem_u32(bars + L::kAccFull), 1);
-  mbar_init(smem_u32(bars + L::kAccEmpty), 128);
+  mbar_init(smem_u32(bars + L::kAccEmpty), kEwWarps);
   mbar_init(smem_u32(bars + L::kMmaDone), 1);
   for (int i = 0; i < L::kStages; ++i) {
     mbar_init(smem_u32(bars + L::kRingFull + i), 1);
@@ -213,92 +220,161 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint8_t* smem, 
   }
 }
 
-// MMA issuer shared by both kernels.
-//  dkdv: tS = K Q_t^T, tD = V dO_t^T; then dV (+)= P^T dO_t, dK (+)= dS^T Q_t
-//  dq:   tS = Q K_t^T, tD = dO V_t^T; then dQ (+)= dS K_t
-// TMEM columns: tS [0,128), tD [128,256), acc0 [256, 256+d), acc1 [384, 384+d).
-template <int HD, bool kKeyStationary>
-__device__ __forceinline__ void bwd_mma(const BwdParams& p, uint8_t* smem, uint64_t* bars,
-                                        uint32_t tmem, volatile int* abort_flag) {
+// One arrival per warp, after every lane's TMEM traffic is ordered before it.
+__device__ __forceinline__ void warp_arrive(uint32_t bar) {
+  tc_fence_before();
+  __syncwarp();
+  if (lane_id() == 0) mbar_arrive(bar);
+}
+
+// Common MMA pieces.  K-major operands: 16-element k-steps are 32 bytes
+// apart inside a 128-byte swizzle row, 64-element chunks 16 KB apart.
+// MN-major B operands (rows = the reduction index): 16 rows = 2 KB per
+// k-step, 64-column chunks 16 KB apart.
+template <int HD>
+__device__ __forceinline__ void mma_kmajor(uint32_t d, uint32_t a, uint32_t b, uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < HD / 16; ++kk) {
+    const uint32_t off = (kk / 4) * (kTile * 128) + (kk % 4) * 32;
+    mma_ss(d, sdesc_sw128(a + off, 16, 1024), sdesc_sw128(b + off, 16, 1024), idesc,
+           kk > 0 ? 1u : 0u);
+  }
+}
+
+// D (+)= A[tmem] * B[smem], reduction over 128 rows of B in 8 k-steps of 16.
+// A is the bf16 output of the two elementwise warpgroups: warpgroup g packed
+// its 64 reduction indices (two per column) into columns [64 g, 64 g + 32)
+// of the region at a_tmem, so k-step kk reads 8 columns at
+// a_tmem + 64 (kk / 4) + 8 (kk % 4).
+__device__ __forceinline__ void mma_tmem_a(uint32_t d, uint32_t a_tmem, uint32_t b,
+                                           uint32_t idesc, bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < kTile / 16; ++kk) {
+    const uint64_t bd = sdesc_sw128(b + kk * 2048, kTile * 128, 1024);
+    mma_ts(d, a_tmem + (kk / 4) * 64 + (kk % 4) * 8, bd, idesc, (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+// MMA issuer of bwd_dq (query-stationary; fixed tiles Q, dO; ring K_t, V_t).
+// TMEM: S double-buffered at [0,128) and [128,256), dP at [256,384), dQ at
+// [384, 384+d).  dS_t (bf16) overwrites S_t.  Order per key tile t:
+//   S(t+1), [dP free] dP(t+1) -> s_full, [P full] dQ(t) -> release K_t, V_t
+// so that the products of tile t+1 run while tile t's elementwise work does.
+template <int HD>
+__device__ __forceinline__ void dq_mma(const BwdParams& p, uint8_t* smem, uint64_t* bars,
+                                       uint32_t tmem, volatile int* abort_flag) {
   using L = BwdLayout<HD>;
   auto bar = [&](int i) { return smem_u32(bars + i); };
   constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);
   constexpr uint32_t kIdAcc = idesc_bf16_f32(128, HD, false, true);
-  const uint32_t tS = tmem, tD = tmem + 128, tA0 = tmem + 256, tA1 = tmem + 384;
-  const uint32_t fa = smem_u32(smem + L::kFixOff);
-  const uint32_t fb = fa + L::kTileBytes;
-  uint32_t cnt = 0, ff_cnt = 0, sp_cnt = 0, ae_cnt = 0;
+  const uint32_t tDP = tmem + 256, tDQ = tmem + 384;
+  const uint32_t fq = smem_u32(smem + L::kFixOff);
+  const uint32_t fdo = fq + L::kTileBytes;
+  auto stage_addr = [&](uint32_t c) {
+    return smem_u32(smem + L::kRingOff + (c % L::kStages) * L::kTileBytes);
+  };
+  uint32_t cnt = 0, ff_cnt = 0, pf_cnt = 0, dpf_cnt = 0, ae_cnt = 0;
+  bool ok = true;
+  int k = 0;
+  Unit un;
+  auto ring_wait = [&](uint32_t c, unsigned where) {
+    return wait_bar(bar(L::kRingFull + c % L::kStages), (c / L::kStages) & 1, abort_flag,
+                    p.status, where);
+  };
+  while (ok && next_unit(k, un, p)) {
+    if (!wait_bar(bar(L::kFixFull), ff_cnt & 1, abort_flag, p.status, 10)) break;
+    ++ff_cnt;
+    // tile 0: S and dP
+    if (!ring_wait(cnt, 11) || !ring_wait(cnt + 1, 12)) break;
+    tc_fence_after();
+    mma_kmajor<HD>(tmem, fq, stage_addr(cnt), kIdS);
+    mma_kmajor<HD>(tDP, fdo, stage_addr(cnt + 1), kIdS);
+    mma_commit(bar(L::kSFull));
+    for (int t = 0; t < un.n && ok; ++t) {
+      const uint32_t c = cnt + 2 * t;  // K_t at c, V_t at c + 1
+      if (t + 1 < un.n) {
+        if (!ring_wait(c + 2, 11) || !ring_wait(c + 3, 12)) { ok = false; break; }
+        tc_fence_after();
+        mma_kmajor<HD>(tmem + ((t + 1) & 1) * 128, fq, stage_addr(c + 2), kIdS);
+        if (!wait_bar(bar(L::kDpFree), dpf_cnt & 1, abort_flag, p.status, 15)) { ok = false; break; }
+        ++dpf_cnt;
+        tc_fence_after();
+        mma_kmajor<HD>(tDP, fdo, stage_addr(c + 3), kIdS);
+        mma_commit(bar(L::kSFull));
+      }
+      if (t == 0) {
+        if (!wait_bar(bar(L::kAccEmpty), (ae_cnt & 1) ^ 1, abort_flag, p.status, 13)) { ok = false; break; }
+        ++ae_cnt;
+      }
+      if (!wait_bar(bar(L::kPFull), pf_cnt & 1, abort_flag, p.status, 14)) { ok = false; break; }
+      ++pf_cnt;
+      tc_fence_after();
+      mma_tmem_a(tDQ, tmem + (t & 1) * 128, stage_addr(c), kIdAcc, t > 0);
+      mma_commit(bar(L::kRingEmpty + c % L::kStages));
+      mma_commit(bar(L::kRingEmpty + (c + 1) % L::kStages));
+    }
+    if (!ok) break;
+    // the last tile's dP was loaded by the elementwise side: consume its dp_free
+    if (!wait_bar(bar(L::kDpFree), dpf_cnt & 1, abort_flag, p.status, 15)) break;
+    ++dpf_cnt;
+    cnt += 2 * un.n;
+    mma_commit(bar(L::kFixEmpty));
+    mma_commit(bar(L::kAccFull));
+  }
+  mma_commit(bar(L::kMmaDone));
+  drain_bar(bar(L::kMmaDone), 0);
+}
+
+// MMA issuer of bwd_dkdv (key-stationary; fixed tiles K, V; ring Q_t, dO_t).
+// TMEM: S^T at [0,128), dP^T at [128,256), dV at [256, 256+d), dK at
+// [384, 384+d); P^T and dS^T (bf16) overwrite S^T and dP^T.  Per query tile:
+//   S^T = K Q_t^T, dP^T = V dO_t^T -> s_full; [P full] dV += P^T dO_t,
+//   dK += dS^T Q_t -> release Q_t, dO_t.
+template <int HD>
+__device__ __forceinline__ void dkdv_mma(const BwdParams& p, uint8_t* smem, uint64_t* bars,
+                                         uint32_t tmem, volatile int* abort_flag) {
+  using L = BwdLayout<HD>;
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+  constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);
+  constexpr uint32_t kIdAcc = idesc_bf16_f32(128, HD, false, true);
+  const uint32_t tS = tmem, tD = tmem + 128, tDV = tmem + 256, tDK = tmem + 384;
+  const uint32_t fk = smem_u32(smem + L::kFixOff);
+  const uint32_t fv = fk + L::kTileBytes;
+  auto stage_addr = [&](uint32_t c) {
+    return smem_u32(smem + L::kRingOff + (c % L::kStages) * L::kTileBytes);
+  };
+  auto ring_wait = [&](uint32_t c, unsigned where) {
+    return wait_bar(bar(L::kRingFull + c % L::kStages), (c / L::kStages) & 1, abort_flag,
+                    p.status, where);
+  };
+  uint32_t cnt = 0, ff_cnt = 0, pf_cnt = 0, ae_cnt = 0;
   bool ok = true;
   int k = 0;
   Unit un;
   while (ok && next_unit(k, un, p)) {
-    if (!wait_bar(bar(L::kFixFull), ff_cnt & 1, abort_flag, p.status, 10)) {
-      ok = false;
-      break;
-    }
+    if (!wait_bar(bar(L::kFixFull), ff_cnt & 1, abort_flag, p.status, 10)) break;
     ++ff_cnt;
-    for (int t = 0; t < un.n; ++t) {
-      const int sa = cnt % L::kStages, sb = (cnt + 1) % L::kStages;
-      if (!wait_bar(bar(L::kRingFull + sa), (cnt / L::kStages) & 1, abort_flag, p.status, 11) ||
-          !wait_bar(bar(L::kRingFull + sb), ((cnt + 1) / L::kStages) & 1, abort_flag, p.status,
-                    12)) {
-        ok = false;
-        break;
-      }
+    for (int t = 0; t < un.n && ok; ++t) {
+      const uint32_t c = cnt + 2 * t;  // Q_t at c, dO_t at c + 1
+      if (!ring_wait(c, 11) || !ring_wait(c + 1, 12)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t ra = smem_u32(smem + L::kRingOff + sa * L::kTileBytes);
-      const uint32_t rb = smem_u32(smem + L::kRingOff + sb * L::kTileBytes);
-#pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk) {
-        const uint32_t off = (kk / 4) * (kTile * 128) + (kk % 4) * 32;
-        mma_ss(tS, sdesc_sw128(fa + off, 16, 1024), sdesc_sw128(ra + off, 16, 1024), kIdS,
-               kk > 0 ? 1u : 0u);
-      }
-#pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk) {
-        const uint32_t off = (kk / 4) * (kTile * 128) + (kk % 4) * 32;
-        mma_ss(tD, sdesc_sw128(fb + off, 16, 1024), sdesc_sw128(rb + off, 16, 1024), kIdS,
-               kk > 0 ? 1u : 0u);
-      }
+      mma_kmajor<HD>(tS, fk, stage_addr(c), kIdS);
+      mma_kmajor<HD>(tD, fv, stage_addr(c + 1), kIdS);
       mma_commit(bar(L::kSFull));
       if (t == 0) {
-        if (!wait_bar(bar(L::kAccEmpty), (ae_cnt & 1) ^ 1, abort_flag, p.status, 13)) {
-          ok = false;
-          break;
-        }
+        if (!wait_bar(bar(L::kAccEmpty), (ae_cnt & 1) ^ 1, abort_flag, p.status, 13)) { ok = false; break; }
         ++ae_cnt;
       }
-      if (!wait_bar(bar(L::kPFull), sp_cnt & 1, abort_flag, p.status, 14)) {
-        ok = false;
-        break;
-      }
-      ++sp_cnt;
+      if (!wait_bar(bar(L::kPFull), pf_cnt & 1, abort_flag, p.status, 14)) { ok = false; break; }
+      ++pf_cnt;
       tc_fence_after();
-      if (kKeyStationary) {
-        // dV += P^T dO_t (P^T bf16 in tS), dK += dS^T Q_t (dS^T bf16 in tD)
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint64_t bo = sdesc_sw128(rb + kk * 2048, kTile * 128, 1024);
-          mma_ts(tA0, tS + kk * 8, bo, kIdAcc, (t > 0 || kk > 0) ? 1u : 0u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint64_t bq = sdesc_sw128(ra + kk * 2048, kTile * 128, 1024);
-          mma_ts(tA1, tD + kk * 8, bq, kIdAcc, (t > 0 || kk > 0) ? 1u : 0u);
-        }
-      } else {
-        // dQ += dS K_t (dS bf16 in tS)
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint64_t bk = sdesc_sw128(ra + kk * 2048, kTile * 128, 1024);
-          mma_ts(tA0, tS + kk * 8, bk, kIdAcc, (t > 0 || kk > 0) ? 1u : 0u);
-        }
-      }
-      mma_commit(bar(L::kRingEmpty + sa));
-      mma_commit(bar(L::kRingEmpty + sb));
-      cnt += 2;
+      mma_tmem_a(tDV, tS, stage_addr(c + 1), kIdAcc, t > 0);
+      mma_tmem_a(tDK, tD, stage_addr(c), kIdAcc, t > 0);
+      mma_commit(bar(L::kRingEmpty + c % L::kStages));
+      mma_commit(bar(L::kRingEmpty + (c + 1) % L::kStages));
     }
     if (!ok) break;
+    cnt += 2 * un.n;
     mma_commit(bar(L::kFixEmpty));
     mma_commit(bar(L::kAccFull));
   }
@@ -328,17 +404,22 @@ __device__ __forceinline__ void zero_row(__nv_bfloat16* dst, int hd, bool valid)
   for (int j = 0; j < hd / 8; ++j) d4[j] = make_uint4(0, 0, 0, 0);
 }
 
-// Elementwise warpgroup of bwd_dkdv: thread = key row j of the key tile.
+// Elementwise warpgroups of bwd_dkdv: thread = key row j of the key tile,
+// warpgroup g = query columns [64 g, 64 g + 64) of each query tile:
+// P^T = exp2(scale*log2e * S^T - LSE*log2e) on live entries,
+// dS^T = P^T o (dP^T - D).  The bf16 results go to the start of the
+// warpgroup's own column range (columns it has already read).
 template <int HD>
 __device__ __forceinline__ void dkdv_elementwise(const BwdParams& p, uint8_t* smem,
-                                                 uint64_t* bars, uint32_t tmem,
+                                                 uint64_t* bars, uint32_t tmem, int g,
                                                  volatile int* abort_flag) {
   using L = BwdLayout<HD>;
   auto bar = [&](int i) { return smem_u32(bars + i); };
   const int wq = int(warp_id()) & 3;
   const int row = wq * 32 + int(lane_id());
   const uint32_t lane_off = uint32_t(wq * 32) << 16;
-  const uint32_t tS = tmem + lane_off, tD = tS + 128, tDV = tS + 256, tDK = tS + 384;
+  const uint32_t tS = tmem + lane_off + 64 * g, tD = tS + 128;
+  const uint32_t tDV = tmem + lane_off + 256, tDK = tmem + lane_off + 384;
   const float sl2 = p.scale_log2;
   uint32_t sp_cnt = 0, af_cnt = 0, cnt = 0;
   for (int k = 0;; ++k) {
@@ -350,8 +431,10 @@ __device__ __forceinline__ void dkdv_elementwise(const BwdParams& p, uint8_t* sm
     __nv_bfloat16* dk_row = p.out_a + ((int64_t(un.b) * p.N + j) * p.H + un.h) * HD;
     __nv_bfloat16* dv_row = p.out_b + ((int64_t(un.b) * p.N + j) * p.H + un.h) * HD;
     if (un.n == 0) {
-      zero_row(dk_row, HD, valid);
-      zero_row(dv_row, HD, valid);
+      if (g == 0) {
+        zero_row(dk_row, HD, valid);
+        zero_row(dv_row, HD, valid);
+      }
       continue;
     }
     for (int t = 0; t < un.n; ++t) {
@@ -362,62 +445,61 @@ __device__ __forceinline__ void dkdv_elementwise(const BwdParams& p, uint8_t* sm
       const float* vec =
           reinterpret_cast<const float*>(smem + L::kVecOff + ((cnt % L::kStages) / 2) * 1024);
       cnt += 2;
-      bool ok = wait_bar(bar(L::kSFull), sp_cnt & 1, abort_flag, p.status, 20);
+      const bool ok = wait_bar(bar(L::kSFull), sp_cnt & 1, abort_flag, p.status, 20);
       if (!__all_sync(0xFFFFFFFFu, ok)) return;
       ++sp_cnt;
       tc_fence_after();
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int ch = 0; ch < 2; ++ch) {
         uint32_t s[32], dp[32], pp[16], dd[16];
         tmem_ld_x32(tS + ch * 32, s);
         tmem_ld_x32(tD + ch * 32, dp);
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const int c = ch * 32 + e;
-          const float4 ld = *reinterpret_cast<const float4*>(vec + (c & ~3));
+          const int c = 64 * g + ch * 32 + e;  // query within the 128-query tile
+          const float2 l2 = *reinterpret_cast<const float2*>(vec + c);
           const float2 dv2 = *reinterpret_cast<const float2*>(vec + 128 + c);
-          const float l0 = (c & 2) ? ld.z : ld.x;
-          const float l1 = (c & 2) ? ld.w : ld.y;
-          float p0 = ex2_approx(fmaf(__uint_as_float(s[e]), sl2, -l0));
-          float p1 = ex2_approx(fmaf(__uint_as_float(s[e + 1]), sl2, -l1));
+          float p0 = ex2_approx(fmaf(__uint_as_float(s[e]), sl2, -l2.x));
+          float p1 = ex2_approx(fmaf(__uint_as_float(s[e + 1]), sl2, -l2.y));
           if (c < lo || c > hi) p0 = 0.f;
           if (c + 1 < lo || c + 1 > hi) p1 = 0.f;
-          const float d0 = p0 * (__uint_as_float(dp[e]) - dv2.x);
-          const float d1 = p1 * (__uint_as_float(dp[e + 1]) - dv2.y);
           pp[e / 2] = pack_bf16x2(p0, p1);
-          dd[e / 2] = pack_bf16x2(d0, d1);
+          dd[e / 2] = pack_bf16x2(p0 * (__uint_as_float(dp[e]) - dv2.x),
+                                  p1 * (__uint_as_float(dp[e + 1]) - dv2.y));
         }
         tmem_st_x16(tS + ch * 16, pp);
         tmem_st_x16(tD + ch * 16, dd);
       }
       tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(L::kPFull));
+      warp_arrive(bar(L::kPFull));
     }
-    bool ok = wait_bar(bar(L::kAccFull), af_cnt & 1, abort_flag, p.status, 21);
+    const bool ok = wait_bar(bar(L::kAccFull), af_cnt & 1, abort_flag, p.status, 21);
     if (!__all_sync(0xFFFFFFFFu, ok)) return;
     ++af_cnt;
     tc_fence_after();
+    // warpgroup g writes dV and dK columns [d/2 g, d/2 (g + 1))
 #pragma unroll
-    for (int c = 0; c < HD / 32; ++c) {
+    for (int c = g * (HD / 64); c < (g + 1) * (HD / 64); ++c) {
       store_row_chunk(tDV + c * 32, 1.f, dv_row + c * 32, valid);
       store_row_chunk(tDK + c * 32, p.scale, dk_row + c * 32, valid);
     }
-    tc_fence_before();
-    mbar_arrive(bar(L::kAccEmpty));
+    warp_arrive(bar(L::kAccEmpty));
   }
 }
 
-// Elementwise warpgroup of bwd_dq: thread = query row i of the query tile.
+// Elementwise warpgroups of bwd_dq: thread = query row i of the query tile,
+// warpgroup g = key columns [64 g, 64 g + 64).  dP is pulled into registers
+// first (releasing its TMEM for the next tile's product), then S is processed
+// in 32-column chunks; dS (bf16) goes to the start of the warpgroup's range.
 template <int HD>
 __device__ __forceinline__ void dq_elementwise(const BwdParams& p, uint64_t* bars, uint32_t tmem,
-                                               volatile int* abort_flag) {
+                                               int g, volatile int* abort_flag) {
   using L = BwdLayout<HD>;
   auto bar = [&](int i) { return smem_u32(bars + i); };
   const int wq = int(warp_id()) & 3;
   const int row = wq * 32 + int(lane_id());
   const uint32_t lane_off = uint32_t(wq * 32) << 16;
-  const uint32_t tS = tmem + lane_off, tD = tS + 128, tDQ = tS + 256;
+  const uint32_t tDP = tmem + lane_off + 256 + 64 * g, tDQ = tmem + lane_off + 384;
   const float sl2 = p.scale_log2;
   uint32_t sp_cnt = 0, af_cnt = 0;
   for (int k = 0;; ++k) {
@@ -428,7 +510,7 @@ __device__ __forceinline__ void dq_elementwise(const BwdParams& p, uint64_t* bar
     const bool valid = i < p.N;
     __nv_bfloat16* dq_row = p.out_a + ((int64_t(un.b) * p.N + i) * p.H + un.h) * HD;
     if (un.n == 0) {
-      zero_row(dq_row, HD, valid);
+      if (g == 0) zero_row(dq_row, HD, valid);
       continue;
     }
     const int64_t vrow = (int64_t(un.b) * p.H + un.h) * p.NP + i;
@@ -439,39 +521,41 @@ __device__ __forceinline__ void dq_elementwise(const BwdParams& p, uint64_t* bar
       int lo = 0, hi = kTile - 1;
       if (it.dead) hi = -1;
       else if (it.partial) row_live_range(i, un.ob, it.blk, p.N, p.mask, lo, hi);
-      bool ok = wait_bar(bar(L::kSFull), sp_cnt & 1, abort_flag, p.status, 20);
+      const bool ok = wait_bar(bar(L::kSFull), sp_cnt & 1, abort_flag, p.status, 20);
       if (!__all_sync(0xFFFFFFFFu, ok)) return;
       ++sp_cnt;
       tc_fence_after();
+      uint32_t dpr[64];
+      tmem_ld_x64(tDP, dpr);
+      warp_arrive(bar(L::kDpFree));
+      const uint32_t tS = tmem + lane_off + (t & 1) * 128 + 64 * g;  // same buffer as dq_mma
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t s[32], dp[32], dd[16];
+      for (int ch = 0; ch < 2; ++ch) {
+        uint32_t s[32], dd[16];
         tmem_ld_x32(tS + ch * 32, s);
-        tmem_ld_x32(tD + ch * 32, dp);
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const int c = ch * 32 + e;
+          const int c = 64 * g + ch * 32 + e;
           float p0 = ex2_approx(fmaf(__uint_as_float(s[e]), sl2, -l2));
           float p1 = ex2_approx(fmaf(__uint_as_float(s[e + 1]), sl2, -l2));
           if (c < lo || c > hi) p0 = 0.f;
           if (c + 1 < lo || c + 1 > hi) p1 = 0.f;
-          dd[e / 2] = pack_bf16x2(p0 * (__uint_as_float(dp[e]) - di),
-                                  p1 * (__uint_as_float(dp[e + 1]) - di));
+          dd[e / 2] = pack_bf16x2(p0 * (__uint_as_float(dpr[ch * 32 + e]) - di),
+                                  p1 * (__uint_as_float(dpr[ch * 32 + e + 1]) - di));
         }
-        tmem_st_x16(tS + ch * 16, dd);
+        tmem_st_x16(tS + ch * 16, dd);  // columns already read
       }
       tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(L::kPFull));
+      warp_arrive(bar(L::kPFull));
     }
-    bool ok = wait_bar(bar(L::kAccFull), af_cnt & 1, abort_flag, p.status, 21);
+    const bool ok = wait_bar(bar(L::kAccFull), af_cnt & 1, abort_flag, p.status, 21);
     if (!__all_sync(0xFFFFFFFFu, ok)) return;
     ++af_cnt;
     tc_fence_after();
 #pragma unroll
-    for (int c = 0; c < HD / 32; ++c) store_row_chunk(tDQ + c * 32, p.scale, dq_row + c * 32, valid);
-    tc_fence_before();
-    mbar_arrive(bar(L::kAccEmpty));
+    for (int c = g * (HD / 64); c < (g + 1) * (HD / 64); ++c)
+      store_row_chunk(tDQ + c * 32, p.scale, dq_row + c * 32, valid);
+    warp_arrive(bar(L::kAccEmpty));
   }
 }
 
@@ -506,10 +590,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
   if (warp == 0) {
     if (lane == 0) bwd_producer<HD, kKeyStationary>(p, smem, bars, abort_flag);
   } else if (warp == 1) {
-    if (lane == 0) bwd_mma<HD, kKeyStationary>(p, smem, bars, tmem, abort_flag);
+    if (lane == 0) {
+      if (kKeyStationary) dkdv_mma<HD>(p, smem, bars, tmem, abort_flag);
+      else dq_mma<HD>(p, smem, bars, tmem, abort_flag);
+    }
   } else if (warp >= 4) {
-    if (kKeyStationary) dkdv_elementwise<HD>(p, smem, bars, tmem, abort_flag);
-    else dq_elementwise<HD>(p, bars, tmem, abort_flag);
+    const int g = (warp - 4) >> 2;  // elementwise warpgroup: columns [64 g, 64 g + 64)
+    if (kKeyStationary) dkdv_elementwise<HD>(p, smem, bars, tmem, g, abort_flag);
+    else dq_elementwise<HD>(p, bars, tmem, g, abort_flag);
   }
   tc_fence_before();
   __syncthreads();

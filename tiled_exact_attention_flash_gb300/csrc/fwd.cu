@@ -12,8 +12,9 @@
 //   warp 2      TMEM allocator
 //   warps 4-7   softmax + epilogue for query slot 0 (thread = query row)
 //   warps 8-11  softmax + epilogue for query slot 1
-// Two independent query slots per CTA keep the tensor core busy with one
-// slot's MMAs while the other slot's softmax runs.  TMEM (512 columns):
+// The two query slots hold two neighbouring query blocks of one head and
+// share every key/value tile load; the tensor core works on one slot's
+// products while the other slot's softmax runs.  TMEM (512 columns):
 //   slot s: S at columns [256 s, 256 s + 128), P (bf16, two per column)
 //   aliased onto the first 64 of them, O at [256 s + 128, 256 s + 128 + d).
 // Shared memory: one Q tile per slot, a ring of K/V tiles, all 128-byte
@@ -55,27 +56,92 @@ struct FwdLayout {
 constexpr int kFwdThreads = 384;
 constexpr uint32_t kNegInfBits = 0xFF800000u;
 
-// Per-slot progress through the sequence of units of one CTA.  Unit k of
-// slot s is u = 2 * (blockIdx.x + k * gridDim.x) + s.  Units without any live
-// tile are skipped by the producer and the MMA issuer.
-struct SlotRun {
-  int k;
-  int t;
-  bool active;
-  Unit un;
+// Work unit = a pair of query blocks of one (b, h): ranks 2r and 2r + 1 of
+// the longest-first order (for causal and window masks, two neighbouring
+// blocks whose key-tile lists nearly coincide).  Slot 0 takes rank 2r, slot
+// 1 rank 2r + 1.  The producer loads each key/value tile of the UNION of the
+// two lists once; the MMA issuer runs Q K^T and P V for whichever slots the
+// tile belongs to.  Pair units are spread over the CTAs round-robin:
+// unit k of CTA c is u = c + k * gridDim.x.
+struct PairUnit {
+  int b, h;
+  int q[2];       // query block per slot (q[1] < 0: no second block)
+  int beg[2], n[2];
 };
 
-__device__ __forceinline__ bool next_nonempty_unit(SlotRun& r, int slot, const FwdParams& p) {
-  while (true) {
-    const int u = 2 * (int(blockIdx.x) + r.k * int(gridDim.x)) + slot;
-    if (u >= p.n_units) return false;
-    ++r.k;
-    r.un = decode_unit(u, p.H, p.list, p.status);
-    if (r.un.n > 0) {
-      r.t = 0;
-      return true;
+__device__ __forceinline__ PairUnit decode_pair(int u, const FwdParams& p) {
+  const ListParams& L = p.list;
+  const int npb = (L.n_blocks + 1) >> 1;
+  const int bh = u / npb;
+  const int r = u - bh * npb;
+  PairUnit pu;
+  pu.b = bh / p.H;
+  pu.h = bh - pu.b * p.H;
+  for (int s = 0; s < 2; ++s) {
+    const int rank = 2 * r + s;
+    pu.q[s] = -1;
+    pu.beg[s] = 0;
+    pu.n[s] = 0;
+    if (rank >= L.n_blocks) continue;
+    // reuse the single-unit decoder for the block id and its list bounds
+    const Unit un = decode_unit(bh * L.n_blocks + rank, p.H, L, p.status);
+    pu.q[s] = un.ob;
+    pu.beg[s] = un.begin;
+    pu.n[s] = un.n;
+  }
+  return pu;
+}
+
+// Merged walk over the two slots' key-tile lists (ascending key block).
+struct PairWalk {
+  int pos[2];  // next position in each list (index mode) or next key block (arithmetic)
+  int end[2];
+};
+
+struct PairTile {
+  int kb;
+  bool in[2];
+};
+
+__device__ __forceinline__ void walk_init(PairWalk& w, const PairUnit& pu, const ListParams& L) {
+  for (int s = 0; s < 2; ++s) {
+    if (L.ptr) {
+      w.pos[s] = pu.beg[s];
+      w.end[s] = pu.beg[s] + pu.n[s];
+    } else {
+      w.pos[s] = 0;
+      w.end[s] = pu.n[s];  // arithmetic lists are 0 .. n-1
     }
   }
+}
+
+__device__ __forceinline__ bool walk_next(PairWalk& w, const ListParams& L, PairTile& t) {
+  int k[2];
+  for (int s = 0; s < 2; ++s) {
+    if (w.pos[s] >= w.end[s]) {
+      k[s] = 0x7FFFFFFF;
+    } else if (L.ptr) {
+      k[s] = __ldg(L.idx + w.pos[s]);
+      if (k[s] < 0 || k[s] >= L.n_blocks) k[s] = 0;  // reported by the softmax side
+    } else {
+      k[s] = w.pos[s];
+    }
+  }
+  const int m = k[0] < k[1] ? k[0] : k[1];
+  if (m == 0x7FFFFFFF) return false;
+  t.kb = m;
+  for (int s = 0; s < 2; ++s) {
+    t.in[s] = (k[s] == m);
+    if (t.in[s]) ++w.pos[s];
+  }
+  return true;
+}
+
+template <int HD>
+__device__ __forceinline__ void load_tile(const CUtensorMap* m, uint32_t dst, uint32_t b, int row,
+                                          int h, int bb) {
+#pragma unroll
+  for (int c = 0; c < HD / 64; ++c) tma_load_4d(dst + c * (kTile * 128), m, b, c * 64, row, h, bb);
 }
 
 template <int HD>
@@ -83,69 +149,46 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, uint8_t* smem, 
                                              volatile int* abort_flag) {
   using L = FwdLayout<HD>;
   auto bar = [&](int i) { return smem_u32(bars + i); };
-  SlotRun st[2];
-  for (int s = 0; s < 2; ++s) {
-    st[s].k = 0;
-    st[s].active = next_nonempty_unit(st[s], s, p);
-  }
   uint32_t kv_cnt = 0, qe_cnt[2] = {0, 0};
   int last_kv[L::kStages];
   for (int i = 0; i < L::kStages; ++i) last_kv[i] = -1;
   int last_q[2] = {-1, -1};
   bool ok = true;
-  auto load_tile = [&](const CUtensorMap* m, uint32_t dst, uint32_t b, int row, const Unit& un) {
-#pragma unroll
-    for (int c = 0; c < HD / 64; ++c)
-      tma_load_4d(dst + c * (kTile * 128), m, b, c * 64, row, un.h, un.b);
-  };
-  while (ok && (st[0].active || st[1].active)) {
-    for (int s = 0; s < 2 && ok; ++s) {
-      SlotRun& r = st[s];
-      if (!r.active) continue;
-      if (r.t > 0) {  // V of tile t-1
-        const int stage = kv_cnt % L::kStages;
-        if (!wait_bar(bar(L::kKvEmpty + stage), ((kv_cnt / L::kStages) & 1) ^ 1, abort_flag,
-                      p.status, 1)) {
-          ok = false;
-          break;
-        }
-        const InnerTile it = inner_tile(r.un, r.t - 1, p.list, p.status);
-        mbar_arrive_expect_tx(bar(L::kKvFull + stage), L::kTileBytes);
-        load_tile(&p.tm_v, smem_u32(smem + L::kRingOff + stage * L::kTileBytes),
-                  bar(L::kKvFull + stage), it.blk * kTile, r.un);
-        last_kv[stage] = int(kv_cnt);
-        ++kv_cnt;
-        if (r.t == r.un.n) {
-          r.active = next_nonempty_unit(r, s, p);
-          continue;
-        }
+  for (int k = 0; ok; ++k) {
+    const int u = int(blockIdx.x) + k * int(gridDim.x);
+    if (u >= p.n_units) break;
+    const PairUnit pu = decode_pair(u, p);
+    if (pu.n[0] + pu.n[1] == 0) continue;
+    for (int s = 0; s < 2; ++s) {
+      if (pu.n[s] == 0) continue;
+      if (!wait_bar(bar(L::kQEmpty + s), (qe_cnt[s] & 1) ^ 1, abort_flag, p.status, 2)) {
+        ok = false;
+        break;
       }
-      if (r.t == 0) {  // Q tile of a new unit
-        if (!wait_bar(bar(L::kQEmpty + s), (qe_cnt[s] & 1) ^ 1, abort_flag, p.status, 2)) {
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(bar(L::kQFull + s), L::kTileBytes);
-        load_tile(&p.tm_q, smem_u32(smem + L::kQOff + s * L::kTileBytes), bar(L::kQFull + s),
-                  r.un.ob * kTile, r.un);
-        last_q[s] = int(qe_cnt[s]);
-        ++qe_cnt[s];
-      }
-      {  // K of tile t
+      mbar_arrive_expect_tx(bar(L::kQFull + s), L::kTileBytes);
+      load_tile<HD>(&p.tm_q, smem_u32(smem + L::kQOff + s * L::kTileBytes), bar(L::kQFull + s),
+                    pu.q[s] * kTile, pu.h, pu.b);
+      last_q[s] = int(qe_cnt[s]);
+      ++qe_cnt[s];
+    }
+    PairWalk w;
+    walk_init(w, pu, p.list);
+    PairTile t;
+    while (ok && walk_next(w, p.list, t)) {
+      for (int kv = 0; kv < 2; ++kv) {  // K then V of the tile
         const int stage = kv_cnt % L::kStages;
         if (!wait_bar(bar(L::kKvEmpty + stage), ((kv_cnt / L::kStages) & 1) ^ 1, abort_flag,
                       p.status, 3)) {
           ok = false;
           break;
         }
-        const InnerTile it = inner_tile(r.un, r.t, p.list, p.status);
         mbar_arrive_expect_tx(bar(L::kKvFull + stage), L::kTileBytes);
-        load_tile(&p.tm_k, smem_u32(smem + L::kRingOff + stage * L::kTileBytes),
-                  bar(L::kKvFull + stage), it.blk * kTile, r.un);
+        load_tile<HD>(kv ? &p.tm_v : &p.tm_k,
+                      smem_u32(smem + L::kRingOff + stage * L::kTileBytes),
+                      bar(L::kKvFull + stage), t.kb * kTile, pu.h, pu.b);
         last_kv[stage] = int(kv_cnt);
         ++kv_cnt;
       }
-      ++r.t;
     }
   }
   if (!ok) {  // let copies already issued land before the CTA exits
@@ -163,85 +206,112 @@ __device__ __forceinline__ void fwd_mma(const FwdParams& p, uint8_t* smem, uint6
   auto bar = [&](int i) { return smem_u32(bars + i); };
   constexpr uint32_t kIdQK = idesc_bf16_f32(128, 128, false, false);
   constexpr uint32_t kIdPV = idesc_bf16_f32(128, HD, false, true);
-  SlotRun st[2];
-  for (int s = 0; s < 2; ++s) {
-    st[s].k = 0;
-    st[s].active = next_nonempty_unit(st[s], s, p);
-  }
   uint32_t kv_cnt = 0, qf_cnt[2] = {0, 0}, pf_cnt[2] = {0, 0}, oe_cnt[2] = {0, 0};
   const uint32_t ring = smem_u32(smem + L::kRingOff);
   bool ok = true;
-  while (ok && (st[0].active || st[1].active)) {
-    for (int s = 0; s < 2 && ok; ++s) {
-      SlotRun& r = st[s];
-      if (!r.active) continue;
-      const uint32_t tS = tmem + uint32_t(s * 256);
-      const uint32_t tO = tS + 128;
-      if (r.t > 0) {  // O (+)= P(t-1) V(t-1)
-        if (!wait_bar(bar(L::kPFull + s), pf_cnt[s] & 1, abort_flag, p.status, 10)) {
-          ok = false;
-          break;
-        }
-        ++pf_cnt[s];
-        if (r.t == 1) {
-          if (!wait_bar(bar(L::kOEmpty + s), (oe_cnt[s] & 1) ^ 1, abort_flag, p.status, 11)) {
-            ok = false;
-            break;
-          }
-          ++oe_cnt[s];
-        }
-        const int stage = kv_cnt % L::kStages;
-        if (!wait_bar(bar(L::kKvFull + stage), (kv_cnt / L::kStages) & 1, abort_flag, p.status,
-                      12)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t vb = ring + stage * L::kTileBytes;
+  // S_s = Q_s K^T for the K tile in ring stage `stage`
+  auto issue_qk = [&](int s, int stage) {
+    const uint32_t qa = smem_u32(smem + L::kQOff + s * L::kTileBytes);
+    const uint32_t ka = ring + stage * L::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          // B = V tile, MN-major: 64-column chunks 16 KB apart, 8-row groups 1 KB apart
-          const uint64_t bd = sdesc_sw128(vb + kk * 2048, kTile * 128, 1024);
-          mma_ts(tO, tS + kk * 8, bd, kIdPV, (r.t > 1 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(bar(L::kKvEmpty + stage));
-        ++kv_cnt;
-        if (r.t == r.un.n) {
-          mma_commit(bar(L::kOFull + s));
-          r.active = next_nonempty_unit(r, s, p);
-          continue;
-        }
-      }
-      if (r.t == 0) {
-        if (!wait_bar(bar(L::kQFull + s), qf_cnt[s] & 1, abort_flag, p.status, 13)) {
+    for (int kk = 0; kk < HD / 16; ++kk) {
+      // A = Q, B = K, both K-major: 16-element k-steps are 32 bytes apart
+      // inside a 128-byte swizzle row, 64-element chunks 16 KB apart
+      const uint32_t off = (kk / 4) * (kTile * 128) + (kk % 4) * 32;
+      mma_ss(tmem + uint32_t(s * 256), sdesc_sw128(qa + off, 16, 1024),
+             sdesc_sw128(ka + off, 16, 1024), kIdQK, kk > 0 ? 1u : 0u);
+    }
+    mma_commit(bar(L::kSFull + s));
+  };
+  for (int k = 0; ok; ++k) {
+    const int u = int(blockIdx.x) + k * int(gridDim.x);
+    if (u >= p.n_units) break;
+    const PairUnit pu = decode_pair(u, p);
+    if (pu.n[0] + pu.n[1] == 0) continue;
+    int seen[2] = {0, 0};    // P V products issued per slot in this unit
+    int issued[2] = {0, 0};  // Q K^T products issued per slot in this unit
+    PairWalk w;
+    walk_init(w, pu, p.list);
+    PairTile cur, nxt;
+    walk_next(w, p.list, cur);  // the union is non-empty
+    // prologue: Q K^T of the first tile
+    {
+      const int ks = kv_cnt % L::kStages;
+      for (int s = 0; s < 2 && ok; ++s)
+        if (cur.in[s] && !wait_bar(bar(L::kQFull + s), qf_cnt[s] & 1, abort_flag, p.status, 13))
           ok = false;
-          break;
-        }
+      if (ok && !wait_bar(bar(L::kKvFull + ks), (kv_cnt / L::kStages) & 1, abort_flag, p.status, 14))
+        ok = false;
+      if (!ok) break;
+      tc_fence_after();
+      for (int s = 0; s < 2; ++s) {
+        if (!cur.in[s]) continue;
         ++qf_cnt[s];
+        issue_qk(s, ks);
+        if (++issued[s] == pu.n[s]) mma_commit(bar(L::kQEmpty + s));
       }
-      const int stage = kv_cnt % L::kStages;
-      if (!wait_bar(bar(L::kKvFull + stage), (kv_cnt / L::kStages) & 1, abort_flag, p.status,
-                    14)) {
+      mma_commit(bar(L::kKvEmpty + ks));
+      ++kv_cnt;
+    }
+    while (ok) {
+      const bool more = walk_next(w, p.list, nxt);
+      const int vs = kv_cnt % L::kStages;            // V of cur
+      const int ks = (kv_cnt + 1) % L::kStages;      // K of nxt
+      if (!wait_bar(bar(L::kKvFull + vs), (kv_cnt / L::kStages) & 1, abort_flag, p.status, 12)) {
         ok = false;
         break;
       }
-      tc_fence_after();
-      const uint32_t qb = smem_u32(smem + L::kQOff + s * L::kTileBytes);
-      const uint32_t kb = ring + stage * L::kTileBytes;
-#pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk) {
-        // A = Q, B = K, both K-major: 16-element k-steps are 32 bytes apart
-        // inside a 128-byte swizzle row, 64-element chunks 16 KB apart
-        const uint32_t off = (kk / 4) * (kTile * 128) + (kk % 4) * 32;
-        mma_ss(tS, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), kIdQK,
-               kk > 0 ? 1u : 0u);
+      if (more) {
+        for (int s = 0; s < 2 && ok; ++s)
+          if (nxt.in[s] && issued[s] == 0 &&
+              !wait_bar(bar(L::kQFull + s), qf_cnt[s] & 1, abort_flag, p.status, 13))
+            ok = false;
+        if (ok && !wait_bar(bar(L::kKvFull + ks), ((kv_cnt + 1) / L::kStages) & 1, abort_flag,
+                            p.status, 14))
+          ok = false;
+        if (!ok) break;
       }
-      mma_commit(bar(L::kSFull + s));
-      mma_commit(bar(L::kKvEmpty + stage));
-      ++kv_cnt;
-      if (r.t == r.un.n - 1) mma_commit(bar(L::kQEmpty + s));
-      ++r.t;
+      for (int s = 0; s < 2 && ok; ++s) {
+        const uint32_t tS = tmem + uint32_t(s * 256);
+        if (cur.in[s]) {  // O_s (+)= P_s V
+          if (!wait_bar(bar(L::kPFull + s), pf_cnt[s] & 1, abort_flag, p.status, 10)) {
+            ok = false;
+            break;
+          }
+          ++pf_cnt[s];
+          if (seen[s] == 0) {
+            if (!wait_bar(bar(L::kOEmpty + s), (oe_cnt[s] & 1) ^ 1, abort_flag, p.status, 11)) {
+              ok = false;
+              break;
+            }
+            ++oe_cnt[s];
+          }
+          tc_fence_after();
+          const uint32_t vb = ring + vs * L::kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            // B = V tile, MN-major: 64-column chunks 16 KB apart, 8-row groups 1 KB apart
+            const uint64_t bd = sdesc_sw128(vb + kk * 2048, kTile * 128, 1024);
+            mma_ts(tS + 128, tS + kk * 8, bd, kIdPV, (seen[s] > 0 || kk > 0) ? 1u : 0u);
+          }
+          ++seen[s];
+          if (seen[s] == pu.n[s]) mma_commit(bar(L::kOFull + s));
+        }
+        if (more && nxt.in[s]) {
+          if (issued[s] == 0) ++qf_cnt[s];
+          tc_fence_after();
+          issue_qk(s, ks);
+          if (++issued[s] == pu.n[s]) mma_commit(bar(L::kQEmpty + s));
+        }
+      }
+      if (!ok) break;
+      mma_commit(bar(L::kKvEmpty + vs));
+      if (!more) break;
+      mma_commit(bar(L::kKvEmpty + ks));
+      kv_cnt += 2;
+      cur = nxt;
     }
+    kv_cnt += 1;  // the last V stage
   }
   // every MMA issued so far has finished before TMEM is released
   mma_commit(bar(L::kMmaDone));
@@ -261,9 +331,16 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint64_t* bars, 
   const float sl2 = p.scale_log2;
   uint32_t sf_cnt = 0, of_cnt = 0;
   for (int k = 0;; ++k) {
-    const int u = 2 * (int(blockIdx.x) + k * int(gridDim.x)) + slot;
+    const int u = int(blockIdx.x) + k * int(gridDim.x);
     if (u >= p.n_units) break;
-    const Unit un = decode_unit(u, p.H, p.list, p.status);
+    const PairUnit pu = decode_pair(u, p);
+    if (pu.q[slot] < 0) continue;
+    Unit un;
+    un.b = pu.b;
+    un.h = pu.h;
+    un.ob = pu.q[slot];
+    un.begin = pu.beg[slot];
+    un.n = pu.n[slot];
     const int64_t i = int64_t(un.ob) * kTile + row;
     float m_run = -INFINITY, l_run = 0.f;
     for (int t = 0; t < un.n; ++t) {
@@ -298,8 +375,11 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint64_t* bars, 
         mx2 = fmaxf(mx2, __uint_as_float(sr[c + 2]));
         mx3 = fmaxf(mx3, __uint_as_float(sr[c + 3]));
       }
-      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-      const float m_new = fmaxf(m_run, mx * sl2);
+      // Reference max: raised only when the tile max exceeds it by more than
+      // 8 (log2 units), so P <= 2^8 and O is rarely rescaled.  The result is
+      // exact for any reference value: O and l carry the same factor.
+      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      const float m_new = (mx > m_run + 8.f) ? mx : m_run;
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = ex2_approx(m_run - m_use);
       float sum0 = 0.f, sum1 = 0.f;
@@ -413,11 +493,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    if (lane == 0) fwd_producer<HD>(p, smem, bars, abort_flag);
-  } else if (warp == 1) {
-    if (lane == 0) fwd_mma<HD>(p, smem, bars, tmem, abort_flag);
-  } else if (warp >= 4) {
+  // 384 threads x 168 registers at launch: the producer / MMA warpgroup
+  // gives registers to the two softmax warpgroups (128 x 80 + 256 x 208).
+  if (warp < 4) {
+    regs_shrink<80>();
+    if (warp == 0) {
+      if (lane == 0) fwd_producer<HD>(p, smem, bars, abort_flag);
+    } else if (warp == 1) {
+      if (lane == 0) fwd_mma<HD>(p, smem, bars, tmem, abort_flag);
+    }
+  } else {
+    regs_grow<208>();
     fwd_softmax<HD>(p, bars, tmem, (warp - 4) >> 2, abort_flag);
   }
 
@@ -449,7 +535,7 @@ static flash_msa_status launch_fwd_hd(const FwdLaunch& a, cudaStream_t stream) {
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.mask = a.mask;
   p.list = a.list;
-  p.n_units = a.B * a.H * a.list.n_blocks;
+  p.n_units = a.B * a.H * ((a.list.n_blocks + 1) / 2);  // pairs of query blocks
   p.status = a.status;
   static bool attr_set[2] = {false, false};
   if (!attr_set[HD == 128]) {
@@ -458,8 +544,7 @@ static flash_msa_status launch_fwd_hd(const FwdLaunch& a, cudaStream_t stream) {
       return set_cuda_error("cudaFuncSetAttribute(fwd)");
     attr_set[HD == 128] = true;
   }
-  const int pairs = (p.n_units + 1) / 2;
-  int grid = pairs;
+  int grid = p.n_units;
   if (a.max_ctas > 0 && grid > a.max_ctas) grid = a.max_ctas;
   fwd_kernel<HD><<<grid, kFwdThreads, L::kSmemBytes, stream>>>(p);
   if (cudaGetLastError() != cudaSuccess) return set_cuda_error("fwd kernel launch");
