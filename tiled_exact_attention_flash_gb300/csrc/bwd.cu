@@ -340,10 +340,14 @@ __device__ __forceinline__ void dq_mma(const BwdParams& p, uint8_t* smem, uint64
 }
 
 // MMA issuer of bwd_dkdv (key-stationary; fixed tiles K, V; ring Q_t, dO_t).
-// TMEM: S^T at [0,128), dP^T at [128,256), dV at [256, 256+d), dK at
-// [384, 384+d); P^T and dS^T (bf16) overwrite S^T and dP^T.  Per query tile:
-//   S^T = K Q_t^T, dP^T = V dO_t^T -> s_full; [P full] dV += P^T dO_t,
-//   dK += dS^T Q_t -> release Q_t, dO_t.
+// TMEM: two 128-column regions R0 = [0,128), R1 = [128,256) that swap roles
+// every query tile (tile t: S^T in R_(t&1), dP^T in R_(1-(t&1))), dV at
+// [256, 256+d), dK at [384, 384+d).  The elementwise side pulls its S^T and
+// dP^T columns into registers first (sdp_free), which frees the dP^T region
+// for the next tile's S^T, and then writes P^T and dS^T (bf16) into the
+// S^T region.  Order per tile t:
+//   [sdp_free(t)] S^T(t+1) -> [P full(t)] dV += P^T dO_t, dK += dS^T Q_t,
+//   release Q_t / dO_t, dP^T(t+1) -> s_full(t+1)
 template <int HD>
 __device__ __forceinline__ void dkdv_mma(const BwdParams& p, uint8_t* smem, uint64_t* bars,
                                          uint32_t tmem, volatile int* abort_flag) {
@@ -351,7 +355,7 @@ __device__ __forceinline__ void dkdv_mma(const BwdParams& p, uint8_t* smem, uint
   auto bar = [&](int i) { return smem_u32(bars + i); };
   constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);
   constexpr uint32_t kIdAcc = idesc_bf16_f32(128, HD, false, true);
-  const uint32_t tS = tmem, tD = tmem + 128, tDV = tmem + 256, tDK = tmem + 384;
+  const uint32_t tDV = tmem + 256, tDK = tmem + 384;
   const uint32_t fk = smem_u32(smem + L::kFixOff);
   const uint32_t fv = fk + L::kTileBytes;
   auto stage_addr = [&](uint32_t c) {
@@ -361,20 +365,29 @@ __device__ __forceinline__ void dkdv_mma(const BwdParams& p, uint8_t* smem, uint
     return wait_bar(bar(L::kRingFull + c % L::kStages), (c / L::kStages) & 1, abort_flag,
                     p.status, where);
   };
-  uint32_t cnt = 0, ff_cnt = 0, pf_cnt = 0, ae_cnt = 0;
+  auto region = [&](int r) { return tmem + uint32_t(r & 1) * 128; };
+  uint32_t cnt = 0, ff_cnt = 0, pf_cnt = 0, sf_cnt = 0, ae_cnt = 0;
   bool ok = true;
   int k = 0;
   Unit un;
   while (ok && next_unit(k, un, p)) {
     if (!wait_bar(bar(L::kFixFull), ff_cnt & 1, abort_flag, p.status, 10)) break;
     ++ff_cnt;
+    if (!ring_wait(cnt, 11) || !ring_wait(cnt + 1, 12)) break;
+    tc_fence_after();
+    mma_kmajor<HD>(region(0), fk, stage_addr(cnt), kIdS);        // S^T(0) -> R0
+    mma_kmajor<HD>(region(1), fv, stage_addr(cnt + 1), kIdS);    // dP^T(0) -> R1
+    mma_commit(bar(L::kSFull));
     for (int t = 0; t < un.n && ok; ++t) {
       const uint32_t c = cnt + 2 * t;  // Q_t at c, dO_t at c + 1
-      if (!ring_wait(c, 11) || !ring_wait(c + 1, 12)) { ok = false; break; }
-      tc_fence_after();
-      mma_kmajor<HD>(tS, fk, stage_addr(c), kIdS);
-      mma_kmajor<HD>(tD, fv, stage_addr(c + 1), kIdS);
-      mma_commit(bar(L::kSFull));
+      const bool more = t + 1 < un.n;
+      if (more) {
+        if (!ring_wait(c + 2, 11) || !ring_wait(c + 3, 12)) { ok = false; break; }
+        if (!wait_bar(bar(L::kDpFree), sf_cnt & 1, abort_flag, p.status, 15)) { ok = false; break; }
+        ++sf_cnt;
+        tc_fence_after();
+        mma_kmajor<HD>(region(t + 1), fk, stage_addr(c + 2), kIdS);  // S^T(t+1) -> old dP^T region
+      }
       if (t == 0) {
         if (!wait_bar(bar(L::kAccEmpty), (ae_cnt & 1) ^ 1, abort_flag, p.status, 13)) { ok = false; break; }
         ++ae_cnt;
@@ -382,12 +395,19 @@ __device__ __forceinline__ void dkdv_mma(const BwdParams& p, uint8_t* smem, uint
       if (!wait_bar(bar(L::kPFull), pf_cnt & 1, abort_flag, p.status, 14)) { ok = false; break; }
       ++pf_cnt;
       tc_fence_after();
-      mma_tmem_a(tDV, tS, stage_addr(c + 1), kIdAcc, t > 0);
-      mma_tmem_a(tDK, tD, stage_addr(c), kIdAcc, t > 0);
+      mma_tmem_a(tDV, region(t), stage_addr(c + 1), kIdAcc, t > 0);       // P^T at +0
+      mma_tmem_a(tDK, region(t) + 32, stage_addr(c), kIdAcc, t > 0);      // dS^T at +32
       mma_commit(bar(L::kRingEmpty + c % L::kStages));
       mma_commit(bar(L::kRingEmpty + (c + 1) % L::kStages));
+      if (more) {
+        mma_kmajor<HD>(region(t), fv, stage_addr(c + 3), kIdS);  // dP^T(t+1) -> old S^T region
+        mma_commit(bar(L::kSFull));
+      }
     }
     if (!ok) break;
+    // the last tile's sdp_free has been signalled too: consume it
+    if (!wait_bar(bar(L::kDpFree), sf_cnt & 1, abort_flag, p.status, 15)) break;
+    ++sf_cnt;
     cnt += 2 * un.n;
     mma_commit(bar(L::kFixEmpty));
     mma_commit(bar(L::kAccFull));
@@ -432,7 +452,6 @@ __device__ __forceinline__ void dkdv_elementwise(const BwdParams& p, uint8_t* sm
   const int wq = int(warp_id()) & 3;
   const int row = wq * 32 + int(lane_id());
   const uint32_t lane_off = uint32_t(wq * 32) << 16;
-  const uint32_t tS = tmem + lane_off + 64 * g, tD = tS + 128;
   const uint32_t tDV = tmem + lane_off + 256, tDK = tmem + lane_off + 384;
   const float sl2 = p.scale_log2;
   uint32_t sp_cnt = 0, af_cnt = 0, cnt = 0;
@@ -463,27 +482,43 @@ __device__ __forceinline__ void dkdv_elementwise(const BwdParams& p, uint8_t* sm
       if (!__all_sync(0xFFFFFFFFu, ok)) return;
       ++sp_cnt;
       tc_fence_after();
+      const bool masked = it.partial || it.dead;
+      // this tile's regions: S^T in R_(t&1), dP^T in the other one
+      const uint32_t tSr = tmem + lane_off + uint32_t(t & 1) * 128 + 64 * g;
+      const uint32_t tDr = tmem + lane_off + uint32_t((t + 1) & 1) * 128 + 64 * g;
+      uint32_t sv[64], dpv[64];
+      tmem_ld_x64(tSr, sv);
+      tmem_ld_x64(tDr, dpv);
+      warp_arrive(bar(L::kDpFree));  // both regions' old contents are in registers now
+      uint32_t pp[32], dd[32];
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        uint32_t s[32], dp[32], pp[16], dd[16];
-        tmem_ld_x32(tS + ch * 32, s);
-        tmem_ld_x32(tD + ch * 32, dp);
+      for (int x = 0; x < 64; x += 4) {
+        const int c0 = 64 * g + x;  // query within the 128-query tile
+        const float4 l4 = *reinterpret_cast<const float4*>(vec + c0);
+        const float4 d4 = *reinterpret_cast<const float4*>(vec + 128 + c0);
+        const float l2[4] = {l4.x, l4.y, l4.z, l4.w};
+        const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int c = 64 * g + ch * 32 + e;  // query within the 128-query tile
-          const float2 l2 = *reinterpret_cast<const float2*>(vec + c);
-          const float2 dv2 = *reinterpret_cast<const float2*>(vec + 128 + c);
-          float p0 = ex2_approx(fmaf(__uint_as_float(s[e]), sl2, -l2.x));
-          float p1 = ex2_approx(fmaf(__uint_as_float(s[e + 1]), sl2, -l2.y));
-          if (c < lo || c > hi) p0 = 0.f;
-          if (c + 1 < lo || c + 1 > hi) p1 = 0.f;
-          pp[e / 2] = pack_bf16x2(p0, p1);
-          dd[e / 2] = pack_bf16x2(p0 * (__uint_as_float(dp[e]) - dv2.x),
-                                  p1 * (__uint_as_float(dp[e + 1]) - dv2.y));
+        for (int e = 0; e < 4; e += 2) {
+          float x0, x1, p0, p1, u0, u1, d0, d1;
+          fma2(x0, x1, __uint_as_float(sv[x + e]), __uint_as_float(sv[x + e + 1]), sl2, sl2,
+               -l2[e], -l2[e + 1]);
+          p0 = ex2_approx(x0);
+          p1 = ex2_approx(x1);
+          if (masked) {
+            if (c0 + e < lo || c0 + e > hi) p0 = 0.f;
+            if (c0 + e + 1 < lo || c0 + e + 1 > hi) p1 = 0.f;
+          }
+          sub2(u0, u1, __uint_as_float(dpv[x + e]), __uint_as_float(dpv[x + e + 1]), dv[e],
+               dv[e + 1]);
+          mul2(d0, d1, p0, p1, u0, u1);
+          pp[(x + e) / 2] = pack_bf16x2(p0, p1);
+          dd[(x + e) / 2] = pack_bf16x2(d0, d1);
         }
-        tmem_st_x16(tS + ch * 16, pp);
-        tmem_st_x16(tD + ch * 16, dd);
       }
+      // P^T to columns [64 g, 64 g + 32), dS^T to [64 g + 32, 64 g + 64) of the S^T region
+      tmem_st_x32(tSr, pp);
+      tmem_st_x32(tSr + 32, dd);
       tmem_wait_st();
       warp_arrive(bar(L::kPFull));
     }
@@ -543,19 +578,26 @@ __device__ __forceinline__ void dq_elementwise(const BwdParams& p, uint64_t* bar
       tmem_ld_x64(tDP, dpr);
       warp_arrive(bar(L::kDpFree));
       const uint32_t tS = tmem + lane_off + (t & 1) * 128 + 64 * g;  // same buffer as dq_mma
+      const bool masked = it.partial || it.dead;
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         uint32_t s[32], dd[16];
         tmem_ld_x32(tS + ch * 32, s);
+        const int c0 = 64 * g + ch * 32;
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const int c = 64 * g + ch * 32 + e;
-          float p0 = ex2_approx(fmaf(__uint_as_float(s[e]), sl2, -l2));
-          float p1 = ex2_approx(fmaf(__uint_as_float(s[e + 1]), sl2, -l2));
-          if (c < lo || c > hi) p0 = 0.f;
-          if (c + 1 < lo || c + 1 > hi) p1 = 0.f;
-          dd[e / 2] = pack_bf16x2(p0 * (__uint_as_float(dpr[ch * 32 + e]) - di),
-                                  p1 * (__uint_as_float(dpr[ch * 32 + e + 1]) - di));
+          float x0, x1, p0, p1, u0, u1, d0, d1;
+          fma2(x0, x1, __uint_as_float(s[e]), __uint_as_float(s[e + 1]), sl2, sl2, -l2, -l2);
+          p0 = ex2_approx(x0);
+          p1 = ex2_approx(x1);
+          if (masked) {
+            if (c0 + e < lo || c0 + e > hi) p0 = 0.f;
+            if (c0 + e + 1 < lo || c0 + e + 1 > hi) p1 = 0.f;
+          }
+          sub2(u0, u1, __uint_as_float(dpr[ch * 32 + e]), __uint_as_float(dpr[ch * 32 + e + 1]),
+               di, di);
+          mul2(d0, d1, p0, p1, u0, u1);
+          dd[e / 2] = pack_bf16x2(d0, d1);
         }
         tmem_st_x16(tS + ch * 16, dd);  // columns already read
       }
@@ -601,6 +643,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (warp < 4) regs_shrink<80>();  // 384 x 168 at launch: 128 x 80 + 256 x 208
   if (warp == 0) {
     if (lane == 0) bwd_producer<HD, kKeyStationary>(p, smem, bars, abort_flag);
   } else if (warp == 1) {
@@ -610,6 +653,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
     }
   } else if (warp >= 4) {
     const int g = (warp - 4) >> 2;  // elementwise warpgroup: columns [64 g, 64 g + 64)
+    regs_grow<208>();
     if (kKeyStationary) dkdv_elementwise<HD>(p, smem, bars, tmem, g, abort_flag);
     else dq_elementwise<HD>(p, bars, tmem, g, abort_flag);
   }

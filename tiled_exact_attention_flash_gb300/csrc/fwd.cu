@@ -369,11 +369,11 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint64_t* bars, 
       }
       float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 128; c += 4) {
-        mx0 = fmaxf(mx0, __uint_as_float(sr[c]));
-        mx1 = fmaxf(mx1, __uint_as_float(sr[c + 1]));
-        mx2 = fmaxf(mx2, __uint_as_float(sr[c + 2]));
-        mx3 = fmaxf(mx3, __uint_as_float(sr[c + 3]));
+      for (int c = 0; c < 128; c += 8) {
+        mx0 = max3(mx0, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+        mx1 = max3(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+        mx2 = max3(mx2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+        mx3 = max3(mx3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
       }
       // Reference max: raised only when the tile max exceeds it by more than
       // 8 (log2 units), so P <= 2^8 and O is rarely rescaled.  The result is
@@ -382,16 +382,21 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint64_t* bars, 
       const float m_new = (mx > m_run + 8.f) ? mx : m_run;
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = ex2_approx(m_run - m_use);
-      float sum0 = 0.f, sum1 = 0.f;
+      float sa[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // four independent pair sums
       uint32_t pk[64];
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
-        const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), sl2, -m_use));
-        const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), sl2, -m_use));
-        sum0 += p0;
-        sum1 += p1;
+        float x0, x1;
+        fma2(x0, x1, __uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1]), sl2, sl2, -m_use,
+             -m_use);
+        const float p0 = ex2_approx(x0);
+        const float p1 = ex2_approx(x1);
+        const int a = 2 * (c & 3);
+        add2(sa[a], sa[a + 1], sa[a], sa[a + 1], p0, p1);
         pk[c] = pack_bf16x2(p0, p1);
       }
+      const float sum0 = (sa[0] + sa[2]) + (sa[4] + sa[6]);
+      const float sum1 = (sa[1] + sa[3]) + (sa[5] + sa[7]);
       tmem_st_x32(tS, *reinterpret_cast<uint32_t(*)[32]>(pk));
       tmem_st_x32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
       l_run = l_run * alpha + (sum0 + sum1);
