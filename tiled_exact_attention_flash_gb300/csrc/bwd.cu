@@ -91,6 +91,8 @@ struct BwdParams {
   __nv_bfloat16* out_b;  // dkdv: dV
   const float* lse2;
   const float* dsum;
+  const __nv_bfloat16* q;     // dQ pass: rows staged into TMEM by the elementwise side
+  const __nv_bfloat16* dout;
   int B, H, N, NP;
   int n_units;
   float scale, scale_log2;
@@ -108,9 +110,9 @@ struct BwdLayout {
   static constexpr int kTileBytes = kTile * HD * 2;
   // dK/dV: even (Q and dO of a tile in consecutive stages share a vector
   // slot); dQ: one more stage of prefetch (no vectors to stage)
-  static constexpr int kStages = KS ? (HD == 128 ? 4 : 8) : (HD == 128 ? 5 : 8);
-  static constexpr int kFixOff = 0;                  // two stationary tiles
-  static constexpr int kRingOff = 2 * kTileBytes;
+  static constexpr int kStages = KS ? (HD == 128 ? 4 : 8) : (HD == 128 ? 6 : 12);
+  static constexpr int kFixOff = 0;  // dK/dV: K and V tiles; dQ: none (Q, dO live in TMEM)
+  static constexpr int kRingOff = KS ? 2 * kTileBytes : 0;
   static constexpr int kVecOff = kRingOff + kStages * kTileBytes;  // (stages/2) x 1 KB
   static constexpr int kBarOff = kVecOff + (KS ? (kStages / 2) * 1024 : 0);  // vectors: dK/dV only
   // kSFull / kPFull: two each (dK/dV: one per half-tile buffer; dQ: only [0])
@@ -142,7 +144,7 @@ __device__ __forceinline__ bool next_unit(int& k, Unit& un, const BwdParams& p) 
 template <int HD, bool KS>
 __device__ __forceinline__ void init_bwd_barriers(uint64_t* bars) {
   using L = BwdLayout<HD, KS>;
-  mbar_init(smem_u32(bars + L::kFixFull), 1);
+  mbar_init(smem_u32(bars + L::kFixFull), KS ? 1 : kEwWarps);
   mbar_init(smem_u32(bars + L::kFixEmpty), 1);
   for (int i = 0; i < 2; ++i) {
     mbar_init(smem_u32(bars + L::kSFull + i), 1);
@@ -179,17 +181,19 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint8_t* smem, 
   int k = 0;
   Unit un;
   while (ok && next_unit(k, un, p)) {
-    if (!wait_bar(bar(L::kFixEmpty), (fe_cnt & 1) ^ 1, abort_flag, p.status, 1)) {
-      ok = false;
-      break;
+    if (kKeyStationary) {
+      if (!wait_bar(bar(L::kFixEmpty), (fe_cnt & 1) ^ 1, abort_flag, p.status, 1)) {
+        ok = false;
+        break;
+      }
+      mbar_arrive_expect_tx(bar(L::kFixFull), 2 * L::kTileBytes);
+      load_tile_2d<HD>(fix_a, smem_u32(smem + L::kFixOff), bar(L::kFixFull), un.ob * kTile, un.h,
+                       un.b);
+      load_tile_2d<HD>(fix_b, smem_u32(smem + L::kFixOff + L::kTileBytes), bar(L::kFixFull),
+                       un.ob * kTile, un.h, un.b);
+      last_fix = int(fe_cnt);
+      ++fe_cnt;
     }
-    mbar_arrive_expect_tx(bar(L::kFixFull), 2 * L::kTileBytes);
-    load_tile_2d<HD>(fix_a, smem_u32(smem + L::kFixOff), bar(L::kFixFull), un.ob * kTile, un.h,
-                     un.b);
-    load_tile_2d<HD>(fix_b, smem_u32(smem + L::kFixOff + L::kTileBytes), bar(L::kFixFull),
-                     un.ob * kTile, un.h, un.b);
-    last_fix = int(fe_cnt);
-    ++fe_cnt;
     for (int t = 0; t < un.n && ok; ++t) {
       const InnerTile it = inner_tile(un, t, p.list, p.status);
       for (int half = 0; half < 2; ++half) {
@@ -269,11 +273,14 @@ __device__ __forceinline__ void mma_tmem_a(uint32_t d, uint32_t a_tmem, uint32_t
   }
 }
 
-// MMA issuer of bwd_dq (query-stationary; fixed tiles Q, dO; ring K_t, V_t).
-// TMEM: S double-buffered at [0,128) and [128,256), dP at [256,384), dQ at
-// [384, 384+d).  dS_t (bf16) overwrites S_t.  Order per key tile t:
-//   S(t+1), [dP free] dP(t+1) -> s_full, [P full] dQ(t) -> release K_t, V_t
-// so that the products of tile t+1 run while tile t's elementwise work does.
+// MMA issuer of bwd_dq (query-stationary; Q and dO of the query block live
+// in TMEM, written there by the elementwise warpgroups; ring K_t, V_t).
+// TMEM: S at [0,128), dP at [128,256), dQ at [256, 256+d), Q (bf16 pairs)
+// at [384, 384+d/2), dO at [448, 448+d/2).  S and dP use Q / dO as TMEM
+// operands, so only K_t / V_t are read from shared memory.  Order per key
+// tile t:  [dP free(t)] dP(t+1);  [P full(t)] dQ(t), release K_t / V_t;
+// S(t+1) -> s_full(t+1)  (dS(t) in the S columns is read before S(t+1)
+// overwrites them: tcgen05 products run in issue order).
 template <int HD>
 __device__ __forceinline__ void dq_mma(const BwdParams& p, uint8_t* smem, uint64_t* bars,
                                        uint32_t tmem, volatile int* abort_flag) {
@@ -281,40 +288,44 @@ __device__ __forceinline__ void dq_mma(const BwdParams& p, uint8_t* smem, uint64
   auto bar = [&](int i) { return smem_u32(bars + i); };
   constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);
   constexpr uint32_t kIdAcc = idesc_bf16_f32(128, HD, false, true);
-  const uint32_t tDP = tmem + 256, tDQ = tmem + 384;
-  const uint32_t fq = smem_u32(smem + L::kFixOff);
-  const uint32_t fdo = fq + L::kTileBytes;
+  const uint32_t tS = tmem, tDP = tmem + 128, tDQ = tmem + 256;
+  const uint32_t tQ = tmem + 384, tDO = tmem + 448;
   auto stage_addr = [&](uint32_t c) {
     return smem_u32(smem + L::kRingOff + (c % L::kStages) * L::kTileBytes);
+  };
+  auto ring_wait = [&](uint32_t c, unsigned where) {
+    return wait_bar(bar(L::kRingFull + c % L::kStages), (c / L::kStages) & 1, abort_flag,
+                    p.status, where);
+  };
+  // D = A[tmem, K-major pairs] * B[smem K-major]^T over the head dimension
+  auto mma_tmem_k = [&](uint32_t d, uint32_t a_tmem, uint32_t b) {
+#pragma unroll
+    for (int kk = 0; kk < HD / 16; ++kk) {
+      const uint32_t off = (kk / 4) * (kTile * 128) + (kk % 4) * 32;
+      mma_ts(d, a_tmem + kk * 8, sdesc_sw128(b + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+    }
   };
   uint32_t cnt = 0, ff_cnt = 0, pf_cnt = 0, dpf_cnt = 0, ae_cnt = 0;
   bool ok = true;
   int k = 0;
   Unit un;
-  auto ring_wait = [&](uint32_t c, unsigned where) {
-    return wait_bar(bar(L::kRingFull + c % L::kStages), (c / L::kStages) & 1, abort_flag,
-                    p.status, where);
-  };
   while (ok && next_unit(k, un, p)) {
     if (!wait_bar(bar(L::kFixFull), ff_cnt & 1, abort_flag, p.status, 10)) break;
     ++ff_cnt;
-    // tile 0: S and dP
     if (!ring_wait(cnt, 11) || !ring_wait(cnt + 1, 12)) break;
     tc_fence_after();
-    mma_kmajor<HD>(tmem, fq, stage_addr(cnt), kIdS);
-    mma_kmajor<HD>(tDP, fdo, stage_addr(cnt + 1), kIdS);
+    mma_tmem_k(tS, tQ, stage_addr(cnt));          // S(0)
+    mma_tmem_k(tDP, tDO, stage_addr(cnt + 1));    // dP(0)
     mma_commit(bar(L::kSFull));
     for (int t = 0; t < un.n && ok; ++t) {
       const uint32_t c = cnt + 2 * t;  // K_t at c, V_t at c + 1
-      if (t + 1 < un.n) {
+      const bool more = t + 1 < un.n;
+      if (more) {
         if (!ring_wait(c + 2, 11) || !ring_wait(c + 3, 12)) { ok = false; break; }
-        tc_fence_after();
-        mma_kmajor<HD>(tmem + ((t + 1) & 1) * 128, fq, stage_addr(c + 2), kIdS);
         if (!wait_bar(bar(L::kDpFree), dpf_cnt & 1, abort_flag, p.status, 15)) { ok = false; break; }
         ++dpf_cnt;
         tc_fence_after();
-        mma_kmajor<HD>(tDP, fdo, stage_addr(c + 3), kIdS);
-        mma_commit(bar(L::kSFull));
+        mma_tmem_k(tDP, tDO, stage_addr(c + 3));  // dP(t+1)
       }
       if (t == 0) {
         if (!wait_bar(bar(L::kAccEmpty), (ae_cnt & 1) ^ 1, abort_flag, p.status, 13)) { ok = false; break; }
@@ -323,16 +334,20 @@ __device__ __forceinline__ void dq_mma(const BwdParams& p, uint8_t* smem, uint64
       if (!wait_bar(bar(L::kPFull), pf_cnt & 1, abort_flag, p.status, 14)) { ok = false; break; }
       ++pf_cnt;
       tc_fence_after();
-      mma_tmem_a(tDQ, tmem + (t & 1) * 128, stage_addr(c), kIdAcc, t > 0);
+      mma_tmem_a(tDQ, tS, stage_addr(c), kIdAcc, t > 0);
       mma_commit(bar(L::kRingEmpty + c % L::kStages));
       mma_commit(bar(L::kRingEmpty + (c + 1) % L::kStages));
+      if (more) {
+        mma_tmem_k(tS, tQ, stage_addr(c + 2));  // S(t+1)
+        mma_commit(bar(L::kSFull));
+      }
     }
     if (!ok) break;
-    // the last tile's dP was loaded by the elementwise side: consume its dp_free
+    // the last tile's dP was pulled by the elementwise side: consume its dp_free
     if (!wait_bar(bar(L::kDpFree), dpf_cnt & 1, abort_flag, p.status, 15)) break;
     ++dpf_cnt;
     cnt += 2 * un.n;
-    mma_commit(bar(L::kFixEmpty));
+    mma_commit(bar(L::kFixEmpty));  // Q / dO columns may be overwritten
     mma_commit(bar(L::kAccFull));
   }
   mma_commit(bar(L::kMmaDone));
@@ -491,11 +506,16 @@ __device__ __forceinline__ void dkdv_elementwise(const BwdParams& p, uint8_t* sm
       tmem_ld_x64(tDr, dpv);
       warp_arrive(bar(L::kDpFree));  // both regions' old contents are in registers now
       uint32_t pp[32], dd[32];
+      float4 l4n = *reinterpret_cast<const float4*>(vec + 64 * g);
+      float4 d4n = *reinterpret_cast<const float4*>(vec + 128 + 64 * g);
 #pragma unroll
       for (int x = 0; x < 64; x += 4) {
         const int c0 = 64 * g + x;  // query within the 128-query tile
-        const float4 l4 = *reinterpret_cast<const float4*>(vec + c0);
-        const float4 d4 = *reinterpret_cast<const float4*>(vec + 128 + c0);
+        const float4 l4 = l4n, d4 = d4n;
+        if (x + 4 < 64) {  // next group's LSE / D, loaded one group ahead
+          l4n = *reinterpret_cast<const float4*>(vec + c0 + 4);
+          d4n = *reinterpret_cast<const float4*>(vec + 128 + c0 + 4);
+        }
         const float l2[4] = {l4.x, l4.y, l4.z, l4.w};
         const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
@@ -548,9 +568,9 @@ __device__ __forceinline__ void dq_elementwise(const BwdParams& p, uint64_t* bar
   const int wq = int(warp_id()) & 3;
   const int row = wq * 32 + int(lane_id());
   const uint32_t lane_off = uint32_t(wq * 32) << 16;
-  const uint32_t tDP = tmem + lane_off + 256 + 64 * g, tDQ = tmem + lane_off + 384;
+  const uint32_t tDP = tmem + lane_off + 128 + 64 * g, tDQ = tmem + lane_off + 256;
   const float sl2 = p.scale_log2;
-  uint32_t sp_cnt = 0, af_cnt = 0;
+  uint32_t sp_cnt = 0, af_cnt = 0, fe_cnt = 0;
   for (int k = 0;; ++k) {
     const int u = int(blockIdx.x) + k * int(gridDim.x);
     if (u >= p.n_units) break;
@@ -561,6 +581,28 @@ __device__ __forceinline__ void dq_elementwise(const BwdParams& p, uint64_t* bar
     if (un.n == 0) {
       if (g == 0) zero_row(dq_row, HD, valid);
       continue;
+    }
+    {  // this row of Q (warpgroup 0) or dO (warpgroup 1) into TMEM as bf16 pairs
+      const bool ok = wait_bar(bar(L::kFixEmpty), (fe_cnt & 1) ^ 1, abort_flag, p.status, 22);
+      if (!__all_sync(0xFFFFFFFFu, ok)) return;
+      ++fe_cnt;
+      const __nv_bfloat16* src = (g == 0 ? p.q : p.dout) +
+                                 ((int64_t(un.b) * p.N + i) * p.H + un.h) * HD;
+      uint32_t rw[HD / 2];
+#pragma unroll
+      for (int j = 0; j < HD / 8; ++j) {
+        const uint4 v = valid ? reinterpret_cast<const uint4*>(src)[j] : make_uint4(0, 0, 0, 0);
+        rw[4 * j] = v.x;
+        rw[4 * j + 1] = v.y;
+        rw[4 * j + 2] = v.z;
+        rw[4 * j + 3] = v.w;
+      }
+      const uint32_t dst = tmem + lane_off + 384 + 64 * g;
+#pragma unroll
+      for (int j = 0; j < HD / 64; ++j)
+        tmem_st_x32(dst + 32 * j, *reinterpret_cast<uint32_t(*)[32]>(rw + 32 * j));
+      tmem_wait_st();
+      warp_arrive(bar(L::kFixFull));
     }
     const int64_t vrow = (int64_t(un.b) * p.H + un.h) * p.NP + i;
     const float l2 = p.lse2[vrow];
@@ -577,7 +619,7 @@ __device__ __forceinline__ void dq_elementwise(const BwdParams& p, uint64_t* bar
       uint32_t dpr[64];
       tmem_ld_x64(tDP, dpr);
       warp_arrive(bar(L::kDpFree));
-      const uint32_t tS = tmem + lane_off + (t & 1) * 128 + 64 * g;  // same buffer as dq_mma
+      const uint32_t tS = tmem + lane_off + 64 * g;
       const bool masked = it.partial || it.dead;
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
@@ -694,6 +736,8 @@ static flash_msa_status launch_bwd_hd(const BwdLaunch& a, cudaStream_t stream) {
   if ((st = make_tile_map(&p.tm_do, a.dout, a.B, a.N, a.H, HD)) != FLASH_MSA_OK) return st;
   p.lse2 = lse2;
   p.dsum = dsum;
+  p.q = reinterpret_cast<const __nv_bfloat16*>(a.q);
+  p.dout = reinterpret_cast<const __nv_bfloat16*>(a.dout);
   p.B = a.B;
   p.H = a.H;
   p.N = int(a.N);
@@ -714,12 +758,13 @@ static flash_msa_status launch_bwd_hd(const BwdLaunch& a, cudaStream_t stream) {
     }
     return FLASH_MSA_OK;
   };
+  const int grid = p.n_units;
   if (a.stages & FLASH_MSA_BWD_DKDV) {
     if ((st = prep(bwd_main_kernel<HD, true>, 0)) != FLASH_MSA_OK) return st;
     p.list = a.cols;
     p.out_a = reinterpret_cast<__nv_bfloat16*>(a.dk);
     p.out_b = reinterpret_cast<__nv_bfloat16*>(a.dv);
-    bwd_main_kernel<HD, true><<<p.n_units, kBwdThreads, LK::kSmemBytes, stream>>>(p);
+    bwd_main_kernel<HD, true><<<grid, kBwdThreads, LK::kSmemBytes, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return set_cuda_error("bwd_dkdv launch");
   }
   if (a.stages & FLASH_MSA_BWD_DQ) {
@@ -727,7 +772,7 @@ static flash_msa_status launch_bwd_hd(const BwdLaunch& a, cudaStream_t stream) {
     p.list = a.rows;
     p.out_a = reinterpret_cast<__nv_bfloat16*>(a.dq);
     p.out_b = nullptr;
-    bwd_main_kernel<HD, false><<<p.n_units, kBwdThreads, LQ::kSmemBytes, stream>>>(p);
+    bwd_main_kernel<HD, false><<<grid, kBwdThreads, LQ::kSmemBytes, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return set_cuda_error("bwd_dq launch");
   }
   return FLASH_MSA_OK;
