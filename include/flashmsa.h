@@ -178,6 +178,24 @@ flash_msa_status flash_msa_bwd_stages(const void* q, const void* k, const void* 
                                       const flash_msa_mask_desc* mask, void* workspace,
                                       size_t workspace_bytes, unsigned stages, void* stream);
 
+/* Grouped-query attention (GQA; MQA when Hkv = 1): H query heads share Hkv
+ * key/value heads, query head h using key/value head h / (H / Hkv) (page
+ * "Flash MSA Attention Kernel Implementation", FAQ on grouped-query and
+ * multi-query attention: the tiling is unchanged, fewer K/V heads are read).
+ * q, o, dq and dO are (B, N, H, d); k, v, dk and dv are (B, N, Hkv, d); lse
+ * is (B, H, N); the workspace is flash_msa_bwd_workspace_bytes(B, H, N, d).
+ * dK and dV sum the contributions of all query heads of the group.  H % Hkv
+ * must be 0, else FLASH_MSA_ERR_INVALID_ARG; everything else as in
+ * flash_msa_fwd() / flash_msa_bwd(). */
+flash_msa_status flash_msa_fwd_gqa(const void* q, const void* k, const void* v, void* o,
+                                   float* lse, int B, int H, int Hkv, int64_t N, int d,
+                                   float scale, const flash_msa_mask_desc* mask, void* stream);
+flash_msa_status flash_msa_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
+                                   const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                                   int B, int H, int Hkv, int64_t N, int d, float scale,
+                                   const flash_msa_mask_desc* mask, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+
 /* Backward for callers that may not allocate device memory at call time (a
  * host framework that owns the whole device memory pool, or a latency-bound
  * loop where cudaMalloc/cudaFree are banned because they can synchronise the

@@ -113,3 +113,55 @@ def sample_positions(N, rng, k=96):
     pos = set(range(min(N, 40))) | set(range(max(0, N - 40), N))
     pos |= set(rng.integers(0, N, size=k).tolist())
     return np.array(sorted(pos))
+
+
+# ---------------------------------------------------------------------------
+# grouped-query attention: query head h reads key/value head h // G
+# ---------------------------------------------------------------------------
+def gqa_reference(q, k, v, do, scale, spec, backward=True):
+    """Per-head oracle for (N, H, d) query tensors and (N, Hkv, d) key/value
+    tensors (float64); dK / dV of a shared head sum the group's contributions."""
+    N, H, d = q.shape
+    Hkv = k.shape[1]
+    G = H // Hkv
+    o = np.zeros(q.shape)
+    lse = np.zeros((H, N))
+    dq = np.zeros(q.shape)
+    dk = np.zeros(k.shape)
+    dv = np.zeros(v.shape)
+    for h in range(H):
+        j = h // G
+        o[:, h], lse[h] = attention.forward_head(q[:, h], k[:, j], v[:, j], scale, spec)
+        if backward:
+            gq, gk, gv = attention.backward_head(q[:, h], k[:, j], v[:, j], do[:, h], scale, spec)
+            dq[:, h] = gq
+            dk[:, j] += gk
+            dv[:, j] += gv
+    return o, lse, dq, dk, dv
+
+
+def run_gpu_gqa(inp, fields, device="cuda"):
+    mask = api.Mask(**fields) if fields else None
+    N = inp["q"].shape[1]
+    index = api.build_block_index(mask, N).to(device) if (mask and mask.needs_index) else None
+    q, k, v, do = (inp[n].to(device) for n in ("q", "k", "v", "do"))
+    o, lse = api.fwd(q, k, v, mask=mask, index=index)
+    dq, dk, dv = api.bwd(q, k, v, o, lse, do, mask=mask, index=index)
+    assert api.get_status() == api.OK
+    f = lambda t: t.float().cpu().numpy()
+    return {"o": f(o), "lse": lse.cpu().numpy(), "dq": f(dq), "dk": f(dk), "dv": f(dv)}
+
+
+def gqa_full_compare(inp, fields, res):
+    B = inp["q"].shape[0]
+    d = inp["q"].shape[3]
+    spec = MaskSpec(**fields)
+    for b in range(B):
+        q, k, v, do = (as_f64(inp[n][b]) for n in ("q", "k", "v", "do"))
+        o, lse, dq, dk, dv = gqa_reference(q, k, v, do, d ** -0.5, spec)
+        for h in range(q.shape[1]):
+            check_o(res["o"][b, :, h], o[:, h])
+            check_lse(res["lse"][b, h], lse[h])
+        check_grad(res["dq"][b], dq, "dQ")
+        check_grad(res["dk"][b], dk, "dK")
+        check_grad(res["dv"][b], dv, "dV")

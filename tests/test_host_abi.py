@@ -93,3 +93,12 @@ def test_build_index_argument_errors(L):
     assert L.flash_msa_build_block_index(ctypes.byref(d), 0, ctypes.byref(hdr)) == api.ERR_INVALID_ARG
     d64 = api.Mask(causal=True, block=64).desc()
     assert L.flash_msa_build_block_index(ctypes.byref(d64), 100, ctypes.byref(hdr)) == api.ERR_UNSUPPORTED
+
+
+def test_gqa_head_count_errors(L):
+    args = [FAKE] * 5
+    assert L.flash_msa_fwd_gqa(*args, 1, 6, 4, 256, 128, 0.0, None, None) == api.ERR_INVALID_ARG
+    assert L.flash_msa_fwd_gqa(*args, 1, 6, 0, 256, 128, 0.0, None, None) == api.ERR_INVALID_ARG
+    need = L.flash_msa_bwd_workspace_bytes(1, 6, 256, 128)
+    assert L.flash_msa_bwd_gqa(*([FAKE] * 9), 1, 6, 4, 256, 128, 0.0, None, FAKE, need,
+                               None) == api.ERR_INVALID_ARG

@@ -32,6 +32,8 @@ SYMBOLS = (
     "flash_msa_bwd_workspace_bytes",
     "flash_msa_bwd",
     "flash_msa_bwd_stages",
+    "flash_msa_fwd_gqa",
+    "flash_msa_bwd_gqa",
     "flash_msa_bwd_noalloc",
     "flash_msa_get_status",
     "flash_msa_last_error_string",
@@ -95,6 +97,10 @@ def lib() -> ctypes.CDLL:
     L.flash_msa_bwd_stages.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i64, i32,
                                        f32, ctypes.POINTER(MaskDescStruct), vp, ctypes.c_size_t,
                                        ctypes.c_uint, vp]
+    L.flash_msa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i64, i32, f32,
+                                    ctypes.POINTER(MaskDescStruct), vp]
+    L.flash_msa_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i64, i32,
+                                    f32, ctypes.POINTER(MaskDescStruct), vp, ctypes.c_size_t, vp]
     L.flash_msa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i64, i32,
                                         f32, ctypes.POINTER(MaskDescStruct), vp]
     L.flash_msa_get_status.argtypes = [vp]
@@ -102,7 +108,7 @@ def lib() -> ctypes.CDLL:
     L.flash_msa_version.restype = ctypes.c_char_p
     for name in ("flash_msa_build_block_index", "flash_msa_check_block_index", "flash_msa_fwd",
                  "flash_msa_bwd", "flash_msa_bwd_stages", "flash_msa_bwd_noalloc",
-                 "flash_msa_get_status"):
+                 "flash_msa_fwd_gqa", "flash_msa_bwd_gqa", "flash_msa_get_status"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -252,23 +258,39 @@ def _mask_desc(mask: Optional[Mask], index: Optional[BlockIndex], n: int):
     return mask.desc(), None
 
 
+def _kv_shape(q, k):
+    """(B, N, Hkv, d) of k; Hkv may be smaller than q's head count (GQA / MQA)."""
+    _check_qkv("k", k)
+    B, N, H, d = q.shape
+    if k.shape[0] != B or k.shape[1] != N or k.shape[3] != d or H % k.shape[2] != 0:
+        raise ValueError(f"k has shape {tuple(k.shape)}: expected (B, N, Hkv, d) with Hkv | {H}")
+    return tuple(k.shape)
+
+
 def fwd(q, k, v, mask: Optional[Mask] = None, index: Optional[BlockIndex] = None,
         scale: Optional[float] = None, out=None, lse=None, stream=None):
-    """O (bf16, like q) and LSE (fp32, (B, H, N))."""
+    """O (bf16, like q) and LSE (fp32, (B, H, N)).  k and v may have fewer
+    heads than q (grouped-query attention): flash_msa_fwd_gqa."""
     _check_qkv("q", q)
     B, N, H, d = q.shape
-    _check_qkv("k", k, q.shape)
-    _check_qkv("v", v, q.shape)
+    kv_shape = _kv_shape(q, k)
+    _check_qkv("v", v, kv_shape)
+    Hkv = kv_shape[2]
     o = torch.empty_like(q) if out is None else out
     _check_qkv("out", o, q.shape)
     l = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
     if l.dtype != torch.float32 or not l.is_contiguous() or tuple(l.shape) != (B, H, N):
         raise ValueError("lse must be contiguous float32 (B, H, N)")
     desc, _keep = _mask_desc(mask, index, N)
-    code = lib().flash_msa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                               l.data_ptr(), B, H, N, d, float(scale or 0.0),
-                               ctypes.byref(desc) if desc is not None else None,
-                               _stream_ptr(stream))
+    dptr = ctypes.byref(desc) if desc is not None else None
+    if Hkv == H:
+        code = lib().flash_msa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                   l.data_ptr(), B, H, N, d, float(scale or 0.0), dptr,
+                                   _stream_ptr(stream))
+    else:
+        code = lib().flash_msa_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                       l.data_ptr(), B, H, Hkv, N, d, float(scale or 0.0), dptr,
+                                       _stream_ptr(stream))
     _check(code, "flash_msa_fwd")
     return o, l
 
@@ -287,13 +309,18 @@ def bwd(q, k, v, o, lse, do, mask: Optional[Mask] = None, index: Optional[BlockI
     three launches through flash_msa_bwd_stages; default: all of them."""
     _check_qkv("q", q)
     B, N, H, d = q.shape
-    for name, t in (("k", k), ("v", v), ("o", o), ("do", do)):
+    kv_shape = _kv_shape(q, k)
+    Hkv = kv_shape[2]
+    _check_qkv("v", v, kv_shape)
+    for name, t in (("o", o), ("do", do)):
         _check_qkv(name, t, q.shape)
     if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (B, H, N):
         raise ValueError("lse must be contiguous float32 (B, H, N)")
+    if Hkv != H and stages is not None:
+        raise ValueError("stages are available for equal query / key-value head counts only")
     dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(q) if dk is None else dk
-    dv = torch.empty_like(q) if dv is None else dv
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
     ws_bytes = bwd_workspace_bytes(B, H, N, d)
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
@@ -302,7 +329,9 @@ def bwd(q, k, v, o, lse, do, mask: Optional[Mask] = None, index: Optional[BlockI
             do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d,
             float(scale or 0.0), ctypes.byref(desc) if desc is not None else None,
             workspace.data_ptr(), workspace.numel() * workspace.element_size())
-    if stages is None:
+    if Hkv != H:
+        code = lib().flash_msa_bwd_gqa(*args[:11], Hkv, *args[11:], _stream_ptr(stream))  # after H
+    elif stages is None:
         code = lib().flash_msa_bwd(*args, _stream_ptr(stream))
     else:
         code = lib().flash_msa_bwd_stages(*args, stages, _stream_ptr(stream))

@@ -301,12 +301,15 @@ flash_msa_status flash_msa_check_block_index(const flash_msa_block_index* ix, in
   return FLASH_MSA_OK;
 }
 
-flash_msa_status flash_msa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
-                               int B, int H, int64_t N, int d, float scale,
-                               const flash_msa_mask_desc* mask, void* stream) {
+static flash_msa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse,
+                                 int B, int H, int Hkv, int64_t N, int d, float scale,
+                                 const flash_msa_mask_desc* mask, void* stream) {
   g_last_error[0] = 0;
   flash_msa_status st = check_dims(B, H, N, d);
   if (st != FLASH_MSA_OK) return st;
+  if (Hkv < 1 || H % Hkv != 0)
+    return set_error(FLASH_MSA_ERR_INVALID_ARG, "key/value heads %d must divide query heads %d",
+                     Hkv, H);
   if (!q || !k || !v || !o || !lse)
     return set_error(FLASH_MSA_ERR_INVALID_ARG, "fwd: null tensor pointer");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
@@ -325,12 +328,25 @@ flash_msa_status flash_msa_fwd(const void* q, const void* k, const void* v, void
   a.lse = lse;
   a.B = B;
   a.H = H;
+  a.Hkv = Hkv;
   a.d = d;
   a.N = N;
   a.scale = resolve_scale(scale, d);
   a.status = status_word_ptr();
   if (!a.status) return set_cuda_error("status word");
   return launch_fwd(a, static_cast<cudaStream_t>(stream));
+}
+
+flash_msa_status flash_msa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                               int B, int H, int64_t N, int d, float scale,
+                               const flash_msa_mask_desc* mask, void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, H, N, d, scale, mask, stream);
+}
+
+flash_msa_status flash_msa_fwd_gqa(const void* q, const void* k, const void* v, void* o,
+                                   float* lse, int B, int H, int Hkv, int64_t N, int d,
+                                   float scale, const flash_msa_mask_desc* mask, void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, Hkv, N, d, scale, mask, stream);
 }
 
 size_t flash_msa_bwd_workspace_bytes(int B, int H, int64_t N, int d) {
@@ -353,16 +369,19 @@ flash_msa_status flash_msa_bwd(const void* q, const void* k, const void* v, cons
                               stream);
 }
 
-flash_msa_status flash_msa_bwd_stages(const void* q, const void* k, const void* v, const void* o,
-                                      const float* lse, const void* dO, void* dq, void* dk,
-                                      void* dv, int B, int H, int64_t N, int d, float scale,
-                                      const flash_msa_mask_desc* mask, void* workspace,
-                                      size_t workspace_bytes, unsigned stages, void* stream) {
+static flash_msa_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
+                                 const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                                 int B, int H, int Hkv, int64_t N, int d, float scale,
+                                 const flash_msa_mask_desc* mask, void* workspace,
+                                 size_t workspace_bytes, unsigned stages, void* stream) {
   g_last_error[0] = 0;
   if (stages == 0 || (stages & ~7u))
     return set_error(FLASH_MSA_ERR_INVALID_ARG, "bwd: stages must be a non-empty subset of 1|2|4");
   flash_msa_status st = check_dims(B, H, N, d);
   if (st != FLASH_MSA_OK) return st;
+  if (Hkv < 1 || H % Hkv != 0)
+    return set_error(FLASH_MSA_ERR_INVALID_ARG, "key/value heads %d must divide query heads %d",
+                     Hkv, H);
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv)
     return set_error(FLASH_MSA_ERR_INVALID_ARG, "bwd: null tensor pointer");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
@@ -390,6 +409,7 @@ flash_msa_status flash_msa_bwd_stages(const void* q, const void* k, const void* 
   a.dsum = static_cast<float*>(workspace);
   a.B = B;
   a.H = H;
+  a.Hkv = Hkv;
   a.d = d;
   a.N = N;
   a.scale = resolve_scale(scale, d);
@@ -397,6 +417,25 @@ flash_msa_status flash_msa_bwd_stages(const void* q, const void* k, const void* 
   a.stages = stages;
   if (!a.status) return set_cuda_error("status word");
   return launch_bwd(a, static_cast<cudaStream_t>(stream));
+}
+
+flash_msa_status flash_msa_bwd_stages(const void* q, const void* k, const void* v, const void* o,
+                                      const float* lse, const void* dO, void* dq, void* dk,
+                                      void* dv, int B, int H, int64_t N, int d, float scale,
+                                      const flash_msa_mask_desc* mask, void* workspace,
+                                      size_t workspace_bytes, unsigned stages, void* stream) {
+  return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, B, H, H, N, d, scale, mask, workspace,
+                  workspace_bytes, stages, stream);
+}
+
+flash_msa_status flash_msa_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
+                                   const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                                   int B, int H, int Hkv, int64_t N, int d, float scale,
+                                   const flash_msa_mask_desc* mask, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, B, H, Hkv, N, d, scale, mask, workspace,
+                  workspace_bytes,
+                  FLASH_MSA_BWD_PREPROCESS | FLASH_MSA_BWD_DKDV | FLASH_MSA_BWD_DQ, stream);
 }
 
 flash_msa_status flash_msa_get_status(void* stream) {

@@ -93,7 +93,8 @@ struct BwdParams {
   const float* dsum;
   const __nv_bfloat16* q;     // dQ pass: rows staged into TMEM by the elementwise side
   const __nv_bfloat16* dout;
-  int B, H, N, NP;
+  int B, H, N, NP;  // H: query heads
+  int Hkv, G;       // key/value heads, query heads per key/value head
   int n_units;
   float scale, scale_log2;
   MaskParams mask;
@@ -131,12 +132,36 @@ __device__ __forceinline__ void load_tile_2d(const CUtensorMap* m, uint32_t dst,
   for (int c = 0; c < HD / 64; ++c) tma_load_4d(dst + c * (kTile * 128), m, bar, c * 64, row, h, b);
 }
 
+// Units: dK/dV pass (b, key/value head, key block), whose inner tiles are the
+// key block's query-block list repeated for each of the G query heads that
+// share the key/value head; dQ pass (b, query head, query block).
+template <bool kKeyStationary>
+__device__ __forceinline__ Unit bwd_decode(int u, const BwdParams& p) {
+  Unit un = decode_unit(u, kKeyStationary ? p.Hkv : p.H, p.list, p.status);
+  if (kKeyStationary) un.n = un.n0 * p.G;
+  return un;
+}
+
+// Inner tile t of a unit and the query head it belongs to.
+template <bool kKeyStationary>
+__device__ __forceinline__ InnerTile bwd_inner(const Unit& un, int t, const BwdParams& p,
+                                               int& hq) {
+  if (!kKeyStationary) {
+    hq = un.h;
+    return inner_tile(un, t, p.list, p.status);
+  }
+  const int g = p.G == 1 ? 0 : t / un.n0;
+  hq = un.h * p.G + g;
+  return inner_tile(un, t - g * un.n0, p.list, p.status);
+}
+
+template <bool kKeyStationary>
 __device__ __forceinline__ bool next_unit(int& k, Unit& un, const BwdParams& p) {
   while (true) {
     const int u = int(blockIdx.x) + k * int(gridDim.x);
     if (u >= p.n_units) return false;
     ++k;
-    un = decode_unit(u, p.H, p.list, p.status);
+    un = bwd_decode<kKeyStationary>(u, p);
     if (un.n > 0) return true;
   }
 }
@@ -180,7 +205,7 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint8_t* smem, 
   bool ok = true;
   int k = 0;
   Unit un;
-  while (ok && next_unit(k, un, p)) {
+  while (ok && next_unit<kKeyStationary>(k, un, p)) {
     if (kKeyStationary) {
       if (!wait_bar(bar(L::kFixEmpty), (fe_cnt & 1) ^ 1, abort_flag, p.status, 1)) {
         ok = false;
@@ -195,7 +220,9 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint8_t* smem, 
       ++fe_cnt;
     }
     for (int t = 0; t < un.n && ok; ++t) {
-      const InnerTile it = inner_tile(un, t, p.list, p.status);
+      int hq;
+      const InnerTile it = bwd_inner<kKeyStationary>(un, t, p, hq);
+      const int hr = kKeyStationary ? hq : un.h / p.G;  // head of the streamed tiles
       for (int half = 0; half < 2; ++half) {
         const int stage = cnt % L::kStages;
         if (!wait_bar(bar(L::kRingEmpty + stage), ((cnt / L::kStages) & 1) ^ 1, abort_flag,
@@ -207,26 +234,28 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint8_t* smem, 
         if (half == 0) {
           const bool vec = kKeyStationary;
           mbar_arrive_expect_tx(bar(L::kRingFull + stage), L::kTileBytes + (vec ? 1024 : 0));
-          load_tile_2d<HD>(ring_a, dst, bar(L::kRingFull + stage), it.blk * kTile, un.h, un.b);
+          load_tile_2d<HD>(ring_a, dst, bar(L::kRingFull + stage), it.blk * kTile, hr, un.b);
           if (vec) {
-            const int64_t row0 = (int64_t(un.b) * p.H + un.h) * p.NP + int64_t(it.blk) * kTile;
+            const int64_t row0 = (int64_t(un.b) * p.H + hq) * p.NP + int64_t(it.blk) * kTile;
             const uint32_t vdst = smem_u32(smem + L::kVecOff + (stage / 2) * 1024);
             bulk_load(vdst, p.lse2 + row0, 512, bar(L::kRingFull + stage));
             bulk_load(vdst + 512, p.dsum + row0, 512, bar(L::kRingFull + stage));
           }
         } else {
           mbar_arrive_expect_tx(bar(L::kRingFull + stage), L::kTileBytes);
-          load_tile_2d<HD>(ring_b, dst, bar(L::kRingFull + stage), it.blk * kTile, un.h, un.b);
+          load_tile_2d<HD>(ring_b, dst, bar(L::kRingFull + stage), it.blk * kTile, hr, un.b);
         }
         last[stage] = int(cnt);
         ++cnt;
       }
       if (t + kL2PrefetchTiles < un.n) {
-        const InnerTile ft = inner_tile(un, t + kL2PrefetchTiles, p.list, p.status);
+        int fq;
+        const InnerTile ft = bwd_inner<kKeyStationary>(un, t + kL2PrefetchTiles, p, fq);
+        const int fr = kKeyStationary ? fq : un.h / p.G;
 #pragma unroll
         for (int c = 0; c < HD / 64; ++c) {
-          tma_prefetch_l2_4d(ring_a, c * 64, ft.blk * kTile, un.h, un.b);
-          tma_prefetch_l2_4d(ring_b, c * 64, ft.blk * kTile, un.h, un.b);
+          tma_prefetch_l2_4d(ring_a, c * 64, ft.blk * kTile, fr, un.b);
+          tma_prefetch_l2_4d(ring_b, c * 64, ft.blk * kTile, fr, un.b);
         }
       }
     }
@@ -309,7 +338,7 @@ __device__ __forceinline__ void dq_mma(const BwdParams& p, uint8_t* smem, uint64
   bool ok = true;
   int k = 0;
   Unit un;
-  while (ok && next_unit(k, un, p)) {
+  while (ok && next_unit<false>(k, un, p)) {
     if (!wait_bar(bar(L::kFixFull), ff_cnt & 1, abort_flag, p.status, 10)) break;
     ++ff_cnt;
     if (!ring_wait(cnt, 11) || !ring_wait(cnt + 1, 12)) break;
@@ -385,7 +414,7 @@ __device__ __forceinline__ void dkdv_mma(const BwdParams& p, uint8_t* smem, uint
   bool ok = true;
   int k = 0;
   Unit un;
-  while (ok && next_unit(k, un, p)) {
+  while (ok && next_unit<true>(k, un, p)) {
     if (!wait_bar(bar(L::kFixFull), ff_cnt & 1, abort_flag, p.status, 10)) break;
     ++ff_cnt;
     if (!ring_wait(cnt, 11) || !ring_wait(cnt + 1, 12)) break;
@@ -473,11 +502,11 @@ __device__ __forceinline__ void dkdv_elementwise(const BwdParams& p, uint8_t* sm
   for (int k = 0;; ++k) {
     const int u = int(blockIdx.x) + k * int(gridDim.x);
     if (u >= p.n_units) break;
-    const Unit un = decode_unit(u, p.H, p.list, p.status);
+    const Unit un = bwd_decode<true>(u, p);
     const int64_t j = int64_t(un.ob) * kTile + row;  // key token
     const bool valid = j < p.N;
-    __nv_bfloat16* dk_row = p.out_a + ((int64_t(un.b) * p.N + j) * p.H + un.h) * HD;
-    __nv_bfloat16* dv_row = p.out_b + ((int64_t(un.b) * p.N + j) * p.H + un.h) * HD;
+    __nv_bfloat16* dk_row = p.out_a + ((int64_t(un.b) * p.N + j) * p.Hkv + un.h) * HD;
+    __nv_bfloat16* dv_row = p.out_b + ((int64_t(un.b) * p.N + j) * p.Hkv + un.h) * HD;
     if (un.n == 0) {
       if (g == 0) {
         zero_row(dk_row, HD, valid);
@@ -486,7 +515,8 @@ __device__ __forceinline__ void dkdv_elementwise(const BwdParams& p, uint8_t* sm
       continue;
     }
     for (int t = 0; t < un.n; ++t) {
-      const InnerTile it = inner_tile(un, t, p.list, p.status);
+      int hq;
+      const InnerTile it = bwd_inner<true>(un, t, p, hq);
       int lo = 0, hi = kTile - 1;
       if (it.dead) hi = -1;
       else if (it.partial) col_live_range(j, it.blk, un.ob, p.N, p.mask, lo, hi);
@@ -574,7 +604,7 @@ __device__ __forceinline__ void dq_elementwise(const BwdParams& p, uint64_t* bar
   for (int k = 0;; ++k) {
     const int u = int(blockIdx.x) + k * int(gridDim.x);
     if (u >= p.n_units) break;
-    const Unit un = decode_unit(u, p.H, p.list, p.status);
+    const Unit un = bwd_decode<false>(u, p);
     const int64_t i = int64_t(un.ob) * kTile + row;
     const bool valid = i < p.N;
     __nv_bfloat16* dq_row = p.out_a + ((int64_t(un.b) * p.N + i) * p.H + un.h) * HD;
@@ -731,8 +761,8 @@ static flash_msa_status launch_bwd_hd(const BwdLaunch& a, cudaStream_t stream) {
   memset(&p, 0, sizeof(p));
   flash_msa_status st;
   if ((st = make_tile_map(&p.tm_q, a.q, a.B, a.N, a.H, HD)) != FLASH_MSA_OK) return st;
-  if ((st = make_tile_map(&p.tm_k, a.k, a.B, a.N, a.H, HD)) != FLASH_MSA_OK) return st;
-  if ((st = make_tile_map(&p.tm_v, a.v, a.B, a.N, a.H, HD)) != FLASH_MSA_OK) return st;
+  if ((st = make_tile_map(&p.tm_k, a.k, a.B, a.N, a.Hkv, HD)) != FLASH_MSA_OK) return st;
+  if ((st = make_tile_map(&p.tm_v, a.v, a.B, a.N, a.Hkv, HD)) != FLASH_MSA_OK) return st;
   if ((st = make_tile_map(&p.tm_do, a.dout, a.B, a.N, a.H, HD)) != FLASH_MSA_OK) return st;
   p.lse2 = lse2;
   p.dsum = dsum;
@@ -742,7 +772,8 @@ static flash_msa_status launch_bwd_hd(const BwdLaunch& a, cudaStream_t stream) {
   p.H = a.H;
   p.N = int(a.N);
   p.NP = NP;
-  p.n_units = a.B * a.H * nb;
+  p.Hkv = a.Hkv;
+  p.G = a.H / a.Hkv;
   p.scale = a.scale;
   p.scale_log2 = a.scale * kLog2e;
   p.mask = a.mask;
@@ -758,21 +789,22 @@ static flash_msa_status launch_bwd_hd(const BwdLaunch& a, cudaStream_t stream) {
     }
     return FLASH_MSA_OK;
   };
-  const int grid = p.n_units;
   if (a.stages & FLASH_MSA_BWD_DKDV) {
     if ((st = prep(bwd_main_kernel<HD, true>, 0)) != FLASH_MSA_OK) return st;
     p.list = a.cols;
+    p.n_units = a.B * a.Hkv * nb;
     p.out_a = reinterpret_cast<__nv_bfloat16*>(a.dk);
     p.out_b = reinterpret_cast<__nv_bfloat16*>(a.dv);
-    bwd_main_kernel<HD, true><<<grid, kBwdThreads, LK::kSmemBytes, stream>>>(p);
+    bwd_main_kernel<HD, true><<<p.n_units, kBwdThreads, LK::kSmemBytes, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return set_cuda_error("bwd_dkdv launch");
   }
   if (a.stages & FLASH_MSA_BWD_DQ) {
     if ((st = prep(bwd_main_kernel<HD, false>, 1)) != FLASH_MSA_OK) return st;
     p.list = a.rows;
+    p.n_units = a.B * a.H * nb;
     p.out_a = reinterpret_cast<__nv_bfloat16*>(a.dq);
     p.out_b = nullptr;
-    bwd_main_kernel<HD, false><<<grid, kBwdThreads, LQ::kSmemBytes, stream>>>(p);
+    bwd_main_kernel<HD, false><<<p.n_units, kBwdThreads, LQ::kSmemBytes, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return set_cuda_error("bwd_dq launch");
   }
   return FLASH_MSA_OK;

@@ -182,7 +182,8 @@ struct ListParams {
 
 struct Unit {
   int b, h, ob;  // batch, head, outer block
-  int begin, n;  // position in idx[] and number of inner blocks
+  int begin, n;  // position in idx[] and number of inner tiles
+  int n0;        // length of the block list (n = n0 * query heads per unit)
 };
 
 __device__ __forceinline__ Unit decode_unit(int u, int H, const ListParams& L, unsigned* status) {
@@ -219,6 +220,7 @@ __device__ __forceinline__ Unit decode_unit(int u, int H, const ListParams& L, u
     un.begin = 0;
     un.n = L.n_blocks;
   }
+  un.n0 = un.n;
   return un;
 }
 

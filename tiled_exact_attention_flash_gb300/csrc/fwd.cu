@@ -31,6 +31,7 @@ struct FwdParams {
   __nv_bfloat16* o;
   float* lse;
   int B, H, N;
+  int G;  // query heads per key/value head
   int n_units;
   float scale_log2;  // scale * log2(e)
   MaskParams mask;
@@ -171,6 +172,7 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, uint8_t* smem, 
       last_q[s] = int(qe_cnt[s]);
       ++qe_cnt[s];
     }
+    const int hkv = pu.h / p.G;  // key/value head of this query head
     PairWalk w;
     walk_init(w, pu, p.list);
     PairTile t;
@@ -185,7 +187,7 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, uint8_t* smem, 
         mbar_arrive_expect_tx(bar(L::kKvFull + stage), L::kTileBytes);
         load_tile<HD>(kv ? &p.tm_v : &p.tm_k,
                       smem_u32(smem + L::kRingOff + stage * L::kTileBytes),
-                      bar(L::kKvFull + stage), t.kb * kTile, pu.h, pu.b);
+                      bar(L::kKvFull + stage), t.kb * kTile, hkv, pu.b);
         last_kv[stage] = int(kv_cnt);
         ++kv_cnt;
       }
@@ -540,9 +542,10 @@ static flash_msa_status launch_fwd_hd(const FwdLaunch& a, cudaStream_t stream) {
   memset(&p, 0, sizeof(p));
   flash_msa_status st;
   if ((st = make_tile_map(&p.tm_q, a.q, a.B, a.N, a.H, HD)) != FLASH_MSA_OK) return st;
-  if ((st = make_tile_map(&p.tm_k, a.k, a.B, a.N, a.H, HD)) != FLASH_MSA_OK) return st;
-  if ((st = make_tile_map(&p.tm_v, a.v, a.B, a.N, a.H, HD)) != FLASH_MSA_OK) return st;
+  if ((st = make_tile_map(&p.tm_k, a.k, a.B, a.N, a.Hkv, HD)) != FLASH_MSA_OK) return st;
+  if ((st = make_tile_map(&p.tm_v, a.v, a.B, a.N, a.Hkv, HD)) != FLASH_MSA_OK) return st;
   p.o = reinterpret_cast<__nv_bfloat16*>(a.o);
+  p.G = a.H / a.Hkv;
   p.lse = a.lse;
   p.B = a.B;
   p.H = a.H;

@@ -28,6 +28,7 @@ struct FwdLaunch {
   void* o;
   float* lse;
   int B, H, d;
+  int Hkv;          // key/value heads (H % Hkv == 0; query head h reads kv head h / (H / Hkv))
   int64_t N;
   float scale;
   MaskParams mask;
@@ -41,8 +42,9 @@ struct BwdLaunch {
   const void *q, *k, *v, *o, *dout;
   const float* lse;
   void *dq, *dk, *dv;
-  float* dsum;  // workspace: D = rowsum(dO o O), fp32 (B, H, N)
+  float* dsum;  // workspace: [LSE * log2(e) | D], fp32 (B, H, padded N) each
   int B, H, d;
+  int Hkv;      // key/value heads
   int64_t N;
   float scale;
   MaskParams mask;
