@@ -91,8 +91,7 @@ struct BwdParams {
   __nv_bfloat16* out_b;  // dkdv: dV
   const float* lse2;
   const float* dsum;
-  const __nv_bfloat16* q;     // dQ pass: rows staged into TMEM by the elementwise side
-  const __nv_bfloat16* dout;
+  const __nv_bfloat16* dout;  // dQ pass: rows staged into TMEM by the elementwise side
   int B, H, N, NP;  // H: query heads
   int Hkv, G;       // key/value heads, query heads per key/value head
   int n_units;
@@ -112,13 +111,14 @@ struct BwdLayout {
   // dK/dV: even (Q and dO of a tile in consecutive stages share a vector
   // slot); dQ: one more stage of prefetch (no vectors to stage)
   static constexpr int kStages = KS ? (HD == 128 ? 4 : 8) : (HD == 128 ? 6 : 12);
-  static constexpr int kFixOff = 0;  // dK/dV: K and V tiles; dQ: none (Q, dO live in TMEM)
-  static constexpr int kRingOff = KS ? 2 * kTileBytes : 0;
+  static constexpr int kFixOff = 0;  // dK/dV: K and V tiles; dQ: the Q tile (dO lives in TMEM)
+  static constexpr int kRingOff = (KS ? 2 : 1) * kTileBytes;
   static constexpr int kVecOff = kRingOff + kStages * kTileBytes;  // (stages/2) x 1 KB
   static constexpr int kBarOff = kVecOff + (KS ? (kStages / 2) * 1024 : 0);  // vectors: dK/dV only
-  // kSFull / kPFull: two each (dK/dV: one per half-tile buffer; dQ: only [0])
-  static constexpr int kFixFull = 0, kFixEmpty = 1, kSFull = 2, kPFull = 4, kDpFree = 6,
-                       kAccFull = 7, kAccEmpty = 8, kMmaDone = 9, kRingFull = 10,
+  // kSFull / kPFull: two slots each; dK/dV uses [0] of both, dQ uses kSFull
+  // and kDsEmpty (= kSFull + 1, the dS columns of TMEM may be overwritten)
+  static constexpr int kFixFull = 0, kFixEmpty = 1, kSFull = 2, kDsEmpty = 3, kPFull = 4,
+                       kDpFree = 6, kAccFull = 7, kAccEmpty = 8, kMmaDone = 9, kRingFull = 10,
                        kRingEmpty = 10 + kStages;
   static constexpr int kNumBars = 10 + 2 * kStages;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
@@ -169,7 +169,8 @@ __device__ __forceinline__ bool next_unit(int& k, Unit& un, const BwdParams& p) 
 template <int HD, bool KS>
 __device__ __forceinline__ void init_bwd_barriers(uint64_t* bars) {
   using L = BwdLayout<HD, KS>;
-  mbar_init(smem_u32(bars + L::kFixFull), KS ? 1 : kEwWarps);
+  // dQ: the producer's Q tile plus every elementwise warp's rows of dO
+  mbar_init(smem_u32(bars + L::kFixFull), KS ? 1 : 1 + kEwWarps);
   mbar_init(smem_u32(bars + L::kFixEmpty), 1);
   for (int i = 0; i < 2; ++i) {
     mbar_init(smem_u32(bars + L::kSFull + i), 1);
@@ -186,9 +187,9 @@ __device__ __forceinline__ void init_bwd_barriers(uint64_t* bars) {
   fence_mbar_init();
 }
 
-// Producer shared by both kernels.  Per unit: the two stationary tiles
-// (dkdv: K, V of the key block; dq: Q, dO of the query block), then per inner
-// tile two ring stages (dkdv: Q_t + its LSE2/D vectors, dO_t; dq: K_t, V_t).
+// Producer shared by both kernels.  Per unit: the stationary tiles (dkdv: K,
+// V of the key block; dq: Q of the query block), then per inner tile two ring
+// stages (dkdv: Q_t + its LSE2/D vectors, dO_t; dq: K_t, V_t).
 template <int HD, bool kKeyStationary>
 __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint8_t* smem, uint64_t* bars,
                                              volatile int* abort_flag) {
@@ -206,19 +207,29 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint8_t* smem, 
   int k = 0;
   Unit un;
   while (ok && next_unit<kKeyStationary>(k, un, p)) {
+    if (!wait_bar(bar(L::kFixEmpty), (fe_cnt & 1) ^ 1, abort_flag, p.status, 1)) {
+      ok = false;
+      break;
+    }
+    mbar_arrive_expect_tx(bar(L::kFixFull), (kKeyStationary ? 2 : 1) * L::kTileBytes);
+    load_tile_2d<HD>(fix_a, smem_u32(smem + L::kFixOff), bar(L::kFixFull), un.ob * kTile, un.h,
+                     un.b);
     if (kKeyStationary) {
-      if (!wait_bar(bar(L::kFixEmpty), (fe_cnt & 1) ^ 1, abort_flag, p.status, 1)) {
-        ok = false;
-        break;
-      }
-      mbar_arrive_expect_tx(bar(L::kFixFull), 2 * L::kTileBytes);
-      load_tile_2d<HD>(fix_a, smem_u32(smem + L::kFixOff), bar(L::kFixFull), un.ob * kTile, un.h,
-                       un.b);
       load_tile_2d<HD>(fix_b, smem_u32(smem + L::kFixOff + L::kTileBytes), bar(L::kFixFull),
                        un.ob * kTile, un.h, un.b);
-      last_fix = int(fe_cnt);
-      ++fe_cnt;
+    } else {
+      // the elementwise warps read the next unit's dO rows with plain loads:
+      // start pulling them into L2 now
+      const int u_next = int(blockIdx.x) + k * int(gridDim.x);
+      if (u_next < p.n_units) {
+        const Unit nx = bwd_decode<false>(u_next, p);
+#pragma unroll
+        for (int c = 0; c < HD / 64; ++c)
+          tma_prefetch_l2_4d(fix_b, c * 64, nx.ob * kTile, nx.h, nx.b);
+      }
     }
+    last_fix = int(fe_cnt);
+    ++fe_cnt;
     for (int t = 0; t < un.n && ok; ++t) {
       int hq;
       const InnerTile it = bwd_inner<kKeyStationary>(un, t, p, hq);
@@ -280,11 +291,11 @@ __device__ __forceinline__ void warp_arrive(uint32_t bar) {
 // k-step, 64-column chunks 16 KB apart.
 template <int HD>
 __device__ __forceinline__ void mma_kmajor(uint32_t d, uint32_t a, uint32_t b, uint32_t idesc) {
+  const uint32_t ad = sdesc_lo(a, 16), bd = sdesc_lo(b, 16);
 #pragma unroll
   for (int kk = 0; kk < HD / 16; ++kk) {
-    const uint32_t off = (kk / 4) * (kTile * 128) + (kk % 4) * 32;
-    mma_ss(d, sdesc_sw128(a + off, 16, 1024), sdesc_sw128(b + off, 16, 1024), idesc,
-           kk > 0 ? 1u : 0u);
+    const uint32_t off = ((kk / 4) * (kTile * 128) + (kk % 4) * 32) >> 4;
+    mma_ss(d, ad + off, bd + off, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -295,21 +306,21 @@ __device__ __forceinline__ void mma_kmajor(uint32_t d, uint32_t a, uint32_t b, u
 // a_tmem + 64 (kk / 4) + 8 (kk % 4).
 __device__ __forceinline__ void mma_tmem_a(uint32_t d, uint32_t a_tmem, uint32_t b,
                                            uint32_t idesc, bool accumulate) {
+  const uint32_t bd = sdesc_lo(b, kTile * 128);
 #pragma unroll
-  for (int kk = 0; kk < kTile / 16; ++kk) {
-    const uint64_t bd = sdesc_sw128(b + kk * 2048, kTile * 128, 1024);
-    mma_ts(d, a_tmem + (kk / 4) * 64 + (kk % 4) * 8, bd, idesc, (accumulate || kk > 0) ? 1u : 0u);
-  }
+  for (int kk = 0; kk < kTile / 16; ++kk)
+    mma_ts(d, a_tmem + (kk / 4) * 64 + (kk % 4) * 8, bd + kk * (2048 >> 4), idesc,
+           (accumulate || kk > 0) ? 1u : 0u);
 }
 
-// MMA issuer of bwd_dq (query-stationary; Q and dO of the query block live
-// in TMEM, written there by the elementwise warpgroups; ring K_t, V_t).
-// TMEM: S at [0,128), dP at [128,256), dQ at [256, 256+d), Q (bf16 pairs)
-// at [384, 384+d/2), dO at [448, 448+d/2).  S and dP use Q / dO as TMEM
-// operands, so only K_t / V_t are read from shared memory.  Order per key
-// tile t:  [dP free(t)] dP(t+1);  [P full(t)] dQ(t), release K_t / V_t;
-// S(t+1) -> s_full(t+1)  (dS(t) in the S columns is read before S(t+1)
-// overwrites them: tcgen05 products run in issue order).
+// MMA issuer of bwd_dq (query-stationary; Q of the query block in shared
+// memory, its dO in TMEM written by the elementwise warpgroups; ring K_t, V_t).
+// TMEM: S at [0,128), dP at [128,256), dQ at [256, 256+d), dS (bf16 pairs)
+// at [384,448), dO (bf16 pairs) at [448, 448+d/2).  The elementwise side
+// pulls S(t) and dP(t) into registers first (sdp_free), so the next tile's
+// products run while it computes dS(t).  Order per key tile t:
+//   [sdp_free(t)] S(t+1), dP(t+1) -> s_full(t+1), release V_(t+1);
+//   [P full(t)] dQ += dS(t) K_t -> ds_empty, release K_t.
 template <int HD>
 __device__ __forceinline__ void dq_mma(const BwdParams& p, uint8_t* smem, uint64_t* bars,
                                        uint32_t tmem, volatile int* abort_flag) {
@@ -318,7 +329,8 @@ __device__ __forceinline__ void dq_mma(const BwdParams& p, uint8_t* smem, uint64
   constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);
   constexpr uint32_t kIdAcc = idesc_bf16_f32(128, HD, false, true);
   const uint32_t tS = tmem, tDP = tmem + 128, tDQ = tmem + 256;
-  const uint32_t tQ = tmem + 384, tDO = tmem + 448;
+  const uint32_t tDS = tmem + 384, tDO = tmem + 448;
+  const uint32_t fq = smem_u32(smem + L::kFixOff);
   auto stage_addr = [&](uint32_t c) {
     return smem_u32(smem + L::kRingOff + (c % L::kStages) * L::kTileBytes);
   };
@@ -326,35 +338,45 @@ __device__ __forceinline__ void dq_mma(const BwdParams& p, uint8_t* smem, uint64
     return wait_bar(bar(L::kRingFull + c % L::kStages), (c / L::kStages) & 1, abort_flag,
                     p.status, where);
   };
-  // D = A[tmem, K-major pairs] * B[smem K-major]^T over the head dimension
-  auto mma_tmem_k = [&](uint32_t d, uint32_t a_tmem, uint32_t b) {
+  // S = Q K^T (both operands in shared memory), dP = dO[tmem] V^T, for the
+  // tile whose K is in ring slot c and V in slot c + 1
+  auto issue_sdp = [&](uint32_t c) {
+    mma_kmajor<HD>(tS, fq, stage_addr(c), kIdS);
+    const uint32_t vd = sdesc_lo(stage_addr(c + 1), 16);
 #pragma unroll
     for (int kk = 0; kk < HD / 16; ++kk) {
-      const uint32_t off = (kk / 4) * (kTile * 128) + (kk % 4) * 32;
-      mma_ts(d, a_tmem + kk * 8, sdesc_sw128(b + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+      const uint32_t off = ((kk / 4) * (kTile * 128) + (kk % 4) * 32) >> 4;
+      mma_ts(tDP, tDO + kk * 8, vd + off, kIdS, kk > 0 ? 1u : 0u);
     }
+    mma_commit(bar(L::kSFull));
+    mma_commit(bar(L::kRingEmpty + (c + 1) % L::kStages));  // V_t is not read again
   };
-  uint32_t cnt = 0, ff_cnt = 0, pf_cnt = 0, dpf_cnt = 0, ae_cnt = 0;
-  bool ok = true;
+  uint32_t cnt = 0, ff_cnt = 0, pf_cnt = 0, sdp_cnt = 0, ae_cnt = 0;
+  bool ok = true, pending_sdp = false;
   int k = 0;
   Unit un;
   while (ok && next_unit<false>(k, un, p)) {
     if (!wait_bar(bar(L::kFixFull), ff_cnt & 1, abort_flag, p.status, 10)) break;
     ++ff_cnt;
     if (!ring_wait(cnt, 11) || !ring_wait(cnt + 1, 12)) break;
+    // the previous unit's last S / dP must be in registers before S(0) and
+    // dP(0) overwrite them
+    if (pending_sdp) {
+      if (!wait_bar(bar(L::kDpFree), sdp_cnt & 1, abort_flag, p.status, 15)) break;
+      ++sdp_cnt;
+    }
     tc_fence_after();
-    mma_tmem_k(tS, tQ, stage_addr(cnt));          // S(0)
-    mma_tmem_k(tDP, tDO, stage_addr(cnt + 1));    // dP(0)
-    mma_commit(bar(L::kSFull));
+    issue_sdp(cnt);
+    if (un.n == 1) mma_commit(bar(L::kFixEmpty));  // Q and dO are not read again
     for (int t = 0; t < un.n && ok; ++t) {
       const uint32_t c = cnt + 2 * t;  // K_t at c, V_t at c + 1
-      const bool more = t + 1 < un.n;
-      if (more) {
+      if (t + 1 < un.n) {
         if (!ring_wait(c + 2, 11) || !ring_wait(c + 3, 12)) { ok = false; break; }
-        if (!wait_bar(bar(L::kDpFree), dpf_cnt & 1, abort_flag, p.status, 15)) { ok = false; break; }
-        ++dpf_cnt;
+        if (!wait_bar(bar(L::kDpFree), sdp_cnt & 1, abort_flag, p.status, 15)) { ok = false; break; }
+        ++sdp_cnt;
         tc_fence_after();
-        mma_tmem_k(tDP, tDO, stage_addr(c + 3));  // dP(t+1)
+        issue_sdp(c + 2);
+        if (t + 2 == un.n) mma_commit(bar(L::kFixEmpty));
       }
       if (t == 0) {
         if (!wait_bar(bar(L::kAccEmpty), (ae_cnt & 1) ^ 1, abort_flag, p.status, 13)) { ok = false; break; }
@@ -363,21 +385,19 @@ __device__ __forceinline__ void dq_mma(const BwdParams& p, uint8_t* smem, uint64
       if (!wait_bar(bar(L::kPFull), pf_cnt & 1, abort_flag, p.status, 14)) { ok = false; break; }
       ++pf_cnt;
       tc_fence_after();
-      mma_tmem_a(tDQ, tS, stage_addr(c), kIdAcc, t > 0);
+      // dQ (+)= dS K_t: dS from TMEM (k-step kk = keys [16 kk, 16 kk + 16) =
+      // columns tDS + 8 kk), K_t as an MN-major B operand
+      const uint32_t kd = sdesc_lo(stage_addr(c), kTile * 128);
+#pragma unroll
+      for (int kk = 0; kk < kTile / 16; ++kk)
+        mma_ts(tDQ, tDS + kk * 8, kd + kk * (2048 >> 4), kIdAcc, (t > 0 || kk > 0) ? 1u : 0u);
+      mma_commit(bar(L::kDsEmpty));
       mma_commit(bar(L::kRingEmpty + c % L::kStages));
-      mma_commit(bar(L::kRingEmpty + (c + 1) % L::kStages));
-      if (more) {
-        mma_tmem_k(tS, tQ, stage_addr(c + 2));  // S(t+1)
-        mma_commit(bar(L::kSFull));
-      }
     }
     if (!ok) break;
-    // the last tile's dP was pulled by the elementwise side: consume its dp_free
-    if (!wait_bar(bar(L::kDpFree), dpf_cnt & 1, abort_flag, p.status, 15)) break;
-    ++dpf_cnt;
     cnt += 2 * un.n;
-    mma_commit(bar(L::kFixEmpty));  // Q / dO columns may be overwritten
     mma_commit(bar(L::kAccFull));
+    pending_sdp = true;
   }
   mma_commit(bar(L::kMmaDone));
   drain_bar(bar(L::kMmaDone), 0);
@@ -587,9 +607,12 @@ __device__ __forceinline__ void dkdv_elementwise(const BwdParams& p, uint8_t* sm
 }
 
 // Elementwise warpgroups of bwd_dq: thread = query row i of the query tile,
-// warpgroup g = key columns [64 g, 64 g + 64).  dP is pulled into registers
-// first (releasing its TMEM for the next tile's product), then S is processed
-// in 32-column chunks; dS (bf16) goes to the start of the warpgroup's range.
+// warpgroup g = key columns [64 g, 64 g + 64).  Per unit the warpgroups first
+// write the row's dO into TMEM (warpgroup g: head-dimension half g).  Per key
+// tile, S and dP are pulled into registers at once (releasing both regions
+// for the next tile's products), dS is computed there and written as bf16
+// to the dS columns.  The next unit's dO is staged before this unit's dQ is
+// stored, so the next unit's first products overlap the store.
 template <int HD>
 __device__ __forceinline__ void dq_elementwise(const BwdParams& p, uint64_t* bars, uint32_t tmem,
                                                int g, volatile int* abort_flag) {
@@ -598,92 +621,113 @@ __device__ __forceinline__ void dq_elementwise(const BwdParams& p, uint64_t* bar
   const int wq = int(warp_id()) & 3;
   const int row = wq * 32 + int(lane_id());
   const uint32_t lane_off = uint32_t(wq * 32) << 16;
-  const uint32_t tDP = tmem + lane_off + 128 + 64 * g, tDQ = tmem + lane_off + 256;
+  const uint32_t tS = tmem + lane_off + 64 * g, tDP = tS + 128, tDQ = tmem + lane_off + 256;
+  const uint32_t tDS = tmem + lane_off + 384 + 32 * g;  // keys [64 g, 64 g + 64) as pairs
+  const uint32_t tDO = tmem + lane_off + 448 + (HD / 4) * g;
   const float sl2 = p.scale_log2;
-  uint32_t sp_cnt = 0, af_cnt = 0, fe_cnt = 0;
-  for (int k = 0;; ++k) {
-    const int u = int(blockIdx.x) + k * int(gridDim.x);
-    if (u >= p.n_units) break;
-    const Unit un = bwd_decode<false>(u, p);
+  uint32_t sp_cnt = 0, af_cnt = 0, fe_cnt = 0, ds_cnt = 0;
+  int k = 0;
+  // next unit with live key tiles; units without any get zero dQ rows here
+  auto next = [&](Unit& un) -> bool {
+    while (true) {
+      const int u = int(blockIdx.x) + k * int(gridDim.x);
+      if (u >= p.n_units) return false;
+      ++k;
+      un = bwd_decode<false>(u, p);
+      if (un.n > 0) return true;
+      const int64_t i = int64_t(un.ob) * kTile + row;
+      if (g == 0)
+        zero_row(p.out_a + ((int64_t(un.b) * p.N + i) * p.H + un.h) * HD, HD, i < p.N);
+    }
+  };
+  // this row's dO half into TMEM (after the previous unit's last dP has
+  // been computed), its LSE * log2(e) and D into l2 / di
+  auto stage_unit = [&](const Unit& un, float& l2, float& di) -> bool {
     const int64_t i = int64_t(un.ob) * kTile + row;
     const bool valid = i < p.N;
-    __nv_bfloat16* dq_row = p.out_a + ((int64_t(un.b) * p.N + i) * p.H + un.h) * HD;
-    if (un.n == 0) {
-      if (g == 0) zero_row(dq_row, HD, valid);
-      continue;
-    }
-    {  // this row of Q (warpgroup 0) or dO (warpgroup 1) into TMEM as bf16 pairs
-      const bool ok = wait_bar(bar(L::kFixEmpty), (fe_cnt & 1) ^ 1, abort_flag, p.status, 22);
-      if (!__all_sync(0xFFFFFFFFu, ok)) return;
-      ++fe_cnt;
-      const __nv_bfloat16* src = (g == 0 ? p.q : p.dout) +
-                                 ((int64_t(un.b) * p.N + i) * p.H + un.h) * HD;
-      uint32_t rw[HD / 2];
+    const uint4* src = reinterpret_cast<const uint4*>(
+        p.dout + ((int64_t(un.b) * p.N + i) * p.H + un.h) * HD + (HD / 2) * g);
+    uint32_t rw[HD / 4];
 #pragma unroll
-      for (int j = 0; j < HD / 8; ++j) {
-        const uint4 v = valid ? reinterpret_cast<const uint4*>(src)[j] : make_uint4(0, 0, 0, 0);
-        rw[4 * j] = v.x;
-        rw[4 * j + 1] = v.y;
-        rw[4 * j + 2] = v.z;
-        rw[4 * j + 3] = v.w;
-      }
-      const uint32_t dst = tmem + lane_off + 384 + 64 * g;
-#pragma unroll
-      for (int j = 0; j < HD / 64; ++j)
-        tmem_st_x32(dst + 32 * j, *reinterpret_cast<uint32_t(*)[32]>(rw + 32 * j));
-      tmem_wait_st();
-      warp_arrive(bar(L::kFixFull));
+    for (int j = 0; j < HD / 16; ++j) {
+      const uint4 v = valid ? src[j] : make_uint4(0, 0, 0, 0);
+      rw[4 * j] = v.x;
+      rw[4 * j + 1] = v.y;
+      rw[4 * j + 2] = v.z;
+      rw[4 * j + 3] = v.w;
     }
-    const int64_t vrow = (int64_t(un.b) * p.H + un.h) * p.NP + i;
-    const float l2 = p.lse2[vrow];
-    const float di = p.dsum[vrow];
-    for (int t = 0; t < un.n; ++t) {
-      const InnerTile it = inner_tile(un, t, p.list, p.status);
+    const int64_t vrow = (int64_t(un.b) * p.H + un.h) * p.NP + i;  // i < NP always
+    l2 = p.lse2[vrow];
+    di = p.dsum[vrow];
+    const bool ok = wait_bar(bar(L::kFixEmpty), (fe_cnt & 1) ^ 1, abort_flag, p.status, 22);
+    if (!__all_sync(0xFFFFFFFFu, ok)) return false;
+    ++fe_cnt;
+    tc_fence_after();
+    if constexpr (HD == 128) tmem_st_x32(tDO, rw);
+    else tmem_st_x16(tDO, rw);
+    tmem_wait_st();
+    warp_arrive(bar(L::kFixFull));
+    return true;
+  };
+  Unit cur;
+  bool has = next(cur);
+  float l2 = 0.f, di = 0.f;
+  if (has && !stage_unit(cur, l2, di)) return;
+  while (has) {
+    const int64_t i = int64_t(cur.ob) * kTile + row;
+    for (int t = 0; t < cur.n; ++t) {
+      const InnerTile it = inner_tile(cur, t, p.list, p.status);
       int lo = 0, hi = kTile - 1;
       if (it.dead) hi = -1;
-      else if (it.partial) row_live_range(i, un.ob, it.blk, p.N, p.mask, lo, hi);
-      const bool ok = wait_bar(bar(L::kSFull), sp_cnt & 1, abort_flag, p.status, 20);
+      else if (it.partial) row_live_range(i, cur.ob, it.blk, p.N, p.mask, lo, hi);
+      bool ok = wait_bar(bar(L::kSFull), sp_cnt & 1, abort_flag, p.status, 20);
       if (!__all_sync(0xFFFFFFFFu, ok)) return;
       ++sp_cnt;
       tc_fence_after();
-      uint32_t dpr[64];
-      tmem_ld_x64(tDP, dpr);
-      warp_arrive(bar(L::kDpFree));
-      const uint32_t tS = tmem + lane_off + 64 * g;
+      uint32_t sv[64], dpv[64];
+      tmem_ld_x64x2(tS, tDP, sv, dpv);
+      warp_arrive(bar(L::kDpFree));  // S and dP of this tile are in registers
       const bool masked = it.partial || it.dead;
+      uint32_t dd[32];
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        uint32_t s[32], dd[16];
-        tmem_ld_x32(tS + ch * 32, s);
-        const int c0 = 64 * g + ch * 32;
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float x0, x1, p0, p1, u0, u1, d0, d1;
-          fma2(x0, x1, __uint_as_float(s[e]), __uint_as_float(s[e + 1]), sl2, sl2, -l2, -l2);
-          p0 = ex2_approx(x0);
-          p1 = ex2_approx(x1);
-          if (masked) {
-            if (c0 + e < lo || c0 + e > hi) p0 = 0.f;
-            if (c0 + e + 1 < lo || c0 + e + 1 > hi) p1 = 0.f;
-          }
-          sub2(u0, u1, __uint_as_float(dpr[ch * 32 + e]), __uint_as_float(dpr[ch * 32 + e + 1]),
-               di, di);
-          mul2(d0, d1, p0, p1, u0, u1);
-          dd[e / 2] = pack_bf16x2(d0, d1);
+      for (int e = 0; e < 64; e += 2) {
+        float x0, x1, p0, p1, u0, u1, d0, d1;
+        fma2(x0, x1, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), sl2, sl2, -l2, -l2);
+        p0 = ex2_approx(x0);
+        p1 = ex2_approx(x1);
+        if (masked) {
+          if (64 * g + e < lo || 64 * g + e > hi) p0 = 0.f;
+          if (64 * g + e + 1 < lo || 64 * g + e + 1 > hi) p1 = 0.f;
         }
-        tmem_st_x16(tS + ch * 16, dd);  // columns already read
+        sub2(u0, u1, __uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1]), di, di);
+        mul2(d0, d1, p0, p1, u0, u1);
+        dd[e / 2] = pack_bf16x2(d0, d1);
       }
+      ok = wait_bar(bar(L::kDsEmpty), (ds_cnt & 1) ^ 1, abort_flag, p.status, 23);
+      if (!__all_sync(0xFFFFFFFFu, ok)) return;
+      ++ds_cnt;
+      tc_fence_after();
+      tmem_st_x32(tDS, dd);
       tmem_wait_st();
       warp_arrive(bar(L::kPFull));
     }
+    Unit nxt;
+    float nl2 = 0.f, ndi = 0.f;
+    const bool has_next = next(nxt);
+    if (has_next && !stage_unit(nxt, nl2, ndi)) return;
     const bool ok = wait_bar(bar(L::kAccFull), af_cnt & 1, abort_flag, p.status, 21);
     if (!__all_sync(0xFFFFFFFFu, ok)) return;
     ++af_cnt;
     tc_fence_after();
+    __nv_bfloat16* dq_row = p.out_a + ((int64_t(cur.b) * p.N + i) * p.H + cur.h) * HD;
 #pragma unroll
     for (int c = g * (HD / 64); c < (g + 1) * (HD / 64); ++c)
-      store_row_chunk(tDQ + c * 32, p.scale, dq_row + c * 32, valid);
+      store_row_chunk(tDQ + c * 32, p.scale, dq_row + c * 32, i < p.N);
     warp_arrive(bar(L::kAccEmpty));
+    cur = nxt;
+    has = has_next;
+    l2 = nl2;
+    di = ndi;
   }
 }
 
@@ -766,7 +810,6 @@ static flash_msa_status launch_bwd_hd(const BwdLaunch& a, cudaStream_t stream) {
   if ((st = make_tile_map(&p.tm_do, a.dout, a.B, a.N, a.H, HD)) != FLASH_MSA_OK) return st;
   p.lse2 = lse2;
   p.dsum = dsum;
-  p.q = reinterpret_cast<const __nv_bfloat16*>(a.q);
   p.dout = reinterpret_cast<const __nv_bfloat16*>(a.dout);
   p.B = a.B;
   p.H = a.H;

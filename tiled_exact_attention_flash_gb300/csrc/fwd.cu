@@ -213,15 +213,14 @@ __device__ __forceinline__ void fwd_mma(const FwdParams& p, uint8_t* smem, uint6
   bool ok = true;
   // S_s = Q_s K^T for the K tile in ring stage `stage`
   auto issue_qk = [&](int s, int stage) {
-    const uint32_t qa = smem_u32(smem + L::kQOff + s * L::kTileBytes);
-    const uint32_t ka = ring + stage * L::kTileBytes;
+    const uint32_t qd = sdesc_lo(smem_u32(smem + L::kQOff + s * L::kTileBytes), 16);
+    const uint32_t kd = sdesc_lo(ring + stage * L::kTileBytes, 16);
 #pragma unroll
     for (int kk = 0; kk < HD / 16; ++kk) {
       // A = Q, B = K, both K-major: 16-element k-steps are 32 bytes apart
       // inside a 128-byte swizzle row, 64-element chunks 16 KB apart
-      const uint32_t off = (kk / 4) * (kTile * 128) + (kk % 4) * 32;
-      mma_ss(tmem + uint32_t(s * 256), sdesc_sw128(qa + off, 16, 1024),
-             sdesc_sw128(ka + off, 16, 1024), kIdQK, kk > 0 ? 1u : 0u);
+      const uint32_t off = ((kk / 4) * (kTile * 128) + (kk % 4) * 32) >> 4;
+      mma_ss(tmem + uint32_t(s * 256), qd + off, kd + off, kIdQK, kk > 0 ? 1u : 0u);
     }
     mma_commit(bar(L::kSFull + s));
   };
@@ -289,13 +288,13 @@ __device__ __forceinline__ void fwd_mma(const FwdParams& p, uint8_t* smem, uint6
             ++oe_cnt[s];
           }
           tc_fence_after();
-          const uint32_t vb = ring + vs * L::kTileBytes;
+          // B = V tile, MN-major: 64-column chunks 16 KB apart, 8-row groups
+          // 1 KB apart, 16 rows (2 KB) per k-step
+          const uint32_t vd = sdesc_lo(ring + vs * L::kTileBytes, kTile * 128);
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            // B = V tile, MN-major: 64-column chunks 16 KB apart, 8-row groups 1 KB apart
-            const uint64_t bd = sdesc_sw128(vb + kk * 2048, kTile * 128, 1024);
-            mma_ts(tS + 128, tS + kk * 8, bd, kIdPV, (seen[s] > 0 || kk > 0) ? 1u : 0u);
-          }
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_ts(tS + 128, tS + kk * 8, vd + kk * (2048 >> 4), kIdPV,
+                   (seen[s] > 0 || kk > 0) ? 1u : 0u);
           ++seen[s];
           if (seen[s] == pu.n[s]) mma_commit(bar(L::kOFull + s));
         }
