@@ -552,9 +552,13 @@ __device__ __forceinline__ void dkdv_elementwise(const BwdParams& p, uint8_t* sm
       const uint32_t tSr = tmem + lane_off + uint32_t(t & 1) * 128 + 64 * g;
       const uint32_t tDr = tmem + lane_off + uint32_t((t + 1) & 1) * 128 + 64 * g;
       uint32_t sv[64], dpv[64];
-      tmem_ld_x64(tSr, sv);
-      tmem_ld_x64(tDr, dpv);
+      tmem_ld_x64x2(tSr, tDr, sv, dpv);
       warp_arrive(bar(L::kDpFree));  // both regions' old contents are in registers now
+      if (masked) {  // dead entries: S^T = -inf, so P^T = 0 below (scale > 0)
+#pragma unroll
+        for (int e = 0; e < 64; ++e)
+          if (64 * g + e < lo || 64 * g + e > hi) sv[e] = kNegInfBits;
+      }
       uint32_t pp[32], dd[32];
       float4 l4n = *reinterpret_cast<const float4*>(vec + 64 * g);
       float4 d4n = *reinterpret_cast<const float4*>(vec + 128 + 64 * g);
@@ -575,10 +579,6 @@ __device__ __forceinline__ void dkdv_elementwise(const BwdParams& p, uint8_t* sm
                -l2[e], -l2[e + 1]);
           p0 = ex2_approx(x0);
           p1 = ex2_approx(x1);
-          if (masked) {
-            if (c0 + e < lo || c0 + e > hi) p0 = 0.f;
-            if (c0 + e + 1 < lo || c0 + e + 1 > hi) p1 = 0.f;
-          }
           sub2(u0, u1, __uint_as_float(dpv[x + e]), __uint_as_float(dpv[x + e + 1]), dv[e],
                dv[e + 1]);
           mul2(d0, d1, p0, p1, u0, u1);
@@ -687,7 +687,11 @@ __device__ __forceinline__ void dq_elementwise(const BwdParams& p, uint64_t* bar
       uint32_t sv[64], dpv[64];
       tmem_ld_x64x2(tS, tDP, sv, dpv);
       warp_arrive(bar(L::kDpFree));  // S and dP of this tile are in registers
-      const bool masked = it.partial || it.dead;
+      if (it.partial || it.dead) {  // dead entries: S = -inf, so P = 0 below (scale > 0)
+#pragma unroll
+        for (int e = 0; e < 64; ++e)
+          if (64 * g + e < lo || 64 * g + e > hi) sv[e] = kNegInfBits;
+      }
       uint32_t dd[32];
 #pragma unroll
       for (int e = 0; e < 64; e += 2) {
@@ -695,10 +699,6 @@ __device__ __forceinline__ void dq_elementwise(const BwdParams& p, uint64_t* bar
         fma2(x0, x1, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), sl2, sl2, -l2, -l2);
         p0 = ex2_approx(x0);
         p1 = ex2_approx(x1);
-        if (masked) {
-          if (64 * g + e < lo || 64 * g + e > hi) p0 = 0.f;
-          if (64 * g + e + 1 < lo || 64 * g + e + 1 > hi) p1 = 0.f;
-        }
         sub2(u0, u1, __uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1]), di, di);
         mul2(d0, d1, p0, p1, u0, u1);
         dd[e / 2] = pack_bf16x2(d0, d1);

@@ -10,6 +10,7 @@
 namespace fmsa {
 
 constexpr int kTile = 128;                 // query / key tile edge (tokens)
+constexpr uint32_t kNegInfBits = 0xFF800000u;  // fp32 -inf: a dead score
 constexpr uint64_t kWaitLimitNs = 500ull * 1000ull * 1000ull;  // any single wait: 0.5 s
 constexpr uint64_t kDrainLimitNs = 50ull * 1000ull * 1000ull;  // draining copies after an abort
 constexpr int64_t kUnbounded = int64_t(1) << 40;

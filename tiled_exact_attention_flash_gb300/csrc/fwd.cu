@@ -55,7 +55,6 @@ struct FwdLayout {
 };
 
 constexpr int kFwdThreads = 384;
-constexpr uint32_t kNegInfBits = 0xFF800000u;
 
 // Work unit = a pair of query blocks of one (b, h): ranks 2r and 2r + 1 of
 // the longest-first order (for causal and window masks, two neighbouring
