@@ -146,7 +146,7 @@ flash_msa_status flash_msa_fwd(const void* q, const void* k, const void* v, void
                                const flash_msa_mask_desc* mask, void* stream);
 
 /* Bytes of device workspace flash_msa_bwd() needs: two fp32 vectors per
- * (b, h), each padded to whole 128-row tiles -- LSE_i * log2(e) and
+ * (b, h), each padded to whole 128-row tiles -- -LSE_i * log2(e) and
  * D_i = sum_c dO_ic * O_ic -- rounded up to 256 bytes.  0 for invalid sizes. */
 size_t flash_msa_bwd_workspace_bytes(int B, int H, int64_t N, int d);
 

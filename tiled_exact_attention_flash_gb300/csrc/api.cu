@@ -352,7 +352,7 @@ flash_msa_status flash_msa_fwd_gqa(const void* q, const void* k, const void* v, 
 size_t flash_msa_bwd_workspace_bytes(int B, int H, int64_t N, int d) {
   (void)d;
   if (B < 1 || H < 1 || N < 1 || N > kMaxN) return 0;
-  // two fp32 vectors per (b, h) padded to whole 128-row tiles: LSE * log2(e) and D
+  // two fp32 vectors per (b, h) padded to whole 128-row tiles: -LSE * log2(e) and D
   const size_t padded = size_t(n_blocks_of(N)) * kTile;
   const size_t bytes = 2 * size_t(B) * size_t(H) * padded * sizeof(float);
   return (bytes + 255) & ~size_t(255);

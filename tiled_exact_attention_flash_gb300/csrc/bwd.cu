@@ -7,8 +7,8 @@
 // (rowsum(P o dP) = rowsum(dO o O) because O = P V.)
 //
 // Three launches:
-//   bwd_pre   D_i = sum_c dO_ic O_ic and LSE_i * log2(e), padded to whole
-//             128-row tiles (padding rows get LSE = +inf, so P = 0 there)
+//   bwd_pre   D_i = sum_c dO_ic O_ic and -LSE_i * log2(e), padded to whole
+//             128-row tiles (padding rows get -LSE = -inf, so P = 0 there)
 //   bwd_dkdv  key-stationary: per (b, h, key tile) loop over the live query
 //             tiles; S^T = K Q^T and dP^T = V dO^T in TMEM, P^T and dS^T
 //             written back to TMEM as bf16, dV += P^T dO and dK += dS^T Q
@@ -41,7 +41,7 @@ struct PreParams {
   const __nv_bfloat16* o;
   const __nv_bfloat16* dout;
   const float* lse;
-  float* lse2;  // (B, H, NP)
+  float* nlse2;  // (B, H, NP)
   float* dsum;  // (B, H, NP)
   int B, H, N, NP;
 };
@@ -72,12 +72,12 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreParams p) {
   for (int s = kTpr / 2; s > 0; s >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, s, kTpr);
   if (c == 0 && i < p.NP) {
     const int64_t at = (int64_t(b) * p.H + h) * p.NP + i;
-    float l2 = INFINITY;
+    float nl2 = -INFINITY;  // a row without live keys has P = 0, like padding
     if (i < p.N) {
       const float l = p.lse[(int64_t(b) * p.H + h) * p.N + i];
-      l2 = (l == -INFINITY) ? INFINITY : l * kLog2e;
+      nl2 = (l == -INFINITY) ? -INFINITY : -l * kLog2e;
     }
-    p.lse2[at] = l2;
+    p.nlse2[at] = nl2;
     p.dsum[at] = acc;
   }
 }
@@ -89,7 +89,7 @@ struct BwdParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;
   __nv_bfloat16* out_a;  // dkdv: dK, dq: dQ
   __nv_bfloat16* out_b;  // dkdv: dV
-  const float* lse2;
+  const float* nlse2;
   const float* dsum;
   const __nv_bfloat16* dout;  // dQ pass: rows staged into TMEM by the elementwise side
   int B, H, N, NP;  // H: query heads
@@ -115,8 +115,9 @@ struct BwdLayout {
   static constexpr int kRingOff = (KS ? 2 : 1) * kTileBytes;
   static constexpr int kVecOff = kRingOff + kStages * kTileBytes;  // (stages/2) x 1 KB
   static constexpr int kBarOff = kVecOff + (KS ? (kStages / 2) * 1024 : 0);  // vectors: dK/dV only
-  // kSFull / kPFull: two slots each; dK/dV uses [0] of both, dQ uses kSFull
-  // and kDsEmpty (= kSFull + 1, the dS columns of TMEM may be overwritten)
+  // kSFull / kPFull: two slots each.  dK/dV: kSFull, kPFull (P^T written)
+  // and kPFull + 1 (dS^T written); dQ: kSFull, kPFull and kDsEmpty
+  // (= kSFull + 1, the dS columns of TMEM may be overwritten)
   static constexpr int kFixFull = 0, kFixEmpty = 1, kSFull = 2, kDsEmpty = 3, kPFull = 4,
                        kDpFree = 6, kAccFull = 7, kAccEmpty = 8, kMmaDone = 9, kRingFull = 10,
                        kRingEmpty = 10 + kStages;
@@ -249,7 +250,7 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint8_t* smem, 
           if (vec) {
             const int64_t row0 = (int64_t(un.b) * p.H + hq) * p.NP + int64_t(it.blk) * kTile;
             const uint32_t vdst = smem_u32(smem + L::kVecOff + (stage / 2) * 1024);
-            bulk_load(vdst, p.lse2 + row0, 512, bar(L::kRingFull + stage));
+            bulk_load(vdst, p.nlse2 + row0, 512, bar(L::kRingFull + stage));
             bulk_load(vdst + 512, p.dsum + row0, 512, bar(L::kRingFull + stage));
           }
         } else {
@@ -409,9 +410,10 @@ __device__ __forceinline__ void dq_mma(const BwdParams& p, uint8_t* smem, uint64
 // [256, 256+d), dK at [384, 384+d).  The elementwise side pulls its S^T and
 // dP^T columns into registers first (sdp_free), which frees the dP^T region
 // for the next tile's S^T, and then writes P^T and dS^T (bf16) into the
-// S^T region.  Order per tile t:
-//   [sdp_free(t)] S^T(t+1) -> [P full(t)] dV += P^T dO_t, dK += dS^T Q_t,
-//   release Q_t / dO_t, dP^T(t+1) -> s_full(t+1)
+// S^T region, P^T first (p_full) and dS^T second (ds_full).  Order per
+// tile t:
+//   [sdp_free(t)] S^T(t+1) -> [p_full(t)] dV += P^T dO_t, release dO_t ->
+//   [ds_full(t)] dK += dS^T Q_t, release Q_t -> dP^T(t+1) -> s_full(t+1)
 template <int HD>
 __device__ __forceinline__ void dkdv_mma(const BwdParams& p, uint8_t* smem, uint64_t* bars,
                                          uint32_t tmem, volatile int* abort_flag) {
@@ -457,12 +459,14 @@ __device__ __forceinline__ void dkdv_mma(const BwdParams& p, uint8_t* smem, uint
         ++ae_cnt;
       }
       if (!wait_bar(bar(L::kPFull), pf_cnt & 1, abort_flag, p.status, 14)) { ok = false; break; }
-      ++pf_cnt;
       tc_fence_after();
       mma_tmem_a(tDV, region(t), stage_addr(c + 1), kIdAcc, t > 0);       // P^T at +0
+      mma_commit(bar(L::kRingEmpty + (c + 1) % L::kStages));               // dO_t
+      if (!wait_bar(bar(L::kPFull + 1), pf_cnt & 1, abort_flag, p.status, 16)) { ok = false; break; }
+      ++pf_cnt;
+      tc_fence_after();
       mma_tmem_a(tDK, region(t) + 32, stage_addr(c), kIdAcc, t > 0);      // dS^T at +32
-      mma_commit(bar(L::kRingEmpty + c % L::kStages));
-      mma_commit(bar(L::kRingEmpty + (c + 1) % L::kStages));
+      mma_commit(bar(L::kRingEmpty + c % L::kStages));                     // Q_t
       if (more) {
         mma_kmajor<HD>(region(t), fv, stage_addr(c + 3), kIdS);  // dP^T(t+1) -> old S^T region
         mma_commit(bar(L::kSFull));
@@ -504,9 +508,11 @@ __device__ __forceinline__ void zero_row(__nv_bfloat16* dst, int hd, bool valid)
 
 // Elementwise warpgroups of bwd_dkdv: thread = key row j of the key tile,
 // warpgroup g = query columns [64 g, 64 g + 64) of each query tile:
-// P^T = exp2(scale*log2e * S^T - LSE*log2e) on live entries,
+// P^T = exp2(scale*log2e * S^T - LSE*log2e) on live entries, then
 // dS^T = P^T o (dP^T - D).  The bf16 results go to the start of the
-// warpgroup's own column range (columns it has already read).
+// warpgroup's own column range (columns it has already read); P^T is
+// published (p_full) before dS^T is computed (ds_full), so dV of this tile
+// runs on the tensor cores during the second pass.
 template <int HD>
 __device__ __forceinline__ void dkdv_elementwise(const BwdParams& p, uint8_t* smem,
                                                  uint64_t* bars, uint32_t tmem, int g,
@@ -559,38 +565,52 @@ __device__ __forceinline__ void dkdv_elementwise(const BwdParams& p, uint8_t* sm
         for (int e = 0; e < 64; ++e)
           if (64 * g + e < lo || 64 * g + e > hi) sv[e] = kNegInfBits;
       }
-      uint32_t pp[32], dd[32];
-      float4 l4n = *reinterpret_cast<const float4*>(vec + 64 * g);
+      // pass 1: P^T (kept in sv as fp32), bf16 to columns [64 g, 64 g + 32)
+      // of the S^T region, then p_full so that dV += P^T dO starts
+      {
+        uint32_t pp[32];
+        float4 l4n = *reinterpret_cast<const float4*>(vec + 64 * g);
+#pragma unroll
+        for (int x = 0; x < 64; x += 4) {
+          const float4 l4 = l4n;
+          if (x + 4 < 64)  // next group's -LSE, loaded one group ahead
+            l4n = *reinterpret_cast<const float4*>(vec + 64 * g + x + 4);
+          const float nl[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+          for (int e = 0; e < 4; e += 2) {
+            float x0, x1;
+            fma2(x0, x1, __uint_as_float(sv[x + e]), __uint_as_float(sv[x + e + 1]), sl2, sl2,
+                 nl[e], nl[e + 1]);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            sv[x + e] = __float_as_uint(p0);
+            sv[x + e + 1] = __float_as_uint(p1);
+            pp[(x + e) / 2] = pack_bf16x2(p0, p1);
+          }
+        }
+        tmem_st_x32(tSr, pp);
+        tmem_wait_st();
+        warp_arrive(bar(L::kPFull));
+      }
+      // pass 2: dS^T = P^T o (dP^T - D), bf16 to [64 g + 32, 64 g + 64), ds_full
+      uint32_t dd[32];
       float4 d4n = *reinterpret_cast<const float4*>(vec + 128 + 64 * g);
 #pragma unroll
       for (int x = 0; x < 64; x += 4) {
-        const int c0 = 64 * g + x;  // query within the 128-query tile
-        const float4 l4 = l4n, d4 = d4n;
-        if (x + 4 < 64) {  // next group's LSE / D, loaded one group ahead
-          l4n = *reinterpret_cast<const float4*>(vec + c0 + 4);
-          d4n = *reinterpret_cast<const float4*>(vec + 128 + c0 + 4);
-        }
-        const float l2[4] = {l4.x, l4.y, l4.z, l4.w};
+        const float4 d4 = d4n;
+        if (x + 4 < 64) d4n = *reinterpret_cast<const float4*>(vec + 128 + 64 * g + x + 4);
         const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
         for (int e = 0; e < 4; e += 2) {
-          float x0, x1, p0, p1, u0, u1, d0, d1;
-          fma2(x0, x1, __uint_as_float(sv[x + e]), __uint_as_float(sv[x + e + 1]), sl2, sl2,
-               -l2[e], -l2[e + 1]);
-          p0 = ex2_approx(x0);
-          p1 = ex2_approx(x1);
+          float u0, u1, d0, d1;
           sub2(u0, u1, __uint_as_float(dpv[x + e]), __uint_as_float(dpv[x + e + 1]), dv[e],
                dv[e + 1]);
-          mul2(d0, d1, p0, p1, u0, u1);
-          pp[(x + e) / 2] = pack_bf16x2(p0, p1);
+          mul2(d0, d1, __uint_as_float(sv[x + e]), __uint_as_float(sv[x + e + 1]), u0, u1);
           dd[(x + e) / 2] = pack_bf16x2(d0, d1);
         }
       }
-      // P^T to columns [64 g, 64 g + 32), dS^T to [64 g + 32, 64 g + 64) of the S^T region
-      tmem_st_x32(tSr, pp);
       tmem_st_x32(tSr + 32, dd);
       tmem_wait_st();
-      warp_arrive(bar(L::kPFull));
+      warp_arrive(bar(L::kPFull + 1));
     }
     const bool ok = wait_bar(bar(L::kAccFull), af_cnt & 1, abort_flag, p.status, 21);
     if (!__all_sync(0xFFFFFFFFu, ok)) return;
@@ -641,8 +661,8 @@ __device__ __forceinline__ void dq_elementwise(const BwdParams& p, uint64_t* bar
     }
   };
   // this row's dO half into TMEM (after the previous unit's last dP has
-  // been computed), its LSE * log2(e) and D into l2 / di
-  auto stage_unit = [&](const Unit& un, float& l2, float& di) -> bool {
+  // been computed), its -LSE * log2(e) and D into nl2 / di
+  auto stage_unit = [&](const Unit& un, float& nl2, float& di) -> bool {
     const int64_t i = int64_t(un.ob) * kTile + row;
     const bool valid = i < p.N;
     const uint4* src = reinterpret_cast<const uint4*>(
@@ -657,7 +677,7 @@ __device__ __forceinline__ void dq_elementwise(const BwdParams& p, uint64_t* bar
       rw[4 * j + 3] = v.w;
     }
     const int64_t vrow = (int64_t(un.b) * p.H + un.h) * p.NP + i;  // i < NP always
-    l2 = p.lse2[vrow];
+    nl2 = p.nlse2[vrow];
     di = p.dsum[vrow];
     const bool ok = wait_bar(bar(L::kFixEmpty), (fe_cnt & 1) ^ 1, abort_flag, p.status, 22);
     if (!__all_sync(0xFFFFFFFFu, ok)) return false;
@@ -671,8 +691,8 @@ __device__ __forceinline__ void dq_elementwise(const BwdParams& p, uint64_t* bar
   };
   Unit cur;
   bool has = next(cur);
-  float l2 = 0.f, di = 0.f;
-  if (has && !stage_unit(cur, l2, di)) return;
+  float nl2 = 0.f, di = 0.f;
+  if (has && !stage_unit(cur, nl2, di)) return;
   while (has) {
     const int64_t i = int64_t(cur.ob) * kTile + row;
     for (int t = 0; t < cur.n; ++t) {
@@ -696,7 +716,7 @@ __device__ __forceinline__ void dq_elementwise(const BwdParams& p, uint64_t* bar
 #pragma unroll
       for (int e = 0; e < 64; e += 2) {
         float x0, x1, p0, p1, u0, u1, d0, d1;
-        fma2(x0, x1, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), sl2, sl2, -l2, -l2);
+        fma2(x0, x1, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), sl2, sl2, nl2, nl2);
         p0 = ex2_approx(x0);
         p1 = ex2_approx(x1);
         sub2(u0, u1, __uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1]), di, di);
@@ -712,9 +732,9 @@ __device__ __forceinline__ void dq_elementwise(const BwdParams& p, uint64_t* bar
       warp_arrive(bar(L::kPFull));
     }
     Unit nxt;
-    float nl2 = 0.f, ndi = 0.f;
+    float nnl2 = 0.f, ndi = 0.f;
     const bool has_next = next(nxt);
-    if (has_next && !stage_unit(nxt, nl2, ndi)) return;
+    if (has_next && !stage_unit(nxt, nnl2, ndi)) return;
     const bool ok = wait_bar(bar(L::kAccFull), af_cnt & 1, abort_flag, p.status, 21);
     if (!__all_sync(0xFFFFFFFFu, ok)) return;
     ++af_cnt;
@@ -726,7 +746,7 @@ __device__ __forceinline__ void dq_elementwise(const BwdParams& p, uint64_t* bar
     warp_arrive(bar(L::kAccEmpty));
     cur = nxt;
     has = has_next;
-    l2 = nl2;
+    nl2 = nnl2;
     di = ndi;
   }
 }
@@ -790,11 +810,11 @@ static flash_msa_status launch_bwd_hd(const BwdLaunch& a, cudaStream_t stream) {
   using LQ = BwdLayout<HD, false>;
   const int nb = a.rows.n_blocks;
   const int NP = nb * kTile;
-  float* lse2 = a.dsum;                        // workspace: [lse2 | dsum]
+  float* nlse2 = a.dsum;                        // workspace: [nlse2 | dsum]
   float* dsum = a.dsum + int64_t(a.B) * a.H * NP;
   if (a.stages & FLASH_MSA_BWD_PREPROCESS) {
     PreParams pp{reinterpret_cast<const __nv_bfloat16*>(a.o),
-                 reinterpret_cast<const __nv_bfloat16*>(a.dout), a.lse, lse2, dsum,
+                 reinterpret_cast<const __nv_bfloat16*>(a.dout), a.lse, nlse2, dsum,
                  a.B, a.H, int(a.N), NP};
     constexpr int kRows = 256 / (HD / 8);
     dim3 grid((NP + kRows - 1) / kRows, a.H, a.B);
@@ -808,7 +828,7 @@ static flash_msa_status launch_bwd_hd(const BwdLaunch& a, cudaStream_t stream) {
   if ((st = make_tile_map(&p.tm_k, a.k, a.B, a.N, a.Hkv, HD)) != FLASH_MSA_OK) return st;
   if ((st = make_tile_map(&p.tm_v, a.v, a.B, a.N, a.Hkv, HD)) != FLASH_MSA_OK) return st;
   if ((st = make_tile_map(&p.tm_do, a.dout, a.B, a.N, a.H, HD)) != FLASH_MSA_OK) return st;
-  p.lse2 = lse2;
+  p.nlse2 = nlse2;
   p.dsum = dsum;
   p.dout = reinterpret_cast<const __nv_bfloat16*>(a.dout);
   p.B = a.B;
