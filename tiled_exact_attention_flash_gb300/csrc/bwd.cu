@@ -115,9 +115,10 @@ struct BwdLayout {
   static constexpr int kRingOff = (KS ? 2 : 1) * kTileBytes;
   static constexpr int kVecOff = kRingOff + kStages * kTileBytes;  // (stages/2) x 1 KB
   static constexpr int kBarOff = kVecOff + (KS ? (kStages / 2) * 1024 : 0);  // vectors: dK/dV only
-  // kSFull / kPFull: two slots each.  dK/dV: kSFull, kPFull (P^T written)
-  // and kPFull + 1 (dS^T written); dQ: kSFull, kPFull and kDsEmpty
-  // (= kSFull + 1, the dS columns of TMEM may be overwritten)
+  // kSFull / kPFull: two slots each.  dK/dV: kSFull (S^T computed),
+  // kSFull + 1 (dP^T computed), kPFull (P^T written), kPFull + 1 (dS^T
+  // written); dQ: kSFull, kPFull, kDpFree and kDsEmpty (= kSFull + 1, the dS
+  // columns of TMEM may be overwritten)
   static constexpr int kFixFull = 0, kFixEmpty = 1, kSFull = 2, kDsEmpty = 3, kPFull = 4,
                        kDpFree = 6, kAccFull = 7, kAccEmpty = 8, kMmaDone = 9, kRingFull = 10,
                        kRingEmpty = 10 + kStages;
@@ -405,15 +406,14 @@ __device__ __forceinline__ void dq_mma(const BwdParams& p, uint8_t* smem, uint64
 }
 
 // MMA issuer of bwd_dkdv (key-stationary; fixed tiles K, V; ring Q_t, dO_t).
-// TMEM: two 128-column regions R0 = [0,128), R1 = [128,256) that swap roles
-// every query tile (tile t: S^T in R_(t&1), dP^T in R_(1-(t&1))), dV at
-// [256, 256+d), dK at [384, 384+d).  The elementwise side pulls its S^T and
-// dP^T columns into registers first (sdp_free), which frees the dP^T region
-// for the next tile's S^T, and then writes P^T and dS^T (bf16) into the
-// S^T region, P^T first (p_full) and dS^T second (ds_full).  Order per
-// tile t:
-//   [sdp_free(t)] S^T(t+1) -> [p_full(t)] dV += P^T dO_t, release dO_t ->
-//   [ds_full(t)] dK += dS^T Q_t, release Q_t -> dP^T(t+1) -> s_full(t+1)
+// TMEM: S^T at A = [0,128), dP^T at B = [128,256), dV at [256, 256+d), dK at
+// [384, 384+d).  The elementwise side reads S^T, writes P^T (bf16) over it
+// and signals p_full; then reads dP^T, writes dS^T (bf16) over it and
+// signals ds_full.  Each region is refilled for the next tile as soon as
+// the product reading it has been issued, so the next tile's S^T is ready
+// while dS^T is still being computed.  Order per tile t:
+//   [p_full(t)] dV += P^T dO_t, release dO_t, S^T(t+1) -> s_full;
+//   [ds_full(t)] dK += dS^T Q_t, release Q_t, dP^T(t+1) -> dp_full.
 template <int HD>
 __device__ __forceinline__ void dkdv_mma(const BwdParams& p, uint8_t* smem, uint64_t* bars,
                                          uint32_t tmem, volatile int* abort_flag) {
@@ -421,7 +421,7 @@ __device__ __forceinline__ void dkdv_mma(const BwdParams& p, uint8_t* smem, uint
   auto bar = [&](int i) { return smem_u32(bars + i); };
   constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);
   constexpr uint32_t kIdAcc = idesc_bf16_f32(128, HD, false, true);
-  const uint32_t tDV = tmem + 256, tDK = tmem + 384;
+  const uint32_t tA = tmem, tB = tmem + 128, tDV = tmem + 256, tDK = tmem + 384;
   const uint32_t fk = smem_u32(smem + L::kFixOff);
   const uint32_t fv = fk + L::kTileBytes;
   auto stage_addr = [&](uint32_t c) {
@@ -431,51 +431,51 @@ __device__ __forceinline__ void dkdv_mma(const BwdParams& p, uint8_t* smem, uint
     return wait_bar(bar(L::kRingFull + c % L::kStages), (c / L::kStages) & 1, abort_flag,
                     p.status, where);
   };
-  auto region = [&](int r) { return tmem + uint32_t(r & 1) * 128; };
-  uint32_t cnt = 0, ff_cnt = 0, pf_cnt = 0, sf_cnt = 0, ae_cnt = 0;
+  uint32_t cnt = 0, ff_cnt = 0, pf_cnt = 0, ae_cnt = 0;
   bool ok = true;
   int k = 0;
   Unit un;
   while (ok && next_unit<true>(k, un, p)) {
     if (!wait_bar(bar(L::kFixFull), ff_cnt & 1, abort_flag, p.status, 10)) break;
     ++ff_cnt;
-    if (!ring_wait(cnt, 11) || !ring_wait(cnt + 1, 12)) break;
+    if (!ring_wait(cnt, 11)) break;
     tc_fence_after();
-    mma_kmajor<HD>(region(0), fk, stage_addr(cnt), kIdS);        // S^T(0) -> R0
-    mma_kmajor<HD>(region(1), fv, stage_addr(cnt + 1), kIdS);    // dP^T(0) -> R1
+    mma_kmajor<HD>(tA, fk, stage_addr(cnt), kIdS);  // S^T(0) = K Q_0^T
     mma_commit(bar(L::kSFull));
+    if (!ring_wait(cnt + 1, 12)) break;
+    tc_fence_after();
+    mma_kmajor<HD>(tB, fv, stage_addr(cnt + 1), kIdS);  // dP^T(0) = V dO_0^T
+    mma_commit(bar(L::kSFull + 1));
     for (int t = 0; t < un.n && ok; ++t) {
       const uint32_t c = cnt + 2 * t;  // Q_t at c, dO_t at c + 1
       const bool more = t + 1 < un.n;
-      if (more) {
-        if (!ring_wait(c + 2, 11) || !ring_wait(c + 3, 12)) { ok = false; break; }
-        if (!wait_bar(bar(L::kDpFree), sf_cnt & 1, abort_flag, p.status, 15)) { ok = false; break; }
-        ++sf_cnt;
-        tc_fence_after();
-        mma_kmajor<HD>(region(t + 1), fk, stage_addr(c + 2), kIdS);  // S^T(t+1) -> old dP^T region
-      }
       if (t == 0) {
         if (!wait_bar(bar(L::kAccEmpty), (ae_cnt & 1) ^ 1, abort_flag, p.status, 13)) { ok = false; break; }
         ++ae_cnt;
       }
       if (!wait_bar(bar(L::kPFull), pf_cnt & 1, abort_flag, p.status, 14)) { ok = false; break; }
       tc_fence_after();
-      mma_tmem_a(tDV, region(t), stage_addr(c + 1), kIdAcc, t > 0);       // P^T at +0
-      mma_commit(bar(L::kRingEmpty + (c + 1) % L::kStages));               // dO_t
+      mma_tmem_a(tDV, tA, stage_addr(c + 1), kIdAcc, t > 0);  // dV += P^T dO_t
+      mma_commit(bar(L::kRingEmpty + (c + 1) % L::kStages));
+      if (more) {
+        if (!ring_wait(c + 2, 11)) { ok = false; break; }
+        tc_fence_after();
+        mma_kmajor<HD>(tA, fk, stage_addr(c + 2), kIdS);  // S^T(t+1) over P^T(t)
+        mma_commit(bar(L::kSFull));
+      }
       if (!wait_bar(bar(L::kPFull + 1), pf_cnt & 1, abort_flag, p.status, 16)) { ok = false; break; }
       ++pf_cnt;
       tc_fence_after();
-      mma_tmem_a(tDK, region(t) + 32, stage_addr(c), kIdAcc, t > 0);      // dS^T at +32
-      mma_commit(bar(L::kRingEmpty + c % L::kStages));                     // Q_t
+      mma_tmem_a(tDK, tB, stage_addr(c), kIdAcc, t > 0);  // dK += dS^T Q_t
+      mma_commit(bar(L::kRingEmpty + c % L::kStages));
       if (more) {
-        mma_kmajor<HD>(region(t), fv, stage_addr(c + 3), kIdS);  // dP^T(t+1) -> old S^T region
-        mma_commit(bar(L::kSFull));
+        if (!ring_wait(c + 3, 12)) { ok = false; break; }
+        tc_fence_after();
+        mma_kmajor<HD>(tB, fv, stage_addr(c + 3), kIdS);  // dP^T(t+1) over dS^T(t)
+        mma_commit(bar(L::kSFull + 1));
       }
     }
     if (!ok) break;
-    // the last tile's sdp_free has been signalled too: consume it
-    if (!wait_bar(bar(L::kDpFree), sf_cnt & 1, abort_flag, p.status, 15)) break;
-    ++sf_cnt;
     cnt += 2 * un.n;
     mma_commit(bar(L::kFixEmpty));
     mma_commit(bar(L::kAccFull));
@@ -507,12 +507,12 @@ __device__ __forceinline__ void zero_row(__nv_bfloat16* dst, int hd, bool valid)
 }
 
 // Elementwise warpgroups of bwd_dkdv: thread = key row j of the key tile,
-// warpgroup g = query columns [64 g, 64 g + 64) of each query tile:
-// P^T = exp2(scale*log2e * S^T - LSE*log2e) on live entries, then
-// dS^T = P^T o (dP^T - D).  The bf16 results go to the start of the
-// warpgroup's own column range (columns it has already read); P^T is
-// published (p_full) before dS^T is computed (ds_full), so dV of this tile
-// runs on the tensor cores during the second pass.
+// warpgroup g = query columns [64 g, 64 g + 64) of each query tile.
+// Pass 1: P^T = exp2(scale*log2e * S^T - LSE*log2e) on live entries, bf16
+// to the start of the warpgroup's S^T columns, p_full.  Pass 2 (once dP^T is
+// in TMEM): dS^T = P^T o (dP^T - D), bf16 to the start of its dP^T columns,
+// ds_full.  dV of the tile runs on the tensor cores during pass 2, and the
+// next tile's S^T during dK.
 template <int HD>
 __device__ __forceinline__ void dkdv_elementwise(const BwdParams& p, uint8_t* smem,
                                                  uint64_t* bars, uint32_t tmem, int g,
@@ -522,6 +522,7 @@ __device__ __forceinline__ void dkdv_elementwise(const BwdParams& p, uint8_t* sm
   const int wq = int(warp_id()) & 3;
   const int row = wq * 32 + int(lane_id());
   const uint32_t lane_off = uint32_t(wq * 32) << 16;
+  const uint32_t tA = tmem + lane_off + 64 * g, tB = tA + 128;
   const uint32_t tDV = tmem + lane_off + 256, tDK = tmem + lane_off + 384;
   const float sl2 = p.scale_log2;
   uint32_t sp_cnt = 0, af_cnt = 0, cnt = 0;
@@ -549,24 +550,17 @@ __device__ __forceinline__ void dkdv_elementwise(const BwdParams& p, uint8_t* sm
       const float* vec =
           reinterpret_cast<const float*>(smem + L::kVecOff + ((cnt % L::kStages) / 2) * 1024);
       cnt += 2;
-      const bool ok = wait_bar(bar(L::kSFull), sp_cnt & 1, abort_flag, p.status, 20);
+      bool ok = wait_bar(bar(L::kSFull), sp_cnt & 1, abort_flag, p.status, 20);
       if (!__all_sync(0xFFFFFFFFu, ok)) return;
-      ++sp_cnt;
       tc_fence_after();
-      const bool masked = it.partial || it.dead;
-      // this tile's regions: S^T in R_(t&1), dP^T in the other one
-      const uint32_t tSr = tmem + lane_off + uint32_t(t & 1) * 128 + 64 * g;
-      const uint32_t tDr = tmem + lane_off + uint32_t((t + 1) & 1) * 128 + 64 * g;
-      uint32_t sv[64], dpv[64];
-      tmem_ld_x64x2(tSr, tDr, sv, dpv);
-      warp_arrive(bar(L::kDpFree));  // both regions' old contents are in registers now
-      if (masked) {  // dead entries: S^T = -inf, so P^T = 0 below (scale > 0)
+      uint32_t sv[64];
+      tmem_ld_x64(tA, sv);
+      if (it.partial || it.dead) {  // dead entries: S^T = -inf, so P^T = 0 below (scale > 0)
 #pragma unroll
         for (int e = 0; e < 64; ++e)
           if (64 * g + e < lo || 64 * g + e > hi) sv[e] = kNegInfBits;
       }
       // pass 1: P^T (kept in sv as fp32), bf16 to columns [64 g, 64 g + 32)
-      // of the S^T region, then p_full so that dV += P^T dO starts
       {
         uint32_t pp[32];
         float4 l4n = *reinterpret_cast<const float4*>(vec + 64 * g);
@@ -587,11 +581,17 @@ __device__ __forceinline__ void dkdv_elementwise(const BwdParams& p, uint8_t* sm
             pp[(x + e) / 2] = pack_bf16x2(p0, p1);
           }
         }
-        tmem_st_x32(tSr, pp);
+        tmem_st_x32(tA, pp);
         tmem_wait_st();
         warp_arrive(bar(L::kPFull));
       }
-      // pass 2: dS^T = P^T o (dP^T - D), bf16 to [64 g + 32, 64 g + 64), ds_full
+      // pass 2: dS^T = P^T o (dP^T - D), bf16 to columns [64 g, 64 g + 32) of B
+      ok = wait_bar(bar(L::kSFull + 1), sp_cnt & 1, abort_flag, p.status, 24);
+      if (!__all_sync(0xFFFFFFFFu, ok)) return;
+      ++sp_cnt;
+      tc_fence_after();
+      uint32_t dpv[64];
+      tmem_ld_x64(tB, dpv);
       uint32_t dd[32];
       float4 d4n = *reinterpret_cast<const float4*>(vec + 128 + 64 * g);
 #pragma unroll
@@ -608,7 +608,7 @@ __device__ __forceinline__ void dkdv_elementwise(const BwdParams& p, uint8_t* sm
           dd[(x + e) / 2] = pack_bf16x2(d0, d1);
         }
       }
-      tmem_st_x32(tSr + 32, dd);
+      tmem_st_x32(tB, dd);
       tmem_wait_st();
       warp_arrive(bar(L::kPFull + 1));
     }
