@@ -95,6 +95,7 @@ struct BwdParams {
   int B, H, N, NP;  // H: query heads
   int Hkv, G;       // key/value heads, query heads per key/value head
   int n_units;
+  int* sched;  // work counter of this launch (zeroed before it)
   float scale, scale_log2;
   MaskParams mask;
   ListParams list;
@@ -121,8 +122,10 @@ struct BwdLayout {
   // columns of TMEM may be overwritten)
   static constexpr int kFixFull = 0, kFixEmpty = 1, kSFull = 2, kDsEmpty = 3, kPFull = 4,
                        kDpFree = 6, kAccFull = 7, kAccEmpty = 8, kMmaDone = 9, kRingFull = 10,
-                       kRingEmpty = 10 + kStages;
-  static constexpr int kNumBars = 10 + 2 * kStages;
+                       kRingEmpty = 10 + kStages, kUnitFull = 10 + 2 * kStages,
+                       kUnitEmpty = kUnitFull + 2;
+  static constexpr int kNumBars = kUnitEmpty + 2;
+  // misc: TMEM base address, abort flag, the two unit-queue slots
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
 };
@@ -157,17 +160,6 @@ __device__ __forceinline__ InnerTile bwd_inner(const Unit& un, int t, const BwdP
   return inner_tile(un, t - g * un.n0, p.list, p.status);
 }
 
-template <bool kKeyStationary>
-__device__ __forceinline__ bool next_unit(int& k, Unit& un, const BwdParams& p) {
-  while (true) {
-    const int u = int(blockIdx.x) + k * int(gridDim.x);
-    if (u >= p.n_units) return false;
-    ++k;
-    un = bwd_decode<kKeyStationary>(u, p);
-    if (un.n > 0) return true;
-  }
-}
-
 template <int HD, bool KS>
 __device__ __forceinline__ void init_bwd_barriers(uint64_t* bars) {
   using L = BwdLayout<HD, KS>;
@@ -186,7 +178,18 @@ __device__ __forceinline__ void init_bwd_barriers(uint64_t* bars) {
     mbar_init(smem_u32(bars + L::kRingFull + i), 1);
     mbar_init(smem_u32(bars + L::kRingEmpty + i), 1);
   }
+  for (int i = 0; i < 2; ++i) {
+    mbar_init(smem_u32(bars + L::kUnitFull + i), 1);               // the producer
+    mbar_init(smem_u32(bars + L::kUnitEmpty + i), 1 + kEwWarps);  // MMA thread, EW warps
+  }
   fence_mbar_init();
+}
+
+template <int HD, bool KS>
+__device__ __forceinline__ UnitQueue unit_queue(uint8_t* smem, uint64_t* bars) {
+  using L = BwdLayout<HD, KS>;
+  return UnitQueue{smem_u32(bars + L::kUnitFull), smem_u32(bars + L::kUnitEmpty),
+                   reinterpret_cast<volatile int*>(smem + L::kMiscOff + 8), 0u};
 }
 
 // Producer shared by both kernels.  Per unit: the stationary tiles (dkdv: K,
@@ -201,14 +204,26 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint8_t* smem, 
   const CUtensorMap* fix_b = kKeyStationary ? &p.tm_v : &p.tm_do;
   const CUtensorMap* ring_a = kKeyStationary ? &p.tm_q : &p.tm_k;
   const CUtensorMap* ring_b = kKeyStationary ? &p.tm_do : &p.tm_v;
-  uint32_t cnt = 0, fe_cnt = 0;
-  int last[L::kStages];
+  // ring position (stage, phase) advanced by one per load; no divisions
+  // (the dQ ring has 6 or 12 stages)
+  int stage = 0;
+  uint32_t phase = 0, fe_cnt = 0;
+  int last[L::kStages];  // phase of the last load into each stage, -1 if none
   for (int i = 0; i < L::kStages; ++i) last[i] = -1;
   int last_fix = -1;
   bool ok = true;
-  int k = 0;
-  Unit un;
-  while (ok && next_unit<kKeyStationary>(k, un, p)) {
+  UnitQueue queue = unit_queue<HD, kKeyStationary>(smem, bars);
+  // units are claimed one ahead (the dQ pass prefetches the next unit's dO)
+  int u = queue_push(queue, p.sched, p.n_units, abort_flag, p.status);
+  while (ok && u >= 0) {
+    const int u_next = queue_push(queue, p.sched, p.n_units, abort_flag, p.status);
+    if (u_next == -2) {
+      ok = false;
+      break;
+    }
+    const Unit un = bwd_decode<kKeyStationary>(u, p);
+    u = u_next;
+    if (un.n == 0) continue;
     if (!wait_bar(bar(L::kFixEmpty), (fe_cnt & 1) ^ 1, abort_flag, p.status, 1)) {
       ok = false;
       break;
@@ -222,8 +237,7 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint8_t* smem, 
     } else {
       // the elementwise warps read the next unit's dO rows with plain loads:
       // start pulling them into L2 now
-      const int u_next = int(blockIdx.x) + k * int(gridDim.x);
-      if (u_next < p.n_units) {
+      if (u_next >= 0) {
         const Unit nx = bwd_decode<false>(u_next, p);
 #pragma unroll
         for (int c = 0; c < HD / 64; ++c)
@@ -232,14 +246,13 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint8_t* smem, 
     }
     last_fix = int(fe_cnt);
     ++fe_cnt;
+    const int hkv = kKeyStationary ? 0 : un.h / p.G;  // dQ pass: head of the K / V tiles
     for (int t = 0; t < un.n && ok; ++t) {
       int hq;
       const InnerTile it = bwd_inner<kKeyStationary>(un, t, p, hq);
-      const int hr = kKeyStationary ? hq : un.h / p.G;  // head of the streamed tiles
+      const int hr = kKeyStationary ? hq : hkv;  // head of the streamed tiles
       for (int half = 0; half < 2; ++half) {
-        const int stage = cnt % L::kStages;
-        if (!wait_bar(bar(L::kRingEmpty + stage), ((cnt / L::kStages) & 1) ^ 1, abort_flag,
-                      p.status, 2)) {
+        if (!wait_bar(bar(L::kRingEmpty + stage), phase ^ 1, abort_flag, p.status, 2)) {
           ok = false;
           break;
         }
@@ -258,13 +271,16 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint8_t* smem, 
           mbar_arrive_expect_tx(bar(L::kRingFull + stage), L::kTileBytes);
           load_tile_2d<HD>(ring_b, dst, bar(L::kRingFull + stage), it.blk * kTile, hr, un.b);
         }
-        last[stage] = int(cnt);
-        ++cnt;
+        last[stage] = int(phase);
+        if (++stage == L::kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
       }
       if (t + kL2PrefetchTiles < un.n) {
         int fq;
         const InnerTile ft = bwd_inner<kKeyStationary>(un, t + kL2PrefetchTiles, p, fq);
-        const int fr = kKeyStationary ? fq : un.h / p.G;
+        const int fr = kKeyStationary ? fq : hkv;
 #pragma unroll
         for (int c = 0; c < HD / 64; ++c) {
           tma_prefetch_l2_4d(ring_a, c * 64, ft.blk * kTile, fr, un.b);
@@ -275,7 +291,7 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint8_t* smem, 
   }
   if (!ok) {
     for (int i = 0; i < L::kStages; ++i)
-      if (last[i] >= 0) drain_bar(bar(L::kRingFull + i), (last[i] / L::kStages) & 1);
+      if (last[i] >= 0) drain_bar(bar(L::kRingFull + i), uint32_t(last[i]));
     if (last_fix >= 0) drain_bar(bar(L::kFixFull), last_fix & 1);
   }
 }
@@ -333,34 +349,49 @@ __device__ __forceinline__ void dq_mma(const BwdParams& p, uint8_t* smem, uint64
   const uint32_t tS = tmem, tDP = tmem + 128, tDQ = tmem + 256;
   const uint32_t tDS = tmem + 384, tDO = tmem + 448;
   const uint32_t fq = smem_u32(smem + L::kFixOff);
-  auto stage_addr = [&](uint32_t c) {
-    return smem_u32(smem + L::kRingOff + (c % L::kStages) * L::kTileBytes);
+  const uint32_t ring = smem_u32(smem + L::kRingOff);
+  // ring position of a key tile: K_t in stage s (even), V_t in s + 1, both
+  // filled in phase ph (the ring has an even number of stages)
+  struct Pos {
+    int s;
+    uint32_t ph;
   };
-  auto ring_wait = [&](uint32_t c, unsigned where) {
-    return wait_bar(bar(L::kRingFull + c % L::kStages), (c / L::kStages) & 1, abort_flag,
-                    p.status, where);
+  auto advance = [](Pos r) {
+    r.s += 2;
+    if (r.s == L::kStages) {
+      r.s = 0;
+      r.ph ^= 1;
+    }
+    return r;
+  };
+  auto stage_addr = [&](int s) { return ring + uint32_t(s) * L::kTileBytes; };
+  auto ring_wait = [&](int s, uint32_t ph, unsigned where) {
+    return wait_bar(bar(L::kRingFull + s), ph, abort_flag, p.status, where);
   };
   // S = Q K^T (both operands in shared memory), dP = dO[tmem] V^T, for the
-  // tile whose K is in ring slot c and V in slot c + 1
-  auto issue_sdp = [&](uint32_t c) {
-    mma_kmajor<HD>(tS, fq, stage_addr(c), kIdS);
-    const uint32_t vd = sdesc_lo(stage_addr(c + 1), 16);
+  // tile at ring position r
+  auto issue_sdp = [&](Pos r) {
+    mma_kmajor<HD>(tS, fq, stage_addr(r.s), kIdS);
+    const uint32_t vd = sdesc_lo(stage_addr(r.s + 1), 16);
 #pragma unroll
     for (int kk = 0; kk < HD / 16; ++kk) {
       const uint32_t off = ((kk / 4) * (kTile * 128) + (kk % 4) * 32) >> 4;
       mma_ts(tDP, tDO + kk * 8, vd + off, kIdS, kk > 0 ? 1u : 0u);
     }
     mma_commit(bar(L::kSFull));
-    mma_commit(bar(L::kRingEmpty + (c + 1) % L::kStages));  // V_t is not read again
+    mma_commit(bar(L::kRingEmpty + r.s + 1));  // V_t is not read again
   };
-  uint32_t cnt = 0, ff_cnt = 0, pf_cnt = 0, sdp_cnt = 0, ae_cnt = 0;
+  Pos pos{0, 0};  // ring position of the current unit's first tile
+  uint32_t ff_cnt = 0, pf_cnt = 0, sdp_cnt = 0, ae_cnt = 0;
   bool ok = true, pending_sdp = false;
-  int k = 0;
-  Unit un;
-  while (ok && next_unit<false>(k, un, p)) {
+  UnitQueue queue = unit_queue<HD, false>(smem, bars);
+  int u;
+  while (ok && (u = queue_pop<false>(queue, abort_flag, p.status)) >= 0) {
+    const Unit un = bwd_decode<false>(u, p);
+    if (un.n == 0) continue;
     if (!wait_bar(bar(L::kFixFull), ff_cnt & 1, abort_flag, p.status, 10)) break;
     ++ff_cnt;
-    if (!ring_wait(cnt, 11) || !ring_wait(cnt + 1, 12)) break;
+    if (!ring_wait(pos.s, pos.ph, 11) || !ring_wait(pos.s + 1, pos.ph, 12)) break;
     // the previous unit's last S / dP must be in registers before S(0) and
     // dP(0) overwrite them
     if (pending_sdp) {
@@ -368,16 +399,16 @@ __device__ __forceinline__ void dq_mma(const BwdParams& p, uint8_t* smem, uint64
       ++sdp_cnt;
     }
     tc_fence_after();
-    issue_sdp(cnt);
+    issue_sdp(pos);
     if (un.n == 1) mma_commit(bar(L::kFixEmpty));  // Q and dO are not read again
     for (int t = 0; t < un.n && ok; ++t) {
-      const uint32_t c = cnt + 2 * t;  // K_t at c, V_t at c + 1
+      const Pos nxt = advance(pos);  // pos: tile t, nxt: tile t + 1
       if (t + 1 < un.n) {
-        if (!ring_wait(c + 2, 11) || !ring_wait(c + 3, 12)) { ok = false; break; }
+        if (!ring_wait(nxt.s, nxt.ph, 11) || !ring_wait(nxt.s + 1, nxt.ph, 12)) { ok = false; break; }
         if (!wait_bar(bar(L::kDpFree), sdp_cnt & 1, abort_flag, p.status, 15)) { ok = false; break; }
         ++sdp_cnt;
         tc_fence_after();
-        issue_sdp(c + 2);
+        issue_sdp(nxt);
         if (t + 2 == un.n) mma_commit(bar(L::kFixEmpty));
       }
       if (t == 0) {
@@ -389,15 +420,15 @@ __device__ __forceinline__ void dq_mma(const BwdParams& p, uint8_t* smem, uint64
       tc_fence_after();
       // dQ (+)= dS K_t: dS from TMEM (k-step kk = keys [16 kk, 16 kk + 16) =
       // columns tDS + 8 kk), K_t as an MN-major B operand
-      const uint32_t kd = sdesc_lo(stage_addr(c), kTile * 128);
+      const uint32_t kd = sdesc_lo(stage_addr(pos.s), kTile * 128);
 #pragma unroll
       for (int kk = 0; kk < kTile / 16; ++kk)
         mma_ts(tDQ, tDS + kk * 8, kd + kk * (2048 >> 4), kIdAcc, (t > 0 || kk > 0) ? 1u : 0u);
       mma_commit(bar(L::kDsEmpty));
-      mma_commit(bar(L::kRingEmpty + c % L::kStages));
+      mma_commit(bar(L::kRingEmpty + pos.s));
+      pos = nxt;
     }
     if (!ok) break;
-    cnt += 2 * un.n;
     mma_commit(bar(L::kAccFull));
     pending_sdp = true;
   }
@@ -433,9 +464,11 @@ __device__ __forceinline__ void dkdv_mma(const BwdParams& p, uint8_t* smem, uint
   };
   uint32_t cnt = 0, ff_cnt = 0, pf_cnt = 0, ae_cnt = 0;
   bool ok = true;
-  int k = 0;
-  Unit un;
-  while (ok && next_unit<true>(k, un, p)) {
+  UnitQueue queue = unit_queue<HD, true>(smem, bars);
+  int u;
+  while (ok && (u = queue_pop<false>(queue, abort_flag, p.status)) >= 0) {
+    const Unit un = bwd_decode<true>(u, p);
+    if (un.n == 0) continue;
     if (!wait_bar(bar(L::kFixFull), ff_cnt & 1, abort_flag, p.status, 10)) break;
     ++ff_cnt;
     if (!ring_wait(cnt, 11)) break;
@@ -446,6 +479,7 @@ __device__ __forceinline__ void dkdv_mma(const BwdParams& p, uint8_t* smem, uint
     tc_fence_after();
     mma_kmajor<HD>(tB, fv, stage_addr(cnt + 1), kIdS);  // dP^T(0) = V dO_0^T
     mma_commit(bar(L::kSFull + 1));
+    if (un.n == 1) mma_commit(bar(L::kFixEmpty));  // K and V are not read again
     for (int t = 0; t < un.n && ok; ++t) {
       const uint32_t c = cnt + 2 * t;  // Q_t at c, dO_t at c + 1
       const bool more = t + 1 < un.n;
@@ -473,11 +507,11 @@ __device__ __forceinline__ void dkdv_mma(const BwdParams& p, uint8_t* smem, uint
         tc_fence_after();
         mma_kmajor<HD>(tB, fv, stage_addr(c + 3), kIdS);  // dP^T(t+1) over dS^T(t)
         mma_commit(bar(L::kSFull + 1));
+        if (t + 2 == un.n) mma_commit(bar(L::kFixEmpty));
       }
     }
     if (!ok) break;
     cnt += 2 * un.n;
-    mma_commit(bar(L::kFixEmpty));
     mma_commit(bar(L::kAccFull));
   }
   mma_commit(bar(L::kMmaDone));
@@ -526,9 +560,10 @@ __device__ __forceinline__ void dkdv_elementwise(const BwdParams& p, uint8_t* sm
   const uint32_t tDV = tmem + lane_off + 256, tDK = tmem + lane_off + 384;
   const float sl2 = p.scale_log2;
   uint32_t sp_cnt = 0, af_cnt = 0, cnt = 0;
-  for (int k = 0;; ++k) {
-    const int u = int(blockIdx.x) + k * int(gridDim.x);
-    if (u >= p.n_units) break;
+  UnitQueue queue = unit_queue<HD, true>(smem, bars);
+  while (true) {
+    const int u = queue_pop<true>(queue, abort_flag, p.status);
+    if (u < 0) return;
     const Unit un = bwd_decode<true>(u, p);
     const int64_t j = int64_t(un.ob) * kTile + row;  // key token
     const bool valid = j < p.N;
@@ -634,8 +669,8 @@ __device__ __forceinline__ void dkdv_elementwise(const BwdParams& p, uint8_t* sm
 // to the dS columns.  The next unit's dO is staged before this unit's dQ is
 // stored, so the next unit's first products overlap the store.
 template <int HD>
-__device__ __forceinline__ void dq_elementwise(const BwdParams& p, uint64_t* bars, uint32_t tmem,
-                                               int g, volatile int* abort_flag) {
+__device__ __forceinline__ void dq_elementwise(const BwdParams& p, uint8_t* smem, uint64_t* bars,
+                                               uint32_t tmem, int g, volatile int* abort_flag) {
   using L = BwdLayout<HD, false>;
   auto bar = [&](int i) { return smem_u32(bars + i); };
   const int wq = int(warp_id()) & 3;
@@ -646,13 +681,12 @@ __device__ __forceinline__ void dq_elementwise(const BwdParams& p, uint64_t* bar
   const uint32_t tDO = tmem + lane_off + 448 + (HD / 4) * g;
   const float sl2 = p.scale_log2;
   uint32_t sp_cnt = 0, af_cnt = 0, fe_cnt = 0, ds_cnt = 0;
-  int k = 0;
+  UnitQueue queue = unit_queue<HD, false>(smem, bars);
   // next unit with live key tiles; units without any get zero dQ rows here
   auto next = [&](Unit& un) -> bool {
     while (true) {
-      const int u = int(blockIdx.x) + k * int(gridDim.x);
-      if (u >= p.n_units) return false;
-      ++k;
+      const int u = queue_pop<true>(queue, abort_flag, p.status);
+      if (u < 0) return false;
       un = bwd_decode<false>(u, p);
       if (un.n > 0) return true;
       const int64_t i = int64_t(un.ob) * kTile + row;
@@ -791,7 +825,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
     const int g = (warp - 4) >> 2;  // elementwise warpgroup: columns [64 g, 64 g + 64)
     regs_grow<208>();
     if (kKeyStationary) dkdv_elementwise<HD>(p, smem, bars, tmem, g, abort_flag);
-    else dq_elementwise<HD>(p, bars, tmem, g, abort_flag);
+    else dq_elementwise<HD>(p, smem, bars, tmem, g, abort_flag);
   }
   tc_fence_before();
   __syncthreads();
@@ -852,22 +886,37 @@ static flash_msa_status launch_bwd_hd(const BwdLaunch& a, cudaStream_t stream) {
     }
     return FLASH_MSA_OK;
   };
+  // persistent launches: one CTA per SM (fewer for small problems), units
+  // handed out in order by a counter zeroed just before each kernel
+  const int sms = sm_count();
+  if (sms <= 0) return set_cuda_error("bwd: multiprocessor count");
+  auto claim_counter = [&]() -> flash_msa_status {
+    p.sched = sched_counter();
+    if (!p.sched) return set_cuda_error("bwd: work counter");
+    if (cudaMemsetAsync(p.sched, 0, sizeof(int), stream) != cudaSuccess)
+      return set_cuda_error("bwd: work counter reset");
+    return FLASH_MSA_OK;
+  };
   if (a.stages & FLASH_MSA_BWD_DKDV) {
     if ((st = prep(bwd_main_kernel<HD, true>, 0)) != FLASH_MSA_OK) return st;
+    if ((st = claim_counter()) != FLASH_MSA_OK) return st;
     p.list = a.cols;
     p.n_units = a.B * a.Hkv * nb;
     p.out_a = reinterpret_cast<__nv_bfloat16*>(a.dk);
     p.out_b = reinterpret_cast<__nv_bfloat16*>(a.dv);
-    bwd_main_kernel<HD, true><<<p.n_units, kBwdThreads, LK::kSmemBytes, stream>>>(p);
+    const int grid = p.n_units < sms ? p.n_units : sms;
+    bwd_main_kernel<HD, true><<<grid, kBwdThreads, LK::kSmemBytes, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return set_cuda_error("bwd_dkdv launch");
   }
   if (a.stages & FLASH_MSA_BWD_DQ) {
     if ((st = prep(bwd_main_kernel<HD, false>, 1)) != FLASH_MSA_OK) return st;
+    if ((st = claim_counter()) != FLASH_MSA_OK) return st;
     p.list = a.rows;
     p.n_units = a.B * a.H * nb;
     p.out_a = reinterpret_cast<__nv_bfloat16*>(a.dq);
     p.out_b = nullptr;
-    bwd_main_kernel<HD, false><<<p.n_units, kBwdThreads, LQ::kSmemBytes, stream>>>(p);
+    const int grid = p.n_units < sms ? p.n_units : sms;
+    bwd_main_kernel<HD, false><<<grid, kBwdThreads, LQ::kSmemBytes, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return set_cuda_error("bwd_dq launch");
   }
   return FLASH_MSA_OK;

@@ -163,6 +163,47 @@ __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
 }
 
 // ---------------------------------------------------------------------------
+// Dynamic work distribution for persistent CTAs (one per SM).  The TMA
+// producer thread claims unit indices from the launch's global counter and
+// hands them, in claim order, to the CTA's other roles through two
+// shared-memory slots, each guarded by a "full" mbarrier (one arrival: the
+// producer) and an "empty" mbarrier (one arrival per consumer).  Index -1
+// means that no unit is left; it is published exactly once.  Both calls
+// return -2 when a wait was abandoned (abort).
+// ---------------------------------------------------------------------------
+struct UnitQueue {
+  uint32_t full, empty;  // mbarriers of slot 0; slot 1's follow 8 bytes later
+  volatile int* slot;    // two shared-memory slots
+  uint32_t seq;          // number of pushes / pops done by this thread
+};
+
+__device__ __forceinline__ int queue_push(UnitQueue& q, int* counter, int n_units,
+                                          volatile int* abort_flag, unsigned* status) {
+  const uint32_t s = q.seq & 1;
+  if (!wait_bar(q.empty + 8 * s, ((q.seq >> 1) & 1) ^ 1, abort_flag, status, 30)) return -2;
+  int u = atomicAdd(counter, 1);
+  if (u >= n_units) u = -1;
+  q.slot[s] = u;
+  mbar_arrive(q.full + 8 * s);  // release: the slot write is visible to the waiters
+  ++q.seq;
+  return u;
+}
+
+// kWarp: called by all 32 lanes of a warp, which then arrive once.
+template <bool kWarp>
+__device__ __forceinline__ int queue_pop(UnitQueue& q, volatile int* abort_flag,
+                                         unsigned* status) {
+  const uint32_t s = q.seq & 1;
+  const bool ok = wait_bar(q.full + 8 * s, (q.seq >> 1) & 1, abort_flag, status, 31);
+  if (kWarp ? !__all_sync(0xFFFFFFFFu, ok) : !ok) return -2;
+  const int u = q.slot[s];
+  if (kWarp) __syncwarp();
+  if (!kWarp || (threadIdx.x & 31) == 0) mbar_arrive(q.empty + 8 * s);
+  ++q.seq;
+  return u;
+}
+
+// ---------------------------------------------------------------------------
 // Work units and tile lists
 // ---------------------------------------------------------------------------
 // A list of blocks for one outer block (key tiles of a query block in the

@@ -22,6 +22,9 @@ flash_msa_status make_tile_map(CUtensorMap* m, const void* base, int B, int64_t 
 
 // device status word (status.cu)
 unsigned* status_word_ptr();  // device address for the current device, or null on error
+constexpr int kSchedSlots = 256;
+int* sched_counter();  // a work counter of the current device for one launch, or null on error
+int sm_count();        // multiprocessors of the current device, 0 on error
 
 struct FwdLaunch {
   const void *q, *k, *v;

@@ -1,6 +1,9 @@
 // The device status word shared by every kernel of the library, one per
-// device (a file-scope __device__ variable, so no allocation is needed).
+// device, and the pool of work counters of the persistent kernels (both
+// file-scope __device__ variables, so no allocation is needed).
 #include <cuda_runtime.h>
+
+#include <atomic>
 
 #include "internal.h"
 
@@ -17,6 +20,39 @@ unsigned* status_word_ptr() {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_status_word) != cudaSuccess) return nullptr;
     cache[dev] = static_cast<unsigned*>(ptr);
+  }
+  return cache[dev];
+}
+
+// Work counters of persistent launches.  Each launch takes the next slot
+// round-robin and zeroes it on its own stream before the kernel runs, so
+// launches that overlap on the GPU (different streams) use different slots
+// unless more than kSchedSlots of them are in flight at once.
+static __device__ int g_sched[kSchedSlots];
+
+int* sched_counter() {
+  constexpr int kMaxDevices = 64;
+  static int* cache[kMaxDevices] = {};
+  static std::atomic<unsigned> next{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (!cache[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_sched) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<int*>(ptr);
+  }
+  return cache[dev] + (next.fetch_add(1, std::memory_order_relaxed) % kSchedSlots);
+}
+
+int sm_count() {
+  constexpr int kMaxDevices = 64;
+  static int cache[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  if (!cache[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
   }
   return cache[dev];
 }
