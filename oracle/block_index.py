@@ -18,8 +18,9 @@ and the lists are built from that classification:
 
 For masks with a local window and no strided part, key blocks farther than
 the window from the query block are skipped without evaluation: by the window
-definition none of their entries is live.  Tests check this shortcut against
-the full evaluation.
+definition none of their entries is live (with global tokens, the key
+blocks holding global keys and every block of a global query block are
+still evaluated).  Tests check this shortcut against the full evaluation.
 """
 from __future__ import annotations
 
@@ -37,12 +38,15 @@ def classify(n: int, spec: MaskSpec, tile: int = 128, prune: bool = True) -> np.
     span = None
     if prune and spec.window is not None and spec.stride is None:
         span = spec.window // tile + 2
+    g = spec.global_tokens
     for qb in range(nb):
         rows = np.arange(qb * tile, qb * tile + tile)
-        if span is None:
+        if span is None or (g is not None and qb * tile < g):
             kbs = range(nb)
         else:
             kbs = range(max(0, qb - span), min(nb, qb + span + 1))
+            if g is not None:
+                kbs = sorted(set(kbs) | set(range(min(nb, (g + tile - 1) // tile))))
         for kb in kbs:
             cols = np.arange(kb * tile, kb * tile + tile)
             live = live_matrix(rows, cols, n, spec)

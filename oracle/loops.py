@@ -35,7 +35,8 @@ def live_scalar(i: int, j: int, n: int, spec: MaskSpec) -> bool:
             if not (delta < spec.dilation_near or delta % spec.dilation == 0):
                 near_ok = False
     stride_ok = spec.stride is not None and (j // spec.block) % spec.stride == spec.stride_phase
-    return near_ok or stride_ok
+    global_ok = spec.global_tokens is not None and (i < spec.global_tokens or j < spec.global_tokens)
+    return near_ok or stride_ok or global_ok
 
 
 def _dot(a, b):

@@ -16,10 +16,17 @@ Definitions, one per mask kind named on the pages:
 * strided -- fixed pattern in the style of Child et al.: every key in key
   block kb with kb % stride == phase (same section, mask kind "Fixed
   pattern").
+* global tokens -- the hybrid of a local window with a few global tokens in
+  the style of Longformer (same page, section "How Do Sparse Attention
+  Kernels Work in GPU Clusters?", the paragraph after the benchmark table;
+  the FAQ "How does Flash-MSA affect model accuracy compared to dense
+  attention?" gives 512 global tokens with an 8K window at 128K).  Read
+  symmetrically: the first G tokens are global, so a global query attends
+  every key and every query attends the global keys.
 
 Combination: live = in_range AND causal_part AND pattern, where pattern is
-true when no window/dilation/stride is set, and otherwise
-(window AND dilation part) OR (strided part).
+true when no window/dilation/stride/global part is set, and otherwise
+(window AND dilation part) OR (strided part) OR (global part).
 """
 from __future__ import annotations
 
@@ -38,10 +45,12 @@ class MaskSpec:
     stride: Optional[int] = None     # key block kb live iff kb % stride == stride_phase
     stride_phase: int = 0
     block: int = 128                 # pattern block, in tokens
+    global_tokens: Optional[int] = None  # G: queries and keys 0..G-1 are global
 
     @property
     def has_pattern(self) -> bool:
-        return self.window is not None or self.dilation is not None or self.stride is not None
+        return (self.window is not None or self.dilation is not None or self.stride is not None
+                or self.global_tokens is not None)
 
 
 DENSE = MaskSpec()
@@ -67,6 +76,8 @@ def live_matrix(rows, cols, n: int, spec: MaskSpec) -> np.ndarray:
             part |= near_part
         if spec.stride is not None:
             part |= (j // spec.block) % spec.stride == spec.stride_phase
+        if spec.global_tokens is not None:
+            part |= (i < spec.global_tokens) | (j < spec.global_tokens)
         ok = ok & part
     return ok
 
@@ -75,12 +86,17 @@ def candidate_cols(r0: int, r1: int, n: int, spec: MaskSpec) -> tuple[int, int]:
     """Half-open key range [c0, c1) outside of which rows r0..r1-1 have no live key.
 
     Pure bound from the definitions above (causal: j <= i; window without a
-    strided part: |i - j| <= W); it only skips keys that the predicate kills.
+    strided part: |i - j| <= W, and with global tokens the global keys
+    j < G stay candidates while global rows i < G see every key); it only
+    skips keys that the predicate kills.
     """
     c0, c1 = 0, n
     if spec.causal:
         c1 = min(c1, r1)
     if spec.window is not None and spec.stride is None:
-        c0 = max(c0, r0 - spec.window)
-        c1 = min(c1, r1 + spec.window)
+        g = spec.global_tokens
+        if g is None:
+            c0 = max(c0, r0 - spec.window)
+        if g is None or r0 >= g:
+            c1 = min(c1, r1 + spec.window)
     return c0, max(c0, c1)

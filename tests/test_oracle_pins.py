@@ -21,6 +21,8 @@ SMALL_SPECS = {
     "causal_window_dilated": MaskSpec(causal=True, window=14, dilation=2, dilation_near=2, block=4),
     "dilated_only": MaskSpec(dilation=3, dilation_near=1, block=4),
     "strided_only": MaskSpec(causal=True, stride=2, stride_phase=0, block=4),
+    "causal_window_global": MaskSpec(causal=True, window=4, global_tokens=8, block=4),
+    "window_global": MaskSpec(window=3, global_tokens=4, block=4),
 }
 
 fwd_full = attention.forward_head
@@ -52,6 +54,15 @@ def test_mask_hand_examples():
     assert live.tolist() == [[True, True, True, False, False]]
     # out of range entries are dead
     assert not live_matrix([3], [7], 5, MaskSpec()).any()
+    # global tokens (G = 4): global keys visible from every query, a global
+    # query sees every key; window 2 elsewhere; causal on top when set
+    spec = MaskSpec(window=2, global_tokens=4)
+    live = live_matrix([15], [0, 3, 4, 12, 13, 17, 18], 20, spec)
+    assert live.tolist() == [[True, True, False, False, True, True, False]]
+    live = live_matrix([2], [0, 9, 19], 20, spec)
+    assert live.tolist() == [[True, True, True]]
+    live = live_matrix([2, 15], [0, 9, 19], 20, MaskSpec(causal=True, window=2, global_tokens=4))
+    assert live.tolist() == [[True, False, False], [True, False, False]]
 
 
 @pytest.mark.parametrize("name", sorted(SMALL_SPECS))
@@ -201,6 +212,7 @@ def test_golden_tile_counts():
         "causal_n16384": (16384, MaskSpec(causal=True)),
         "window1024_strided8_n32768": (32768, MaskSpec(causal=True, window=1024, stride=8)),
         "window4096_dilation2_n131072": (131072, MaskSpec(causal=True, window=4096, dilation=2, dilation_near=2)),
+        "window8192_global512_n32768": (32768, MaskSpec(causal=True, window=8192, global_tokens=512)),
     }
     for key, (n, spec) in cases.items():
         idx = block_index.build(n, spec)
@@ -216,12 +228,22 @@ def test_closed_form_counts_formulas():
     assert (win, strided, win + strided) == (2268, 3937, 6205)
     dil = 992 * 18 + sum(1 + min(qb, 1) + qb // 2 for qb in range(32))
     assert dil == 18159
+    # causal window of w = 64 blocks plus gb = 4 global blocks: a query block
+    # sees [0, qb] while its window reaches the global blocks, else 65 + 4
+    def glob(nb, w=64, gb=4):
+        return sum(qb + 1 if qb - w <= gb - 1 else w + 1 + gb for qb in range(nb))
+    assert (glob(1024), glob(256)) == (68310, 15318)
+    # partial: the diagonal plus the window edge kb = qb - 64 when it is not global
+    assert (1024 + sum(1 for qb in range(1024) if qb - 64 >= 4),
+            256 + sum(1 for qb in range(256) if qb - 64 >= 4)) == (1980, 444)
 
 
 @pytest.mark.parametrize("n,spec", [
     (1000, MaskSpec(causal=True, window=200)),
     (1500, MaskSpec(window=300, dilation=2, dilation_near=1)),
     (2100, MaskSpec(causal=True, window=129, dilation=3, dilation_near=2)),
+    (2000, MaskSpec(causal=True, window=300, global_tokens=256)),
+    (1700, MaskSpec(window=200, global_tokens=384)),
 ])
 def test_window_shortcut_matches_full_scan(n, spec):
     a = block_index.classify(n, spec, prune=True)
