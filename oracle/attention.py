@@ -32,7 +32,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .mask import MaskSpec, candidate_cols, live_matrix
+from .mask import MaskSpec, candidate_col_array, live_matrix
 
 
 def default_scale(d: int) -> float:
@@ -101,8 +101,7 @@ def _row_block(q, k, scale, spec, rows):
     Key columns that are dead for every row of the chunk are dropped before
     the product (they would only contribute exp(-inf) = 0)."""
     n = q.shape[0]
-    c0, c1 = candidate_cols(int(rows.min()), int(rows.max()) + 1, n, spec)
-    cols = np.arange(c0, c1)
+    cols = candidate_col_array(int(rows.min()), int(rows.max()) + 1, n, spec)
     live = live_matrix(rows, cols, n, spec)
     keep = live.any(axis=0)
     if keep.size and keep.mean() < 0.75:

@@ -100,3 +100,18 @@ def candidate_cols(r0: int, r1: int, n: int, spec: MaskSpec) -> tuple[int, int]:
         if g is None or r0 >= g:
             c1 = min(c1, r1 + spec.window)
     return c0, max(c0, c1)
+
+
+def candidate_col_array(r0: int, r1: int, n: int, spec: MaskSpec) -> np.ndarray:
+    """Key indices outside of which rows r0..r1-1 have no live key.
+
+    The span of ``candidate_cols``, narrowed for a window with global tokens
+    to the global keys [0, G) plus the window span of the rows (rows r0 >= G;
+    same definitions as above, so only dead keys are left out).
+    """
+    c0, c1 = candidate_cols(r0, r1, n, spec)
+    g = spec.global_tokens
+    if g is None or spec.window is None or spec.stride is not None or r0 < g:
+        return np.arange(c0, c1)
+    lo = max(g, r0 - spec.window)
+    return np.concatenate([np.arange(0, min(g, c1)), np.arange(lo, max(lo, c1))])

@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 
 from oracle import attention, block_index, loops
-from oracle.mask import MaskSpec, candidate_cols, live_matrix
+from oracle.mask import MaskSpec, candidate_col_array, candidate_cols, live_matrix
 from tests import oracle_pins as pins
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -85,6 +85,11 @@ def test_candidate_span_only_drops_dead_keys(name):
         live = live_matrix(np.arange(r0, r1), np.arange(n), n, spec)
         outside = np.ones(n, dtype=bool)
         outside[c0:c1] = False
+        assert not live[:, outside].any()
+        kept = candidate_col_array(r0, r1, n, spec)
+        assert len(np.unique(kept)) == len(kept)
+        outside = np.ones(n, dtype=bool)
+        outside[kept] = False
         assert not live[:, outside].any()
 
 
@@ -171,6 +176,8 @@ def test_tiled_online_softmax_agrees(name, n, blk):
     MaskSpec(causal=True, window=100, stride=4, stride_phase=0, block=32),
     MaskSpec(causal=True, window=150, dilation=2, dilation_near=2, block=32),
     MaskSpec(window=90),
+    MaskSpec(causal=True, window=70, global_tokens=64, block=32),
+    MaskSpec(window=50, global_tokens=96, block=32),
 ])
 def test_chunked_evaluation_matches_full(spec):
     r = rng(11)
