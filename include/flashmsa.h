@@ -51,7 +51,7 @@ extern "C" {
 typedef enum {
   FLASH_MSA_OK = 0,
   FLASH_MSA_ERR_INVALID_ARG = 1, /* null / misaligned pointer, bad size, bad mask field */
-  FLASH_MSA_ERR_UNSUPPORTED = 2, /* head dimension other than 64 or 128, pattern block != 128 */
+  FLASH_MSA_ERR_UNSUPPORTED = 2, /* head dimension not 64/128, block != 128, G not whole blocks */
   FLASH_MSA_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed */
   FLASH_MSA_ERR_TIMEOUT = 4,     /* device: a bounded wait inside a kernel ran out */
   FLASH_MSA_ERR_WORKSPACE = 5,   /* workspace missing or smaller than required */
@@ -60,21 +60,26 @@ typedef enum {
 
 /* Mask flags.  Element predicate for query i, key j of a length-N sequence:
  *   live(i,j) = (i < N) && (j < N) && (!CAUSAL || j <= i) && pattern(i,j)
- *   pattern   = true                                   if no WINDOW/DILATED/STRIDED flag
- *             = near(i,j) || strided(j)                otherwise
+ *   pattern   = true                          if no WINDOW/DILATED/STRIDED/GLOBAL flag
+ *             = near(i,j) || strided(j) || global(i,j)   otherwise
  *   near      = (WINDOW or DILATED set) && (!WINDOW || |i-j| <= window)
  *               && (!DILATED || D < dilation_near || D % dilation == 0),
  *               D = | floor(i/block) - floor(j/block) |
  *   strided   = STRIDED && floor(j/block) % stride == stride_phase
+ *   global    = GLOBAL && (i < global_tokens || j < global_tokens)
  * Window: "Local window -- attend only to +-W tokens"; dilated: "skip every
  * few tokens", read at block level; strided: the fixed pattern of Child et
  * al. (page "How Does Flash-MSA Sparse Attention Work", section "How
- * Flash-MSA Sparse Attention Works", list of masks). */
+ * Flash-MSA Sparse Attention Works", list of masks).  Global: the local
+ * window plus a few global tokens in the style of Longformer (same page,
+ * section "How Do Sparse Attention Kernels Work in GPU Clusters?"), the
+ * first global_tokens tokens attending and attended in both directions. */
 enum {
   FLASH_MSA_CAUSAL = 1,
   FLASH_MSA_WINDOW = 2,
   FLASH_MSA_DILATED = 4,
-  FLASH_MSA_STRIDED = 8
+  FLASH_MSA_STRIDED = 8,
+  FLASH_MSA_GLOBAL = 16
 };
 
 /* Per-query-block list of live key blocks ("a precomputed index list", page
@@ -107,10 +112,14 @@ typedef struct flash_msa_block_index {
 
 /* Mask description (host memory).  A NULL mask, or flags == 0, is dense
  * attention.  flags == CAUSAL may pass index = NULL (tiles are derived
- * arithmetically); any WINDOW/DILATED/STRIDED flag requires an index built for
- * the same N and mask, else FLASH_MSA_ERR_INDEX.  block must be 128.
+ * arithmetically); any WINDOW/DILATED/STRIDED/GLOBAL flag requires an index
+ * built for the same N and mask, else FLASH_MSA_ERR_INDEX.  block must be 128.
  * window >= 0 (tokens, inclusive); dilation >= 1; dilation_near >= 0;
- * stride >= 1 and 0 <= stride_phase < stride when the flag is set. */
+ * stride >= 1 and 0 <= stride_phase < stride when the flag is set;
+ * global_tokens >= 1 when GLOBAL is set (FLASH_MSA_ERR_INVALID_ARG
+ * otherwise) and a multiple of the 128-token block (else
+ * FLASH_MSA_ERR_UNSUPPORTED: every tile then keeps one interval of live
+ * keys per row). */
 typedef struct {
   uint32_t flags;
   int32_t block;
@@ -118,6 +127,7 @@ typedef struct {
   int32_t dilation, dilation_near;
   int32_t stride, stride_phase;
   const flash_msa_block_index* index;
+  int64_t global_tokens;
 } flash_msa_mask_desc;
 
 /* Build the block index for `mask` and sequence length N on the HOST (no GPU

@@ -48,6 +48,10 @@ MASKS = [
     {"dilation": 2, "dilation_near": 0},
     {"causal": True, "stride": 4, "stride_phase": 3},
     {"stride": 2, "stride_phase": 0, "window": 64},
+    {"causal": True, "window": 200, "global_tokens": 128},
+    {"window": 130, "global_tokens": 256},
+    {"causal": True, "global_tokens": 384},
+    {"causal": True, "window": 300, "dilation": 2, "dilation_near": 1, "global_tokens": 128},
 ]
 
 
@@ -71,7 +75,23 @@ def test_random_indices_bit_exact():
             s = int(rng.integers(1, 9))
             f["stride"] = s
             f["stride_phase"] = int(rng.integers(0, s))
+        if rng.integers(0, 3) == 0:
+            f["global_tokens"] = 128 * int(rng.integers(1, 5))
         compare(n, f)
+
+
+def test_global_token_index_matches_hand_counts():
+    # the causal 8K window + 512 global tokens index at 128K and 32K tokens,
+    # against the counts derived by hand in tests/golden/tile_counts.json
+    import json, os
+    gold = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "tile_counts.json")))
+    for key, n in (("window8192_global512_n131072", 131072), ("window8192_global512_n32768", 32768)):
+        idx = api.build_block_index(api.Mask(causal=True, window=8192, global_tokens=512), n)
+        kind = idx.host["kind"]
+        g = gold[key]
+        assert (idx.nnz, int((kind == 0).sum()), int((kind == 1).sum())) == \
+            (g["nnz"], g["full"], g["partial"]), key
+        assert api.check_block_index(idx) == api.OK
 
 
 def test_checker_rejects_corruption():

@@ -65,6 +65,11 @@ def test_fwd_argument_errors(L):
     assert fwd_raw(L, mask=bad_stride) == api.ERR_INVALID_ARG
     neg_window = api.MaskDescStruct(api.WINDOW, 128, -1, 1, 0, 1, 0, None)
     assert fwd_raw(L, mask=neg_window) == api.ERR_INVALID_ARG
+    no_global = api.MaskDescStruct(api.WINDOW | api.GLOBAL, 128, 10, 1, 0, 1, 0, None, 0)
+    assert fwd_raw(L, mask=no_global) == api.ERR_INVALID_ARG
+    ragged_global = api.Mask(causal=True, window=100, global_tokens=100).desc()
+    assert fwd_raw(L, mask=ragged_global) == api.ERR_UNSUPPORTED
+    assert b"multiple of the 128-token block" in L.flash_msa_last_error_string()
 
 
 def test_index_for_another_n_is_rejected(L):

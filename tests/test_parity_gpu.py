@@ -30,6 +30,8 @@ SMALL_MASKS = {
     "window_dilated": {"causal": True, "window": 400, "dilation": 2, "dilation_near": 1},
     "window_noncausal": {"window": 100},
     "strided_only": {"causal": True, "stride": 3, "stride_phase": 2},
+    "window_global": {"causal": True, "window": 130, "global_tokens": 128},
+    "global_noncausal": {"window": 100, "global_tokens": 256},
 }
 
 
@@ -50,7 +52,7 @@ def test_small_cases(d, n, mname):
     gc.full_compare(inp, fields, res)
 
 
-@pytest.mark.parametrize("cid", [2, 3, 4, 5])
+@pytest.mark.parametrize("cid", [2, 3, 4, 5, 6])
 def test_full_size_workloads(cid):
     w = WORKLOADS[cid]
     inp = workload_inputs(w)
@@ -79,6 +81,24 @@ def test_closed_form_uniform_on_gpu():
             ref = v[0, lo:i + 1, h].mean(axis=0)
             assert np.abs(res["o"][0, i, h] - ref).max() <= gc.O_TOL
             assert abs(res["lse"][0, h, i] - np.log(i + 1 - lo)) <= gc.LSE_TOL
+
+
+def test_closed_form_uniform_global_tokens_on_gpu():
+    # Q = 0 with a causal window of 130 and 256 global tokens: O_i is the mean
+    # of V over keys j <= i with j < 256 or i - j <= 130, or over all j <= i
+    # when i itself is global
+    B, N, H, d = 1, 700, 2, 128
+    inp = small_inputs(B, N, H, d, seed=98)
+    inp["q"] = torch.zeros_like(inp["q"])
+    fields = {"causal": True, "window": 130, "global_tokens": 256}
+    res = gc.run_gpu(inp, fields, backward=False)
+    v = inp["v"].double().numpy()
+    for h in range(H):
+        for i in range(N):
+            keys = [j for j in range(i + 1) if i < 256 or j < 256 or i - j <= 130]
+            ref = v[0, keys, h].mean(axis=0)
+            assert np.abs(res["o"][0, i, h] - ref).max() <= gc.O_TOL
+            assert abs(res["lse"][0, h, i] - np.log(len(keys))) <= gc.LSE_TOL
 
 
 def test_smoke_shape_from_the_pages():

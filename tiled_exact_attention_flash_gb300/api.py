@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(_HERE, "libflashmsa.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE, ERR_INDEX = range(7)
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "TIMEOUT",
                 5: "WORKSPACE", 6: "INDEX"}
-CAUSAL, WINDOW, DILATED, STRIDED = 1, 2, 4, 8
+CAUSAL, WINDOW, DILATED, STRIDED, GLOBAL = 1, 2, 4, 8, 16
 
 # exported symbols, in the order include/flashmsa.h declares them
 SYMBOLS = (
@@ -69,6 +69,7 @@ class MaskDescStruct(ctypes.Structure):
         ("stride", ctypes.c_int32),
         ("stride_phase", ctypes.c_int32),
         ("index", ctypes.c_void_p),
+        ("global_tokens", ctypes.c_int64),
     ]
 
 
@@ -139,6 +140,7 @@ class Mask:
     stride: Optional[int] = None
     stride_phase: int = 0
     block: int = 128
+    global_tokens: Optional[int] = None
 
     @classmethod
     def from_fields(cls, fields: dict) -> "Mask":
@@ -150,16 +152,17 @@ class Mask:
         f |= WINDOW if self.window is not None else 0
         f |= DILATED if self.dilation is not None else 0
         f |= STRIDED if self.stride is not None else 0
+        f |= GLOBAL if self.global_tokens is not None else 0
         return f
 
     @property
     def needs_index(self) -> bool:
-        return bool(self.flags & (WINDOW | DILATED | STRIDED))
+        return bool(self.flags & (WINDOW | DILATED | STRIDED | GLOBAL))
 
     def desc(self, index_ptr=None) -> MaskDescStruct:
         return MaskDescStruct(self.flags, self.block, self.window or 0, self.dilation or 1,
                               self.dilation_near, self.stride or 1, self.stride_phase,
-                              index_ptr)
+                              index_ptr, self.global_tokens or 0)
 
 
 _INDEX_ARRAYS = (("row_ptr", np.int32, "nq1"), ("col_idx", np.int32, "nnz"),

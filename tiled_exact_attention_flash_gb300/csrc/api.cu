@@ -77,9 +77,10 @@ static flash_msa_status check_mask(const flash_msa_mask_desc* m, MaskParams& mp,
   need_index = false;
   if (!m) return FLASH_MSA_OK;
   if (m->flags & ~uint32_t(FLASH_MSA_CAUSAL | FLASH_MSA_WINDOW | FLASH_MSA_DILATED |
-                           FLASH_MSA_STRIDED))
+                           FLASH_MSA_STRIDED | FLASH_MSA_GLOBAL))
     return set_error(FLASH_MSA_ERR_INVALID_ARG, "mask: unknown flag bits 0x%x", m->flags);
-  const uint32_t pat = m->flags & (FLASH_MSA_WINDOW | FLASH_MSA_DILATED | FLASH_MSA_STRIDED);
+  const uint32_t pat = m->flags & (FLASH_MSA_WINDOW | FLASH_MSA_DILATED | FLASH_MSA_STRIDED |
+                                   FLASH_MSA_GLOBAL);
   if (m->block != kTile && !(m->block == 0 && pat == 0))
     return set_error(FLASH_MSA_ERR_UNSUPPORTED, "mask: pattern block %d (only 128 is supported)",
                      m->block);
@@ -99,6 +100,16 @@ static flash_msa_status check_mask(const flash_msa_mask_desc* m, MaskParams& mp,
       return set_error(FLASH_MSA_ERR_INVALID_ARG, "mask: stride must be >= 1, 0 <= phase < stride");
     mp.stride = m->stride;
     mp.phase = m->stride_phase;
+  }
+  if (m->flags & FLASH_MSA_GLOBAL) {
+    if (m->global_tokens < 1)
+      return set_error(FLASH_MSA_ERR_INVALID_ARG, "mask: global_tokens must be >= 1");
+    if (m->global_tokens % kTile != 0)
+      return set_error(FLASH_MSA_ERR_UNSUPPORTED,
+                       "mask: global_tokens %lld is not a multiple of the 128-token block",
+                       static_cast<long long>(m->global_tokens));
+    const int64_t gb = m->global_tokens / kTile;
+    mp.global_blocks = gb < (int64_t(1) << 30) ? int32_t(gb) : int32_t(1) << 30;
   }
   need_index = pat != 0;
   return FLASH_MSA_OK;
@@ -185,18 +196,25 @@ flash_msa_status flash_msa_build_block_index(const flash_msa_mask_desc* mask, in
   flash_msa_status st = check_mask(mask, mp, need);
   if (st != FLASH_MSA_OK) return st;
   const int64_t nb = n_blocks_of(N);
-  // candidate key blocks per query block: causal and a plain window bound the span
+  // candidate key blocks per query block: causal and a plain window bound the
+  // span; with global tokens the global key blocks come first, and a global
+  // query block scans every key block
   const bool window_bound = (mp.flags & FLASH_MSA_WINDOW) && !(mp.flags & FLASH_MSA_STRIDED);
   const int64_t span = window_bound ? mp.window / kTile + 2 : nb;
+  const int64_t gb = (mp.flags & FLASH_MSA_GLOBAL) ? std::min<int64_t>(mp.global_blocks, nb) : 0;
   auto for_each_tile = [&](auto&& fn) {
     for (int64_t qb = 0; qb < nb; ++qb) {
-      int64_t k0 = window_bound ? std::max<int64_t>(0, qb - span) : 0;
-      int64_t k1 = window_bound ? std::min<int64_t>(nb - 1, qb + span) : nb - 1;
+      const bool scan_all = !window_bound || qb < gb;
+      int64_t k0 = scan_all ? 0 : std::max<int64_t>(0, qb - span);
+      int64_t k1 = scan_all ? nb - 1 : std::min<int64_t>(nb - 1, qb + span);
       if (mp.flags & FLASH_MSA_CAUSAL) k1 = std::min(k1, qb);
-      for (int64_t kb = k0; kb <= k1; ++kb) {
+      const int64_t g_end = std::min(gb, k0);  // global key blocks before the window span
+      auto visit = [&](int64_t kb) {
         const int c = classify_tile(int(qb), int(kb), N, mp);
         if (c >= 0) fn(int(qb), int(kb), c);
-      }
+      };
+      for (int64_t kb = 0; kb < g_end; ++kb) visit(kb);  // ascending: they precede k0
+      for (int64_t kb = k0; kb <= k1; ++kb) visit(kb);
     }
   };
   out->seq_len = N;

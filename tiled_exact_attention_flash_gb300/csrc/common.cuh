@@ -21,14 +21,15 @@ struct MaskParams {
   int32_t dilation, near;
   int32_t stride, phase;
   int64_t window;
+  int32_t global_blocks;  // GLOBAL: the first global_blocks blocks of queries and keys
 };
 
 // ---------------------------------------------------------------------------
 // Mask semantics (see flashmsa.h).  With a 128-token pattern block equal to
-// the 128-token tile, the dilation and stride parts are constant over a tile,
-// and the causal / window parts depend only on delta = i - j.  So over one
-// tile the live entries are exactly those whose delta lies in one interval
-// [dlo, dhi] (or none at all).
+// the 128-token tile, the dilation, stride and (block-aligned) global parts
+// are constant over a tile, and the causal / window parts depend only on
+// delta = i - j.  So over one tile the live entries are exactly those whose
+// delta lies in one interval [dlo, dhi] (or none at all).
 // ---------------------------------------------------------------------------
 struct DeltaRange {
   bool none;  // no entry of the tile can be live
@@ -37,9 +38,14 @@ struct DeltaRange {
 
 __host__ __device__ inline DeltaRange tile_delta_range(int qb, int kb, const MaskParams& m) {
   DeltaRange r{false, -kUnbounded, kUnbounded};
-  const uint32_t pat = m.flags & (FLASH_MSA_WINDOW | FLASH_MSA_DILATED | FLASH_MSA_STRIDED);
+  const uint32_t pat =
+      m.flags & (FLASH_MSA_WINDOW | FLASH_MSA_DILATED | FLASH_MSA_STRIDED | FLASH_MSA_GLOBAL);
+  // a tile of a global query block or global key block: every pair passes
+  // the pattern, only the causal part remains
+  const bool global_tile =
+      (m.flags & FLASH_MSA_GLOBAL) && (qb < m.global_blocks || kb < m.global_blocks);
   bool window_applies = false;
-  if (pat) {
+  if (pat && !global_tile) {
     const bool strided_ok = (m.flags & FLASH_MSA_STRIDED) && (kb % m.stride == m.phase);
     if (!strided_ok) {
       if (!(m.flags & (FLASH_MSA_WINDOW | FLASH_MSA_DILATED))) {

@@ -8,7 +8,8 @@ the oracle consumes the same values promoted exactly to float64.
 
 Workloads: the five attention configurations the pages' discussion motivates
 (7B-style layer, d = 128, long context; causal, local window + strided, and
-local window with block dilation).  Seeds: Q, K, V, dO of workload c use
+local window with block dilation), plus a sixth for the local window with
+global tokens hybrid (8K window, 512 global tokens, 128K tokens).  Seeds: Q, K, V, dO of workload c use
 1000*c + 1 .. 1000*c + 4.
 """
 from __future__ import annotations
@@ -43,6 +44,9 @@ WORKLOADS = {
                 {"causal": True, "window": 1024, "stride": 8, "stride_phase": 0}),
     5: Workload(5, "causal window4096 dilation2 B1 H8 N131072 d128", 1, 8, 131072, 128,
                 {"causal": True, "window": 4096, "dilation": 2, "dilation_near": 2}),
+    # local window plus global tokens: 8K window and 512 global tokens at 128K
+    6: Workload(6, "causal window8192 + global512 B1 H8 N131072 d128", 1, 8, 131072, 128,
+                {"causal": True, "window": 8192, "global_tokens": 512}),
 }
 
 
