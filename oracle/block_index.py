@@ -36,7 +36,7 @@ def classify(n: int, spec: MaskSpec, tile: int = 128, prune: bool = True) -> np.
     nb = (n + tile - 1) // tile
     kinds = np.full((nb, nb), DEAD, dtype=np.int8)
     span = None
-    if prune and spec.window is not None and spec.stride is None:
+    if prune and spec.window_bounded:
         span = spec.window // tile + 2
     g = spec.global_tokens
     for qb in range(nb):

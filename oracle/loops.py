@@ -25,18 +25,26 @@ def live_scalar(i: int, j: int, n: int, spec: MaskSpec) -> bool:
         return False
     if not spec.has_pattern:
         return True
+    qb, kb = i // spec.block, j // spec.block
     near_ok = False
-    if spec.window is not None or spec.dilation is not None:
+    near_dilated = spec.dilation is not None and not spec.dilation_far
+    if spec.window is not None or near_dilated:
         near_ok = True
         if spec.window is not None and abs(i - j) > spec.window:
             near_ok = False
-        if spec.dilation is not None:
-            delta = abs(i // spec.block - j // spec.block)
+        if near_dilated:
+            delta = abs(qb - kb)
             if not (delta < spec.dilation_near or delta % spec.dilation == 0):
                 near_ok = False
-    stride_ok = spec.stride is not None and (j // spec.block) % spec.stride == spec.stride_phase
+    far_ok = spec.dilation is not None and spec.dilation_far and abs(qb - kb) % spec.dilation == 0
+    stride_ok = False
+    if spec.stride is not None:
+        if spec.stride_relative:
+            stride_ok = (qb - kb) % spec.stride == spec.stride_phase   # Python % is non-negative
+        else:
+            stride_ok = kb % spec.stride == spec.stride_phase
     global_ok = spec.global_tokens is not None and (i < spec.global_tokens or j < spec.global_tokens)
-    return near_ok or stride_ok or global_ok
+    return near_ok or far_ok or stride_ok or global_ok
 
 
 def _dot(a, b):

@@ -16,6 +16,12 @@ Definitions, one per mask kind named on the pages:
 * strided -- fixed pattern in the style of Child et al.: every key in key
   block kb with kb % stride == phase (same section, mask kind "Fixed
   pattern").
+* relative strided -- the strided pattern of Child et al. read relative to
+  the query: with Delta = i // blk - j // blk, keep the pair iff
+  Delta mod stride == phase (the alternative to the absolute reading above).
+* far dilation -- the alternative reading of dilation: the window stays
+  dense and dilated blocks (|Delta| mod dilation == 0) are kept at every
+  distance, beyond the window too.
 * global tokens -- the hybrid of a local window with a few global tokens in
   the style of Longformer (same page, section "How Do Sparse Attention
   Kernels Work in GPU Clusters?", the paragraph after the benchmark table;
@@ -26,7 +32,8 @@ Definitions, one per mask kind named on the pages:
 
 Combination: live = in_range AND causal_part AND pattern, where pattern is
 true when no window/dilation/stride/global part is set, and otherwise
-(window AND dilation part) OR (strided part) OR (global part).
+(window AND dilation part) OR (strided part) OR (far dilation part) OR
+(global part).
 """
 from __future__ import annotations
 
@@ -46,11 +53,18 @@ class MaskSpec:
     stride_phase: int = 0
     block: int = 128                 # pattern block, in tokens
     global_tokens: Optional[int] = None  # G: queries and keys 0..G-1 are global
+    stride_relative: bool = False    # stride part relative to the query block
+    dilation_far: bool = False       # dilation as its own part, at every distance
 
     @property
     def has_pattern(self) -> bool:
         return (self.window is not None or self.dilation is not None or self.stride is not None
                 or self.global_tokens is not None)
+
+    @property
+    def window_bounded(self) -> bool:
+        """Only the window reaches far keys' blocks (no strided / far-dilated part)."""
+        return self.window is not None and self.stride is None and not self.dilation_far
 
 
 DENSE = MaskSpec()
@@ -66,16 +80,22 @@ def live_matrix(rows, cols, n: int, spec: MaskSpec) -> np.ndarray:
         ok = ok & (j <= i)
     if spec.has_pattern:
         part = np.zeros(ok.shape, dtype=bool)
-        if spec.window is not None or spec.dilation is not None:
+        near_dilated = spec.dilation is not None and not spec.dilation_far
+        if spec.window is not None or near_dilated:
             near_part = np.ones(ok.shape, dtype=bool)
             if spec.window is not None:
                 near_part &= np.abs(i - j) <= spec.window
-            if spec.dilation is not None:
+            if near_dilated:
                 delta = np.abs(i // spec.block - j // spec.block)
                 near_part &= (delta < spec.dilation_near) | (delta % spec.dilation == 0)
             part |= near_part
+        if spec.dilation is not None and spec.dilation_far:
+            part |= np.abs(i // spec.block - j // spec.block) % spec.dilation == 0
         if spec.stride is not None:
-            part |= (j // spec.block) % spec.stride == spec.stride_phase
+            if spec.stride_relative:
+                part |= np.mod(i // spec.block - j // spec.block, spec.stride) == spec.stride_phase
+            else:
+                part |= (j // spec.block) % spec.stride == spec.stride_phase
         if spec.global_tokens is not None:
             part |= (i < spec.global_tokens) | (j < spec.global_tokens)
         ok = ok & part
@@ -93,7 +113,7 @@ def candidate_cols(r0: int, r1: int, n: int, spec: MaskSpec) -> tuple[int, int]:
     c0, c1 = 0, n
     if spec.causal:
         c1 = min(c1, r1)
-    if spec.window is not None and spec.stride is None:
+    if spec.window_bounded:
         g = spec.global_tokens
         if g is None:
             c0 = max(c0, r0 - spec.window)
@@ -111,7 +131,7 @@ def candidate_col_array(r0: int, r1: int, n: int, spec: MaskSpec) -> np.ndarray:
     """
     c0, c1 = candidate_cols(r0, r1, n, spec)
     g = spec.global_tokens
-    if g is None or spec.window is None or spec.stride is not None or r0 < g:
+    if g is None or not spec.window_bounded or r0 < g:
         return np.arange(c0, c1)
     lo = max(g, r0 - spec.window)
     return np.concatenate([np.arange(0, min(g, c1)), np.arange(lo, max(lo, c1))])

@@ -23,6 +23,10 @@ SMALL_SPECS = {
     "strided_only": MaskSpec(causal=True, stride=2, stride_phase=0, block=4),
     "causal_window_global": MaskSpec(causal=True, window=4, global_tokens=8, block=4),
     "window_global": MaskSpec(window=3, global_tokens=4, block=4),
+    "causal_window_relstride": MaskSpec(causal=True, window=3, stride=3, stride_phase=0,
+                                        stride_relative=True, block=4),
+    "relstride_noncausal": MaskSpec(stride=2, stride_phase=1, stride_relative=True, block=4),
+    "causal_window_fardil": MaskSpec(causal=True, window=5, dilation=3, dilation_far=True, block=4),
 }
 
 fwd_full = attention.forward_head
@@ -63,6 +67,20 @@ def test_mask_hand_examples():
     assert live.tolist() == [[True, True, True]]
     live = live_matrix([2, 15], [0, 9, 19], 20, MaskSpec(causal=True, window=2, global_tokens=4))
     assert live.tolist() == [[True, False, False], [True, False, False]]
+    # relative strided (block 4, stride 3, phase 0): query block 4 keeps key
+    # blocks 4, 1 (distance 0, 3) and, not causal, 7 (distance -3)
+    spec = MaskSpec(stride=3, stride_phase=0, stride_relative=True, block=4)
+    live = live_matrix([17], [17, 4, 7, 8, 12, 28, 24], 32, spec)
+    assert live.tolist() == [[True, True, True, False, False, True, False]]
+    # phase 1 keeps distances 1, 4, -2, -5 (mod 3 = 1)
+    spec = MaskSpec(stride=3, stride_phase=1, stride_relative=True, block=4)
+    live = live_matrix([17], [12, 0, 24, 17], 32, spec)
+    assert live.tolist() == [[True, True, True, False]]
+    # far dilation (block 4, dilation 3): dense window 2 plus key blocks at
+    # block distance 0, 3, 6, ... anywhere
+    spec = MaskSpec(causal=True, window=2, dilation=3, dilation_far=True, block=4)
+    live = live_matrix([29], [27, 26, 25, 17, 16, 12, 5, 4], 32, spec)
+    assert live.tolist() == [[True, False, False, True, True, False, True, True]]
 
 
 @pytest.mark.parametrize("name", sorted(SMALL_SPECS))
@@ -220,6 +238,8 @@ def test_golden_tile_counts():
         "window1024_strided8_n32768": (32768, MaskSpec(causal=True, window=1024, stride=8)),
         "window4096_dilation2_n131072": (131072, MaskSpec(causal=True, window=4096, dilation=2, dilation_near=2)),
         "window8192_global512_n32768": (32768, MaskSpec(causal=True, window=8192, global_tokens=512)),
+        "window1024_relstride8_n32768": (32768, MaskSpec(causal=True, window=1024, stride=8, stride_relative=True)),
+        "window4096_fardilation2_n16384": (16384, MaskSpec(causal=True, window=4096, dilation=2, dilation_far=True)),
     }
     for key, (n, spec) in cases.items():
         idx = block_index.build(n, spec)
@@ -240,6 +260,12 @@ def test_closed_form_counts_formulas():
     def glob(nb, w=64, gb=4):
         return sum(qb + 1 if qb - w <= gb - 1 else w + 1 + gb for qb in range(nb))
     assert (glob(1024), glob(256)) == (68310, 15318)
+    # causal window of w blocks plus key blocks at block distances divisible
+    # by p beyond it (relative strides of p = 8, far dilation p = 2)
+    def beyond(nb, w, p):
+        return sum(min(qb, w) + 1 + sum(1 for dd in range(w + 1, qb + 1) if dd % p == 0)
+                   for qb in range(nb))
+    assert (beyond(256, 8, 8), beyond(1024, 32, 2), beyond(128, 32, 2)) == (5988, 278784, 5952)
     # partial: the diagonal plus the window edge kb = qb - 64 when it is not global
     assert (1024 + sum(1 for qb in range(1024) if qb - 64 >= 4),
             256 + sum(1 for qb in range(256) if qb - 64 >= 4)) == (1980, 444)
