@@ -60,12 +60,15 @@ typedef enum {
 
 /* Mask flags.  Element predicate for query i, key j of a length-N sequence:
  *   live(i,j) = (i < N) && (j < N) && (!CAUSAL || j <= i) && pattern(i,j)
- *   pattern   = true                          if no WINDOW/DILATED/STRIDED/GLOBAL flag
- *             = near(i,j) || strided(j) || global(i,j)   otherwise
+ *   pattern   = true                          if no pattern flag (all but CAUSAL)
+ *             = near || strided || strided_rel || far || global   otherwise
  *   near      = (WINDOW or DILATED set) && (!WINDOW || |i-j| <= window)
  *               && (!DILATED || D < dilation_near || D % dilation == 0),
  *               D = | floor(i/block) - floor(j/block) |
  *   strided   = STRIDED && floor(j/block) % stride == stride_phase
+ *   strided_rel = STRIDED_REL && (floor(i/block) - floor(j/block)) mod stride
+ *                 == stride_phase   (mod >= 0)
+ *   far       = DILATED_FAR && D % dilation == 0
  *   global    = GLOBAL && (i < global_tokens || j < global_tokens)
  * Window: "Local window -- attend only to +-W tokens"; dilated: "skip every
  * few tokens", read at block level; strided: the fixed pattern of Child et
@@ -73,13 +76,18 @@ typedef enum {
  * Flash-MSA Sparse Attention Works", list of masks).  Global: the local
  * window plus a few global tokens in the style of Longformer (same page,
  * section "How Do Sparse Attention Kernels Work in GPU Clusters?"), the
- * first global_tokens tokens attending and attended in both directions. */
+ * first global_tokens tokens attending and attended in both directions.
+ * STRIDED_REL and DILATED_FAR are the second readings of the strided and
+ * dilated masks: Child et al.'s strides counted from the query block, and
+ * a dense window with dilated key blocks kept at every distance. */
 enum {
   FLASH_MSA_CAUSAL = 1,
   FLASH_MSA_WINDOW = 2,
   FLASH_MSA_DILATED = 4,
   FLASH_MSA_STRIDED = 8,
-  FLASH_MSA_GLOBAL = 16
+  FLASH_MSA_GLOBAL = 16,
+  FLASH_MSA_STRIDED_REL = 32,
+  FLASH_MSA_DILATED_FAR = 64
 };
 
 /* Per-query-block list of live key blocks ("a precomputed index list", page
@@ -112,10 +120,11 @@ typedef struct flash_msa_block_index {
 
 /* Mask description (host memory).  A NULL mask, or flags == 0, is dense
  * attention.  flags == CAUSAL may pass index = NULL (tiles are derived
- * arithmetically); any WINDOW/DILATED/STRIDED/GLOBAL flag requires an index
- * built for the same N and mask, else FLASH_MSA_ERR_INDEX.  block must be 128.
- * window >= 0 (tokens, inclusive); dilation >= 1; dilation_near >= 0;
- * stride >= 1 and 0 <= stride_phase < stride when the flag is set;
+ * arithmetically); any other flag requires an index built for the same N
+ * and mask, else FLASH_MSA_ERR_INDEX.  block must be 128.
+ * window >= 0 (tokens, inclusive); dilation >= 1 (DILATED, DILATED_FAR);
+ * dilation_near >= 0; stride >= 1 and 0 <= stride_phase < stride when
+ * STRIDED or STRIDED_REL is set;
  * global_tokens >= 1 when GLOBAL is set (FLASH_MSA_ERR_INVALID_ARG
  * otherwise) and a multiple of the 128-token block (else
  * FLASH_MSA_ERR_UNSUPPORTED: every tile then keeps one interval of live

@@ -52,6 +52,10 @@ MASKS = [
     {"window": 130, "global_tokens": 256},
     {"causal": True, "global_tokens": 384},
     {"causal": True, "window": 300, "dilation": 2, "dilation_near": 1, "global_tokens": 128},
+    {"causal": True, "window": 200, "stride": 3, "stride_phase": 0, "stride_relative": True},
+    {"stride": 2, "stride_phase": 1, "stride_relative": True},
+    {"causal": True, "window": 300, "dilation": 3, "dilation_far": True},
+    {"window": 129, "dilation": 2, "dilation_far": True},
 ]
 
 
@@ -77,16 +81,28 @@ def test_random_indices_bit_exact():
             f["stride_phase"] = int(rng.integers(0, s))
         if rng.integers(0, 3) == 0:
             f["global_tokens"] = 128 * int(rng.integers(1, 5))
+        if "stride" in f and rng.integers(0, 2):
+            f["stride_relative"] = True
+        if "dilation" in f and rng.integers(0, 2):
+            f["dilation_far"] = True
         compare(n, f)
 
 
-def test_global_token_index_matches_hand_counts():
-    # the causal 8K window + 512 global tokens index at 128K and 32K tokens,
+def test_pattern_indices_match_hand_counts():
+    # global tokens, relative strides and far dilation at benchmark sizes,
     # against the counts derived by hand in tests/golden/tile_counts.json
     import json, os
     gold = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "tile_counts.json")))
-    for key, n in (("window8192_global512_n131072", 131072), ("window8192_global512_n32768", 32768)):
-        idx = api.build_block_index(api.Mask(causal=True, window=8192, global_tokens=512), n)
+    cases = (("window8192_global512_n131072", 131072, dict(causal=True, window=8192, global_tokens=512)),
+             ("window8192_global512_n32768", 32768, dict(causal=True, window=8192, global_tokens=512)),
+             ("window1024_relstride8_n32768", 32768,
+              dict(causal=True, window=1024, stride=8, stride_relative=True)),
+             ("window4096_fardilation2_n131072", 131072,
+              dict(causal=True, window=4096, dilation=2, dilation_far=True)),
+             ("window4096_fardilation2_n16384", 16384,
+              dict(causal=True, window=4096, dilation=2, dilation_far=True)))
+    for key, n, fields in cases:
+        idx = api.build_block_index(api.Mask(**fields), n)
         kind = idx.host["kind"]
         g = gold[key]
         assert (idx.nnz, int((kind == 0).sum()), int((kind == 1).sum())) == \

@@ -55,7 +55,7 @@ def test_fwd_argument_errors(L):
     assert fwd_raw(L, k=FAKE + 2) == api.ERR_INVALID_ARG
     assert fwd_raw(L, lse=FAKE + 1) == api.ERR_INVALID_ARG
     assert b"aligned" in L.flash_msa_last_error_string()
-    bad_flags = api.MaskDescStruct(64, 128, 0, 1, 0, 1, 0, None)
+    bad_flags = api.MaskDescStruct(128, 128, 0, 1, 0, 1, 0, None)
     assert fwd_raw(L, mask=bad_flags) == api.ERR_INVALID_ARG
     bad_block = api.Mask(causal=True, window=10, block=64).desc()
     assert fwd_raw(L, mask=bad_block) == api.ERR_UNSUPPORTED
@@ -70,6 +70,10 @@ def test_fwd_argument_errors(L):
     ragged_global = api.Mask(causal=True, window=100, global_tokens=100).desc()
     assert fwd_raw(L, mask=ragged_global) == api.ERR_UNSUPPORTED
     assert b"multiple of the 128-token block" in L.flash_msa_last_error_string()
+    bad_rel = api.Mask(causal=True, stride=4, stride_phase=5, stride_relative=True).desc()
+    assert fwd_raw(L, mask=bad_rel) == api.ERR_INVALID_ARG
+    bad_far = api.MaskDescStruct(api.WINDOW | api.DILATED_FAR, 128, 100, 0, 0, 1, 0, None, 0)
+    assert fwd_raw(L, mask=bad_far) == api.ERR_INVALID_ARG
 
 
 def test_index_for_another_n_is_rejected(L):

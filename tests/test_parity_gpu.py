@@ -32,6 +32,10 @@ SMALL_MASKS = {
     "strided_only": {"causal": True, "stride": 3, "stride_phase": 2},
     "window_global": {"causal": True, "window": 130, "global_tokens": 128},
     "global_noncausal": {"window": 100, "global_tokens": 256},
+    "relstride": {"causal": True, "window": 150, "stride": 2, "stride_phase": 0,
+                  "stride_relative": True},
+    "relstride_noncausal": {"stride": 3, "stride_phase": 1, "stride_relative": True},
+    "fardil": {"causal": True, "window": 200, "dilation": 2, "dilation_far": True},
 }
 
 
@@ -52,7 +56,7 @@ def test_small_cases(d, n, mname):
     gc.full_compare(inp, fields, res)
 
 
-@pytest.mark.parametrize("cid", [2, 3, 4, 5, 6])
+@pytest.mark.parametrize("cid", [2, 3, 4, 5, 6, 7])
 def test_full_size_workloads(cid):
     w = WORKLOADS[cid]
     inp = workload_inputs(w)
@@ -65,6 +69,34 @@ def test_full_size_workloads(cid):
     # outputs are finite everywhere (spot check of the whole tensors)
     for name in ("o", "dq", "dk", "dv"):
         assert np.isfinite(res[name]).all(), name
+
+
+def test_full_size_far_dilation_workload():
+    # 278784 live tiles per head: the oracle checks sampled forward rows at
+    # full size; the backward is checked there through properties that hold
+    # at any size (sum_j dK_j = 0 since every row of dS sums to 0, and
+    # sum_j dV_j = sum_i dO_i since every row of P sums to 1), and against
+    # the oracle on sampled rows / columns of the same mask at N = 16384
+    w = WORKLOADS[8]
+    inp = workload_inputs(w)
+    res = gc.run_gpu(inp, w.mask)
+    rng = np.random.default_rng(8)
+    rows = gc.sample_positions(w.N, rng)
+    gc.sampled_compare(inp, w.mask, res, [(0, 0), (w.B - 1, w.H - 1)], rows, [], backward=False)
+    do = inp["do"].double().numpy()
+    for h in range(w.H):
+        dk = res["dk"][0, :, h].astype(np.float64)
+        dv = res["dv"][0, :, h].astype(np.float64)
+        assert np.abs(dk.sum(axis=0)).max() <= 1e-2 * np.abs(dk).sum(axis=0).max()
+        assert np.abs(dv.sum(axis=0) - do[0, :, h].sum(axis=0)).max() <= \
+            1e-2 * np.abs(dv).sum(axis=0).max()
+    for name in ("o", "dq", "dk", "dv"):
+        assert np.isfinite(res[name]).all(), name
+    small = small_inputs(1, 16384, 2, 128, seed=88)
+    res = gc.run_gpu(small, w.mask)
+    rng = np.random.default_rng(88)
+    gc.sampled_compare(small, w.mask, res, [(0, 0), (0, 1)], gc.sample_positions(16384, rng),
+                       gc.sample_positions(16384, rng))
 
 
 def test_closed_form_uniform_on_gpu():

@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(_HERE, "libflashmsa.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE, ERR_INDEX = range(7)
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "TIMEOUT",
                 5: "WORKSPACE", 6: "INDEX"}
-CAUSAL, WINDOW, DILATED, STRIDED, GLOBAL = 1, 2, 4, 8, 16
+CAUSAL, WINDOW, DILATED, STRIDED, GLOBAL, STRIDED_REL, DILATED_FAR = 1, 2, 4, 8, 16, 32, 64
 
 # exported symbols, in the order include/flashmsa.h declares them
 SYMBOLS = (
@@ -141,6 +141,8 @@ class Mask:
     stride_phase: int = 0
     block: int = 128
     global_tokens: Optional[int] = None
+    stride_relative: bool = False  # the stride counted from the query block
+    dilation_far: bool = False     # dilated key blocks at every distance, window dense
 
     @classmethod
     def from_fields(cls, fields: dict) -> "Mask":
@@ -150,14 +152,16 @@ class Mask:
     def flags(self) -> int:
         f = CAUSAL if self.causal else 0
         f |= WINDOW if self.window is not None else 0
-        f |= DILATED if self.dilation is not None else 0
-        f |= STRIDED if self.stride is not None else 0
+        if self.dilation is not None:
+            f |= DILATED_FAR if self.dilation_far else DILATED
+        if self.stride is not None:
+            f |= STRIDED_REL if self.stride_relative else STRIDED
         f |= GLOBAL if self.global_tokens is not None else 0
         return f
 
     @property
     def needs_index(self) -> bool:
-        return bool(self.flags & (WINDOW | DILATED | STRIDED | GLOBAL))
+        return bool(self.flags & ~CAUSAL)
 
     def desc(self, index_ptr=None) -> MaskDescStruct:
         return MaskDescStruct(self.flags, self.block, self.window or 0, self.dilation or 1,

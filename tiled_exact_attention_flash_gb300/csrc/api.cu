@@ -77,10 +77,10 @@ static flash_msa_status check_mask(const flash_msa_mask_desc* m, MaskParams& mp,
   need_index = false;
   if (!m) return FLASH_MSA_OK;
   if (m->flags & ~uint32_t(FLASH_MSA_CAUSAL | FLASH_MSA_WINDOW | FLASH_MSA_DILATED |
-                           FLASH_MSA_STRIDED | FLASH_MSA_GLOBAL))
+                           FLASH_MSA_STRIDED | FLASH_MSA_GLOBAL | FLASH_MSA_STRIDED_REL |
+                           FLASH_MSA_DILATED_FAR))
     return set_error(FLASH_MSA_ERR_INVALID_ARG, "mask: unknown flag bits 0x%x", m->flags);
-  const uint32_t pat = m->flags & (FLASH_MSA_WINDOW | FLASH_MSA_DILATED | FLASH_MSA_STRIDED |
-                                   FLASH_MSA_GLOBAL);
+  const uint32_t pat = m->flags & ~uint32_t(FLASH_MSA_CAUSAL);
   if (m->block != kTile && !(m->block == 0 && pat == 0))
     return set_error(FLASH_MSA_ERR_UNSUPPORTED, "mask: pattern block %d (only 128 is supported)",
                      m->block);
@@ -89,13 +89,13 @@ static flash_msa_status check_mask(const flash_msa_mask_desc* m, MaskParams& mp,
     if (m->window < 0) return set_error(FLASH_MSA_ERR_INVALID_ARG, "mask: window < 0");
     mp.window = m->window < kUnbounded ? m->window : kUnbounded;
   }
-  if (m->flags & FLASH_MSA_DILATED) {
+  if (m->flags & (FLASH_MSA_DILATED | FLASH_MSA_DILATED_FAR)) {
     if (m->dilation < 1 || m->dilation_near < 0)
       return set_error(FLASH_MSA_ERR_INVALID_ARG, "mask: dilation must be >= 1, near >= 0");
     mp.dilation = m->dilation;
     mp.near = m->dilation_near;
   }
-  if (m->flags & FLASH_MSA_STRIDED) {
+  if (m->flags & (FLASH_MSA_STRIDED | FLASH_MSA_STRIDED_REL)) {
     if (m->stride < 1 || m->stride_phase < 0 || m->stride_phase >= m->stride)
       return set_error(FLASH_MSA_ERR_INVALID_ARG, "mask: stride must be >= 1, 0 <= phase < stride");
     mp.stride = m->stride;
@@ -199,7 +199,9 @@ flash_msa_status flash_msa_build_block_index(const flash_msa_mask_desc* mask, in
   // candidate key blocks per query block: causal and a plain window bound the
   // span; with global tokens the global key blocks come first, and a global
   // query block scans every key block
-  const bool window_bound = (mp.flags & FLASH_MSA_WINDOW) && !(mp.flags & FLASH_MSA_STRIDED);
+  const bool window_bound =
+      (mp.flags & FLASH_MSA_WINDOW) &&
+      !(mp.flags & (FLASH_MSA_STRIDED | FLASH_MSA_STRIDED_REL | FLASH_MSA_DILATED_FAR));
   const int64_t span = window_bound ? mp.window / kTile + 2 : nb;
   const int64_t gb = (mp.flags & FLASH_MSA_GLOBAL) ? std::min<int64_t>(mp.global_blocks, nb) : 0;
   auto for_each_tile = [&](auto&& fn) {

@@ -38,22 +38,29 @@ struct DeltaRange {
 
 __host__ __device__ inline DeltaRange tile_delta_range(int qb, int kb, const MaskParams& m) {
   DeltaRange r{false, -kUnbounded, kUnbounded};
-  const uint32_t pat =
-      m.flags & (FLASH_MSA_WINDOW | FLASH_MSA_DILATED | FLASH_MSA_STRIDED | FLASH_MSA_GLOBAL);
+  const uint32_t pat = m.flags & (FLASH_MSA_WINDOW | FLASH_MSA_DILATED | FLASH_MSA_STRIDED |
+                                  FLASH_MSA_GLOBAL | FLASH_MSA_STRIDED_REL | FLASH_MSA_DILATED_FAR);
   // a tile of a global query block or global key block: every pair passes
   // the pattern, only the causal part remains
   const bool global_tile =
       (m.flags & FLASH_MSA_GLOBAL) && (qb < m.global_blocks || kb < m.global_blocks);
   bool window_applies = false;
   if (pat && !global_tile) {
-    const bool strided_ok = (m.flags & FLASH_MSA_STRIDED) && (kb % m.stride == m.phase);
+    // parts that keep a whole tile (subject to causal): strided key block,
+    // relative stride, dilated block distance at any range
+    const int dq = qb - kb;
+    const int dd = dq < 0 ? -dq : dq;
+    int rel = dq % m.stride;
+    if (rel < 0) rel += m.stride;
+    const bool strided_ok = ((m.flags & FLASH_MSA_STRIDED) && (kb % m.stride == m.phase)) ||
+                            ((m.flags & FLASH_MSA_STRIDED_REL) && rel == m.phase) ||
+                            ((m.flags & FLASH_MSA_DILATED_FAR) && dd % m.dilation == 0);
     if (!strided_ok) {
       if (!(m.flags & (FLASH_MSA_WINDOW | FLASH_MSA_DILATED))) {
         r.none = true;
         return r;
       }
       if (m.flags & FLASH_MSA_DILATED) {
-        const int dd = qb > kb ? qb - kb : kb - qb;
         if (!(dd < m.near || dd % m.dilation == 0)) {
           r.none = true;
           return r;

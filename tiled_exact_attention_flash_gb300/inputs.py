@@ -9,7 +9,8 @@ the oracle consumes the same values promoted exactly to float64.
 Workloads: the five attention configurations the pages' discussion motivates
 (7B-style layer, d = 128, long context; causal, local window + strided, and
 local window with block dilation), plus a sixth for the local window with
-global tokens hybrid (8K window, 512 global tokens, 128K tokens).  Seeds: Q, K, V, dO of workload c use
+global tokens hybrid (8K window, 512 global tokens, 128K tokens) and two
+more with the second readings of the strided and dilated masks.  Seeds: Q, K, V, dO of workload c use
 1000*c + 1 .. 1000*c + 4.
 """
 from __future__ import annotations
@@ -47,6 +48,12 @@ WORKLOADS = {
     # local window plus global tokens: 8K window and 512 global tokens at 128K
     6: Workload(6, "causal window8192 + global512 B1 H8 N131072 d128", 1, 8, 131072, 128,
                 {"causal": True, "window": 8192, "global_tokens": 512}),
+    # the second readings of the strided and dilated masks on the shapes of 4 and 5
+    7: Workload(7, "causal window1024 + relative strided8 B1 H32 N32768 d128", 1, 32, 32768, 128,
+                {"causal": True, "window": 1024, "stride": 8, "stride_phase": 0,
+                 "stride_relative": True}),
+    8: Workload(8, "causal window4096 + far dilation2 B1 H8 N131072 d128", 1, 8, 131072, 128,
+                {"causal": True, "window": 4096, "dilation": 2, "dilation_far": True}),
 }
 
 
