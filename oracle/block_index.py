@@ -16,6 +16,13 @@ and the lists are built from that classification:
     q_order / k_order:   query / key blocks sorted by descending live-tile
                          count, ties by ascending index (longest work first)
 
+With a bit-packed mask, a partial tile whose live set differs from the live
+set of the same mask without the bits carries its live entries as bits:
+slots are numbered in CSR order; bits[slot] holds 128 rows (query) of four
+32-bit words (key bit c in word c // 32, bit c % 32) and bits_t[slot] the
+transpose (128 key rows of four words over the queries); bit_slot /
+bit_slot_t give each CSR / CSC entry its slot or -1.
+
 For masks with a local window and no strided part, key blocks farther than
 the window from the query block are skipped without evaluation: by the window
 definition none of their entries is live (with global tokens, the key
@@ -25,6 +32,8 @@ still evaluated).  Tests check this shortcut against the full evaluation.
 from __future__ import annotations
 
 import numpy as np
+
+import dataclasses
 
 from .mask import MaskSpec, live_matrix
 
@@ -57,6 +66,12 @@ def classify(n: int, spec: MaskSpec, tile: int = 128, prune: bool = True) -> np.
     return kinds
 
 
+def _pack_rows(live: np.ndarray) -> np.ndarray:
+    """(rows, 128) booleans -> (rows, 4) uint32 words, column c in word c // 32, bit c % 32."""
+    weights = (np.uint32(1) << np.arange(32, dtype=np.uint32))
+    return (live.reshape(live.shape[0], 4, 32).astype(np.uint32) * weights).sum(axis=2).astype(np.uint32)
+
+
 def build(n: int, spec: MaskSpec, tile: int = 128, prune: bool = True) -> dict:
     kinds = classify(n, spec, tile, prune)
     nb = kinds.shape[0]
@@ -74,6 +89,27 @@ def build(n: int, spec: MaskSpec, tile: int = 128, prune: bool = True) -> dict:
         row_idx.extend(qbs.tolist())
         kind_t.extend(kinds[qbs, kb].tolist())
         col_ptr[kb + 1] = col_ptr[kb] + len(qbs)
+    # bit tiles (bit-packed masks only)
+    bit_slot = np.full(len(col_idx), -1, dtype=np.int32)
+    bits, bits_t = [], []
+    if spec.bitmask is not None:
+        plain = dataclasses.replace(spec, bitmask=None)
+        for qb in range(nb):
+            rows = np.arange(qb * tile, qb * tile + tile)
+            for e in range(row_ptr[qb], row_ptr[qb + 1]):
+                if kind[e] != PARTIAL:
+                    continue
+                cols = np.arange(col_idx[e] * tile, col_idx[e] * tile + tile)
+                live = live_matrix(rows, cols, n, spec)
+                if np.array_equal(live, live_matrix(rows, cols, n, plain)):
+                    continue
+                bit_slot[e] = len(bits)
+                bits.append(_pack_rows(live))
+                bits_t.append(_pack_rows(live.T))
+    slot_of = {(qb, int(col_idx[e])): int(bit_slot[e])
+               for qb in range(nb) for e in range(row_ptr[qb], row_ptr[qb + 1])}
+    bit_slot_t = np.array([slot_of[(int(qb), kb)] for kb in range(nb)
+                           for qb in row_idx[col_ptr[kb]:col_ptr[kb + 1]]], dtype=np.int32)
     row_len = np.diff(row_ptr)
     col_len = np.diff(col_ptr)
     q_order = np.array(sorted(range(nb), key=lambda b: (-row_len[b], b)), dtype=np.int32)
@@ -89,4 +125,9 @@ def build(n: int, spec: MaskSpec, tile: int = 128, prune: bool = True) -> dict:
         "kind_t": np.array(kind_t, dtype=np.uint8),
         "q_order": q_order,
         "k_order": k_order,
+        "n_bit_tiles": len(bits),
+        "bit_slot": bit_slot,
+        "bit_slot_t": bit_slot_t,
+        "bits": (np.concatenate(bits).reshape(-1) if bits else np.zeros(0, np.uint32)),
+        "bits_t": (np.concatenate(bits_t).reshape(-1) if bits_t else np.zeros(0, np.uint32)),
     }

@@ -23,6 +23,12 @@ def live_scalar(i: int, j: int, n: int, spec: MaskSpec) -> bool:
         return False
     if spec.causal and j > i:
         return False
+    if spec.bitmask is not None:
+        w = (n + 31) // 32
+        at = 4 * (i * w + j // 32)
+        word = int.from_bytes(spec.bitmask[at:at + 4], "little")
+        if not (word >> (j % 32)) & 1:
+            return False
     if not spec.has_pattern:
         return True
     qb, kb = i // spec.block, j // spec.block

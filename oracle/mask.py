@@ -30,7 +30,14 @@ Definitions, one per mask kind named on the pages:
   symmetrically: the first G tokens are global, so a global query attends
   every key and every query attends the global keys.
 
-Combination: live = in_range AND causal_part AND pattern, where pattern is
+* bit-packed mask -- an arbitrary element mask given as bits, the "bitmask"
+  the pages name beside the block index as the cheap way to keep a mask
+  ("Flash MSA Attention Kernel Implementation", section "Optimization Tricks
+  That Actually Matter", paragraph "Masking and causal attention"): row i is
+  ceil(N/32) little-endian 32-bit words, bit j % 32 of word j // 32 set iff
+  the pair may be live.  It is AND-ed with everything else.
+
+Combination: live = in_range AND causal_part AND pattern [AND bit], where pattern is
 true when no window/dilation/stride/global part is set, and otherwise
 (window AND dilation part) OR (strided part) OR (far dilation part) OR
 (global part).
@@ -55,6 +62,7 @@ class MaskSpec:
     global_tokens: Optional[int] = None  # G: queries and keys 0..G-1 are global
     stride_relative: bool = False    # stride part relative to the query block
     dilation_far: bool = False       # dilation as its own part, at every distance
+    bitmask: Optional[bytes] = None  # packed rows, N x ceil(N/32) little-endian uint32
 
     @property
     def has_pattern(self) -> bool:
@@ -99,7 +107,23 @@ def live_matrix(rows, cols, n: int, spec: MaskSpec) -> np.ndarray:
         if spec.global_tokens is not None:
             part |= (i < spec.global_tokens) | (j < spec.global_tokens)
         ok = ok & part
+    if spec.bitmask is not None:
+        ok = ok & bit_matrix(spec.bitmask, n, i, j)
     return ok
+
+
+def bit_matrix(bitmask: bytes, n: int, i, j) -> np.ndarray:
+    """bit(i, j) of a packed row-major mask (indices outside [0, n) read as 0)."""
+    w = (n + 31) // 32
+    words = np.frombuffer(bitmask, dtype="<u4")
+    if words.size != n * w:
+        raise ValueError(f"bitmask has {words.size} words, expected {n} x {w}")
+    words = words.reshape(n, w)
+    inside = (i >= 0) & (i < n) & (j >= 0) & (j < n)
+    ii = np.clip(i, 0, n - 1)
+    jj = np.clip(j, 0, n - 1)
+    bit = (words[ii, jj // 32] >> (jj % 32).astype(np.uint32)) & np.uint32(1)
+    return inside & (bit != 0)
 
 
 def candidate_cols(r0: int, r1: int, n: int, spec: MaskSpec) -> tuple[int, int]:

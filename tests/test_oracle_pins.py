@@ -407,3 +407,104 @@ def test_backward_mistakes_fail_a_pin(mutant):
         pins.finite_differences(fwd_full, mutant, 6, 2, spec, r),
     ]
     assert max(errs) > 1e-3, errs
+
+
+# ---------------------------------------------------------------- bit-packed masks
+def _random_bits(n, seed, p=0.5):
+    return np.random.default_rng(seed).random((n, n)) < p
+
+
+def test_bitmask_hand_example():
+    from tiled_exact_attention_flash_gb300.inputs import pack_bitmask
+    live = np.zeros((8, 8), dtype=bool)
+    live[5, [0, 2, 5, 7]] = True
+    live[1, 1] = True
+    b = pack_bitmask(live)
+    spec = MaskSpec(bitmask=b)
+    assert live_matrix([5], range(8), 8, spec).tolist() == [[True, False, True, False, False, True, False, True]]
+    # AND-ed with causal and with the pattern parts
+    spec = MaskSpec(causal=True, bitmask=b)
+    assert live_matrix([5], range(8), 8, spec).tolist() == [[True, False, True, False, False, True, False, False]]
+    spec = MaskSpec(window=2, bitmask=b)
+    assert live_matrix([5], range(8), 8, spec).tolist() == [[False] * 5 + [True, False, True]]
+    # the packed layout itself: row 5 is one word with bits 0, 2, 5, 7
+    assert int.from_bytes(b[4 * 5:4 * 6], "little") == 1 | 4 | 32 | 128
+
+
+BIT_CASES = [(37, {}), (37, {"causal": True}), (41, {"causal": True, "window": 6}),
+             (29, {"window": 4, "stride": 2, "stride_phase": 1, "block": 4})]
+
+
+@pytest.mark.parametrize("case", range(len(BIT_CASES)))
+def test_bitmask_scalar_and_closed_forms(case):
+    from tiled_exact_attention_flash_gb300.inputs import pack_bitmask
+    n, fields = BIT_CASES[case]
+    bits = _random_bits(n, 100 + case)
+    spec = MaskSpec(bitmask=pack_bitmask(bits), **fields)
+    idx = np.arange(-2, n + 3)
+    m = live_matrix(idx, idx, n, spec)
+    ref = np.array([[loops.live_scalar(int(i), int(j), n, spec) for j in idx] for i in idx])
+    assert (m == ref).all()
+    # the bits act as an AND on top of the mask without them
+    plain = live_matrix(np.arange(n), np.arange(n), n, MaskSpec(**fields))
+    assert (live_matrix(np.arange(n), np.arange(n), n, spec) == (plain & bits)).all()
+    # Q = 0: O_i is the mean of v_j over j with bit and mask set, counted from the
+    # boolean matrix the bits were packed from
+    r = rng(case)
+    q = np.zeros((n, 5))
+    k, v = r.standard_normal((n, 5)), r.standard_normal((n, 5))
+    o, lse = fwd_full(q, k, v, 0.4, spec)
+    for i in range(n):
+        sel = plain[i] & bits[i]
+        if sel.any():
+            assert np.abs(o[i] - v[sel].mean(axis=0)).max() < 1e-12
+            assert abs(lse[i] - np.log(sel.sum())) < 1e-12
+        else:
+            assert lse[i] == -np.inf and not o[i].any()
+
+
+def test_bitmask_finite_differences():
+    from tiled_exact_attention_flash_gb300.inputs import pack_bitmask
+    bits = _random_bits(8, 5, 0.6)
+    spec = MaskSpec(causal=True, bitmask=pack_bitmask(bits))
+    assert pins.finite_differences(fwd_full, bwd_full, 8, 3, spec, rng(9)) < 1e-6
+
+
+@pytest.mark.parametrize("n,fields", [(300, {}), (300, {"causal": True, "window": 100}),
+                                      (519, {"causal": True})])
+def test_bitmask_index_tiles_hold_the_live_entries(n, fields):
+    # every partial tile that the bits cut carries exactly its live entries,
+    # unpacked here with numpy's unpackbits (independent of the packing code)
+    from tiled_exact_attention_flash_gb300.inputs import document_bitmask, document_lengths
+    spec = MaskSpec(bitmask=document_bitmask(n, document_lengths(n, n, 60)), **fields)
+    idx = block_index.build(n, spec)
+    full = live_matrix(np.arange(n), np.arange(n), n, spec)
+    plain = live_matrix(np.arange(n), np.arange(n), n, MaskSpec(**fields))
+    nb = idx["n_blocks"]
+
+    def unpack(words):
+        return np.unpackbits(words.astype("<u4").view(np.uint8).reshape(128, 16), axis=1,
+                             bitorder="little").astype(bool)
+
+    def tile(mat, qb, kb):
+        t = np.zeros((128, 128), dtype=bool)
+        sub = mat[qb * 128:(qb + 1) * 128, kb * 128:(kb + 1) * 128]
+        t[:sub.shape[0], :sub.shape[1]] = sub
+        return t
+    slots = 0
+    for qb in range(nb):
+        for e in range(idx["row_ptr"][qb], idx["row_ptr"][qb + 1]):
+            kb, slot = int(idx["col_idx"][e]), int(idx["bit_slot"][e])
+            cut = not np.array_equal(tile(full, qb, kb), tile(plain, qb, kb))
+            assert (slot >= 0) == (cut and idx["kind"][e] == 1)
+            if slot >= 0:
+                slots += 1
+                assert np.array_equal(unpack(idx["bits"][slot * 512:(slot + 1) * 512]), tile(full, qb, kb))
+                assert np.array_equal(unpack(idx["bits_t"][slot * 512:(slot + 1) * 512]), tile(full, qb, kb).T)
+    assert slots == idx["n_bit_tiles"]
+    # the CSC entries point at the same slots
+    for kb in range(nb):
+        for e in range(idx["col_ptr"][kb], idx["col_ptr"][kb + 1]):
+            qb = int(idx["row_idx"][e])
+            row = np.nonzero(idx["col_idx"][idx["row_ptr"][qb]:idx["row_ptr"][qb + 1]] == kb)[0][0]
+            assert idx["bit_slot_t"][e] == idx["bit_slot"][idx["row_ptr"][qb] + row]

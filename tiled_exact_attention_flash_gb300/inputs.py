@@ -77,3 +77,47 @@ def small_inputs(B, N, H, d, seed: int, names=("q", "k", "v", "do")) -> dict:
 def as_f64(t: torch.Tensor) -> np.ndarray:
     """Exact promotion of a (bf16) tensor to a float64 numpy array."""
     return t.detach().to("cpu").to(torch.float64).numpy()
+
+
+# ---------------------------------------------------------------------------
+# bit-packed masks: row i is ceil(N/32) little-endian uint32 words, bit j % 32
+# of word j // 32 set iff the pair (i, j) may be live
+# ---------------------------------------------------------------------------
+def pack_bitmask(live: np.ndarray) -> bytes:
+    """(N, N) booleans -> packed rows."""
+    n = live.shape[0]
+    w = (n + 31) // 32
+    padded = np.zeros((n, w * 32), dtype=bool)
+    padded[:, :n] = live
+    words = np.packbits(padded.reshape(n, w, 4, 8)[..., ::-1], axis=-1).reshape(n, w, 4)
+    return words.astype(np.uint8).tobytes()
+
+
+def document_lengths(n: int, seed: int, mean: int) -> list:
+    """Seeded lengths of the documents packed into one sequence of n tokens
+    (exponentially distributed around `mean`, at least 1 token each)."""
+    rng = np.random.default_rng(seed)
+    lens, total = [], 0
+    while total < n:
+        ln = max(1, int(rng.exponential(mean)))
+        ln = min(ln, n - total)
+        lens.append(ln)
+        total += ln
+    return lens
+
+
+def document_bitmask(n: int, lengths) -> bytes:
+    """Packed mask of a sequence of packed documents: (i, j) may be live iff
+    both tokens belong to the same document (built row block by row block,
+    without an (N, N) boolean matrix)."""
+    w = (n + 31) // 32
+    words = np.zeros((n, w), dtype=np.uint32)
+    start = 0
+    for ln in lengths:
+        end = start + ln
+        row = np.zeros(w * 32, dtype=bool)
+        row[start:end] = True
+        packed = (row.reshape(w, 32).astype(np.uint64) << np.arange(32, dtype=np.uint64)).sum(axis=1)
+        words[start:end] = packed.astype(np.uint32)
+        start = end
+    return words.astype("<u4").tobytes()
