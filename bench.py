@@ -98,6 +98,14 @@ def live_flops(w, nnz):
 FULL_ORACLE_MAX_N = 4096  # above this a head's (N, N) float64 matrices get too large
 
 
+def mask_config(w):
+    """The workload's mask for the JSON line (packed documents described, not listed)."""
+    cfg = dict(w.mask)
+    if w.docs is not None:
+        cfg["documents"] = {"mean_tokens": w.docs[0], "seed": w.docs[1], "bitmask": True}
+    return cfg
+
+
 def _oracle_head_job(args):
     """Oracle on one head: fwd + bwd with full materialisation for N <= 4096,
     else the row-chunked forward only."""
@@ -127,7 +135,7 @@ def oracle_sample_inputs(w, n_heads):
     jobs = []
     for idx in range(n_heads):
         b, h = divmod(idx, w.H)
-        jobs.append(tuple(as_f64(inp[n][b, :, h]) for n in ("q", "k", "v", "do")) + (dict(w.mask),))
+        jobs.append(tuple(as_f64(inp[n][b, :, h]) for n in ("q", "k", "v", "do")) + (w.mask_fields(),))
     return jobs
 
 
@@ -245,7 +253,8 @@ def run_ours(args):
     dev = torch.device("cuda", local if world > 1 else 0)
     stream = torch.cuda.current_stream(dev)
 
-    mask = api.Mask(**w.mask) if w.mask else None
+    fields = w.mask_fields()
+    mask = api.Mask(**fields) if fields else None
     index = None
     if mask is not None and mask.needs_index:
         index = api.build_block_index(mask, w.N).to(dev)
@@ -393,7 +402,7 @@ def run_ours(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic: seeded N(0,1) fp32 rounded to bf16",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
-                       "mask": w.mask, "live_tiles_per_head": nnz, "layout": "(B,N,H,d)",
+                       "mask": mask_config(w), "live_tiles_per_head": nnz, "layout": "(B,N,H,d)",
                        "l2": "no flush: working set of 8 (B,N,H,d) bf16 tensors "
                              f"= {8 * B * N * H * d * 2 / 2**20:.0f} MiB > 129 MB L2"},
             "fwd_tflops": round(fwd_tflops, 2), "bwd_tflops": round(bwd_tflops, 2),
@@ -430,8 +439,9 @@ def run_reference(args):
     w = WORKLOADS[args.config]
     from oracle import block_index
     from oracle.mask import MaskSpec
-    nnz = block_index.build(w.N, MaskSpec(**w.mask))["nnz"] if w.mask.get("window") or \
-        w.mask.get("stride") or w.mask.get("dilation") else None
+    fields = w.mask_fields()
+    nnz = block_index.build(w.N, MaskSpec(**fields))["nnz"] \
+        if any(key != "causal" for key in fields) else None
     if nnz is None:
         nb = (w.N + TILE - 1) // TILE
         nnz = nb * (nb + 1) // 2 if w.mask.get("causal") else nb * nb
@@ -454,7 +464,7 @@ def run_reference(args):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic: seeded N(0,1) fp32 rounded to bf16",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "mask": w.mask},
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "mask": mask_config(w)},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": pool.workers,
                          "kind": "oracle",
                          "sample": f"each step: {n_heads} of {w.B * w.H} heads, float64 "

@@ -70,6 +70,10 @@ typedef enum {
  *                 == stride_phase   (mod >= 0)
  *   far       = DILATED_FAR && D % dilation == 0
  *   global    = GLOBAL && (i < global_tokens || j < global_tokens)
+ * and with BITMASK, live(i,j) is further AND-ed with bit(i,j) of the bit-packed
+ * mask given to flash_msa_build_block_index (the "bitmask" named beside the
+ * block index, page "Flash MSA Attention Kernel Implementation", section
+ * "Optimization Tricks That Actually Matter", "Masking and causal attention").
  * Window: "Local window -- attend only to +-W tokens"; dilated: "skip every
  * few tokens", read at block level; strided: the fixed pattern of Child et
  * al. (page "How Does Flash-MSA Sparse Attention Work", section "How
@@ -87,7 +91,8 @@ enum {
   FLASH_MSA_STRIDED = 8,
   FLASH_MSA_GLOBAL = 16,
   FLASH_MSA_STRIDED_REL = 32,
-  FLASH_MSA_DILATED_FAR = 64
+  FLASH_MSA_DILATED_FAR = 64,
+  FLASH_MSA_BITMASK = 128
 };
 
 /* Per-query-block list of live key blocks ("a precomputed index list", page
@@ -100,6 +105,12 @@ enum {
  *   CSC by key block:   col_ptr[n_k_blocks+1], row_idx[nnz] (ascending), kind_t[nnz]
  *   q_order[n_q_blocks] / k_order[n_k_blocks]: blocks by descending live-tile
  *   count, ties by ascending index (longest work is scheduled first).
+ * With a BITMASK mask, a partial tile whose live entries are not all given
+ * by the other mask parts carries them as bits, in a slot numbered in CSR
+ * order: bits[512 slot + 4 r + c / 32] bit c % 32 = live(128 qb + r,
+ * 128 kb + c), and bits_t the transpose (4 words per key row over the
+ * queries); bit_slot[e] / bit_slot_t[e] give the slot of CSR / CSC entry e or
+ * -1.  n_bit_tiles = 0 (and null bit arrays) for every other mask.
  * The struct itself always lives in HOST memory.  Its array pointers are host
  * pointers when filled by flash_msa_build_block_index() and DEVICE pointers
  * when passed to flash_msa_fwd()/flash_msa_bwd() (copy the arrays over and
@@ -116,6 +127,11 @@ typedef struct flash_msa_block_index {
   uint8_t* kind_t;
   int32_t* q_order;
   int32_t* k_order;
+  int64_t n_bit_tiles;
+  int32_t* bit_slot;   /* [nnz] */
+  int32_t* bit_slot_t; /* [nnz] */
+  uint32_t* bits;      /* [512 n_bit_tiles] */
+  uint32_t* bits_t;    /* [512 n_bit_tiles] */
 } flash_msa_block_index;
 
 /* Mask description (host memory).  A NULL mask, or flags == 0, is dense
@@ -128,7 +144,9 @@ typedef struct flash_msa_block_index {
  * global_tokens >= 1 when GLOBAL is set (FLASH_MSA_ERR_INVALID_ARG
  * otherwise) and a multiple of the 128-token block (else
  * FLASH_MSA_ERR_UNSUPPORTED: every tile then keeps one interval of live
- * keys per row). */
+ * keys per row).  bitmask (BITMASK only, HOST memory, read only by
+ * flash_msa_build_block_index): N rows of ceil(N/32) little-endian uint32
+ * words, bit j % 32 of word j / 32 of row i set iff (i, j) may be live. */
 typedef struct {
   uint32_t flags;
   int32_t block;
@@ -137,15 +155,18 @@ typedef struct {
   int32_t stride, stride_phase;
   const flash_msa_block_index* index;
   int64_t global_tokens;
+  const uint32_t* bitmask;
 } flash_msa_mask_desc;
 
 /* Build the block index for `mask` and sequence length N on the HOST (no GPU
  * work).  Two phases: call with out->row_ptr == NULL to fill only the counts
- * (seq_len, n_q_blocks, n_k_blocks, block, nnz); allocate every array with
- * those sizes (row_ptr/col_ptr n+1 int32, col_idx/row_idx nnz int32,
- * kind/kind_t nnz uint8, q_order/k_order n int32) and call again to fill
- * them.  mask->index is ignored.  Errors: INVALID_ARG (null, N < 1, bad
- * field), UNSUPPORTED (block != 128). */
+ * (seq_len, n_q_blocks, n_k_blocks, block, nnz, n_bit_tiles); allocate every
+ * array with those sizes (row_ptr/col_ptr n+1 int32, col_idx/row_idx nnz
+ * int32, kind/kind_t nnz uint8, q_order/k_order n int32; with BITMASK also
+ * bit_slot/bit_slot_t nnz int32 and bits/bits_t 512 n_bit_tiles uint32) and
+ * call again to fill them.  mask->index is ignored.  Errors: INVALID_ARG
+ * (null, N < 1, bad field, BITMASK without mask->bitmask), UNSUPPORTED
+ * (block != 128). */
 flash_msa_status flash_msa_build_block_index(const flash_msa_mask_desc* mask, int64_t N,
                                              flash_msa_block_index* out);
 

@@ -20,7 +20,11 @@ def compare(n, fields):
     got = api.build_block_index(api.Mask(**fields), n)
     assert got.nnz == ref["nnz"]
     assert got.header.n_q_blocks == ref["n_blocks"] == got.header.n_k_blocks
-    for name in ARRAYS:
+    names = ARRAYS
+    if fields.get("bitmask") is not None:
+        assert got.header.n_bit_tiles == ref["n_bit_tiles"]
+        names = ARRAYS + ("bit_slot", "bit_slot_t", "bits", "bits_t")
+    for name in names:
         a, b = got.host[name], ref[name]
         assert a.dtype == b.dtype, name
         assert np.array_equal(a, b), name
@@ -28,13 +32,10 @@ def compare(n, fields):
     return got
 
 
-@pytest.mark.parametrize("cid", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("cid", [1, 2, 3, 4, 5, 9])
 def test_workload_indices_bit_exact(cid):
     w = WORKLOADS[cid]
-    fields = dict(w.mask)
-    if not fields:
-        fields = {}
-    compare(w.N, fields)
+    compare(w.N, w.mask_fields())
 
 
 MASKS = [
@@ -120,3 +121,27 @@ def test_checker_rejects_corruption():
         assert api.check_block_index(idx) == api.ERR_INDEX, name
         idx.host[name][pos] = saved
     assert api.check_block_index(idx) == api.OK
+
+
+@pytest.mark.parametrize("n,fields,seed", [
+    (300, {}, 1), (519, {"causal": True}, 2), (1000, {"causal": True, "window": 200}, 3),
+    (700, {"window": 130, "stride": 2, "stride_phase": 1}, 4),
+    (640, {"causal": True, "global_tokens": 128, "window": 100}, 5)])
+def test_bitmask_indices_bit_exact(n, fields, seed):
+    from tiled_exact_attention_flash_gb300.inputs import (document_bitmask, document_lengths,
+                                                          pack_bitmask)
+    # packed documents, then a random element mask
+    compare(n, dict(fields, bitmask=document_bitmask(n, document_lengths(n, seed, 90))))
+    live = np.random.default_rng(seed).random((n, n)) < 0.7
+    live[:, :64] = True  # some tiles stay untouched by the bits
+    compare(n, dict(fields, bitmask=pack_bitmask(live)))
+
+
+def test_bitmask_requires_the_bits():
+    m = api.Mask(causal=True)
+    desc = m.desc()
+    desc.flags |= api.BITMASK
+    hdr = api.BlockIndexStruct()
+    import ctypes
+    assert api.lib().flash_msa_build_block_index(ctypes.byref(desc), 300, ctypes.byref(hdr)) == \
+        api.ERR_INVALID_ARG

@@ -42,8 +42,8 @@ SMALL_MASKS = {
 def test_workload1_full():
     w = WORKLOADS[1]
     inp = workload_inputs(w)
-    res = gc.run_gpu(inp, w.mask)
-    gc.full_compare(inp, w.mask, res)
+    res = gc.run_gpu(inp, w.mask_fields())
+    gc.full_compare(inp, w.mask_fields(), res)
 
 
 @pytest.mark.parametrize("d", [64, 128])
@@ -56,16 +56,16 @@ def test_small_cases(d, n, mname):
     gc.full_compare(inp, fields, res)
 
 
-@pytest.mark.parametrize("cid", [2, 3, 4, 5, 6, 7])
+@pytest.mark.parametrize("cid", [2, 3, 4, 5, 6, 7, 9])
 def test_full_size_workloads(cid):
     w = WORKLOADS[cid]
     inp = workload_inputs(w)
-    res = gc.run_gpu(inp, w.mask)
+    res = gc.run_gpu(inp, w.mask_fields())
     rng = np.random.default_rng(cid)
     heads = [(0, 0), (w.B - 1, w.H - 1)]
     rows = gc.sample_positions(w.N, rng)
     cols = gc.sample_positions(w.N, rng)
-    gc.sampled_compare(inp, w.mask, res, heads, rows, cols)
+    gc.sampled_compare(inp, w.mask_fields(), res, heads, rows, cols)
     # outputs are finite everywhere (spot check of the whole tensors)
     for name in ("o", "dq", "dk", "dv"):
         assert np.isfinite(res[name]).all(), name
@@ -79,10 +79,10 @@ def test_full_size_far_dilation_workload():
     # the oracle on sampled rows / columns of the same mask at N = 16384
     w = WORKLOADS[8]
     inp = workload_inputs(w)
-    res = gc.run_gpu(inp, w.mask)
+    res = gc.run_gpu(inp, w.mask_fields())
     rng = np.random.default_rng(8)
     rows = gc.sample_positions(w.N, rng)
-    gc.sampled_compare(inp, w.mask, res, [(0, 0), (w.B - 1, w.H - 1)], rows, [], backward=False)
+    gc.sampled_compare(inp, w.mask_fields(), res, [(0, 0), (w.B - 1, w.H - 1)], rows, [], backward=False)
     do = inp["do"].double().numpy()
     for h in range(w.H):
         dk = res["dk"][0, :, h].astype(np.float64)
@@ -93,9 +93,9 @@ def test_full_size_far_dilation_workload():
     for name in ("o", "dq", "dk", "dv"):
         assert np.isfinite(res[name]).all(), name
     small = small_inputs(1, 16384, 2, 128, seed=88)
-    res = gc.run_gpu(small, w.mask)
+    res = gc.run_gpu(small, w.mask_fields())
     rng = np.random.default_rng(88)
-    gc.sampled_compare(small, w.mask, res, [(0, 0), (0, 1)], gc.sample_positions(16384, rng),
+    gc.sampled_compare(small, w.mask_fields(), res, [(0, 0), (0, 1)], gc.sample_positions(16384, rng),
                        gc.sample_positions(16384, rng))
 
 
@@ -147,3 +147,21 @@ def test_repeat_calls_are_deterministic():
     b = gc.run_gpu(inp, {"causal": True})
     for name in ("o", "lse", "dq", "dk", "dv"):
         assert np.array_equal(a[name], b[name]), name
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("n", [129, 300, 517])
+@pytest.mark.parametrize("kind", ["random_causal", "documents_causal", "documents_window"])
+def test_bitmask_small_cases(d, n, kind):
+    from tiled_exact_attention_flash_gb300.inputs import (document_bitmask, document_lengths,
+                                                          pack_bitmask)
+    if kind == "random_causal":
+        live = np.random.default_rng(n + d).random((n, n)) < 0.7
+        fields = {"causal": True, "bitmask": pack_bitmask(live)}
+    elif kind == "documents_causal":
+        fields = {"causal": True, "bitmask": document_bitmask(n, document_lengths(n, n, 70))}
+    else:
+        fields = {"window": 90, "bitmask": document_bitmask(n, document_lengths(n, n + 1, 100))}
+    inp = small_inputs(2, n, 3, d, seed=n * 11 + d)
+    res = gc.run_gpu(inp, fields)
+    gc.full_compare(inp, fields, res)

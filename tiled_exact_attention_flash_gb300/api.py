@@ -10,7 +10,7 @@ from __future__ import annotations
 
 import ctypes
 import os
-from dataclasses import dataclass
+from dataclasses import dataclass, field
 from typing import Optional
 
 import numpy as np
@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(_HERE, "libflashmsa.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE, ERR_INDEX = range(7)
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "TIMEOUT",
                 5: "WORKSPACE", 6: "INDEX"}
-CAUSAL, WINDOW, DILATED, STRIDED, GLOBAL, STRIDED_REL, DILATED_FAR = 1, 2, 4, 8, 16, 32, 64
+CAUSAL, WINDOW, DILATED, STRIDED, GLOBAL, STRIDED_REL, DILATED_FAR, BITMASK = 1, 2, 4, 8, 16, 32, 64, 128
 
 # exported symbols, in the order include/flashmsa.h declares them
 SYMBOLS = (
@@ -56,6 +56,11 @@ class BlockIndexStruct(ctypes.Structure):
         ("kind_t", ctypes.c_void_p),
         ("q_order", ctypes.c_void_p),
         ("k_order", ctypes.c_void_p),
+        ("n_bit_tiles", ctypes.c_int64),
+        ("bit_slot", ctypes.c_void_p),
+        ("bit_slot_t", ctypes.c_void_p),
+        ("bits", ctypes.c_void_p),
+        ("bits_t", ctypes.c_void_p),
     ]
 
 
@@ -70,6 +75,7 @@ class MaskDescStruct(ctypes.Structure):
         ("stride_phase", ctypes.c_int32),
         ("index", ctypes.c_void_p),
         ("global_tokens", ctypes.c_int64),
+        ("bitmask", ctypes.c_void_p),
     ]
 
 
@@ -143,6 +149,9 @@ class Mask:
     global_tokens: Optional[int] = None
     stride_relative: bool = False  # the stride counted from the query block
     dilation_far: bool = False     # dilated key blocks at every distance, window dense
+    # bit-packed element mask (flag BITMASK): N rows of ceil(N/32) little-endian
+    # uint32 words, read by build_block_index only (see inputs.pack_bitmask)
+    bitmask: Optional[bytes] = field(default=None, repr=False)
 
     @classmethod
     def from_fields(cls, fields: dict) -> "Mask":
@@ -157,6 +166,7 @@ class Mask:
         if self.stride is not None:
             f |= STRIDED_REL if self.stride_relative else STRIDED
         f |= GLOBAL if self.global_tokens is not None else 0
+        f |= BITMASK if self.bitmask is not None else 0
         return f
 
     @property
@@ -164,15 +174,18 @@ class Mask:
         return bool(self.flags & ~CAUSAL)
 
     def desc(self, index_ptr=None) -> MaskDescStruct:
+        bits = ctypes.cast(ctypes.c_char_p(self.bitmask), ctypes.c_void_p) if self.bitmask else None
         return MaskDescStruct(self.flags, self.block, self.window or 0, self.dilation or 1,
                               self.dilation_near, self.stride or 1, self.stride_phase,
-                              index_ptr, self.global_tokens or 0)
+                              index_ptr, self.global_tokens or 0, bits)
 
 
 _INDEX_ARRAYS = (("row_ptr", np.int32, "nq1"), ("col_idx", np.int32, "nnz"),
                  ("kind", np.uint8, "nnz"), ("col_ptr", np.int32, "nk1"),
                  ("row_idx", np.int32, "nnz"), ("kind_t", np.uint8, "nnz"),
-                 ("q_order", np.int32, "nq"), ("k_order", np.int32, "nk"))
+                 ("q_order", np.int32, "nq"), ("k_order", np.int32, "nk"),
+                 ("bit_slot", np.int32, "nnz"), ("bit_slot_t", np.int32, "nnz"),
+                 ("bits", np.uint32, "nbits"), ("bits_t", np.uint32, "nbits"))
 
 
 class BlockIndex:
@@ -190,6 +203,7 @@ class BlockIndex:
     def host_struct(self) -> BlockIndexStruct:
         s = BlockIndexStruct(self.header.seq_len, self.header.n_q_blocks, self.header.n_k_blocks,
                              self.header.block, self.header.nnz)
+        s.n_bit_tiles = self.header.n_bit_tiles
         for name, _, _ in _INDEX_ARRAYS:
             setattr(s, name, self.host[name].ctypes.data)
         return s
@@ -200,6 +214,7 @@ class BlockIndex:
                        for name, arr in self.host.items()}
         s = BlockIndexStruct(self.header.seq_len, self.header.n_q_blocks, self.header.n_k_blocks,
                              self.header.block, self.header.nnz)
+        s.n_bit_tiles = self.header.n_bit_tiles
         for name, _, _ in _INDEX_ARRAYS:
             t = self.device[name]
             setattr(s, name, t.data_ptr())
@@ -215,9 +230,10 @@ def build_block_index(mask: Mask, n: int) -> BlockIndex:
     _check(L.flash_msa_build_block_index(ctypes.byref(desc), n, ctypes.byref(hdr)),
            "build_block_index(count)")
     sizes = {"nq1": hdr.n_q_blocks + 1, "nk1": hdr.n_k_blocks + 1, "nnz": hdr.nnz,
-             "nq": hdr.n_q_blocks, "nk": hdr.n_k_blocks}
+             "nq": hdr.n_q_blocks, "nk": hdr.n_k_blocks, "nbits": 512 * hdr.n_bit_tiles}
     host = {name: np.zeros(max(1, sizes[kind]), dtype=dt) for name, dt, kind in _INDEX_ARRAYS}
     out = BlockIndexStruct(hdr.seq_len, hdr.n_q_blocks, hdr.n_k_blocks, hdr.block, hdr.nnz)
+    out.n_bit_tiles = hdr.n_bit_tiles
     for name, _, _ in _INDEX_ARRAYS:
         setattr(out, name, host[name].ctypes.data)
     _check(L.flash_msa_build_block_index(ctypes.byref(desc), n, ctypes.byref(out)),

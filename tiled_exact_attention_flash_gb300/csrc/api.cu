@@ -78,8 +78,9 @@ static flash_msa_status check_mask(const flash_msa_mask_desc* m, MaskParams& mp,
   if (!m) return FLASH_MSA_OK;
   if (m->flags & ~uint32_t(FLASH_MSA_CAUSAL | FLASH_MSA_WINDOW | FLASH_MSA_DILATED |
                            FLASH_MSA_STRIDED | FLASH_MSA_GLOBAL | FLASH_MSA_STRIDED_REL |
-                           FLASH_MSA_DILATED_FAR))
+                           FLASH_MSA_DILATED_FAR | FLASH_MSA_BITMASK))
     return set_error(FLASH_MSA_ERR_INVALID_ARG, "mask: unknown flag bits 0x%x", m->flags);
+  // every flag but CAUSAL needs an index (the bits travel in it)
   const uint32_t pat = m->flags & ~uint32_t(FLASH_MSA_CAUSAL);
   if (m->block != kTile && !(m->block == 0 && pat == 0))
     return set_error(FLASH_MSA_ERR_UNSUPPORTED, "mask: pattern block %d (only 128 is supported)",
@@ -152,11 +153,19 @@ static flash_msa_status make_lists(const flash_msa_mask_desc* m, int64_t N, bool
                      ix->n_k_blocks, static_cast<long long>(N));
   if (!ix->row_ptr || !ix->col_idx || !ix->kind || !ix->q_order)
     return set_error(FLASH_MSA_ERR_INDEX, "index: CSR arrays or q_order missing");
+  const bool bits = (m->flags & FLASH_MSA_BITMASK) && ix->n_bit_tiles > 0;
+  if (bits && (!ix->bit_slot || !ix->bits || (want_csc && (!ix->bit_slot_t || !ix->bits_t))))
+    return set_error(FLASH_MSA_ERR_INDEX, "index: bit arrays missing");
   rows.ptr = ix->row_ptr;
   rows.idx = ix->col_idx;
   rows.kind = ix->kind;
   rows.order = ix->q_order;
   rows.nnz = ix->nnz;
+  if (bits) {
+    rows.slot = ix->bit_slot;
+    rows.bits = ix->bits;
+    rows.n_bit_tiles = ix->n_bit_tiles;
+  }
   if (want_csc) {
     if (!ix->col_ptr || !ix->row_idx || !ix->kind_t || !ix->k_order)
       return set_error(FLASH_MSA_ERR_INDEX, "index: CSC arrays or k_order missing");
@@ -165,6 +174,11 @@ static flash_msa_status make_lists(const flash_msa_mask_desc* m, int64_t N, bool
     cols.kind = ix->kind_t;
     cols.order = ix->k_order;
     cols.nnz = ix->nnz;
+    if (bits) {
+      cols.slot = ix->bit_slot_t;
+      cols.bits = ix->bits_t;
+      cols.n_bit_tiles = ix->n_bit_tiles;
+    }
   }
   return FLASH_MSA_OK;
 }
@@ -195,7 +209,42 @@ flash_msa_status flash_msa_build_block_index(const flash_msa_mask_desc* mask, in
   bool need = false;
   flash_msa_status st = check_mask(mask, mp, need);
   if (st != FLASH_MSA_OK) return st;
+  const bool with_bits = (mask->flags & FLASH_MSA_BITMASK) != 0;
+  if (with_bits && !mask->bitmask)
+    return set_error(FLASH_MSA_ERR_INVALID_ARG, "build_block_index: BITMASK without mask->bitmask");
   const int64_t nb = n_blocks_of(N);
+  const int64_t words_per_row = (N + 31) / 32;
+  // Tile class with the bits: live entries of row r = interval of the other
+  // mask parts AND the row's 128 mask bits.  Returns -1 dead, 0 full,
+  // 1 partial; `cut` tells whether the bits removed an entry of the interval
+  // (the tile then carries its live entries, written to tb when non-null).
+  auto bit_class = [&](int qb, int kb, int c, bool& cut, uint32_t* tb) -> int {
+    cut = false;
+    if (!with_bits) return c;
+    const DeltaRange r = tile_delta_range(qb, kb, mp);
+    const int64_t j0 = int64_t(kb) * kTile;
+    int64_t live = 0;
+    for (int row = 0; row < kTile; ++row) {
+      const int64_t i = int64_t(qb) * kTile + row;
+      uint32_t iv[4] = {0, 0, 0, 0};
+      if (i < N && !r.none) {
+        int64_t clo = std::max<int64_t>(i - r.hi - j0, 0);
+        int64_t chi = std::min<int64_t>({i - r.lo - j0, N - 1 - j0, int64_t(kTile - 1)});
+        for (int64_t col = clo; col <= chi; ++col) iv[col >> 5] |= 1u << (col & 31);
+      }
+      for (int w = 0; w < 4; ++w) {
+        const int64_t word = int64_t(kb) * 4 + w;
+        const uint32_t mbits = (i < N && word < words_per_row) ? mask->bitmask[i * words_per_row + word] : 0u;
+        const uint32_t f = iv[w] & mbits;
+        if (f != iv[w]) cut = true;
+        live += __builtin_popcount(f);
+        if (tb) tb[row * 4 + w] = f;
+      }
+    }
+    if (live == 0) return -1;
+    if (c == 0 && !cut) return 0;
+    return 1;
+  };
   // candidate key blocks per query block: causal and a plain window bound the
   // span; with global tokens the global key blocks come first, and a global
   // query block scans every key block
@@ -213,7 +262,7 @@ flash_msa_status flash_msa_build_block_index(const flash_msa_mask_desc* mask, in
       const int64_t g_end = std::min(gb, k0);  // global key blocks before the window span
       auto visit = [&](int64_t kb) {
         const int c = classify_tile(int(qb), int(kb), N, mp);
-        if (c >= 0) fn(int(qb), int(kb), c);
+        if (c >= 0) fn(int(qb), int(kb), c);  // the bits are applied by fn
       };
       for (int64_t kb = 0; kb < g_end; ++kb) visit(kb);  // ascending: they precede k0
       for (int64_t kb = k0; kb <= k1; ++kb) visit(kb);
@@ -223,35 +272,68 @@ flash_msa_status flash_msa_build_block_index(const flash_msa_mask_desc* mask, in
   out->block = kTile;
   out->n_q_blocks = out->n_k_blocks = int32_t(nb);
   if (!out->row_ptr) {
-    int64_t nnz = 0;
-    for_each_tile([&](int, int, int) { ++nnz; });
+    int64_t nnz = 0, n_bits = 0;
+    for_each_tile([&](int qb, int kb, int c) {
+      bool cut;
+      const int k = bit_class(qb, kb, c, cut, nullptr);
+      if (k < 0) return;
+      ++nnz;
+      if (k == 1 && cut) ++n_bits;
+    });
     if (nnz > INT32_MAX)
       return set_error(FLASH_MSA_ERR_INVALID_ARG, "build_block_index: more than 2^31 live tiles");
     out->nnz = nnz;
+    out->n_bit_tiles = n_bits;
     return FLASH_MSA_OK;
   }
   if (!out->col_idx || !out->kind || !out->col_ptr || !out->row_idx || !out->kind_t ||
       !out->q_order || !out->k_order)
     return set_error(FLASH_MSA_ERR_INVALID_ARG, "build_block_index: some output arrays are null");
+  if (with_bits && (!out->bit_slot || !out->bit_slot_t ||
+                    (out->n_bit_tiles > 0 && (!out->bits || !out->bits_t))))
+    return set_error(FLASH_MSA_ERR_INVALID_ARG, "build_block_index: bit arrays are null");
   // CSR
   std::vector<int32_t> col_count(size_t(nb), 0);
-  int64_t pos = 0;
+  std::vector<uint32_t> tb(size_t(kTile) * 4);
+  int64_t pos = 0, slot = 0;
   int64_t cur = 0;
   out->row_ptr[0] = 0;
   for_each_tile([&](int qb, int kb, int c) {
+    bool cut;
+    const int k = bit_class(qb, kb, c, cut, tb.data());
+    if (k < 0) return;
     while (cur < qb) out->row_ptr[++cur] = int32_t(pos);
     if (pos < out->nnz) {
       out->col_idx[pos] = kb;
-      out->kind[pos] = uint8_t(c);
+      out->kind[pos] = uint8_t(k);
+      if (with_bits) {
+        int32_t s = -1;
+        if (k == 1 && cut && slot < out->n_bit_tiles) {
+          s = int32_t(slot);
+          uint32_t* dst = out->bits + slot * 512;
+          uint32_t* dst_t = out->bits_t + slot * 512;
+          std::copy(tb.begin(), tb.end(), dst);
+          std::fill(dst_t, dst_t + 512, 0u);
+          for (int row = 0; row < kTile; ++row)
+            for (int col = 0; col < kTile; ++col)
+              if ((tb[size_t(row) * 4 + (col >> 5)] >> (col & 31)) & 1u)
+                dst_t[col * 4 + (row >> 5)] |= 1u << (row & 31);
+        }
+        if (k == 1 && cut) ++slot;
+        out->bit_slot[pos] = s;
+      }
     }
     ++pos;
     ++col_count[size_t(kb)];
   });
   while (cur < nb) out->row_ptr[++cur] = int32_t(pos);
-  if (pos != out->nnz)
+  if (pos != out->nnz || (with_bits && slot != out->n_bit_tiles))
     return set_error(FLASH_MSA_ERR_INVALID_ARG,
-                     "build_block_index: nnz %lld does not match the counting pass (%lld)",
-                     static_cast<long long>(out->nnz), static_cast<long long>(pos));
+                     "build_block_index: nnz %lld / bit tiles %lld do not match the counting pass "
+                     "(%lld / %lld)",
+                     static_cast<long long>(out->nnz), static_cast<long long>(out->n_bit_tiles),
+                     static_cast<long long>(pos), static_cast<long long>(slot));
+  if (!with_bits) out->n_bit_tiles = 0;
   // CSC by counting sort: query blocks come out ascending within each column
   out->col_ptr[0] = 0;
   for (int64_t kb = 0; kb < nb; ++kb) out->col_ptr[kb + 1] = out->col_ptr[kb] + col_count[size_t(kb)];
@@ -262,6 +344,7 @@ flash_msa_status flash_msa_build_block_index(const flash_msa_mask_desc* mask, in
       const int32_t dst = fill[size_t(kb)]++;
       out->row_idx[dst] = int32_t(qb);
       out->kind_t[dst] = out->kind[e];
+      if (with_bits) out->bit_slot_t[dst] = out->bit_slot[e];
     }
   // longest-first orders (stable)
   for (int64_t b = 0; b < nb; ++b) out->q_order[b] = out->k_order[b] = int32_t(b);
@@ -299,6 +382,17 @@ flash_msa_status flash_msa_check_block_index(const flash_msa_block_index* ix, in
   };
   if (!check_lists(ix->row_ptr, ix->col_idx, ix->kind, "CSR"))
     return set_error(FLASH_MSA_ERR_INDEX, "index: CSR arrays are inconsistent");
+  if (ix->n_bit_tiles < 0)
+    return set_error(FLASH_MSA_ERR_INDEX, "index: negative bit tile count");
+  if (ix->n_bit_tiles > 0) {
+    if (!ix->bit_slot || !ix->bit_slot_t || !ix->bits || !ix->bits_t)
+      return set_error(FLASH_MSA_ERR_INDEX, "index: bit arrays missing");
+    for (int64_t e = 0; e < ix->nnz; ++e)
+      if (ix->bit_slot[e] < -1 || ix->bit_slot[e] >= ix->n_bit_tiles ||
+          (ix->bit_slot[e] >= 0 && ix->kind[e] != 1))
+        return set_error(FLASH_MSA_ERR_INDEX, "index: bad bit slot at entry %lld",
+                         static_cast<long long>(e));
+  }
   if (!check_lists(ix->col_ptr, ix->row_idx, ix->kind_t, "CSC"))
     return set_error(FLASH_MSA_ERR_INDEX, "index: CSC arrays are inconsistent");
   // CSC must be the transpose of CSR
@@ -309,6 +403,8 @@ flash_msa_status flash_msa_check_block_index(const flash_msa_block_index* ix, in
       const int32_t at = fill[size_t(kb)]++;
       if (at >= ix->col_ptr[kb + 1] || ix->row_idx[at] != qb || ix->kind_t[at] != ix->kind[e])
         return set_error(FLASH_MSA_ERR_INDEX, "index: CSC is not the transpose of CSR");
+      if (ix->n_bit_tiles > 0 && ix->bit_slot[e] != ix->bit_slot_t[at])
+        return set_error(FLASH_MSA_ERR_INDEX, "index: CSC bit slots differ from CSR");
     }
   for (const int32_t* ord : {ix->q_order, ix->k_order}) {
     std::vector<char> seen(size_t(nb), 0);

@@ -582,6 +582,7 @@ __device__ __forceinline__ void dkdv_elementwise(const BwdParams& p, uint8_t* sm
       int lo = 0, hi = kTile - 1;
       if (it.dead) hi = -1;
       else if (it.partial) col_live_range(j, it.blk, un.ob, p.N, p.mask, lo, hi);
+      prefetch_tile_bits(p.list, it.slot, row);
       const float* vec =
           reinterpret_cast<const float*>(smem + L::kVecOff + ((cnt % L::kStages) / 2) * 1024);
       cnt += 2;
@@ -594,6 +595,13 @@ __device__ __forceinline__ void dkdv_elementwise(const BwdParams& p, uint8_t* sm
 #pragma unroll
         for (int e = 0; e < 64; ++e)
           if (64 * g + e < lo || 64 * g + e > hi) sv[e] = kNegInfBits;
+        if (it.slot >= 0) {  // bit-packed mask tile: this key row's bits over 64 queries
+          uint32_t bw[2];
+          load_tile_bits<2>(p.list, it.slot, row, 2 * g, bw);
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            if (!((bw[e >> 5] >> (e & 31)) & 1u)) sv[e] = kNegInfBits;
+        }
       }
       // pass 1: P^T (kept in sv as fp32), bf16 to columns [64 g, 64 g + 32)
       {
@@ -734,6 +742,7 @@ __device__ __forceinline__ void dq_elementwise(const BwdParams& p, uint8_t* smem
       int lo = 0, hi = kTile - 1;
       if (it.dead) hi = -1;
       else if (it.partial) row_live_range(i, cur.ob, it.blk, p.N, p.mask, lo, hi);
+      prefetch_tile_bits(p.list, it.slot, row);
       bool ok = wait_bar(bar(L::kSFull), sp_cnt & 1, abort_flag, p.status, 20);
       if (!__all_sync(0xFFFFFFFFu, ok)) return;
       ++sp_cnt;
@@ -745,6 +754,13 @@ __device__ __forceinline__ void dq_elementwise(const BwdParams& p, uint8_t* smem
 #pragma unroll
         for (int e = 0; e < 64; ++e)
           if (64 * g + e < lo || 64 * g + e > hi) sv[e] = kNegInfBits;
+        if (it.slot >= 0) {  // bit-packed mask tile: this query row's bits over 64 keys
+          uint32_t bw[2];
+          load_tile_bits<2>(p.list, it.slot, row, 2 * g, bw);
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            if (!((bw[e >> 5] >> (e & 31)) & 1u)) sv[e] = kNegInfBits;
+        }
       }
       uint32_t dd[32];
 #pragma unroll

@@ -228,6 +228,9 @@ struct ListParams {
   const int32_t* idx;    // col_idx / row_idx
   const uint8_t* kind;   // kind / kind_t
   const int32_t* order;  // q_order / k_order
+  const int32_t* slot;   // bit-packed masks: bit_slot / bit_slot_t (null otherwise)
+  const uint32_t* bits;  // bits / bits_t: 512 words per slot
+  int64_t n_bit_tiles;
   int64_t nnz;
   int n_blocks;          // blocks along both axes (square tiling)
   int causal;            // arithmetic mode: causal mask
@@ -286,12 +289,14 @@ struct InnerTile {
   int blk;
   bool partial;
   bool dead;
+  int slot;  // bit tile of a bit-packed mask, -1 if none
 };
 
 __device__ __forceinline__ InnerTile inner_tile(const Unit& un, int t, const ListParams& L,
                                                 unsigned* status) {
   InnerTile it;
   it.dead = false;
+  it.slot = -1;
   if (L.ptr) {
     it.blk = __ldg(L.idx + un.begin + t);
     it.partial = __ldg(L.kind + un.begin + t) != 0;
@@ -300,6 +305,14 @@ __device__ __forceinline__ InnerTile inner_tile(const Unit& un, int t, const Lis
       it.blk = 0;
       it.dead = true;
     }
+    if (L.slot && it.partial) {
+      it.slot = __ldg(L.slot + un.begin + t);
+      if (it.slot >= L.n_bit_tiles) {  // corrupt: treat the tile as dead
+        record_status(status, FLASH_MSA_ERR_INDEX, 0xF3);
+        it.slot = -1;
+        it.dead = true;
+      }
+    }
   } else {
     it.blk = L.transposed ? (L.causal ? un.ob + t : t) : t;
     const int last = L.n_blocks - 1;
@@ -307,6 +320,30 @@ __device__ __forceinline__ InnerTile inner_tile(const Unit& un, int t, const Lis
                  (L.tail && (it.blk == last || un.ob == last));
   }
   return it;
+}
+
+// Bits of one row of a bit tile (bit-packed masks): kWords 32-bit words
+// starting at word w0 of tile-local row r.  prefetch_tile_bits pulls the row
+// into L1 before the tile's barrier wait without holding registers across
+// it; load_tile_bits reads it after the wait, only for tiles with bits.
+__device__ __forceinline__ const uint32_t* tile_bits_row(const ListParams& L, int slot, int r,
+                                                         int w0) {
+  return L.bits + int64_t(slot) * 512 + r * 4 + w0;
+}
+__device__ __forceinline__ void prefetch_tile_bits(const ListParams& L, int slot, int r) {
+  if (slot >= 0) asm volatile("prefetch.global.L1 [%0];" ::"l"(tile_bits_row(L, slot, r, 0)));
+}
+template <int kWords>
+__device__ __forceinline__ void load_tile_bits(const ListParams& L, int slot, int r, int w0,
+                                               uint32_t (&w)[kWords]) {
+  const uint32_t* src = tile_bits_row(L, slot, r, w0);
+  if constexpr (kWords == 4) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(src));
+    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+  } else {
+    const uint2 v = __ldg(reinterpret_cast<const uint2*>(src));
+    w[0] = v.x; w[1] = v.y;
+  }
 }
 
 __device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {

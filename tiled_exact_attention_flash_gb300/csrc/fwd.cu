@@ -351,6 +351,7 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint64_t* bars, 
       } else if (it.partial) {
         row_live_range(i, un.ob, it.blk, p.N, p.mask, lo, hi);
       }
+      prefetch_tile_bits(p.list, it.slot, row);
       const bool ok = wait_bar(bar(L::kSFull + slot), sf_cnt & 1, abort_flag, p.status, 20);
       if (!__all_sync(0xFFFFFFFFu, ok)) return;  // tcgen05.ld below needs the whole warp
       ++sf_cnt;
@@ -361,6 +362,13 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint64_t* bars, 
 #pragma unroll
         for (int c = 0; c < 128; ++c)
           if (c < lo || c > hi) sr[c] = kNegInfBits;
+        if (it.slot >= 0) {  // bit-packed mask tile: this row's bits
+          uint32_t bw[4];
+          load_tile_bits<4>(p.list, it.slot, row, 0, bw);
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (!((bw[c >> 5] >> (c & 31)) & 1u)) sr[c] = kNegInfBits;
+        }
       }
       // Optimistic pass: exponentials against the current reference max while
       // the tile's row max is formed alongside.  Only if some row's max

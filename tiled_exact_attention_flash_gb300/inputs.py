@@ -9,13 +9,16 @@ the oracle consumes the same values promoted exactly to float64.
 Workloads: the five attention configurations the pages' discussion motivates
 (7B-style layer, d = 128, long context; causal, local window + strided, and
 local window with block dilation), plus a sixth for the local window with
-global tokens hybrid (8K window, 512 global tokens, 128K tokens) and two
-more with the second readings of the strided and dilated masks.  Seeds: Q, K, V, dO of workload c use
+global tokens hybrid (8K window, 512 global tokens, 128K tokens), two more
+with the second readings of the strided and dilated masks, and one of packed
+documents under a bit-packed mask.  Seeds: Q, K, V, dO of workload c use
 1000*c + 1 .. 1000*c + 4.
 """
 from __future__ import annotations
 
+import functools
 from dataclasses import dataclass, field
+from typing import Optional
 
 import numpy as np
 import torch
@@ -31,10 +34,20 @@ class Workload:
     d: int
     # mask description: plain fields, converted by each side into its own type
     mask: dict = field(default_factory=dict)
+    # packed documents: (mean length, seed) of the seeded document lengths; the
+    # bit-packed mask is added by mask_fields()
+    docs: Optional[tuple] = None
 
     @property
     def shape(self):
         return (self.B, self.N, self.H, self.d)
+
+    def mask_fields(self) -> dict:
+        """The mask fields with the packed-documents bitmask when there is one."""
+        f = dict(self.mask)
+        if self.docs is not None:
+            f["bitmask"] = _documents_bitmask(self.N, *self.docs)
+        return f
 
 
 WORKLOADS = {
@@ -54,6 +67,9 @@ WORKLOADS = {
                  "stride_relative": True}),
     8: Workload(8, "causal window4096 + far dilation2 B1 H8 N131072 d128", 1, 8, 131072, 128,
                 {"causal": True, "window": 4096, "dilation": 2, "dilation_far": True}),
+    # packed documents under a bit-packed mask, causal inside each document
+    9: Workload(9, "causal packed documents (mean 2048 tokens) B1 H16 N32768 d128", 1, 16, 32768,
+                128, {"causal": True}, docs=(2048, 9009)),
 }
 
 
@@ -121,3 +137,8 @@ def document_bitmask(n: int, lengths) -> bytes:
         words[start:end] = packed.astype(np.uint32)
         start = end
     return words.astype("<u4").tobytes()
+
+
+@functools.lru_cache(maxsize=2)
+def _documents_bitmask(n: int, mean: int, seed: int) -> bytes:
+    return document_bitmask(n, document_lengths(n, seed, mean))
