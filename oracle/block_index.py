@@ -16,8 +16,9 @@ and the lists are built from that classification:
     q_order / k_order:   query / key blocks sorted by descending live-tile
                          count, ties by ascending index (longest work first)
 
-With a bit-packed mask, a partial tile whose live set differs from the live
-set of the same mask without the bits carries its live entries as bits:
+With a bit-packed mask (or packed documents), a partial tile whose live set
+differs from the live set of the same mask without the bits (and without
+the documents) carries its live entries as bits:
 slots are numbered in CSR order; bits[slot] holds 128 rows (query) of four
 32-bit words (key bit c in word c // 32, bit c % 32) and bits_t[slot] the
 transpose (128 key rows of four words over the queries); bit_slot /
@@ -92,8 +93,8 @@ def build(n: int, spec: MaskSpec, tile: int = 128, prune: bool = True) -> dict:
     # bit tiles (bit-packed masks only)
     bit_slot = np.full(len(col_idx), -1, dtype=np.int32)
     bits, bits_t = [], []
-    if spec.bitmask is not None:
-        plain = dataclasses.replace(spec, bitmask=None)
+    if spec.bitmask is not None or spec.doc_starts is not None:
+        plain = dataclasses.replace(spec, bitmask=None, doc_starts=None)
         for qb in range(nb):
             rows = np.arange(qb * tile, qb * tile + tile)
             for e in range(row_ptr[qb], row_ptr[qb + 1]):

@@ -23,6 +23,11 @@ def live_scalar(i: int, j: int, n: int, spec: MaskSpec) -> bool:
         return False
     if spec.causal and j > i:
         return False
+    if spec.doc_starts is not None:
+        doc_i = max(d for d, st in enumerate(spec.doc_starts[:-1]) if st <= i)
+        doc_j = max(d for d, st in enumerate(spec.doc_starts[:-1]) if st <= j)
+        if doc_i != doc_j:
+            return False
     if spec.bitmask is not None:
         w = (n + 31) // 32
         at = 4 * (i * w + j // 32)

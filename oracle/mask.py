@@ -30,12 +30,19 @@ Definitions, one per mask kind named on the pages:
   symmetrically: the first G tokens are global, so a global query attends
   every key and every query attends the global keys.
 
-* bit-packed mask -- an arbitrary element mask given as bits, the "bitmask"
-  the pages name beside the block index as the cheap way to keep a mask
-  ("Flash MSA Attention Kernel Implementation", section "Optimization Tricks
-  That Actually Matter", paragraph "Masking and causal attention"): row i is
-  ceil(N/32) little-endian 32-bit words, bit j % 32 of word j // 32 set iff
-  the pair may be live.  It is AND-ed with everything else.
+* bit-packed mask -- an arbitrary element mask given as bits, the mask tiles
+  "in a bit-packed format" of "Flash MSA Attention Kernel Implementation",
+  section "Optimization Tricks That Actually Matter", paragraph "Masking and
+  causal attention": row i is ceil(N/32) little-endian 32-bit words, bit
+  j % 32 of word j // 32 set iff the pair may be live.  It is AND-ed with
+  everything else.
+* documents (variable-length batches) -- sequences of different lengths
+  packed back to back on one token axis, with offsets doc_starts (0 = s_0 <
+  s_1 < ... < s_D = N); a token attends only to tokens of its own sequence,
+  the batch being handled by masking (same page, section "The Production
+  Pipeline: From Kernel to Service", request batching; "How to Use Flash
+  MSA Kernels for Long Context", FAQ on flash-batch inference).  AND-ed with
+  everything else, so causal means causal inside each sequence.
 
 Combination: live = in_range AND causal_part AND pattern [AND bit], where pattern is
 true when no window/dilation/stride/global part is set, and otherwise
@@ -63,6 +70,7 @@ class MaskSpec:
     stride_relative: bool = False    # stride part relative to the query block
     dilation_far: bool = False       # dilation as its own part, at every distance
     bitmask: Optional[bytes] = None  # packed rows, N x ceil(N/32) little-endian uint32
+    doc_starts: Optional[tuple] = None  # packed sequences: offsets 0 = s_0 < ... < s_D = N
 
     @property
     def has_pattern(self) -> bool:
@@ -109,7 +117,17 @@ def live_matrix(rows, cols, n: int, spec: MaskSpec) -> np.ndarray:
         ok = ok & part
     if spec.bitmask is not None:
         ok = ok & bit_matrix(spec.bitmask, n, i, j)
+    if spec.doc_starts is not None:
+        starts = np.asarray(spec.doc_starts, dtype=np.int64)
+        if starts[0] != 0 or starts[-1] != n or (np.diff(starts) <= 0).any():
+            raise ValueError("doc_starts must rise strictly from 0 to n")
+        ok = ok & (document_of(starts, i) == document_of(starts, j))
     return ok
+
+
+def document_of(starts: np.ndarray, t) -> np.ndarray:
+    """Index of the sequence holding token t (clipped into [0, D))."""
+    return np.clip(np.searchsorted(starts, t, side="right") - 1, 0, len(starts) - 2)
 
 
 def bit_matrix(bitmask: bytes, n: int, i, j) -> np.ndarray:

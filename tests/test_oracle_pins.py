@@ -508,3 +508,63 @@ def test_bitmask_index_tiles_hold_the_live_entries(n, fields):
             qb = int(idx["row_idx"][e])
             row = np.nonzero(idx["col_idx"][idx["row_ptr"][qb]:idx["row_ptr"][qb + 1]] == kb)[0][0]
             assert idx["bit_slot_t"][e] == idx["bit_slot"][idx["row_ptr"][qb] + row]
+
+
+# ---------------------------------------------------------------- packed documents (varlen)
+def test_documents_hand_example():
+    starts = (0, 3, 7, 10)
+    spec = MaskSpec(causal=True, doc_starts=starts)
+    # token 8 (third sequence, positions 7..9) sees 7 and 8 only
+    assert live_matrix([8], range(10), 10, spec).tolist() == [[False] * 7 + [True, True, False]]
+    # without causal: the whole first sequence for token 1
+    spec = MaskSpec(doc_starts=starts)
+    assert live_matrix([1], range(10), 10, spec).tolist() == [[True, True, True] + [False] * 7]
+    with pytest.raises(ValueError):
+        live_matrix([1], [1], 10, MaskSpec(doc_starts=(0, 5, 5, 10)))
+
+
+@pytest.mark.parametrize("fields", [{}, {"causal": True}, {"causal": True, "window": 5},
+                                    {"window": 3, "stride": 2, "stride_phase": 0, "block": 4}])
+def test_documents_equal_their_bitmask_and_scalar(fields):
+    from tiled_exact_attention_flash_gb300.inputs import document_bitmask
+    lens = [5, 1, 9, 13, 4, 8]
+    n = sum(lens)
+    starts = tuple(int(x) for x in np.cumsum([0] + lens))
+    a = MaskSpec(doc_starts=starts, **fields)
+    b = MaskSpec(bitmask=document_bitmask(n, lens), **fields)
+    idx = np.arange(-2, n + 3)
+    la = live_matrix(idx, idx, n, a)
+    assert (la == live_matrix(idx, idx, n, b)).all()
+    ref = np.array([[loops.live_scalar(int(i), int(j), n, a) for j in idx] for i in idx])
+    assert (la == ref).all()
+
+
+def test_packed_documents_equal_separate_sequences():
+    # attention over packed sequences equals attention over each sequence
+    # alone (outputs, LSE and all three gradients)
+    lens = [17, 3, 30, 1, 12]
+    n = sum(lens)
+    starts = np.cumsum([0] + lens)
+    r = rng(21)
+    q, k, v, do = (r.standard_normal((n, 8)) for _ in range(4))
+    spec = MaskSpec(causal=True, doc_starts=tuple(int(x) for x in starts))
+    o, lse = fwd_full(q, k, v, 0.3, spec)
+    dq, dk, dv = bwd_full(q, k, v, do, 0.3, spec)
+    for a, e in zip(starts[:-1], starts[1:]):
+        sl = slice(a, e)
+        o1, l1 = fwd_full(q[sl], k[sl], v[sl], 0.3, MaskSpec(causal=True))
+        g = bwd_full(q[sl], k[sl], v[sl], do[sl], 0.3, MaskSpec(causal=True))
+        assert np.abs(o[sl] - o1).max() < 1e-12 and np.abs(lse[sl] - l1).max() < 1e-12
+        for got, ref in zip((dq, dk, dv), g):
+            assert np.abs(got[sl] - ref).max() < 1e-12
+
+
+def test_documents_index_equals_bitmask_index():
+    from tiled_exact_attention_flash_gb300.inputs import document_bitmask, document_lengths
+    n = 700
+    lens = document_lengths(n, 4, 90)
+    starts = tuple(int(x) for x in np.cumsum([0] + lens))
+    a = block_index.build(n, MaskSpec(causal=True, doc_starts=starts))
+    b = block_index.build(n, MaskSpec(causal=True, bitmask=document_bitmask(n, lens)))
+    for key in a:
+        assert np.array_equal(np.asarray(a[key]), np.asarray(b[key])), key
