@@ -102,7 +102,8 @@ def mask_config(w):
     """The workload's mask for the JSON line (packed documents described, not listed)."""
     cfg = dict(w.mask)
     if w.docs is not None:
-        cfg["documents"] = {"mean_tokens": w.docs[0], "seed": w.docs[1], "bitmask": True}
+        cfg["documents"] = {"mean_tokens": w.docs[0], "seed": w.docs[1],
+                            "as": "bit-packed mask" if w.docs_as == "bitmask" else "varlen offsets"}
     return cfg
 
 

@@ -71,9 +71,14 @@ typedef enum {
  *   far       = DILATED_FAR && D % dilation == 0
  *   global    = GLOBAL && (i < global_tokens || j < global_tokens)
  * and with BITMASK, live(i,j) is further AND-ed with bit(i,j) of the bit-packed
- * mask given to flash_msa_build_block_index (the "bitmask" named beside the
- * block index, page "Flash MSA Attention Kernel Implementation", section
- * "Optimization Tricks That Actually Matter", "Masking and causal attention").
+ * mask given to flash_msa_build_block_index (the mask tiles "in a bit-packed
+ * format" of page "Flash MSA Attention Kernel Implementation", section
+ * "Optimization Tricks That Actually Matter", "Masking and causal
+ * attention"); with DOCUMENTS, with doc(i) == doc(j): variable-length
+ * sequences packed back to back on the token axis (offsets doc_starts), each
+ * attending only to itself (same page, section "The Production Pipeline:
+ * From Kernel to Service", request batching), causal inside each sequence
+ * when CAUSAL is set.
  * Window: "Local window -- attend only to +-W tokens"; dilated: "skip every
  * few tokens", read at block level; strided: the fixed pattern of Child et
  * al. (page "How Does Flash-MSA Sparse Attention Work", section "How
@@ -92,7 +97,8 @@ enum {
   FLASH_MSA_GLOBAL = 16,
   FLASH_MSA_STRIDED_REL = 32,
   FLASH_MSA_DILATED_FAR = 64,
-  FLASH_MSA_BITMASK = 128
+  FLASH_MSA_BITMASK = 128,
+  FLASH_MSA_DOCUMENTS = 256
 };
 
 /* Per-query-block list of live key blocks ("a precomputed index list", page
@@ -105,7 +111,7 @@ enum {
  *   CSC by key block:   col_ptr[n_k_blocks+1], row_idx[nnz] (ascending), kind_t[nnz]
  *   q_order[n_q_blocks] / k_order[n_k_blocks]: blocks by descending live-tile
  *   count, ties by ascending index (longest work is scheduled first).
- * With a BITMASK mask, a partial tile whose live entries are not all given
+ * With a BITMASK or DOCUMENTS mask, a partial tile whose live entries are not all given
  * by the other mask parts carries them as bits, in a slot numbered in CSR
  * order: bits[512 slot + 4 r + c / 32] bit c % 32 = live(128 qb + r,
  * 128 kb + c), and bits_t the transpose (4 words per key row over the
@@ -146,7 +152,11 @@ typedef struct flash_msa_block_index {
  * FLASH_MSA_ERR_UNSUPPORTED: every tile then keeps one interval of live
  * keys per row).  bitmask (BITMASK only, HOST memory, read only by
  * flash_msa_build_block_index): N rows of ceil(N/32) little-endian uint32
- * words, bit j % 32 of word j / 32 of row i set iff (i, j) may be live. */
+ * words, bit j % 32 of word j / 32 of row i set iff (i, j) may be live.
+ * doc_starts / n_docs (DOCUMENTS only, HOST memory, read only by
+ * flash_msa_build_block_index): n_docs + 1 offsets 0 = s_0 < s_1 < ... <
+ * s_n_docs = N (cu_seqlens); sequence d holds tokens [s_d, s_{d+1}).  Boundary
+ * tiles carry bit tiles, as with BITMASK. */
 typedef struct {
   uint32_t flags;
   int32_t block;
@@ -156,6 +166,8 @@ typedef struct {
   const flash_msa_block_index* index;
   int64_t global_tokens;
   const uint32_t* bitmask;
+  const int64_t* doc_starts;
+  int64_t n_docs;
 } flash_msa_mask_desc;
 
 /* Build the block index for `mask` and sequence length N on the HOST (no GPU
@@ -165,8 +177,8 @@ typedef struct {
  * int32, kind/kind_t nnz uint8, q_order/k_order n int32; with BITMASK also
  * bit_slot/bit_slot_t nnz int32 and bits/bits_t 512 n_bit_tiles uint32) and
  * call again to fill them.  mask->index is ignored.  Errors: INVALID_ARG
- * (null, N < 1, bad field, BITMASK without mask->bitmask), UNSUPPORTED
- * (block != 128). */
+ * (null, N < 1, bad field, BITMASK without mask->bitmask, DOCUMENTS without
+ * offsets rising strictly from 0 to N), UNSUPPORTED (block != 128). */
 flash_msa_status flash_msa_build_block_index(const flash_msa_mask_desc* mask, int64_t N,
                                              flash_msa_block_index* out);
 

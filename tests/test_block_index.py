@@ -32,7 +32,7 @@ def compare(n, fields):
     return got
 
 
-@pytest.mark.parametrize("cid", [1, 2, 3, 4, 5, 9])
+@pytest.mark.parametrize("cid", [1, 2, 3, 4, 5, 9, 10])
 def test_workload_indices_bit_exact(cid):
     w = WORKLOADS[cid]
     compare(w.N, w.mask_fields())
@@ -145,3 +145,22 @@ def test_bitmask_requires_the_bits():
     import ctypes
     assert api.lib().flash_msa_build_block_index(ctypes.byref(desc), 300, ctypes.byref(hdr)) == \
         api.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("n,fields,seed", [
+    (300, {}, 11), (519, {"causal": True}, 12), (1000, {"causal": True, "window": 200}, 13),
+    (777, {"causal": True, "global_tokens": 128, "window": 64}, 14)])
+def test_document_indices_bit_exact(n, fields, seed):
+    from tiled_exact_attention_flash_gb300.inputs import document_lengths
+    lens = document_lengths(n, seed, 120)
+    starts = tuple(int(x) for x in np.cumsum([0] + lens))
+    compare(n, dict(fields, doc_starts=starts))
+
+
+def test_documents_require_valid_offsets():
+    import ctypes
+    for starts in ((0, 50, 50, 300), (0, 100, 299), (1, 300)):
+        desc = api.Mask(causal=True, doc_starts=starts).desc()
+        hdr = api.BlockIndexStruct()
+        assert api.lib().flash_msa_build_block_index(ctypes.byref(desc), 300, ctypes.byref(hdr)) == \
+            api.ERR_INVALID_ARG, starts

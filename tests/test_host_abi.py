@@ -55,7 +55,7 @@ def test_fwd_argument_errors(L):
     assert fwd_raw(L, k=FAKE + 2) == api.ERR_INVALID_ARG
     assert fwd_raw(L, lse=FAKE + 1) == api.ERR_INVALID_ARG
     assert b"aligned" in L.flash_msa_last_error_string()
-    bad_flags = api.MaskDescStruct(256, 128, 0, 1, 0, 1, 0, None)
+    bad_flags = api.MaskDescStruct(512, 128, 0, 1, 0, 1, 0, None)
     assert fwd_raw(L, mask=bad_flags) == api.ERR_INVALID_ARG
     bad_block = api.Mask(causal=True, window=10, block=64).desc()
     assert fwd_raw(L, mask=bad_block) == api.ERR_UNSUPPORTED

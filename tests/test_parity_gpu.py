@@ -56,7 +56,7 @@ def test_small_cases(d, n, mname):
     gc.full_compare(inp, fields, res)
 
 
-@pytest.mark.parametrize("cid", [2, 3, 4, 5, 6, 7, 9])
+@pytest.mark.parametrize("cid", [2, 3, 4, 5, 6, 7, 9, 10])
 def test_full_size_workloads(cid):
     w = WORKLOADS[cid]
     inp = workload_inputs(w)
@@ -165,3 +165,32 @@ def test_bitmask_small_cases(d, n, kind):
     inp = small_inputs(2, n, 3, d, seed=n * 11 + d)
     res = gc.run_gpu(inp, fields)
     gc.full_compare(inp, fields, res)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("lens", [(1, 200, 7, 129, 64), (300,), (128, 128, 5, 1, 250, 33)])
+def test_varlen_equals_separate_sequences(d, causal, lens):
+    # a variable-length batch through fwd_varlen / bwd_varlen against the
+    # oracle run on every sequence alone
+    from oracle import attention
+    from oracle.mask import MaskSpec
+    T, H = sum(lens), 3
+    inp = small_inputs(1, T, H, d, seed=sum(lens) + d)
+    cu = np.cumsum([0] + list(lens))
+    q, k, v, do = (inp[n][0].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = api.fwd_varlen(q, k, v, cu, causal=causal)
+    dq, dk, dv = api.bwd_varlen(q, k, v, o, lse, do, cu, causal=causal)
+    assert api.get_status() == api.OK
+    got = {n: t.float().cpu().numpy() for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+    f64 = {n: inp[n][0].double().numpy() for n in ("q", "k", "v", "do")}
+    for h in range(H):
+        for a, e in zip(cu[:-1], cu[1:]):
+            sl = slice(int(a), int(e))
+            args = [f64[n][sl, h] for n in ("q", "k", "v")]
+            o_ref, l_ref = attention.forward_head(*args, d ** -0.5, MaskSpec(causal=causal))
+            g_ref = attention.backward_head(*args, f64["do"][sl, h], d ** -0.5, MaskSpec(causal=causal))
+            gc.check_o(got["o"][sl, h], o_ref)
+            gc.check_lse(got["lse"][h, sl], l_ref)
+            for name, ref in zip(("dq", "dk", "dv"), g_ref):
+                gc.check_grad(got[name][sl, h], ref, name)

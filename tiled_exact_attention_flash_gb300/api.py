@@ -22,7 +22,8 @@ LIB_PATH = os.path.join(_HERE, "libflashmsa.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE, ERR_INDEX = range(7)
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "TIMEOUT",
                 5: "WORKSPACE", 6: "INDEX"}
-CAUSAL, WINDOW, DILATED, STRIDED, GLOBAL, STRIDED_REL, DILATED_FAR, BITMASK = 1, 2, 4, 8, 16, 32, 64, 128
+CAUSAL, WINDOW, DILATED, STRIDED, GLOBAL, STRIDED_REL, DILATED_FAR, BITMASK, DOCUMENTS = \
+    1, 2, 4, 8, 16, 32, 64, 128, 256
 
 # exported symbols, in the order include/flashmsa.h declares them
 SYMBOLS = (
@@ -76,6 +77,8 @@ class MaskDescStruct(ctypes.Structure):
         ("index", ctypes.c_void_p),
         ("global_tokens", ctypes.c_int64),
         ("bitmask", ctypes.c_void_p),
+        ("doc_starts", ctypes.c_void_p),
+        ("n_docs", ctypes.c_int64),
     ]
 
 
@@ -152,6 +155,8 @@ class Mask:
     # bit-packed element mask (flag BITMASK): N rows of ceil(N/32) little-endian
     # uint32 words, read by build_block_index only (see inputs.pack_bitmask)
     bitmask: Optional[bytes] = field(default=None, repr=False)
+    # packed sequences (flag DOCUMENTS): offsets 0 = s_0 < s_1 < ... < s_D = N
+    doc_starts: Optional[tuple] = field(default=None, repr=False)
 
     @classmethod
     def from_fields(cls, fields: dict) -> "Mask":
@@ -167,6 +172,7 @@ class Mask:
             f |= STRIDED_REL if self.stride_relative else STRIDED
         f |= GLOBAL if self.global_tokens is not None else 0
         f |= BITMASK if self.bitmask is not None else 0
+        f |= DOCUMENTS if self.doc_starts is not None else 0
         return f
 
     @property
@@ -175,9 +181,16 @@ class Mask:
 
     def desc(self, index_ptr=None) -> MaskDescStruct:
         bits = ctypes.cast(ctypes.c_char_p(self.bitmask), ctypes.c_void_p) if self.bitmask else None
-        return MaskDescStruct(self.flags, self.block, self.window or 0, self.dilation or 1,
-                              self.dilation_near, self.stride or 1, self.stride_phase,
-                              index_ptr, self.global_tokens or 0, bits)
+        starts = None
+        if self.doc_starts is not None:
+            starts = np.ascontiguousarray(self.doc_starts, dtype=np.int64)
+        d = MaskDescStruct(self.flags, self.block, self.window or 0, self.dilation or 1,
+                           self.dilation_near, self.stride or 1, self.stride_phase,
+                           index_ptr, self.global_tokens or 0, bits,
+                           starts.ctypes.data if starts is not None else None,
+                           len(starts) - 1 if starts is not None else 0)
+        d._keep = starts  # the offsets must outlive the struct
+        return d
 
 
 _INDEX_ARRAYS = (("row_ptr", np.int32, "nq1"), ("col_idx", np.int32, "nnz"),
@@ -245,6 +258,44 @@ def build_block_index(mask: Mask, n: int) -> BlockIndex:
 def check_block_index(index: BlockIndex) -> int:
     s = index.host_struct()
     return lib().flash_msa_check_block_index(ctypes.byref(s), index.n)
+
+
+_VARLEN_INDEX: dict = {}
+
+
+def varlen_mask(cu_seqlens, causal: bool = True, device="cuda"):
+    """Mask and (cached) device index of a variable-length batch: sequences
+    packed back to back on one token axis with offsets cu_seqlens."""
+    starts = tuple(int(x) for x in (cu_seqlens.tolist() if hasattr(cu_seqlens, "tolist") else cu_seqlens))
+    key = (starts, bool(causal), str(device))
+    if key not in _VARLEN_INDEX:
+        mask = Mask(causal=bool(causal), doc_starts=starts)
+        _VARLEN_INDEX.clear()  # keep one layout: indices can be large
+        _VARLEN_INDEX[key] = (mask, build_block_index(mask, starts[-1]).to(device))
+    return _VARLEN_INDEX[key]
+
+
+def fwd_varlen(q, k, v, cu_seqlens, causal: bool = True, scale: Optional[float] = None,
+               out=None, lse=None, stream=None):
+    """Forward of a variable-length batch: q, k, v of shape (T, H, d) hold the
+    sequences back to back (offsets cu_seqlens, T = cu_seqlens[-1]); returns
+    O (T, H, d) and LSE (H, T).  Runs flash_msa_fwd on the packed axis with the
+    DOCUMENTS mask."""
+    mask, index = varlen_mask(cu_seqlens, causal, q.device)
+    o, l = fwd(q.unsqueeze(0), k.unsqueeze(0), v.unsqueeze(0), mask=mask, index=index,
+               scale=scale, out=None if out is None else out.unsqueeze(0),
+               lse=None if lse is None else lse.unsqueeze(0), stream=stream)
+    return o[0], l[0]
+
+
+def bwd_varlen(q, k, v, o, lse, do, cu_seqlens, causal: bool = True,
+               scale: Optional[float] = None, stream=None):
+    """dQ, dK, dV of a variable-length batch (shapes as in fwd_varlen)."""
+    mask, index = varlen_mask(cu_seqlens, causal, q.device)
+    dq, dk, dv = bwd(q.unsqueeze(0), k.unsqueeze(0), v.unsqueeze(0), o.unsqueeze(0),
+                     lse.unsqueeze(0), do.unsqueeze(0), mask=mask, index=index, scale=scale,
+                     stream=stream)
+    return dq[0], dk[0], dv[0]
 
 
 # ---------------------------------------------------------------------------

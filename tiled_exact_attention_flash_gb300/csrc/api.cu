@@ -78,7 +78,7 @@ static flash_msa_status check_mask(const flash_msa_mask_desc* m, MaskParams& mp,
   if (!m) return FLASH_MSA_OK;
   if (m->flags & ~uint32_t(FLASH_MSA_CAUSAL | FLASH_MSA_WINDOW | FLASH_MSA_DILATED |
                            FLASH_MSA_STRIDED | FLASH_MSA_GLOBAL | FLASH_MSA_STRIDED_REL |
-                           FLASH_MSA_DILATED_FAR | FLASH_MSA_BITMASK))
+                           FLASH_MSA_DILATED_FAR | FLASH_MSA_BITMASK | FLASH_MSA_DOCUMENTS))
     return set_error(FLASH_MSA_ERR_INVALID_ARG, "mask: unknown flag bits 0x%x", m->flags);
   // every flag but CAUSAL needs an index (the bits travel in it)
   const uint32_t pat = m->flags & ~uint32_t(FLASH_MSA_CAUSAL);
@@ -153,7 +153,7 @@ static flash_msa_status make_lists(const flash_msa_mask_desc* m, int64_t N, bool
                      ix->n_k_blocks, static_cast<long long>(N));
   if (!ix->row_ptr || !ix->col_idx || !ix->kind || !ix->q_order)
     return set_error(FLASH_MSA_ERR_INDEX, "index: CSR arrays or q_order missing");
-  const bool bits = (m->flags & FLASH_MSA_BITMASK) && ix->n_bit_tiles > 0;
+  const bool bits = (m->flags & (FLASH_MSA_BITMASK | FLASH_MSA_DOCUMENTS)) && ix->n_bit_tiles > 0;
   if (bits && (!ix->bit_slot || !ix->bits || (want_csc && (!ix->bit_slot_t || !ix->bits_t))))
     return set_error(FLASH_MSA_ERR_INDEX, "index: bit arrays missing");
   rows.ptr = ix->row_ptr;
@@ -209,9 +209,32 @@ flash_msa_status flash_msa_build_block_index(const flash_msa_mask_desc* mask, in
   bool need = false;
   flash_msa_status st = check_mask(mask, mp, need);
   if (st != FLASH_MSA_OK) return st;
-  const bool with_bits = (mask->flags & FLASH_MSA_BITMASK) != 0;
-  if (with_bits && !mask->bitmask)
+  const bool with_bitmask = (mask->flags & FLASH_MSA_BITMASK) != 0;
+  const bool with_docs = (mask->flags & FLASH_MSA_DOCUMENTS) != 0;
+  const bool with_bits = with_bitmask || with_docs;
+  if (with_bitmask && !mask->bitmask)
     return set_error(FLASH_MSA_ERR_INVALID_ARG, "build_block_index: BITMASK without mask->bitmask");
+  // packed documents: the sequence range [doc_lo, doc_hi) of every token
+  std::vector<int64_t> doc_lo, doc_hi;
+  if (with_docs) {
+    const int64_t* ds = mask->doc_starts;
+    if (!ds || mask->n_docs < 1 || ds[0] != 0 || ds[mask->n_docs] != N)
+      return set_error(FLASH_MSA_ERR_INVALID_ARG,
+                       "build_block_index: DOCUMENTS needs offsets from 0 to N=%lld",
+                       static_cast<long long>(N));
+    doc_lo.resize(size_t(N));
+    doc_hi.resize(size_t(N));
+    for (int64_t d = 0; d < mask->n_docs; ++d) {
+      if (ds[d + 1] <= ds[d])
+        return set_error(FLASH_MSA_ERR_INVALID_ARG,
+                         "build_block_index: document offsets must rise strictly (at %lld)",
+                         static_cast<long long>(d));
+      for (int64_t t = ds[d]; t < ds[d + 1]; ++t) {
+        doc_lo[size_t(t)] = ds[d];
+        doc_hi[size_t(t)] = ds[d + 1];
+      }
+    }
+  }
   const int64_t nb = n_blocks_of(N);
   const int64_t words_per_row = (N + 31) / 32;
   // Tile class with the bits: live entries of row r = interval of the other
@@ -232,9 +255,20 @@ flash_msa_status flash_msa_build_block_index(const flash_msa_mask_desc* mask, in
         int64_t chi = std::min<int64_t>({i - r.lo - j0, N - 1 - j0, int64_t(kTile - 1)});
         for (int64_t col = clo; col <= chi; ++col) iv[col >> 5] |= 1u << (col & 31);
       }
+      uint32_t dbits[4] = {~0u, ~0u, ~0u, ~0u};  // keys of row i's own document
+      if (with_docs) {
+        for (int w = 0; w < 4; ++w) dbits[w] = 0;
+        if (i < N) {
+          const int64_t a = std::max(doc_lo[size_t(i)] - j0, int64_t(0));
+          const int64_t e = std::min(doc_hi[size_t(i)] - j0, int64_t(kTile));
+          for (int64_t col = a; col < e; ++col) dbits[col >> 5] |= 1u << (col & 31);
+        }
+      }
       for (int w = 0; w < 4; ++w) {
         const int64_t word = int64_t(kb) * 4 + w;
-        const uint32_t mbits = (i < N && word < words_per_row) ? mask->bitmask[i * words_per_row + word] : 0u;
+        uint32_t mbits = dbits[w];
+        if (with_bitmask)
+          mbits &= (i < N && word < words_per_row) ? mask->bitmask[i * words_per_row + word] : 0u;
         const uint32_t f = iv[w] & mbits;
         if (f != iv[w]) cut = true;
         live += __builtin_popcount(f);

@@ -10,8 +10,8 @@ Workloads: the five attention configurations the pages' discussion motivates
 (7B-style layer, d = 128, long context; causal, local window + strided, and
 local window with block dilation), plus a sixth for the local window with
 global tokens hybrid (8K window, 512 global tokens, 128K tokens), two more
-with the second readings of the strided and dilated masks, and one of packed
-documents under a bit-packed mask.  Seeds: Q, K, V, dO of workload c use
+with the second readings of the strided and dilated masks, one of packed
+documents under a bit-packed mask and one variable-length batch.  Seeds: Q, K, V, dO of workload c use
 1000*c + 1 .. 1000*c + 4.
 """
 from __future__ import annotations
@@ -34,9 +34,11 @@ class Workload:
     d: int
     # mask description: plain fields, converted by each side into its own type
     mask: dict = field(default_factory=dict)
-    # packed documents: (mean length, seed) of the seeded document lengths; the
-    # bit-packed mask is added by mask_fields()
+    # packed documents: (mean length, seed) of the seeded document lengths,
+    # added by mask_fields() as a bit-packed mask ("bitmask") or as sequence
+    # offsets ("starts": a variable-length batch)
     docs: Optional[tuple] = None
+    docs_as: str = "bitmask"
 
     @property
     def shape(self):
@@ -46,7 +48,11 @@ class Workload:
         """The mask fields with the packed-documents bitmask when there is one."""
         f = dict(self.mask)
         if self.docs is not None:
-            f["bitmask"] = _documents_bitmask(self.N, *self.docs)
+            if self.docs_as == "starts":
+                lens = document_lengths(self.N, self.docs[1], self.docs[0])
+                f["doc_starts"] = tuple(int(x) for x in np.cumsum([0] + lens))
+            else:
+                f["bitmask"] = _documents_bitmask(self.N, *self.docs)
         return f
 
 
@@ -70,6 +76,10 @@ WORKLOADS = {
     # packed documents under a bit-packed mask, causal inside each document
     9: Workload(9, "causal packed documents (mean 2048 tokens) B1 H16 N32768 d128", 1, 16, 32768,
                 128, {"causal": True}, docs=(2048, 9009)),
+    # a variable-length batch: seeded sequence lengths (mean 2048) packed into
+    # 65536 tokens, causal inside each sequence
+    10: Workload(10, "causal varlen batch (mean 2048 tokens) T65536 H16 d128", 1, 16, 65536, 128,
+                 {"causal": True}, docs=(2048, 10010), docs_as="starts"),
 }
 
 
