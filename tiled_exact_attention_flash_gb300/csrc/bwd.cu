@@ -518,20 +518,26 @@ __device__ __forceinline__ void dkdv_mma(const BwdParams& p, uint8_t* smem, uint
   drain_bar(bar(L::kMmaDone), 0);
 }
 
-// Write 32 fp32 TMEM columns of one row, times `mul`, as bf16 to global.
-__device__ __forceinline__ void store_row_chunk(uint32_t taddr, float mul, __nv_bfloat16* dst,
-                                                bool valid) {
-  uint32_t v[32];
-  tmem_ld_x32(taddr, v);
-  uint32_t w[16];
+// Write the warpgroup's HD/2 fp32 accumulator columns of this thread's row
+// (TMEM address taddr), times `mul`, as bf16 to dst (the row's first element
+// of the piece); rows of consecutive lanes are `stride` bytes apart.
+template <int HD>
+__device__ __forceinline__ void store_acc_piece(uint32_t taddr, float mul, __nv_bfloat16* dst,
+                                                int64_t stride, bool valid) {
+  constexpr int kC = HD / 16;  // 16-byte chunks: HD/2 bf16 = HD bytes
+  uint4 c[kC];
 #pragma unroll
-  for (int j = 0; j < 16; ++j)
-    w[j] = pack_bf16x2(__uint_as_float(v[2 * j]) * mul, __uint_as_float(v[2 * j + 1]) * mul);
-  if (valid) {
-    uint4* d4 = reinterpret_cast<uint4*>(dst);
+  for (int q = 0; q < HD / 64; ++q) {
+    uint32_t v[32];
+    tmem_ld_x32(taddr + q * 32, v);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) d4[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+    for (int j = 0; j < 4; ++j) {
+      const float* f = reinterpret_cast<const float*>(v + 8 * j);
+      c[4 * q + j] = make_uint4(pack_bf16x2(f[0] * mul, f[1] * mul), pack_bf16x2(f[2] * mul, f[3] * mul),
+                                pack_bf16x2(f[4] * mul, f[5] * mul), pack_bf16x2(f[6] * mul, f[7] * mul));
+    }
   }
+  store_rows_transposed<kC>(c, reinterpret_cast<char*>(dst), stride, valid);
 }
 
 __device__ __forceinline__ void zero_row(__nv_bfloat16* dst, int hd, bool valid) {
@@ -660,11 +666,9 @@ __device__ __forceinline__ void dkdv_elementwise(const BwdParams& p, uint8_t* sm
     ++af_cnt;
     tc_fence_after();
     // warpgroup g writes dV and dK columns [d/2 g, d/2 (g + 1))
-#pragma unroll
-    for (int c = g * (HD / 64); c < (g + 1) * (HD / 64); ++c) {
-      store_row_chunk(tDV + c * 32, 1.f, dv_row + c * 32, valid);
-      store_row_chunk(tDK + c * 32, p.scale, dk_row + c * 32, valid);
-    }
+    const int64_t stride = int64_t(p.Hkv) * HD * 2;  // bytes between consecutive key rows
+    store_acc_piece<HD>(tDV + g * (HD / 2), 1.f, dv_row + g * (HD / 2), stride, valid);
+    store_acc_piece<HD>(tDK + g * (HD / 2), p.scale, dk_row + g * (HD / 2), stride, valid);
     warp_arrive(bar(L::kAccEmpty));
   }
 }
@@ -790,9 +794,8 @@ __device__ __forceinline__ void dq_elementwise(const BwdParams& p, uint8_t* smem
     ++af_cnt;
     tc_fence_after();
     __nv_bfloat16* dq_row = p.out_a + ((int64_t(cur.b) * p.N + i) * p.H + cur.h) * HD;
-#pragma unroll
-    for (int c = g * (HD / 64); c < (g + 1) * (HD / 64); ++c)
-      store_row_chunk(tDQ + c * 32, p.scale, dq_row + c * 32, i < p.N);
+    store_acc_piece<HD>(tDQ + g * (HD / 2), p.scale, dq_row + g * (HD / 2),
+                        int64_t(p.H) * HD * 2, i < p.N);
     warp_arrive(bar(L::kAccEmpty));
     cur = nxt;
     has = has_next;

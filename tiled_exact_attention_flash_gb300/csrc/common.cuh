@@ -322,6 +322,44 @@ __device__ __forceinline__ InnerTile inner_tile(const Unit& un, int t, const Lis
   return it;
 }
 
+// Coalesced store of one piece of kC 16-byte chunks per row.  Lane l of the
+// warp holds chunks c[0..kC) of its own row's piece, to be written at `dst`;
+// the rows of consecutive lanes are `stride` bytes apart.  Written as is,
+// every store instruction would touch 32 rows; instead the kC lanes of each
+// group first exchange chunks in log2(kC) butterfly steps (a kC x kC
+// transpose: afterwards lane i of the group holds chunk i of every row of
+// the group), so that store k writes the whole piece of row (group base + k)
+// from kC consecutive lanes.  row_ok: whether this lane's row exists.
+template <int kC>
+__device__ __forceinline__ void store_rows_transposed(uint4 (&c)[kC], char* dst, int64_t stride,
+                                                      bool row_ok) {
+  const int lane = int(threadIdx.x & 31);
+  const int i = lane & (kC - 1);
+#pragma unroll
+  for (int m = kC / 2; m >= 1; m >>= 1) {
+    const bool upper = (i & m) != 0;
+#pragma unroll
+    for (int j = 0; j < kC; ++j) {
+      if (j & m) continue;
+      // the lower lane of the pair gives chunk j | m and takes the partner's chunk j
+      const uint4 send = upper ? c[j] : c[j | m];
+      uint4 recv;
+      recv.x = __shfl_xor_sync(0xFFFFFFFFu, send.x, m);
+      recv.y = __shfl_xor_sync(0xFFFFFFFFu, send.y, m);
+      recv.z = __shfl_xor_sync(0xFFFFFFFFu, send.z, m);
+      recv.w = __shfl_xor_sync(0xFFFFFFFFu, send.w, m);
+      if (upper) c[j] = recv;
+      else c[j | m] = recv;
+    }
+  }
+  const uint32_t ok = __ballot_sync(0xFFFFFFFFu, row_ok);
+  const int base = lane - i;
+#pragma unroll
+  for (int k = 0; k < kC; ++k)
+    if ((ok >> (base + k)) & 1u)
+      *reinterpret_cast<uint4*>(dst + int64_t(k - i) * stride + i * 16) = c[k];
+}
+
 // Bits of one row of a bit tile (bit-packed masks): kWords 32-bit words
 // starting at word w0 of tile-local row r.  prefetch_tile_bits pulls the row
 // into L1 before the tile's barrier wait without holding registers across
