@@ -268,6 +268,15 @@ flash_msa_status flash_msa_bwd_noalloc(const void* q, const void* k, const void*
                                        void* dk, void* dv, int B, int H, int64_t N, int d,
                                        float scale, const flash_msa_mask_desc* mask, void* stream);
 
+/* Failure-detection self-test (no counterpart on the pages): launches on
+ * `stream` one thread that waits, with the bounded wait every kernel here
+ * uses, on an mbarrier that nothing arrives on.  The wait gives up after the
+ * library's limit (0.5 s), records FLASH_MSA_ERR_TIMEOUT in the device status
+ * word and returns, so the next flash_msa_get_status() reports TIMEOUT and
+ * the context stays usable; nothing faults or hangs.  Returns OK or ERR_CUDA
+ * (launch). */
+flash_msa_status flash_msa_selftest_wait_timeout(void* stream);
+
 /* Synchronise `stream`, then read and clear the device status word shared by
  * every kernel of this library on the current device.  Returns OK, or the
  * first device-side error recorded since the last call (TIMEOUT, INDEX), or

@@ -36,6 +36,7 @@ SYMBOLS = (
     "flash_msa_fwd_gqa",
     "flash_msa_bwd_gqa",
     "flash_msa_bwd_noalloc",
+    "flash_msa_selftest_wait_timeout",
     "flash_msa_get_status",
     "flash_msa_last_error_string",
     "flash_msa_version",
@@ -114,11 +115,13 @@ def lib() -> ctypes.CDLL:
     L.flash_msa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i64, i32,
                                         f32, ctypes.POINTER(MaskDescStruct), vp]
     L.flash_msa_get_status.argtypes = [vp]
+    L.flash_msa_selftest_wait_timeout.argtypes = [vp]
     L.flash_msa_last_error_string.restype = ctypes.c_char_p
     L.flash_msa_version.restype = ctypes.c_char_p
     for name in ("flash_msa_build_block_index", "flash_msa_check_block_index", "flash_msa_fwd",
                  "flash_msa_bwd", "flash_msa_bwd_stages", "flash_msa_bwd_noalloc",
-                 "flash_msa_fwd_gqa", "flash_msa_bwd_gqa", "flash_msa_get_status"):
+                 "flash_msa_fwd_gqa", "flash_msa_bwd_gqa", "flash_msa_get_status",
+                 "flash_msa_selftest_wait_timeout"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -443,6 +446,12 @@ def bwd_noalloc(q, k, v, o, lse, do, mask: Optional[Mask] = None,
 def get_status(stream=None) -> int:
     """Synchronise the stream and read + clear the device status word."""
     return lib().flash_msa_get_status(_stream_ptr(stream))
+
+
+def selftest_wait_timeout(stream=None) -> int:
+    """Launch the bounded-wait probe (a wait that must run out); the next
+    get_status() then reports ERR_TIMEOUT."""
+    return lib().flash_msa_selftest_wait_timeout(_stream_ptr(stream))
 
 
 def check_status(stream=None):

@@ -588,6 +588,11 @@ flash_msa_status flash_msa_bwd_gqa(const void* q, const void* k, const void* v, 
                   FLASH_MSA_BWD_PREPROCESS | FLASH_MSA_BWD_DKDV | FLASH_MSA_BWD_DQ, stream);
 }
 
+flash_msa_status flash_msa_selftest_wait_timeout(void* stream) {
+  g_last_error[0] = 0;
+  return launch_wait_timeout_probe(static_cast<cudaStream_t>(stream));
+}
+
 flash_msa_status flash_msa_get_status(void* stream) {
   g_last_error[0] = 0;
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)

@@ -25,6 +25,7 @@ unsigned* status_word_ptr();  // device address for the current device, or null 
 constexpr int kSchedSlots = 256;
 int* sched_counter();  // a work counter of the current device for one launch, or null on error
 int sm_count();        // multiprocessors of the current device, 0 on error
+flash_msa_status launch_wait_timeout_probe(cudaStream_t stream);
 
 struct FwdLaunch {
   const void *q, *k, *v;

@@ -5,6 +5,7 @@
 
 #include <atomic>
 
+#include "common.cuh"
 #include "internal.h"
 
 namespace fmsa {
@@ -55,6 +56,31 @@ int sm_count() {
     cache[dev] = n;
   }
   return cache[dev];
+}
+
+// Failure-detection probe: one thread waits, through the same bounded wait
+// every kernel of the library uses, on an mbarrier that nothing arrives on.
+// The wait gives up after kWaitLimitNs and records FLASH_MSA_ERR_TIMEOUT
+// (site kTimeoutProbeSite) in the status word; the kernel then returns, so
+// the context stays usable.
+constexpr unsigned kTimeoutProbeSite = 0xEE;
+
+__global__ void wait_timeout_probe_kernel(unsigned* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  abort_flag = 0;
+  mbar_init(smem_u32(&bar), 1);
+  fence_mbar_init();
+  wait_bar(smem_u32(&bar), 0, &abort_flag, status, kTimeoutProbeSite);
+}
+
+flash_msa_status launch_wait_timeout_probe(cudaStream_t stream) {
+  unsigned* status = status_word_ptr();
+  if (!status) return set_cuda_error("selftest: status word");
+  wait_timeout_probe_kernel<<<1, 32, 0, stream>>>(status);
+  if (cudaGetLastError() != cudaSuccess) return set_cuda_error("selftest: launch");
+  return FLASH_MSA_OK;
 }
 
 }  // namespace fmsa
