@@ -1,12 +1,12 @@
 // Forward attention kernel for sm_103a: O = softmax(mask(Q K^T * scale)) V
-// and LSE, one 128-row query tile per work unit, tile by tile over the unit's
-// live key tiles with an online softmax ("Flash MSA Attention Kernel
+// and LSE, two neighbouring 128-row query tiles per CTA, tile by tile over
+// their live key tiles with an online softmax ("Flash MSA Attention Kernel
 // Implementation", sections "The Flash Core: Tiling Over the Memory
 // Hierarchy" and "Optimization Tricks That Actually Matter"; sparse lists
 // from "How Does Flash-MSA Sparse Attention Work", section "How Flash-MSA
 // Sparse Attention Works").
 //
-// CTA layout (384 threads, one CTA per SM):
+// CTA layout (384 threads, one CTA resident per SM, one CTA per pair unit):
 //   warp 0      TMA producer: Q tiles and the K/V ring, one elected lane
 //   warp 1      MMA issuer: tcgen05.mma for S = Q K^T and O += P V, one lane
 //   warp 2      TMEM allocator
