@@ -9,6 +9,7 @@
 // CTA layout (384 threads, one CTA resident per SM, one CTA per pair unit):
 //   warp 0      TMA producer: Q tiles and the K/V ring, one elected lane
 //   warp 1      MMA issuer: tcgen05.mma for S = Q K^T and O += P V, one lane
+//               (with an index: slot 0 only, warp 3 issuing for slot 1)
 //   warp 2      TMEM allocator
 //   warps 4-7   softmax + epilogue for query slot 0 (thread = query row)
 //   warps 8-11  softmax + epilogue for query slot 1
@@ -319,6 +320,127 @@ __device__ __forceinline__ void fwd_mma(const FwdParams& p, uint8_t* smem, uint6
 }
 
 template <int HD>
+__device__ __forceinline__ void fwd_mma_slot(const FwdParams& p, uint8_t* smem, uint64_t* bars,
+                                             uint32_t tmem, int s, volatile int* abort_flag) {
+  // MMA issuer of query slot s, used for lists from a block index: one
+  // thread per slot, both walking the same union of key tiles (so both see
+  // the same ring stages) and both releasing every stage (kKvEmpty then
+  // counts two commits).  Where the two slots' lists differ, neither slot
+  // waits for the other's softmax; with identical dense / causal lists the
+  // single issuer (fwd_mma), whose order staggers the slots, is faster.
+  using L = FwdLayout<HD>;
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+  constexpr uint32_t kIdQK = idesc_bf16_f32(128, 128, false, false);
+  constexpr uint32_t kIdPV = idesc_bf16_f32(128, HD, false, true);
+  uint32_t kv_cnt = 0, qf_cnt = 0, pf_cnt = 0, oe_cnt = 0;
+  const uint32_t ring = smem_u32(smem + L::kRingOff);
+  const uint32_t tS = tmem + uint32_t(s * 256);
+  const uint32_t qd = sdesc_lo(smem_u32(smem + L::kQOff + s * L::kTileBytes), 16);
+  bool ok = true;
+  // S_s = Q_s K^T for the K tile in ring stage `stage`
+  auto issue_qk = [&](int stage) {
+    const uint32_t kd = sdesc_lo(ring + stage * L::kTileBytes, 16);
+#pragma unroll
+    for (int kk = 0; kk < HD / 16; ++kk) {
+      // A = Q, B = K, both K-major: 16-element k-steps are 32 bytes apart
+      // inside a 128-byte swizzle row, 64-element chunks 16 KB apart
+      const uint32_t off = ((kk / 4) * (kTile * 128) + (kk % 4) * 32) >> 4;
+      mma_ss(tS, qd + off, kd + off, kIdQK, kk > 0 ? 1u : 0u);
+    }
+    mma_commit(bar(L::kSFull + s));
+  };
+  for (int k = 0; ok; ++k) {
+    const int u = int(blockIdx.x) + k * int(gridDim.x);
+    if (u >= p.n_units) break;
+    const PairUnit pu = decode_pair(u, p);
+    if (pu.n[0] + pu.n[1] == 0) continue;
+    int seen = 0;    // P V products issued in this unit
+    int issued = 0;  // Q K^T products issued in this unit
+    PairWalk w;
+    walk_init(w, pu, p.list);
+    PairTile cur, nxt;
+    walk_next(w, p.list, cur);  // the union is non-empty
+    // prologue: Q K^T of the first tile
+    {
+      const int ks = kv_cnt % L::kStages;
+      if (cur.in[s] && !wait_bar(bar(L::kQFull + s), qf_cnt & 1, abort_flag, p.status, 13))
+        ok = false;
+      if (ok && !wait_bar(bar(L::kKvFull + ks), (kv_cnt / L::kStages) & 1, abort_flag, p.status, 14))
+        ok = false;
+      if (!ok) break;
+      tc_fence_after();
+      if (cur.in[s]) {
+        ++qf_cnt;
+        issue_qk(ks);
+        if (++issued == pu.n[s]) mma_commit(bar(L::kQEmpty + s));
+      }
+      mma_commit(bar(L::kKvEmpty + ks));
+      ++kv_cnt;
+    }
+    while (ok) {
+      const bool more = walk_next(w, p.list, nxt);
+      const int vs = kv_cnt % L::kStages;        // V of cur
+      const int ks = (kv_cnt + 1) % L::kStages;  // K of nxt
+      // both threads wait for every stage they release, used or not: a
+      // thread that skipped the wait could release a later use of the stage
+      // before the other thread released this one (arrivals are not tagged)
+      if (!wait_bar(bar(L::kKvFull + vs), (kv_cnt / L::kStages) & 1, abort_flag, p.status, 12)) {
+        ok = false;
+        break;
+      }
+      if (cur.in[s]) {  // O_s (+)= P_s V
+        if (!wait_bar(bar(L::kPFull + s), pf_cnt & 1, abort_flag, p.status, 10)) {
+          ok = false;
+          break;
+        }
+        ++pf_cnt;
+        if (seen == 0) {
+          if (!wait_bar(bar(L::kOEmpty + s), (oe_cnt & 1) ^ 1, abort_flag, p.status, 11)) {
+            ok = false;
+            break;
+          }
+          ++oe_cnt;
+        }
+        tc_fence_after();
+        // B = V tile, MN-major: 64-column chunks 16 KB apart, 8-row groups
+        // 1 KB apart, 16 rows (2 KB) per k-step
+        const uint32_t vd = sdesc_lo(ring + vs * L::kTileBytes, kTile * 128);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts(tS + 128, tS + kk * 8, vd + kk * (2048 >> 4), kIdPV,
+                 (seen > 0 || kk > 0) ? 1u : 0u);
+        ++seen;
+        if (seen == pu.n[s]) mma_commit(bar(L::kOFull + s));
+      }
+      mma_commit(bar(L::kKvEmpty + vs));
+      if (!more) break;
+      if (!wait_bar(bar(L::kKvFull + ks), ((kv_cnt + 1) / L::kStages) & 1, abort_flag, p.status,
+                    14)) {
+        ok = false;
+        break;
+      }
+      if (nxt.in[s]) {
+        if (issued == 0 && !wait_bar(bar(L::kQFull + s), qf_cnt & 1, abort_flag, p.status, 13)) {
+          ok = false;
+          break;
+        }
+        if (issued == 0) ++qf_cnt;
+        tc_fence_after();
+        issue_qk(ks);
+        if (++issued == pu.n[s]) mma_commit(bar(L::kQEmpty + s));
+      }
+      mma_commit(bar(L::kKvEmpty + ks));
+      kv_cnt += 2;
+      cur = nxt;
+    }
+    kv_cnt += 1;  // the last V stage
+  }
+  // every MMA issued so far has finished before TMEM is released
+  mma_commit(bar(L::kMmaDone));
+  drain_bar(bar(L::kMmaDone), 0);
+}
+
+template <int HD>
 __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint64_t* bars, uint32_t tmem,
                                             int slot, volatile int* abort_flag) {
   using L = FwdLayout<HD>;
@@ -499,10 +621,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       mbar_init(smem_u32(bars + L::kOFull + s), 1);
       mbar_init(smem_u32(bars + L::kOEmpty + s), 128);
     }
-    mbar_init(smem_u32(bars + L::kMmaDone), 1);
+    const uint32_t issuers = p.list.ptr ? 2 : 1;  // MMA threads (see fwd_mma_slot)
+    mbar_init(smem_u32(bars + L::kMmaDone), issuers);
     for (int i = 0; i < L::kStages; ++i) {
       mbar_init(smem_u32(bars + L::kKvFull + i), 1);
-      mbar_init(smem_u32(bars + L::kKvEmpty + i), 1);
+      mbar_init(smem_u32(bars + L::kKvEmpty + i), issuers);
     }
     fence_mbar_init();
   }
@@ -522,6 +645,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     regs_shrink<80>();
     if (warp == 0) {
       if (lane == 0) fwd_producer<HD>(p, smem, bars, abort_flag);
+    } else if (p.list.ptr) {  // index lists: one MMA issuer per slot (warps 1 and 3)
+      if ((warp == 1 || warp == 3) && lane == 0)
+        fwd_mma_slot<HD>(p, smem, bars, tmem, warp == 1 ? 0 : 1, abort_flag);
     } else if (warp == 1) {
       if (lane == 0) fwd_mma<HD>(p, smem, bars, tmem, abort_flag);
     }
