@@ -209,6 +209,18 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def sources_sha(names):
+    """First 16 hex digits of the SHA-256 of the named kernel sources, concatenated."""
+    h = hashlib.sha256()
+    for n in names:
+        path = os.path.join(ROOT, "tiled_exact_attention_flash_gb300", "csrc", n)
+        if not os.path.exists(path):
+            return None
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16] if names else None
+
+
 def traffic_per_launch(kernel, workload_name):
     """DRAM bytes per launch from a committed ncu summary, or None when the
     kernel source changed since the counters were taken."""
@@ -217,12 +229,8 @@ def traffic_per_launch(kernel, workload_name):
         return None
     with open(path) as f:
         rec = json.load(f).get(kernel, {})
-    src = os.path.join(ROOT, "tiled_exact_attention_flash_gb300", "csrc", rec.get("source", ""))
-    if not rec or not os.path.exists(src):
-        return None
-    with open(src, "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()[:16]
-    if sha != rec.get("source_sha") or rec.get("workload") != workload_name:
+    sha = sources_sha(rec.get("sources", []))
+    if not rec or sha is None or sha != rec.get("source_sha") or rec.get("workload") != workload_name:
         return None
     return rec.get("bytes_per_launch")
 
