@@ -537,7 +537,9 @@ __device__ __forceinline__ void store_acc_piece(uint32_t taddr, float mul, __nv_
                                 pack_bf16x2(f[4] * mul, f[5] * mul), pack_bf16x2(f[6] * mul, f[7] * mul));
     }
   }
-  store_rows_transposed<kC>(c, reinterpret_cast<char*>(dst), stride, valid);
+  // lane groups of 4: each store writes 64 contiguous bytes of 8 rows (fewer
+  // shuffles than a full 8-lane transpose, still whole 32-byte sectors)
+  store_rows_transposed<kC, 4>(c, reinterpret_cast<char*>(dst), stride, valid);
 }
 
 __device__ __forceinline__ void zero_row(__nv_bfloat16* dst, int hd, bool valid) {

@@ -325,39 +325,47 @@ __device__ __forceinline__ InnerTile inner_tile(const Unit& un, int t, const Lis
 // Coalesced store of one piece of kC 16-byte chunks per row.  Lane l of the
 // warp holds chunks c[0..kC) of its own row's piece, to be written at `dst`;
 // the rows of consecutive lanes are `stride` bytes apart.  Written as is,
-// every store instruction would touch 32 rows; instead the kC lanes of each
-// group first exchange chunks in log2(kC) butterfly steps (a kC x kC
-// transpose: afterwards lane i of the group holds chunk i of every row of
-// the group), so that store k writes the whole piece of row (group base + k)
-// from kC consecutive lanes.  row_ok: whether this lane's row exists.
-template <int kC>
+// every store instruction would touch 32 rows.  Instead the chunks are taken
+// in groups of kG (kG divides kC), and for each group the kG lanes of each
+// lane group exchange chunks in log2(kG) butterfly steps (a kG x kG
+// transpose: afterwards lane i of the lane group holds chunk i of the group
+// for every row of the lane group), so that every store instruction writes
+// kG * 16 contiguous bytes of each of 32 / kG rows.  row_ok: whether this
+// lane's row exists.
+template <int kC, int kG = kC>
 __device__ __forceinline__ void store_rows_transposed(uint4 (&c)[kC], char* dst, int64_t stride,
                                                       bool row_ok) {
+  static_assert(kC % kG == 0 && (kG & (kG - 1)) == 0, "kG: a power of two dividing kC");
   const int lane = int(threadIdx.x & 31);
-  const int i = lane & (kC - 1);
+  const int i = lane & (kG - 1);
 #pragma unroll
-  for (int m = kC / 2; m >= 1; m >>= 1) {
-    const bool upper = (i & m) != 0;
+  for (int q = 0; q < kC; q += kG) {
 #pragma unroll
-    for (int j = 0; j < kC; ++j) {
-      if (j & m) continue;
-      // the lower lane of the pair gives chunk j | m and takes the partner's chunk j
-      const uint4 send = upper ? c[j] : c[j | m];
-      uint4 recv;
-      recv.x = __shfl_xor_sync(0xFFFFFFFFu, send.x, m);
-      recv.y = __shfl_xor_sync(0xFFFFFFFFu, send.y, m);
-      recv.z = __shfl_xor_sync(0xFFFFFFFFu, send.z, m);
-      recv.w = __shfl_xor_sync(0xFFFFFFFFu, send.w, m);
-      if (upper) c[j] = recv;
-      else c[j | m] = recv;
+    for (int m = kG / 2; m >= 1; m >>= 1) {
+      const bool upper = (i & m) != 0;
+#pragma unroll
+      for (int j = 0; j < kG; ++j) {
+        if (j & m) continue;
+        // the lower lane of the pair gives chunk j | m and takes the partner's chunk j
+        const uint4 send = upper ? c[q + j] : c[q + (j | m)];
+        uint4 recv;
+        recv.x = __shfl_xor_sync(0xFFFFFFFFu, send.x, m);
+        recv.y = __shfl_xor_sync(0xFFFFFFFFu, send.y, m);
+        recv.z = __shfl_xor_sync(0xFFFFFFFFu, send.z, m);
+        recv.w = __shfl_xor_sync(0xFFFFFFFFu, send.w, m);
+        if (upper) c[q + j] = recv;
+        else c[q + (j | m)] = recv;
+      }
     }
   }
   const uint32_t ok = __ballot_sync(0xFFFFFFFFu, row_ok);
   const int base = lane - i;
 #pragma unroll
-  for (int k = 0; k < kC; ++k)
-    if ((ok >> (base + k)) & 1u)
-      *reinterpret_cast<uint4*>(dst + int64_t(k - i) * stride + i * 16) = c[k];
+  for (int q = 0; q < kC; q += kG)
+#pragma unroll
+    for (int k = 0; k < kG; ++k)
+      if ((ok >> (base + k)) & 1u)
+        *reinterpret_cast<uint4*>(dst + int64_t(k - i) * stride + (q + i) * 16) = c[q + k];
 }
 
 // Bits of one row of a bit tile (bit-packed masks): kWords 32-bit words

@@ -579,11 +579,13 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint64_t* bars, 
 #pragma unroll
       for (int j = 0; j < 16; ++j)
         w[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv_l, __uint_as_float(o[2 * j + 1]) * inv_l);
-      if (i < p.N) {
-        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+      // pairs of lanes swap 16-byte chunks, so each store writes 32 contiguous
+      // bytes (a whole sector) of 16 rows instead of 16 bytes of 32 rows
+      uint4 cc[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-      }
+      for (int j = 0; j < 4; ++j) cc[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+      store_rows_transposed<4, 2>(cc, reinterpret_cast<char*>(orow + c * 32),
+                                  int64_t(p.H) * HD * 2, i < p.N);
     }
     if (un.n > 0) {
       tc_fence_before();
