@@ -18,7 +18,7 @@
 // products while the other slot's softmax runs.  TMEM (512 columns):
 //   slot s: S at columns [256 s, 256 s + 128), P (bf16, two per column)
 //   aliased onto the first 64 of them, O at [256 s + 128, 256 s + 128 + d).
-// Shared memory: one Q tile per slot, a ring of K/V tiles, all 128-byte
+// Shared memory: one Q tile per slot, a ring of K/V tile pairs, all 128-byte
 // swizzled by TMA and read by the tensor core through matrix descriptors.
 #include <cuda_runtime.h>
 
@@ -43,14 +43,18 @@ struct FwdParams {
 template <int HD>
 struct FwdLayout {
   static constexpr int kTileBytes = kTile * HD * 2;
-  static constexpr int kStages = HD == 128 ? 4 : 8;
+  // K/V ring: kSlots slots of two tile buffers; a slot holds what one step
+  // of the MMA loop consumes and releases together: V of tile t in its first
+  // buffer and K of the next tile in its second (a unit's first slot holds
+  // only K of its first tile, its last only V of its last tile)
+  static constexpr int kSlots = HD == 128 ? 2 : 4;
   static constexpr int kQOff = 0;
   static constexpr int kRingOff = 2 * kTileBytes;
-  static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
+  static constexpr int kBarOff = kRingOff + 2 * kSlots * kTileBytes;
   // barrier slots
   static constexpr int kQFull = 0, kQEmpty = 2, kSFull = 4, kPFull = 6, kOFull = 8, kOEmpty = 10,
-                       kMmaDone = 12, kKvFull = 13, kKvEmpty = 13 + kStages;
-  static constexpr int kNumBars = 13 + 2 * kStages;
+                       kMmaDone = 12, kKvFull = 13, kKvEmpty = 13 + kSlots;
+  static constexpr int kNumBars = 13 + 2 * kSlots;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack for 1024-byte alignment
 };
@@ -150,9 +154,9 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, uint8_t* smem, 
                                              volatile int* abort_flag) {
   using L = FwdLayout<HD>;
   auto bar = [&](int i) { return smem_u32(bars + i); };
-  uint32_t kv_cnt = 0, qe_cnt[2] = {0, 0};
-  int last_kv[L::kStages];
-  for (int i = 0; i < L::kStages; ++i) last_kv[i] = -1;
+  uint32_t g_cnt = 0, qe_cnt[2] = {0, 0};
+  int last_g[L::kSlots];  // last group loaded into each slot, -1 if none
+  for (int i = 0; i < L::kSlots; ++i) last_g[i] = -1;
   int last_q[2] = {-1, -1};
   bool ok = true;
   for (int k = 0; ok; ++k) {
@@ -172,30 +176,39 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, uint8_t* smem, 
       last_q[s] = int(qe_cnt[s]);
       ++qe_cnt[s];
     }
+    if (!ok) break;
     const int hkv = pu.h / p.G;  // key/value head of this query head
+    // one ring slot: tile kb_a of map `ma` into its first buffer and, if
+    // kb_b >= 0, K tile kb_b into its second
+    auto load_group = [&](const CUtensorMap* ma, int kb_a, int kb_b) {
+      const int slot = int(g_cnt % L::kSlots);
+      if (!wait_bar(bar(L::kKvEmpty + slot), ((g_cnt / L::kSlots) & 1) ^ 1, abort_flag, p.status,
+                    3))
+        return false;
+      mbar_arrive_expect_tx(bar(L::kKvFull + slot), (kb_b >= 0 ? 2 : 1) * L::kTileBytes);
+      const uint32_t dst = smem_u32(smem + L::kRingOff + 2 * slot * L::kTileBytes);
+      load_tile<HD>(ma, dst, bar(L::kKvFull + slot), kb_a * kTile, hkv, pu.b);
+      if (kb_b >= 0)
+        load_tile<HD>(&p.tm_k, dst + L::kTileBytes, bar(L::kKvFull + slot), kb_b * kTile, hkv, pu.b);
+      last_g[slot] = int(g_cnt);
+      ++g_cnt;
+      return true;
+    };
     PairWalk w;
     walk_init(w, pu, p.list);
-    PairTile t;
-    while (ok && walk_next(w, p.list, t)) {
-      for (int kv = 0; kv < 2; ++kv) {  // K then V of the tile
-        const int stage = kv_cnt % L::kStages;
-        if (!wait_bar(bar(L::kKvEmpty + stage), ((kv_cnt / L::kStages) & 1) ^ 1, abort_flag,
-                      p.status, 3)) {
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(bar(L::kKvFull + stage), L::kTileBytes);
-        load_tile<HD>(kv ? &p.tm_v : &p.tm_k,
-                      smem_u32(smem + L::kRingOff + stage * L::kTileBytes),
-                      bar(L::kKvFull + stage), t.kb * kTile, hkv, pu.b);
-        last_kv[stage] = int(kv_cnt);
-        ++kv_cnt;
-      }
+    PairTile cur, nxt;
+    walk_next(w, p.list, cur);  // the union is non-empty
+    ok = load_group(&p.tm_k, cur.kb, -1);  // K of the first tile
+    while (ok) {
+      const bool more = walk_next(w, p.list, nxt);
+      ok = load_group(&p.tm_v, cur.kb, more ? nxt.kb : -1);  // V of cur, K of nxt
+      if (!more) break;
+      cur = nxt;
     }
   }
   if (!ok) {  // let copies already issued land before the CTA exits
-    for (int i = 0; i < L::kStages; ++i)
-      if (last_kv[i] >= 0) drain_bar(bar(L::kKvFull + i), (last_kv[i] / L::kStages) & 1);
+    for (int i = 0; i < L::kSlots; ++i)
+      if (last_g[i] >= 0) drain_bar(bar(L::kKvFull + i), (last_g[i] / L::kSlots) & 1);
     for (int s = 0; s < 2; ++s)
       if (last_q[s] >= 0) drain_bar(bar(L::kQFull + s), last_q[s] & 1);
   }
@@ -208,13 +221,19 @@ __device__ __forceinline__ void fwd_mma(const FwdParams& p, uint8_t* smem, uint6
   auto bar = [&](int i) { return smem_u32(bars + i); };
   constexpr uint32_t kIdQK = idesc_bf16_f32(128, 128, false, false);
   constexpr uint32_t kIdPV = idesc_bf16_f32(128, HD, false, true);
-  uint32_t kv_cnt = 0, qf_cnt[2] = {0, 0}, pf_cnt[2] = {0, 0}, oe_cnt[2] = {0, 0};
+  uint32_t g_cnt = 0, qf_cnt[2] = {0, 0}, pf_cnt[2] = {0, 0}, oe_cnt[2] = {0, 0};
   const uint32_t ring = smem_u32(smem + L::kRingOff);
+  // buffer h of the slot holding group g
+  auto buf = [&](uint32_t g, int h) { return ring + (2 * (g % L::kSlots) + h) * L::kTileBytes; };
+  auto wait_group = [&](uint32_t g, unsigned where) {
+    return wait_bar(bar(L::kKvFull + g % L::kSlots), (g / L::kSlots) & 1, abort_flag, p.status,
+                    where);
+  };
   bool ok = true;
-  // S_s = Q_s K^T for the K tile in ring stage `stage`
-  auto issue_qk = [&](int s, int stage) {
+  // S_s = Q_s K^T for the K tile at shared address kaddr
+  auto issue_qk = [&](int s, uint32_t kaddr) {
     const uint32_t qd = sdesc_lo(smem_u32(smem + L::kQOff + s * L::kTileBytes), 16);
-    const uint32_t kd = sdesc_lo(ring + stage * L::kTileBytes, 16);
+    const uint32_t kd = sdesc_lo(kaddr, 16);
 #pragma unroll
     for (int kk = 0; kk < HD / 16; ++kk) {
       // A = Q, B = K, both K-major: 16-element k-steps are 32 bytes apart
@@ -235,30 +254,27 @@ __device__ __forceinline__ void fwd_mma(const FwdParams& p, uint8_t* smem, uint6
     walk_init(w, pu, p.list);
     PairTile cur, nxt;
     walk_next(w, p.list, cur);  // the union is non-empty
-    // prologue: Q K^T of the first tile
+    // prologue: Q K^T of the first tile (the unit's first ring group: its K)
     {
-      const int ks = kv_cnt % L::kStages;
       for (int s = 0; s < 2 && ok; ++s)
         if (cur.in[s] && !wait_bar(bar(L::kQFull + s), qf_cnt[s] & 1, abort_flag, p.status, 13))
           ok = false;
-      if (ok && !wait_bar(bar(L::kKvFull + ks), (kv_cnt / L::kStages) & 1, abort_flag, p.status, 14))
-        ok = false;
+      if (ok && !wait_group(g_cnt, 14)) ok = false;
       if (!ok) break;
       tc_fence_after();
       for (int s = 0; s < 2; ++s) {
         if (!cur.in[s]) continue;
         ++qf_cnt[s];
-        issue_qk(s, ks);
+        issue_qk(s, buf(g_cnt, 0));
         if (++issued[s] == pu.n[s]) mma_commit(bar(L::kQEmpty + s));
       }
-      mma_commit(bar(L::kKvEmpty + ks));
-      ++kv_cnt;
+      mma_commit(bar(L::kKvEmpty + g_cnt % L::kSlots));
+      ++g_cnt;
     }
     while (ok) {
       const bool more = walk_next(w, p.list, nxt);
-      const int vs = kv_cnt % L::kStages;            // V of cur
-      const int ks = (kv_cnt + 1) % L::kStages;      // K of nxt
-      if (!wait_bar(bar(L::kKvFull + vs), (kv_cnt / L::kStages) & 1, abort_flag, p.status, 12)) {
+      // this step's group: V of cur (first buffer) and K of nxt (second)
+      if (!wait_group(g_cnt, 12)) {
         ok = false;
         break;
       }
@@ -267,11 +283,9 @@ __device__ __forceinline__ void fwd_mma(const FwdParams& p, uint8_t* smem, uint6
           if (nxt.in[s] && issued[s] == 0 &&
               !wait_bar(bar(L::kQFull + s), qf_cnt[s] & 1, abort_flag, p.status, 13))
             ok = false;
-        if (ok && !wait_bar(bar(L::kKvFull + ks), ((kv_cnt + 1) / L::kStages) & 1, abort_flag,
-                            p.status, 14))
-          ok = false;
         if (!ok) break;
       }
+      const uint32_t vaddr = buf(g_cnt, 0), kaddr = buf(g_cnt, 1);
       for (int s = 0; s < 2 && ok; ++s) {
         const uint32_t tS = tmem + uint32_t(s * 256);
         if (cur.in[s]) {  // O_s (+)= P_s V
@@ -290,7 +304,7 @@ __device__ __forceinline__ void fwd_mma(const FwdParams& p, uint8_t* smem, uint6
           tc_fence_after();
           // B = V tile, MN-major: 64-column chunks 16 KB apart, 8-row groups
           // 1 KB apart, 16 rows (2 KB) per k-step
-          const uint32_t vd = sdesc_lo(ring + vs * L::kTileBytes, kTile * 128);
+          const uint32_t vd = sdesc_lo(vaddr, kTile * 128);
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
             mma_ts(tS + 128, tS + kk * 8, vd + kk * (2048 >> 4), kIdPV,
@@ -301,18 +315,16 @@ __device__ __forceinline__ void fwd_mma(const FwdParams& p, uint8_t* smem, uint6
         if (more && nxt.in[s]) {
           if (issued[s] == 0) ++qf_cnt[s];
           tc_fence_after();
-          issue_qk(s, ks);
+          issue_qk(s, kaddr);
           if (++issued[s] == pu.n[s]) mma_commit(bar(L::kQEmpty + s));
         }
       }
       if (!ok) break;
-      mma_commit(bar(L::kKvEmpty + vs));
+      mma_commit(bar(L::kKvEmpty + g_cnt % L::kSlots));
+      ++g_cnt;
       if (!more) break;
-      mma_commit(bar(L::kKvEmpty + ks));
-      kv_cnt += 2;
       cur = nxt;
     }
-    kv_cnt += 1;  // the last V stage
   }
   // every MMA issued so far has finished before TMEM is released
   mma_commit(bar(L::kMmaDone));
@@ -324,7 +336,7 @@ __device__ __forceinline__ void fwd_mma_slot(const FwdParams& p, uint8_t* smem, 
                                              uint32_t tmem, int s, volatile int* abort_flag) {
   // MMA issuer of query slot s, used for lists from a block index: one
   // thread per slot, both walking the same union of key tiles (so both see
-  // the same ring stages) and both releasing every stage (kKvEmpty then
+  // the same ring groups) and both releasing every group (kKvEmpty then
   // counts two commits).  Where the two slots' lists differ, neither slot
   // waits for the other's softmax; with identical dense / causal lists the
   // single issuer (fwd_mma), whose order staggers the slots, is faster.
@@ -332,14 +344,22 @@ __device__ __forceinline__ void fwd_mma_slot(const FwdParams& p, uint8_t* smem, 
   auto bar = [&](int i) { return smem_u32(bars + i); };
   constexpr uint32_t kIdQK = idesc_bf16_f32(128, 128, false, false);
   constexpr uint32_t kIdPV = idesc_bf16_f32(128, HD, false, true);
-  uint32_t kv_cnt = 0, qf_cnt = 0, pf_cnt = 0, oe_cnt = 0;
+  uint32_t g_cnt = 0, qf_cnt = 0, pf_cnt = 0, oe_cnt = 0;
   const uint32_t ring = smem_u32(smem + L::kRingOff);
+  auto buf = [&](uint32_t g, int h) { return ring + (2 * (g % L::kSlots) + h) * L::kTileBytes; };
+  // both threads wait for every group they release, used or not: a thread
+  // that skipped the wait could release a later use of the slot before the
+  // other thread released this one (arrivals are not tagged)
+  auto wait_group = [&](uint32_t g, unsigned where) {
+    return wait_bar(bar(L::kKvFull + g % L::kSlots), (g / L::kSlots) & 1, abort_flag, p.status,
+                    where);
+  };
   const uint32_t tS = tmem + uint32_t(s * 256);
   const uint32_t qd = sdesc_lo(smem_u32(smem + L::kQOff + s * L::kTileBytes), 16);
   bool ok = true;
-  // S_s = Q_s K^T for the K tile in ring stage `stage`
-  auto issue_qk = [&](int stage) {
-    const uint32_t kd = sdesc_lo(ring + stage * L::kTileBytes, 16);
+  // S_s = Q_s K^T for the K tile at shared address kaddr
+  auto issue_qk = [&](uint32_t kaddr) {
+    const uint32_t kd = sdesc_lo(kaddr, 16);
 #pragma unroll
     for (int kk = 0; kk < HD / 16; ++kk) {
       // A = Q, B = K, both K-major: 16-element k-steps are 32 bytes apart
@@ -360,31 +380,24 @@ __device__ __forceinline__ void fwd_mma_slot(const FwdParams& p, uint8_t* smem, 
     walk_init(w, pu, p.list);
     PairTile cur, nxt;
     walk_next(w, p.list, cur);  // the union is non-empty
-    // prologue: Q K^T of the first tile
+    // prologue: Q K^T of the first tile (the unit's first ring group: its K)
     {
-      const int ks = kv_cnt % L::kStages;
       if (cur.in[s] && !wait_bar(bar(L::kQFull + s), qf_cnt & 1, abort_flag, p.status, 13))
         ok = false;
-      if (ok && !wait_bar(bar(L::kKvFull + ks), (kv_cnt / L::kStages) & 1, abort_flag, p.status, 14))
-        ok = false;
+      if (ok && !wait_group(g_cnt, 14)) ok = false;
       if (!ok) break;
       tc_fence_after();
       if (cur.in[s]) {
         ++qf_cnt;
-        issue_qk(ks);
+        issue_qk(buf(g_cnt, 0));
         if (++issued == pu.n[s]) mma_commit(bar(L::kQEmpty + s));
       }
-      mma_commit(bar(L::kKvEmpty + ks));
-      ++kv_cnt;
+      mma_commit(bar(L::kKvEmpty + g_cnt % L::kSlots));
+      ++g_cnt;
     }
     while (ok) {
       const bool more = walk_next(w, p.list, nxt);
-      const int vs = kv_cnt % L::kStages;        // V of cur
-      const int ks = (kv_cnt + 1) % L::kStages;  // K of nxt
-      // both threads wait for every stage they release, used or not: a
-      // thread that skipped the wait could release a later use of the stage
-      // before the other thread released this one (arrivals are not tagged)
-      if (!wait_bar(bar(L::kKvFull + vs), (kv_cnt / L::kStages) & 1, abort_flag, p.status, 12)) {
+      if (!wait_group(g_cnt, 12)) {  // V of cur, K of nxt
         ok = false;
         break;
       }
@@ -404,7 +417,7 @@ __device__ __forceinline__ void fwd_mma_slot(const FwdParams& p, uint8_t* smem, 
         tc_fence_after();
         // B = V tile, MN-major: 64-column chunks 16 KB apart, 8-row groups
         // 1 KB apart, 16 rows (2 KB) per k-step
-        const uint32_t vd = sdesc_lo(ring + vs * L::kTileBytes, kTile * 128);
+        const uint32_t vd = sdesc_lo(buf(g_cnt, 0), kTile * 128);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
           mma_ts(tS + 128, tS + kk * 8, vd + kk * (2048 >> 4), kIdPV,
@@ -412,28 +425,21 @@ __device__ __forceinline__ void fwd_mma_slot(const FwdParams& p, uint8_t* smem, 
         ++seen;
         if (seen == pu.n[s]) mma_commit(bar(L::kOFull + s));
       }
-      mma_commit(bar(L::kKvEmpty + vs));
-      if (!more) break;
-      if (!wait_bar(bar(L::kKvFull + ks), ((kv_cnt + 1) / L::kStages) & 1, abort_flag, p.status,
-                    14)) {
-        ok = false;
-        break;
-      }
-      if (nxt.in[s]) {
+      if (more && nxt.in[s]) {
         if (issued == 0 && !wait_bar(bar(L::kQFull + s), qf_cnt & 1, abort_flag, p.status, 13)) {
           ok = false;
           break;
         }
         if (issued == 0) ++qf_cnt;
         tc_fence_after();
-        issue_qk(ks);
+        issue_qk(buf(g_cnt, 1));
         if (++issued == pu.n[s]) mma_commit(bar(L::kQEmpty + s));
       }
-      mma_commit(bar(L::kKvEmpty + ks));
-      kv_cnt += 2;
+      mma_commit(bar(L::kKvEmpty + g_cnt % L::kSlots));
+      ++g_cnt;
+      if (!more) break;
       cur = nxt;
     }
-    kv_cnt += 1;  // the last V stage
   }
   // every MMA issued so far has finished before TMEM is released
   mma_commit(bar(L::kMmaDone));
@@ -625,7 +631,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     }
     const uint32_t issuers = p.list.ptr ? 2 : 1;  // MMA threads (see fwd_mma_slot)
     mbar_init(smem_u32(bars + L::kMmaDone), issuers);
-    for (int i = 0; i < L::kStages; ++i) {
+    for (int i = 0; i < L::kSlots; ++i) {
       mbar_init(smem_u32(bars + L::kKvFull + i), 1);
       mbar_init(smem_u32(bars + L::kKvEmpty + i), issuers);
     }
