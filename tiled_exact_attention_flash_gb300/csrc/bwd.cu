@@ -142,7 +142,8 @@ __device__ __forceinline__ void load_tile_2d(const CUtensorMap* m, uint32_t dst,
 // share the key/value head; dQ pass (b, query head, query block).
 template <bool kKeyStationary>
 __device__ __forceinline__ Unit bwd_decode(int u, const BwdParams& p) {
-  Unit un = decode_unit(u, kKeyStationary ? p.Hkv : p.H, p.list, p.status);
+  const int H = kKeyStationary ? p.Hkv : p.H;
+  Unit un = decode_unit(u, p.B * H, H, p.list, p.status);
   if (kKeyStationary) un.n = un.n0 * p.G;
   return un;
 }

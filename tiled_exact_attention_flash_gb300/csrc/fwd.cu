@@ -66,8 +66,9 @@ constexpr int kFwdThreads = 384;
 // blocks whose key-tile lists nearly coincide).  Slot 0 takes rank 2r, slot
 // 1 rank 2r + 1.  The producer loads each key/value tile of the UNION of the
 // two lists once; the MMA issuer runs Q K^T and P V for whichever slots the
-// tile belongs to.  Pair units are spread over the CTAs round-robin:
-// unit k of CTA c is u = c + k * gridDim.x.
+// tile belongs to.  Pair units are numbered rank-major (unit_order: pair r
+// of every (b, h) before pair r + 1), so the launch runs its longest units
+// first; unit k of CTA c is u = c + k * gridDim.x.
 struct PairUnit {
   int b, h;
   int q[2];       // query block per slot (q[1] < 0: no second block)
@@ -76,9 +77,8 @@ struct PairUnit {
 
 __device__ __forceinline__ PairUnit decode_pair(int u, const FwdParams& p) {
   const ListParams& L = p.list;
-  const int npb = (L.n_blocks + 1) >> 1;
-  const int bh = u / npb;
-  const int r = u - bh * npb;
+  int bh, r;
+  unit_order(u, p.B * p.H, bh, r);
   PairUnit pu;
   pu.b = bh / p.H;
   pu.h = bh - pu.b * p.H;
@@ -89,7 +89,7 @@ __device__ __forceinline__ PairUnit decode_pair(int u, const FwdParams& p) {
     pu.n[s] = 0;
     if (rank >= L.n_blocks) continue;
     // reuse the single-unit decoder for the block id and its list bounds
-    const Unit un = decode_unit(bh * L.n_blocks + rank, p.H, L, p.status);
+    const Unit un = decode_unit_at(bh, rank, p.H, L, p.status);
     pu.q[s] = un.ob;
     pu.beg[s] = un.begin;
     pu.n[s] = un.n;
