@@ -192,7 +192,8 @@ flash_msa_status flash_msa_check_block_index(const flash_msa_block_index* host_i
 
 /* Forward: o = attention(q, k, v), lse[b,h,i] = log sum_j exp(scale q_i.k_j)
  * over live j (natural log; -inf and o_i = 0 for a row with no live key).
- * One kernel launch on `stream` (one CTA per pair of query blocks). */
+ * One kernel launch on `stream` (one CTA per SM, each working through pairs
+ * of query blocks). */
 flash_msa_status flash_msa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                                int B, int H, int64_t N, int d, float scale,
                                const flash_msa_mask_desc* mask, void* stream);

@@ -6,7 +6,7 @@
 // from "How Does Flash-MSA Sparse Attention Work", section "How Flash-MSA
 // Sparse Attention Works").
 //
-// CTA layout (384 threads, one CTA resident per SM, one CTA per pair unit):
+// CTA layout (384 threads, one CTA per SM, each working through pair units):
 //   warp 0      TMA producer: Q tiles and the K/V ring, one elected lane
 //   warp 1      MMA issuer: tcgen05.mma for S = Q K^T and O += P V, one lane
 //               (with an index: slot 0 only, warp 3 issuing for slot 1)
@@ -68,12 +68,20 @@ constexpr int kFwdThreads = 384;
 // two lists once; the MMA issuer runs Q K^T and P V for whichever slots the
 // tile belongs to.  Pair units are numbered rank-major (unit_order: pair r
 // of every (b, h) before pair r + 1), so the launch runs its longest units
-// first; unit k of CTA c is u = c + k * gridDim.x.
+// first; each CTA takes its units in the order of fwd_unit.
 struct PairUnit {
   int b, h;
   int q[2];       // query block per slot (q[1] < 0: no second block)
   int beg[2], n[2];
 };
+
+// Unit k of this CTA.  One CTA per SM; units are dealt serpentine-wise (CTA c
+// takes c, then 2G - 1 - c, then 2G + c, ...), which evens out the CTAs'
+// shares of the rank-major (longest first) unit lengths.
+__device__ __forceinline__ int fwd_unit(int k) {
+  const int c = int(blockIdx.x), g = int(gridDim.x);
+  return k * g + ((k & 1) ? g - 1 - c : c);
+}
 
 __device__ __forceinline__ PairUnit decode_pair(int u, const FwdParams& p) {
   const ListParams& L = p.list;
@@ -160,7 +168,7 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, uint8_t* smem, 
   int last_q[2] = {-1, -1};
   bool ok = true;
   for (int k = 0; ok; ++k) {
-    const int u = int(blockIdx.x) + k * int(gridDim.x);
+    const int u = fwd_unit(k);
     if (u >= p.n_units) break;
     const PairUnit pu = decode_pair(u, p);
     if (pu.n[0] + pu.n[1] == 0) continue;
@@ -244,7 +252,7 @@ __device__ __forceinline__ void fwd_mma(const FwdParams& p, uint8_t* smem, uint6
     mma_commit(bar(L::kSFull + s));
   };
   for (int k = 0; ok; ++k) {
-    const int u = int(blockIdx.x) + k * int(gridDim.x);
+    const int u = fwd_unit(k);
     if (u >= p.n_units) break;
     const PairUnit pu = decode_pair(u, p);
     if (pu.n[0] + pu.n[1] == 0) continue;
@@ -370,7 +378,7 @@ __device__ __forceinline__ void fwd_mma_slot(const FwdParams& p, uint8_t* smem, 
     mma_commit(bar(L::kSFull + s));
   };
   for (int k = 0; ok; ++k) {
-    const int u = int(blockIdx.x) + k * int(gridDim.x);
+    const int u = fwd_unit(k);
     if (u >= p.n_units) break;
     const PairUnit pu = decode_pair(u, p);
     if (pu.n[0] + pu.n[1] == 0) continue;
@@ -459,7 +467,7 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint64_t* bars, 
   const float sl2 = p.scale_log2;
   uint32_t sf_cnt = 0, of_cnt = 0;
   for (int k = 0;; ++k) {
-    const int u = int(blockIdx.x) + k * int(gridDim.x);
+    const int u = fwd_unit(k);
     if (u >= p.n_units) break;
     const PairUnit pu = decode_pair(u, p);
     if (pu.q[slot] < 0) continue;
@@ -703,6 +711,8 @@ static flash_msa_status launch_fwd_hd(const FwdLaunch& a, cudaStream_t stream) {
     attr_set[HD == 128] = true;
   }
   int grid = p.n_units;
+  const int sms = sm_count();
+  if (sms > 0 && grid > sms) grid = sms;  // persistent: one CTA per SM
   if (a.max_ctas > 0 && grid > a.max_ctas) grid = a.max_ctas;
   fwd_kernel<HD><<<grid, kFwdThreads, L::kSmemBytes, stream>>>(p);
   if (cudaGetLastError() != cudaSuccess) return set_cuda_error("fwd kernel launch");
