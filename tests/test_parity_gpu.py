@@ -194,3 +194,20 @@ def test_varlen_equals_separate_sequences(d, causal, lens):
             gc.check_lse(got["lse"][h, sl], l_ref)
             for name, ref in zip(("dq", "dk", "dv"), g_ref):
                 gc.check_grad(got[name][sl, h], ref, name)
+
+
+@pytest.mark.parametrize("mname", ["causal", "window_global"])
+def test_many_units_per_cta(mname):
+    """More work units than SMs, so the persistent kernels (one CTA per SM)
+    take several units each, dealt in rank-major order: B=2, H=96, N=300 gives
+    384 forward pair units and 576 units per backward kernel.  Sampled heads
+    spread over the unit order are compared element by element; every head
+    must have been computed."""
+    fields = SMALL_MASKS[mname]
+    inp = small_inputs(2, 300, 96, 128, seed=4242)
+    res = gc.run_gpu(inp, fields)
+    heads = [(b, h) for b in range(2) for h in range(96) if (b * 96 + h) % 11 == 0] + [(1, 95)]
+    gc.full_compare(inp, fields, res, heads=heads)
+    for name in ("o", "dq", "dk", "dv"):
+        per_head = np.abs(res[name]).max(axis=(1, 3))  # (B, N, H, d) -> (B, H)
+        assert (per_head > 0).all(), name
