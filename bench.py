@@ -164,7 +164,7 @@ def oracle_heads_for(w, budget_s=15.0):
     per_head_s = {1: 0.01, 2: 3.5, 3: 20.0, 4: 20.0, 5: 30.0}.get(w.cid, 10.0)
     cores = os.cpu_count() or 1
     n = max(1, min(w.B * w.H, int(budget_s * cores / per_head_s)))
-    return min(n, cores * 2, w.B * w.H)
+    return min(n, cores * 4, w.B * w.H)
 
 
 # ---------------------------------------------------------------------------
