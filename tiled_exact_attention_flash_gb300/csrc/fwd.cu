@@ -713,7 +713,6 @@ static flash_msa_status launch_fwd_hd(const FwdLaunch& a, cudaStream_t stream) {
   int grid = p.n_units;
   const int sms = sm_count();
   if (sms > 0 && grid > sms) grid = sms;  // persistent: one CTA per SM
-  if (a.max_ctas > 0 && grid > a.max_ctas) grid = a.max_ctas;
   fwd_kernel<HD><<<grid, kFwdThreads, L::kSmemBytes, stream>>>(p);
   if (cudaGetLastError() != cudaSuccess) return set_cuda_error("fwd kernel launch");
   return FLASH_MSA_OK;

@@ -38,7 +38,6 @@ struct FwdLaunch {
   MaskParams mask;
   ListParams list;  // CSR by query block (or arithmetic)
   unsigned* status;
-  int max_ctas;     // 0: one CTA per SM (at most one per pair unit)
 };
 flash_msa_status launch_fwd(const FwdLaunch& a, cudaStream_t stream);
 
