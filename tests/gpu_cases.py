@@ -19,17 +19,18 @@ GRAD_REL_TOL = 3e-2
 GRAD_ABS_FLOOR = 1e-4
 
 
-def run_gpu(inp: dict, fields: dict, device="cuda", backward=True):
+def run_gpu(inp: dict, fields: dict, device="cuda", backward=True, scale=None):
+    """scale: softmax scale passed to the library (None: its default d^-1/2)."""
     mask = api.Mask(**fields) if fields else None
     N = inp["q"].shape[1]
     index = None
     if mask is not None and mask.needs_index:
         index = api.build_block_index(mask, N).to(device)
     q, k, v, do = (inp[n].to(device) for n in ("q", "k", "v", "do"))
-    o, lse = api.fwd(q, k, v, mask=mask, index=index)
+    o, lse = api.fwd(q, k, v, mask=mask, index=index, scale=scale)
     out = {"o": o, "lse": lse}
     if backward:
-        dq, dk, dv = api.bwd(q, k, v, o, lse, do, mask=mask, index=index)
+        dq, dk, dv = api.bwd(q, k, v, o, lse, do, mask=mask, index=index, scale=scale)
         out.update(dq=dq, dk=dk, dv=dv)
     st = api.get_status()
     assert st == api.OK, f"device status {st}"
@@ -72,11 +73,11 @@ def check_grad(got, ref, name):
     assert err <= tol, f"{name} max err {err} vs max(3e-2 x {scale}, {GRAD_ABS_FLOOR})"
 
 
-def full_compare(inp, fields, res, heads=None, backward=True):
+def full_compare(inp, fields, res, heads=None, backward=True, scale=None):
     """Element-by-element comparison for every (or the given) head."""
     B, N, H, d = inp["q"].shape
     spec = MaskSpec(**fields)
-    scale = d ** -0.5
+    scale = d ** -0.5 if scale is None else scale
     heads = [(b, h) for b in range(B) for h in range(H)] if heads is None else heads
     for b, h in heads:
         q, k, v, do = (head(inp[n], b, h) for n in ("q", "k", "v", "do"))

@@ -211,3 +211,17 @@ def test_many_units_per_cta(mname):
     for name in ("o", "dq", "dk", "dv"):
         per_head = np.abs(res[name]).max(axis=(1, 3))  # (B, N, H, d) -> (B, H)
         assert (per_head > 0).all(), name
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("scale", [0.05, 0.3])
+@pytest.mark.parametrize("mname", ["dense", "causal", "window_dilated"])
+def test_custom_scale(d, scale, mname):
+    """A softmax scale other than d^-1/2 reaches every step that uses it: the
+    forward's exponent and LSE, and the backward's dQ = scale dS K and
+    dK = scale dS^T Q (a backward that kept the default would be off by the
+    ratio of the two scales)."""
+    fields = SMALL_MASKS[mname]
+    inp = small_inputs(1, 300, 2, d, seed=900 + d)
+    res = gc.run_gpu(inp, fields, scale=scale)
+    gc.full_compare(inp, fields, res, scale=scale)
