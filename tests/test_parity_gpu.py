@@ -225,3 +225,38 @@ def test_custom_scale(d, scale, mname):
     inp = small_inputs(1, 300, 2, d, seed=900 + d)
     res = gc.run_gpu(inp, fields, scale=scale)
     gc.full_compare(inp, fields, res, scale=scale)
+
+
+@pytest.mark.parametrize("order", ["dkdv_first", "dq_first"])
+@pytest.mark.parametrize("mname", ["causal", "window_strided"])
+def test_bwd_stages_match_full_backward(order, mname):
+    """flash_msa_bwd_stages: the preprocessing stage, then dK/dV and dQ in
+    either order on one workspace, gives bit-for-bit the gradients of
+    flash_msa_bwd; a stage leaves the other stage's outputs untouched."""
+    fields = SMALL_MASKS[mname]
+    inp = small_inputs(2, 517, 3, 128, seed=31)
+    mask = api.Mask(**fields)
+    N = inp["q"].shape[1]
+    index = api.build_block_index(mask, N).to("cuda") if mask.needs_index else None
+    q, k, v, do = (inp[n].to("cuda") for n in ("q", "k", "v", "do"))
+    o, lse = api.fwd(q, k, v, mask=mask, index=index)
+    dq, dk, dv = api.bwd(q, k, v, o, lse, do, mask=mask, index=index)
+    B, _, H, d = q.shape
+    ws = torch.empty(api.bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device="cuda")
+    sentinel = torch.tensor(7.0, dtype=torch.bfloat16)
+    sq, sk, sv = (torch.full_like(t, 7.0) for t in (dq, dk, dv))
+    api.bwd(q, k, v, o, lse, do, mask=mask, index=index, dq=sq, dk=sk, dv=sv, workspace=ws,
+            stages=api.BWD_PREPROCESS)
+    first, second = ((api.BWD_DKDV, api.BWD_DQ) if order == "dkdv_first"
+                     else (api.BWD_DQ, api.BWD_DKDV))
+    api.bwd(q, k, v, o, lse, do, mask=mask, index=index, dq=sq, dk=sk, dv=sv, workspace=ws,
+            stages=first)
+    torch.cuda.synchronize()
+    untouched = (sq,) if first == api.BWD_DKDV else (sk, sv)
+    for t in untouched:
+        assert bool((t.cpu() == sentinel).all())
+    api.bwd(q, k, v, o, lse, do, mask=mask, index=index, dq=sq, dk=sk, dv=sv, workspace=ws,
+            stages=second)
+    assert api.get_status() == api.OK
+    for a, b in ((sq, dq), (sk, dk), (sv, dv)):
+        assert torch.equal(a, b)
