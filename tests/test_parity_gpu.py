@@ -260,3 +260,31 @@ def test_bwd_stages_match_full_backward(order, mname):
     assert api.get_status() == api.OK
     for a, b in ((sq, dq), (sk, dk), (sv, dv)):
         assert torch.equal(a, b)
+
+
+def test_side_streams_match_default_stream():
+    """The calls run on the caller's current stream: forward and backward
+    issued on two side streams at once (each with its own work counters)
+    give bit-for-bit the results of the default stream."""
+    fields = {"causal": True, "window": 300, "dilation": 2, "dilation_near": 1}
+    inp = small_inputs(2, 517, 3, 128, seed=77)
+    mask = api.Mask(**fields)
+    N = inp["q"].shape[1]
+    index = api.build_block_index(mask, N).to("cuda")
+    dev = {n: inp[n].to("cuda") for n in ("q", "k", "v", "do")}
+    o, lse = api.fwd(dev["q"], dev["k"], dev["v"], mask=mask, index=index)
+    ref = (o, lse) + api.bwd(dev["q"], dev["k"], dev["v"], o, lse, dev["do"], mask=mask, index=index)
+    torch.cuda.synchronize()
+    outs = []
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            so, slse = api.fwd(dev["q"], dev["k"], dev["v"], mask=mask, index=index)
+            outs.append((so, slse) + api.bwd(dev["q"], dev["k"], dev["v"], so, slse, dev["do"],
+                                              mask=mask, index=index))
+    torch.cuda.synchronize()
+    assert api.get_status() == api.OK
+    for got in outs:
+        for a, b in zip(got, ref):
+            assert torch.equal(a, b)
