@@ -138,6 +138,7 @@ typedef struct flash_msa_block_index {
   int32_t* bit_slot_t; /* [nnz] */
   uint32_t* bits;      /* [512 n_bit_tiles] */
   uint32_t* bits_t;    /* [512 n_bit_tiles] */
+  int64_t live_elements; /* live (i, j) pairs of the mask over N x N; set by both build calls */
 } flash_msa_block_index;
 
 /* Mask description (host memory).  A NULL mask, or flags == 0, is dense

@@ -164,3 +164,36 @@ def test_documents_require_valid_offsets():
         hdr = api.BlockIndexStruct()
         assert api.lib().flash_msa_build_block_index(ctypes.byref(desc), 300, ctypes.byref(hdr)) == \
             api.ERR_INVALID_ARG, starts
+
+
+def _oracle_live_count(n, fields):
+    from oracle.mask import MaskSpec, live_matrix
+    idx = np.arange(n)
+    return int(live_matrix(idx, idx, n, MaskSpec(**fields)).sum())
+
+
+@pytest.mark.parametrize("n", [1, 129, 517, 1000])
+@pytest.mark.parametrize("mi", range(len(MASKS)))
+def test_live_element_counts_match_the_mask(n, mi):
+    """live_elements (both build calls) equals the number of live (i, j)
+    pairs of the mask's definition."""
+    import ctypes
+    fields = MASKS[mi]
+    got = api.build_block_index(api.Mask(**fields), n)
+    want = _oracle_live_count(n, fields)
+    assert got.live_elements == want
+    hdr = api.BlockIndexStruct()  # the counting call alone
+    assert api.lib().flash_msa_build_block_index(ctypes.byref(api.Mask(**fields).desc()), n,
+                                                 ctypes.byref(hdr)) == api.OK
+    assert hdr.live_elements == want
+
+
+@pytest.mark.parametrize("n,fields,seed", [
+    (519, {"causal": True}, 2), (700, {"window": 130, "stride": 2, "stride_phase": 1}, 4)])
+def test_live_element_counts_with_bits(n, fields, seed):
+    from tiled_exact_attention_flash_gb300.inputs import document_lengths, pack_bitmask
+    live = np.random.default_rng(seed).random((n, n)) < 0.7
+    for extra in ({"bitmask": pack_bitmask(live)},
+                  {"doc_starts": tuple(int(x) for x in np.cumsum([0] + document_lengths(n, seed, 90)))}):
+        f = dict(fields, **extra)
+        assert api.build_block_index(api.Mask(**f), n).live_elements == _oracle_live_count(n, f)

@@ -63,6 +63,7 @@ class BlockIndexStruct(ctypes.Structure):
         ("bit_slot_t", ctypes.c_void_p),
         ("bits", ctypes.c_void_p),
         ("bits_t", ctypes.c_void_p),
+        ("live_elements", ctypes.c_int64),
     ]
 
 
@@ -216,10 +217,16 @@ class BlockIndex:
     def nnz(self) -> int:
         return int(self.header.nnz)
 
+    @property
+    def live_elements(self) -> int:
+        """Live (i, j) pairs of the mask over the N x N score matrix."""
+        return int(self.header.live_elements)
+
     def host_struct(self) -> BlockIndexStruct:
         s = BlockIndexStruct(self.header.seq_len, self.header.n_q_blocks, self.header.n_k_blocks,
                              self.header.block, self.header.nnz)
         s.n_bit_tiles = self.header.n_bit_tiles
+        s.live_elements = self.header.live_elements
         for name, _, _ in _INDEX_ARRAYS:
             setattr(s, name, self.host[name].ctypes.data)
         return s
@@ -231,6 +238,7 @@ class BlockIndex:
         s = BlockIndexStruct(self.header.seq_len, self.header.n_q_blocks, self.header.n_k_blocks,
                              self.header.block, self.header.nnz)
         s.n_bit_tiles = self.header.n_bit_tiles
+        s.live_elements = self.header.live_elements
         for name, _, _ in _INDEX_ARRAYS:
             t = self.device[name]
             setattr(s, name, t.data_ptr())

@@ -241,7 +241,7 @@ flash_msa_status flash_msa_build_block_index(const flash_msa_mask_desc* mask, in
   // mask parts AND the row's 128 mask bits.  Returns -1 dead, 0 full,
   // 1 partial; `cut` tells whether the bits removed an entry of the interval
   // (the tile then carries its live entries, written to tb when non-null).
-  auto bit_class = [&](int qb, int kb, int c, bool& cut, uint32_t* tb) -> int {
+  auto bit_class = [&](int qb, int kb, int c, bool& cut, uint32_t* tb, int64_t* live_out) -> int {
     cut = false;
     if (!with_bits) return c;
     const DeltaRange r = tile_delta_range(qb, kb, mp);
@@ -275,9 +275,29 @@ flash_msa_status flash_msa_build_block_index(const flash_msa_mask_desc* mask, in
         if (tb) tb[row * 4 + w] = f;
       }
     }
+    if (live_out) *live_out = live;
     if (live == 0) return -1;
     if (c == 0 && !cut) return 0;
     return 1;
+  };
+  // live (i, j) pairs of a live tile of class k: every valid entry of a full
+  // tile, one interval of columns per row of a partial tile (the kernels'
+  // row_live_range), the set bits when the mask has bits
+  auto tile_live = [&](int qb, int kb, int k, int64_t bits_live) -> int64_t {
+    if (with_bits) return bits_live;
+    const int64_t i0 = int64_t(qb) * kTile, j0 = int64_t(kb) * kTile;
+    const int64_t rows = std::min<int64_t>(kTile, N - i0), cols = std::min<int64_t>(kTile, N - j0);
+    if (k == 0) return rows * cols;
+    const DeltaRange r = tile_delta_range(qb, kb, mp);
+    if (r.none) return 0;
+    int64_t live = 0;
+    for (int64_t row = 0; row < rows; ++row) {
+      const int64_t i = i0 + row;
+      const int64_t clo = std::max<int64_t>(i - r.hi - j0, 0);
+      const int64_t chi = std::min<int64_t>({i - r.lo - j0, N - 1 - j0, int64_t(kTile - 1)});
+      if (chi >= clo) live += chi - clo + 1;
+    }
+    return live;
   };
   // candidate key blocks per query block: causal and a plain window bound the
   // span; with global tokens the global key blocks come first, and a global
@@ -306,14 +326,17 @@ flash_msa_status flash_msa_build_block_index(const flash_msa_mask_desc* mask, in
   out->block = kTile;
   out->n_q_blocks = out->n_k_blocks = int32_t(nb);
   if (!out->row_ptr) {
-    int64_t nnz = 0, n_bits = 0;
+    int64_t nnz = 0, n_bits = 0, live = 0;
     for_each_tile([&](int qb, int kb, int c) {
       bool cut;
-      const int k = bit_class(qb, kb, c, cut, nullptr);
+      int64_t bl = 0;
+      const int k = bit_class(qb, kb, c, cut, nullptr, &bl);
       if (k < 0) return;
       ++nnz;
+      live += tile_live(qb, kb, k, bl);
       if (k == 1 && cut) ++n_bits;
     });
+    out->live_elements = live;
     if (nnz > INT32_MAX)
       return set_error(FLASH_MSA_ERR_INVALID_ARG, "build_block_index: more than 2^31 live tiles");
     out->nnz = nnz;
@@ -329,13 +352,15 @@ flash_msa_status flash_msa_build_block_index(const flash_msa_mask_desc* mask, in
   // CSR
   std::vector<int32_t> col_count(size_t(nb), 0);
   std::vector<uint32_t> tb(size_t(kTile) * 4);
-  int64_t pos = 0, slot = 0;
+  int64_t pos = 0, slot = 0, live = 0;
   int64_t cur = 0;
   out->row_ptr[0] = 0;
   for_each_tile([&](int qb, int kb, int c) {
     bool cut;
-    const int k = bit_class(qb, kb, c, cut, tb.data());
+    int64_t bl = 0;
+    const int k = bit_class(qb, kb, c, cut, tb.data(), &bl);
     if (k < 0) return;
+    live += tile_live(qb, kb, k, bl);
     while (cur < qb) out->row_ptr[++cur] = int32_t(pos);
     if (pos < out->nnz) {
       out->col_idx[pos] = kb;
@@ -368,6 +393,7 @@ flash_msa_status flash_msa_build_block_index(const flash_msa_mask_desc* mask, in
                      static_cast<long long>(out->nnz), static_cast<long long>(out->n_bit_tiles),
                      static_cast<long long>(pos), static_cast<long long>(slot));
   if (!with_bits) out->n_bit_tiles = 0;
+  out->live_elements = live;
   // CSC by counting sort: query blocks come out ascending within each column
   out->col_ptr[0] = 0;
   for (int64_t kb = 0; kb < nb; ++kb) out->col_ptr[kb + 1] = out->col_ptr[kb] + col_count[size_t(kb)];
