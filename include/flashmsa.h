@@ -173,7 +173,9 @@ typedef struct {
 
 /* Build the block index for `mask` and sequence length N on the HOST (no GPU
  * work).  Two phases: call with out->row_ptr == NULL to fill only the counts
- * (seq_len, n_q_blocks, n_k_blocks, block, nnz, n_bit_tiles); allocate every
+ * (seq_len, n_q_blocks, n_k_blocks, block, nnz, n_bit_tiles, and
+ * live_elements, the mask's live (i, j) pairs, set again by the second call);
+ * allocate every
  * array with those sizes (row_ptr/col_ptr n+1 int32, col_idx/row_idx nnz
  * int32, kind/kind_t nnz uint8, q_order/k_order n int32; with BITMASK also
  * bit_slot/bit_slot_t nnz int32 and bits/bits_t 512 n_bit_tiles uint32) and
