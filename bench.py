@@ -6,8 +6,12 @@ One step = the whole hot path over one batch of synthetic input: the forward
 kernel (O, LSE) and the three backward launches (D, dK/dV, dQ), called through
 the C-ABI library.  FLOPs are counted on live 128 x 128 tiles only:
 fwd = B * H * nnz * 4 * 128 * 128 * d, bwd = 2.5 x fwd (five products per
-tile), step = 3.5 x fwd.  The default workload is B=4, H=16, N=4096, d=128,
-causal; ``--config`` picks another of the five workloads.
+tile), step = 3.5 x fwd.  The default workload is B=1, H=32, N=16384,
+d=128, causal (a 7B-style layer at long context); ``--config`` picks another
+workload.  After the headline, ``sparse_scaling`` times the two block-sparse
+workloads (causal window 1024 + strided, N=32768; causal window 4096 +
+dilation, N=131072) for a few GPU-only steps each and reports their time per
+live tile against the headline's.
 
 Timing: W untimed warm-up steps, then K steps bracketed by a barrier and
 cuda synchronize, CUDA events on the launching stream, max over ranks.  The
@@ -47,12 +51,13 @@ TILE = 128
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--config", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-sparse-scaling", action="store_true")
     return ap.parse_args()
 
 
@@ -238,11 +243,95 @@ def traffic_per_launch(kernel, workload_name):
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
+# The backward's launches, each timed on its own: (name, stage bits, the
+# tensor-core FLOPs it issues per live tile in units of the forward's 4 x
+# 128 x 128 x d, for the per-kernel roofline).
+BWD_LAUNCHES = (("bwd_pre", "BWD_PREPROCESS", 0.0),
+                ("bwd_dkdv", "BWD_DKDV", 2.0),
+                ("bwd_dq", "BWD_DQ", 1.5))
+
+
+class Problem:
+    """One workload resident on the device: inputs, outputs, workspace, mask
+    and index, and its live-tile FLOP counts."""
+
+    def __init__(self, w, dev, api, host=None):
+        import torch
+        from tiled_exact_attention_flash_gb300.inputs import workload_inputs
+        self.w = w
+        fields = w.mask_fields()
+        self.mask = api.Mask(**fields) if fields else None
+        self.index = None
+        if self.mask is not None and self.mask.needs_index:
+            self.index = api.build_block_index(self.mask, w.N).to(dev)
+            self.nnz = self.index.nnz
+        else:
+            nb = (w.N + TILE - 1) // TILE
+            self.nnz = nb * (nb + 1) // 2 if (self.mask and self.mask.causal) else nb * nb
+        self.fwd_flops, self.bwd_flops = live_flops(w, self.nnz)
+        self.step_flops = self.fwd_flops + self.bwd_flops
+        self.host = workload_inputs(w) if host is None else host
+        self.q, self.k, self.v, self.do = (self.host[n].to(dev) for n in ("q", "k", "v", "do"))
+        B, N, H, d = self.q.shape
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        self.dq, self.dk, self.dv = (torch.empty_like(self.q) for _ in range(3))
+        self.ws = torch.empty(api.bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
+
+    def step(self, api, stream, ev=None):
+        """fwd, then the backward's launches one by one; ev: events recorded
+        before the forward and after every launch."""
+        if ev is not None:
+            ev[0].record(stream)
+        api.fwd(self.q, self.k, self.v, mask=self.mask, index=self.index, out=self.o,
+                lse=self.lse, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        for i, (_, bits, _) in enumerate(BWD_LAUNCHES):
+            api.bwd(self.q, self.k, self.v, self.o, self.lse, self.do, mask=self.mask,
+                    index=self.index, dq=self.dq, dk=self.dk, dv=self.dv, workspace=self.ws,
+                    stream=stream, stages=getattr(api, bits))
+            if ev is not None:
+                ev[2 + i].record(stream)
+
+
+def sparse_scaling(api, dev, stream, ms_per_tile_ref, ref_name, steps=5, warmup=2):
+    """GPU-only fwd+bwd steps of the two block-sparse workloads: time per live
+    tile (ms per step / (B * H * live tiles per head)) as a ratio to the
+    headline workload's."""
+    import torch
+    from tiled_exact_attention_flash_gb300.inputs import WORKLOADS
+    out = {"reference_workload": ref_name, "steps": steps,
+           "note": "ratio = (ms per step / live tiles) / the same for the reference workload; "
+                   "1.0 means time scales exactly with the live-tile count"}
+    for cid in (4, 5):
+        w = WORKLOADS[cid]
+        prob = Problem(w, dev, api)
+        for _ in range(warmup):
+            prob.step(api, stream)
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            prob.step(api, stream)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        api.check_status(stream)
+        ms = a.elapsed_time(b) / steps
+        tiles = w.B * w.H * prob.nnz
+        out[f"C{cid}"] = {"workload": w.name, "live_tiles": tiles, "ms_per_step": round(ms, 4),
+                          "step_tflops": round(prob.step_flops / (ms * 1e-3) / 1e12, 2),
+                          "ms_per_live_tile_ratio": round((ms / tiles) / ms_per_tile_ref, 4)}
+        del prob
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
 
     from tiled_exact_attention_flash_gb300 import api
-    from tiled_exact_attention_flash_gb300.inputs import WORKLOADS, workload_inputs
+    from tiled_exact_attention_flash_gb300.inputs import WORKLOADS
 
     rank, world, local = dist_env()
     w = WORKLOADS[args.config]
@@ -262,17 +351,9 @@ def run_ours(args):
     dev = torch.device("cuda", local if world > 1 else 0)
     stream = torch.cuda.current_stream(dev)
 
-    fields = w.mask_fields()
-    mask = api.Mask(**fields) if fields else None
-    index = None
-    if mask is not None and mask.needs_index:
-        index = api.build_block_index(mask, w.N).to(dev)
-        nnz = index.nnz
-    else:
-        nb = (w.N + TILE - 1) // TILE
-        nnz = nb * (nb + 1) // 2 if (mask and mask.causal) else nb * nb
-    fwd_flops, bwd_flops = live_flops(w, nnz)
-    step_flops = fwd_flops + bwd_flops
+    prob = Problem(w, dev, api)
+    mask, index, nnz = prob.mask, prob.index, prob.nnz
+    fwd_flops, bwd_flops, step_flops = prob.fwd_flops, prob.bwd_flops, prob.step_flops
     # element-exact count beside the tile count: live (i, j) pairs per head
     # (the builder's count; closed forms for the arithmetic dense / causal lists)
     if index is not None:
@@ -283,32 +364,14 @@ def run_ours(args):
         live_elems = w.N * w.N
     exact_fwd_flops = w.B * w.H * live_elems * 4.0 * w.d
 
-    host = workload_inputs(w)
-    q, k, v, do = (host[n].to(dev) for n in ("q", "k", "v", "do"))
+    host = prob.host
+    q, k, v, do, o, lse = prob.q, prob.k, prob.v, prob.do, prob.o, prob.lse
+    dq, dk, dv, ws = prob.dq, prob.dk, prob.dv, prob.ws
     B, N, H, d = q.shape
-    o = torch.empty_like(q)
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
-    ws = torch.empty(api.bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
+    n_ev = 2 + len(BWD_LAUNCHES)
 
     def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        api.fwd(q, k, v, mask=mask, index=index, out=o, lse=lse, stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
-        api.bwd(q, k, v, o, lse, do, mask=mask, index=index, dq=dq, dk=dk, dv=dv,
-                workspace=ws, stream=stream, stages=api.BWD_PREPROCESS)
-        if ev is not None:
-            ev[2].record(stream)
-        api.bwd(q, k, v, o, lse, do, mask=mask, index=index, dq=dq, dk=dk, dv=dv,
-                workspace=ws, stream=stream, stages=api.BWD_DKDV)
-        if ev is not None:
-            ev[3].record(stream)
-        api.bwd(q, k, v, o, lse, do, mask=mask, index=index, dq=dq, dk=dk, dv=dv,
-                workspace=ws, stream=stream, stages=api.BWD_DQ)
-        if ev is not None:
-            ev[4].record(stream)
+        prob.step(api, stream, ev)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -320,7 +383,7 @@ def run_ours(args):
         gpu_index = str(local)
     clocks = ClockSampler(gpu_index)
     time.sleep(0.3)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
@@ -338,16 +401,18 @@ def run_ours(args):
     api.check_status(stream)
     total_ms = reduce_max(t_start.elapsed_time(t_end), dev)
     ms_per_step = total_ms / args.steps
+    names = ["fwd"] + [name for name, _, _ in BWD_LAUNCHES]
     per_kernel = {name: sum(evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(args.steps))
-                  / args.steps for i, name in enumerate(["fwd", "bwd_pre", "bwd_dkdv", "bwd_dq"])}
+                  / args.steps for i, name in enumerate(names)}
 
     value = job_value(step_flops, ms_per_step, world)
     fwd_tflops = fwd_flops / (per_kernel["fwd"] * 1e-3) / 1e12
-    bwd_ms = per_kernel["bwd_pre"] + per_kernel["bwd_dkdv"] + per_kernel["bwd_dq"]
+    bwd_ms = sum(per_kernel[name] for name, _, _ in BWD_LAUNCHES)
     bwd_tflops = bwd_flops / (bwd_ms * 1e-3) / 1e12
 
     # roofline of the dominant kernel: tensor-core FLOPs it issues on live tiles
-    kernel_flops = {"fwd": fwd_flops, "bwd_dkdv": 2.0 * fwd_flops, "bwd_dq": 1.5 * fwd_flops}
+    kernel_flops = {"fwd": fwd_flops}
+    kernel_flops.update({name: f * fwd_flops for name, _, f in BWD_LAUNCHES if f > 0})
     dominant = max(kernel_flops, key=lambda n: per_kernel[n])
     peak = peaks["bf16_tflops"]
     achieved = kernel_flops[dominant] / (per_kernel[dominant] * 1e-3) / 1e12
@@ -426,6 +491,12 @@ def run_ours(args):
                "d2h_bytes_per_step": 2 * elem + 2 * kv_elem + lse.numel() * 4,
                "pipeline": "copy-in, compute, copy-out on three streams, two buffer sets"}
 
+    # sparse workloads against the headline's time per live tile (one GPU;
+    # only with the dense causal headline as the reference)
+    scaling = None
+    if world == 1 and args.config == 3 and not args.no_sparse_scaling:
+        scaling = sparse_scaling(api, dev, stream, ms_per_step / (w.B * w.H * nnz), w.name)
+
     cpu_baseline = None
     if pool is not None:
         sample_s = pool.time_sample(oracle_jobs)
@@ -457,7 +528,8 @@ def run_ours(args):
             "bwd_pct_peak": round(100 * bwd_tflops / peak, 2),
             "step_pct_peak": round(100 * value / world / peak, 2),
             "roofline": roofline, "cpu_baseline": cpu_baseline, "e2e": e2e,
-            "gpu_launches": 4 * args.steps, "clocks": clock_rec,
+            "sparse_scaling": scaling,
+            "gpu_launches": (1 + len(BWD_LAUNCHES)) * args.steps, "clocks": clock_rec,
             "element_exact": {
                 "live_elements_per_head": live_elems,
                 "fwd_gflop": round(exact_fwd_flops / 1e9, 3),

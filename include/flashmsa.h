@@ -33,8 +33,9 @@
  *   - stream is a cudaStream_t (NULL = legacy default stream).  Calls are
  *     asynchronous on that stream.  The return value covers argument
  *     validation and launch errors only; a kernel that gives up waiting (see
- *     FLASH_MSA_ERR_TIMEOUT) or meets a corrupt index records that in a device
- *     status word read by flash_msa_get_status().
+ *     FLASH_MSA_ERR_TIMEOUT and flash_msa_set_wait_limit_ms()), meets a corrupt
+ *     index or loses its work counter records that in a device status word
+ *     read by flash_msa_get_status().
  *   - No entry point aborts, throws, or falls back to a CPU implementation.
  *     On error the last message is available from flash_msa_last_error_string().
  */
@@ -55,7 +56,10 @@ typedef enum {
   FLASH_MSA_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed */
   FLASH_MSA_ERR_TIMEOUT = 4,     /* device: a bounded wait inside a kernel ran out */
   FLASH_MSA_ERR_WORKSPACE = 5,   /* workspace missing or smaller than required */
-  FLASH_MSA_ERR_INDEX = 6        /* block index missing, built for another N, or corrupt */
+  FLASH_MSA_ERR_INDEX = 6,       /* block index missing, built for another N, or corrupt */
+  FLASH_MSA_ERR_SCHEDULE = 7     /* device: a persistent kernel found its work counter taken by
+                                    an overlapping launch (more than 256 backward launches in
+                                    flight on one device); that call's results are invalid */
 } flash_msa_status;
 
 /* Mask flags.  Element predicate for query i, key j of a length-N sequence:
@@ -228,6 +232,9 @@ flash_msa_status flash_msa_bwd(const void* q, const void* k, const void* v, cons
 #define FLASH_MSA_BWD_PREPROCESS 1u
 #define FLASH_MSA_BWD_DKDV 2u
 #define FLASH_MSA_BWD_DQ 4u
+/* Workspace bytes flash_msa_bwd_stages() needs for this set of stages (0 for
+ * invalid sizes or stage bits). */
+size_t flash_msa_bwd_stages_workspace_bytes(int B, int H, int64_t N, int d, unsigned stages);
 flash_msa_status flash_msa_bwd_stages(const void* q, const void* k, const void* v, const void* o,
                                       const float* lse, const void* dO, void* dq, void* dk,
                                       void* dv, int B, int H, int64_t N, int d, float scale,
@@ -264,7 +271,13 @@ flash_msa_status flash_msa_bwd_gqa(const void* q, const void* k, const void* v, 
  * FLASH_MSA_ERR_WORKSPACE without launching anything.  Allocates nothing and
  * calls no allocating routine.  The first call on a device looks the array's
  * device address up (cudaGetSymbolAddress); make that first call before any
- * stream capture.  All calls on a device share the array: calls whose kernels
+ * stream capture.  CUDA loads a library's device code lazily by default, so
+ * the 16 MiB are committed on a device only when the library's device image
+ * is first loaded there (at the latest by that first call), and that load
+ * can fail with an out-of-memory error if the device has no room left: a
+ * caller that reserves the whole device pool for its own allocator should
+ * make its first call (or any other call of this library) on each device
+ * before reserving the pool.  All calls on a device share the array: calls whose kernels
  * overlap on the GPU (e.g. on unordered streams) race and must be avoided;
  * sequential calls are fine (each rewrites every scratch element it reads). */
 flash_msa_status flash_msa_bwd_noalloc(const void* q, const void* k, const void* v,
@@ -274,16 +287,28 @@ flash_msa_status flash_msa_bwd_noalloc(const void* q, const void* k, const void*
 
 /* Failure-detection self-test (no counterpart on the pages): launches on
  * `stream` one thread that waits, with the bounded wait every kernel here
- * uses, on an mbarrier that nothing arrives on.  The wait gives up after the
- * library's limit (0.5 s), records FLASH_MSA_ERR_TIMEOUT in the device status
- * word and returns, so the next flash_msa_get_status() reports TIMEOUT and
- * the context stays usable; nothing faults or hangs.  Returns OK or ERR_CUDA
- * (launch). */
+ * uses, on an mbarrier that nothing arrives on.  The wait gives up after a
+ * fixed 200 ms (independent of flash_msa_set_wait_limit_ms()), records
+ * FLASH_MSA_ERR_TIMEOUT in the device status word and returns, so the next
+ * flash_msa_get_status() reports TIMEOUT and the context stays usable;
+ * nothing faults or hangs.  Returns OK or ERR_CUDA (launch). */
 flash_msa_status flash_msa_selftest_wait_timeout(void* stream);
+
+/* Limit, in milliseconds, of any single bounded wait inside the attention
+ * kernels (no counterpart on the pages): a CTA whose wait on one of its
+ * pipeline barriers exceeds it records FLASH_MSA_ERR_TIMEOUT, stops and
+ * leaves its outputs incomplete instead of hanging.  Default 4000 ms, long
+ * enough for a GPU time-sliced with other contexts.  Process-wide; applies to
+ * launches made after the call.  ms must be in [1, 600000], else
+ * FLASH_MSA_ERR_INVALID_ARG.  flash_msa_get_wait_limit_ms() returns the
+ * current value. */
+flash_msa_status flash_msa_set_wait_limit_ms(unsigned ms);
+unsigned flash_msa_get_wait_limit_ms(void);
 
 /* Synchronise `stream`, then read and clear the device status word shared by
  * every kernel of this library on the current device.  Returns OK, or the
- * first device-side error recorded since the last call (TIMEOUT, INDEX), or
+ * first device-side error recorded since the last call (TIMEOUT, INDEX,
+ * SCHEDULE), or
  * ERR_CUDA if the synchronisation itself failed. */
 flash_msa_status flash_msa_get_status(void* stream);
 

@@ -126,12 +126,15 @@ def forward_rows(q, k, v, scale, spec: MaskSpec, rows=None, chunk=256):
     return o, lse
 
 
-def row_stats(q, k, v, do, scale, spec: MaskSpec, chunk=256):
-    """LSE_i and D_i = sum_j P_ij dP_ij for every row of one head."""
+def row_stats(q, k, v, do, scale, spec: MaskSpec, chunk=256, rows=None):
+    """LSE_i and D_i = sum_j P_ij dP_ij for every row of one head, or only for
+    `rows` (the others are left at LSE = -inf, D = 0).  A causal mask makes
+    column j of P depend only on rows i >= j, so the statistics of rows
+    i >= min(cols) suffice for the key columns cols of ``backward_sampled``."""
     n = q.shape[0]
     lse = np.full(n, -np.inf)
     dsum = np.zeros(n)
-    for r in _chunks(np.arange(n), chunk):
+    for r in _chunks(np.arange(n) if rows is None else rows, chunk):
         cols, s = _row_block(q, k, scale, spec, r)
         p, l = _softmax_rows(s)
         dp = do[r] @ v[cols].T

@@ -111,3 +111,16 @@ def test_gqa_head_count_errors(L):
     need = L.flash_msa_bwd_workspace_bytes(1, 6, 256, 128)
     assert L.flash_msa_bwd_gqa(*([FAKE] * 9), 1, 6, 4, 256, 128, 0.0, None, FAKE, need,
                                None) == api.ERR_INVALID_ARG
+
+
+def test_wait_limit_setting(L):
+    old = api.get_wait_limit_ms()
+    assert old == 4000
+    try:
+        assert L.flash_msa_set_wait_limit_ms(0) == api.ERR_INVALID_ARG
+        assert L.flash_msa_set_wait_limit_ms(600001) == api.ERR_INVALID_ARG
+        assert api.get_wait_limit_ms() == old
+        api.set_wait_limit_ms(12000)
+        assert api.get_wait_limit_ms() == 12000
+    finally:
+        api.set_wait_limit_ms(old)

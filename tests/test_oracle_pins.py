@@ -213,6 +213,30 @@ def test_chunked_evaluation_matches_full(spec):
     assert np.abs(dv[cols] - dv2).max() < 1e-12
 
 
+@pytest.mark.parametrize("spec", [
+    MaskSpec(causal=True),
+    MaskSpec(causal=True, window=60, dilation=2, dilation_far=True, block=32),
+])
+def test_row_stats_of_tail_rows_give_tail_columns(spec):
+    # under a causal mask, column j of P involves only rows i >= j: the
+    # statistics of the rows from min(cols) on reproduce the full-materialisation
+    # gradients of those key columns, and match the full statistics there
+    r = rng(13)
+    n, d = 333, 8
+    q, k, v, do = (r.standard_normal((n, d)) for _ in range(4))
+    dq, dk, dv = bwd_full(q, k, v, do, 0.3, spec)
+    cols = np.array([250, 251, 300, 331, 332])
+    tail = np.arange(cols.min(), n)
+    stats = attention.row_stats(q, k, v, do, 0.3, spec, chunk=40, rows=tail)
+    full = attention.row_stats(q, k, v, do, 0.3, spec, chunk=40)
+    assert np.abs(stats[0][tail] - full[0][tail]).max() < 1e-12
+    assert np.abs(stats[1][tail] - full[1][tail]).max() < 1e-12
+    assert (stats[0][:cols.min()] == -np.inf).all() and (stats[1][:cols.min()] == 0).all()
+    _, dk2, dv2 = attention.backward_sampled(q, k, v, do, 0.3, spec, [], cols, stats=stats)
+    assert np.abs(dk[cols] - dk2).max() < 1e-12
+    assert np.abs(dv[cols] - dv2).max() < 1e-12
+
+
 def test_empty_rows_are_zero_not_nan():
     # strided-only causal mask at block 4 with phase 1: rows 0..3 have no live key
     spec = MaskSpec(causal=True, stride=2, stride_phase=1, block=4)

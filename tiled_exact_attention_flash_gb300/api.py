@@ -19,9 +19,10 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libflashmsa.so")
 
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE, ERR_INDEX = range(7)
+(OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE, ERR_INDEX,
+ ERR_SCHEDULE) = range(8)
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "TIMEOUT",
-                5: "WORKSPACE", 6: "INDEX"}
+                5: "WORKSPACE", 6: "INDEX", 7: "SCHEDULE"}
 CAUSAL, WINDOW, DILATED, STRIDED, GLOBAL, STRIDED_REL, DILATED_FAR, BITMASK, DOCUMENTS = \
     1, 2, 4, 8, 16, 32, 64, 128, 256
 
@@ -33,10 +34,13 @@ SYMBOLS = (
     "flash_msa_bwd_workspace_bytes",
     "flash_msa_bwd",
     "flash_msa_bwd_stages",
+    "flash_msa_bwd_stages_workspace_bytes",
     "flash_msa_fwd_gqa",
     "flash_msa_bwd_gqa",
     "flash_msa_bwd_noalloc",
     "flash_msa_selftest_wait_timeout",
+    "flash_msa_set_wait_limit_ms",
+    "flash_msa_get_wait_limit_ms",
     "flash_msa_get_status",
     "flash_msa_last_error_string",
     "flash_msa_version",
@@ -104,6 +108,8 @@ def lib() -> ctypes.CDLL:
                                 ctypes.POINTER(MaskDescStruct), vp]
     L.flash_msa_bwd_workspace_bytes.argtypes = [i32, i32, i64, i32]
     L.flash_msa_bwd_workspace_bytes.restype = ctypes.c_size_t
+    L.flash_msa_bwd_stages_workspace_bytes.argtypes = [i32, i32, i64, i32, ctypes.c_uint]
+    L.flash_msa_bwd_stages_workspace_bytes.restype = ctypes.c_size_t
     L.flash_msa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i64, i32, f32,
                                 ctypes.POINTER(MaskDescStruct), vp, ctypes.c_size_t, vp]
     L.flash_msa_bwd_stages.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i64, i32,
@@ -117,12 +123,14 @@ def lib() -> ctypes.CDLL:
                                         f32, ctypes.POINTER(MaskDescStruct), vp]
     L.flash_msa_get_status.argtypes = [vp]
     L.flash_msa_selftest_wait_timeout.argtypes = [vp]
+    L.flash_msa_set_wait_limit_ms.argtypes = [ctypes.c_uint]
+    L.flash_msa_get_wait_limit_ms.restype = ctypes.c_uint
     L.flash_msa_last_error_string.restype = ctypes.c_char_p
     L.flash_msa_version.restype = ctypes.c_char_p
     for name in ("flash_msa_build_block_index", "flash_msa_check_block_index", "flash_msa_fwd",
                  "flash_msa_bwd", "flash_msa_bwd_stages", "flash_msa_bwd_noalloc",
                  "flash_msa_fwd_gqa", "flash_msa_bwd_gqa", "flash_msa_get_status",
-                 "flash_msa_selftest_wait_timeout"):
+                 "flash_msa_selftest_wait_timeout", "flash_msa_set_wait_limit_ms"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -385,13 +393,20 @@ def bwd_workspace_bytes(B, H, N, d) -> int:
 
 
 BWD_PREPROCESS, BWD_DKDV, BWD_DQ = 1, 2, 4
+BWD_DETERMINISTIC = BWD_PREPROCESS | BWD_DKDV | BWD_DQ
+
+
+def bwd_stages_workspace_bytes(B, H, N, d, stages) -> int:
+    """Workspace of flash_msa_bwd_stages for this set of stages."""
+    return int(lib().flash_msa_bwd_stages_workspace_bytes(B, H, N, d, stages))
 
 
 def bwd(q, k, v, o, lse, do, mask: Optional[Mask] = None, index: Optional[BlockIndex] = None,
         scale: Optional[float] = None, dq=None, dk=None, dv=None, workspace=None, stream=None,
-        stages: Optional[int] = None):
+        stages: Optional[int] = None, deterministic: bool = False):
     """dQ, dK, dV (bf16, like q).  ``stages`` (bits BWD_*) runs a subset of the
-    three launches through flash_msa_bwd_stages; default: all of them."""
+    launches through flash_msa_bwd_stages; ``deterministic`` runs the
+    two-kernel backward (stages BWD_DETERMINISTIC); default: flash_msa_bwd."""
     _check_qkv("q", q)
     B, N, H, d = q.shape
     kv_shape = _kv_shape(q, k)
@@ -401,12 +416,17 @@ def bwd(q, k, v, o, lse, do, mask: Optional[Mask] = None, index: Optional[BlockI
         _check_qkv(name, t, q.shape)
     if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (B, H, N):
         raise ValueError("lse must be contiguous float32 (B, H, N)")
+    if deterministic:
+        if stages is not None:
+            raise ValueError("pass either stages or deterministic")
+        stages = BWD_DETERMINISTIC
     if Hkv != H and stages is not None:
         raise ValueError("stages are available for equal query / key-value head counts only")
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    ws_bytes = bwd_workspace_bytes(B, H, N, d)
+    ws_bytes = (bwd_workspace_bytes(B, H, N, d) if stages is None
+                else bwd_stages_workspace_bytes(B, H, N, d, stages))
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
     desc, _keep = _mask_desc(mask, index, N)
@@ -460,6 +480,15 @@ def selftest_wait_timeout(stream=None) -> int:
     """Launch the bounded-wait probe (a wait that must run out); the next
     get_status() then reports ERR_TIMEOUT."""
     return lib().flash_msa_selftest_wait_timeout(_stream_ptr(stream))
+
+
+def set_wait_limit_ms(ms: int):
+    """Limit of any single bounded wait inside the kernels (process-wide)."""
+    _check(lib().flash_msa_set_wait_limit_ms(int(ms)), "flash_msa_set_wait_limit_ms")
+
+
+def get_wait_limit_ms() -> int:
+    return int(lib().flash_msa_get_wait_limit_ms())
 
 
 def check_status(stream=None):

@@ -534,6 +534,11 @@ size_t flash_msa_bwd_workspace_bytes(int B, int H, int64_t N, int d) {
   return (bytes + 255) & ~size_t(255);
 }
 
+size_t flash_msa_bwd_stages_workspace_bytes(int B, int H, int64_t N, int d, unsigned stages) {
+  if (stages == 0 || (stages & ~7u)) return 0;
+  return flash_msa_bwd_workspace_bytes(B, H, N, d);
+}
+
 flash_msa_status flash_msa_bwd(const void* q, const void* k, const void* v, const void* o,
                                const float* lse, const void* dO, void* dq, void* dk, void* dv,
                                int B, int H, int64_t N, int d, float scale,
@@ -613,6 +618,16 @@ flash_msa_status flash_msa_bwd_gqa(const void* q, const void* k, const void* v, 
                   workspace_bytes,
                   FLASH_MSA_BWD_PREPROCESS | FLASH_MSA_BWD_DKDV | FLASH_MSA_BWD_DQ, stream);
 }
+
+flash_msa_status flash_msa_set_wait_limit_ms(unsigned ms) {
+  g_last_error[0] = 0;
+  if (ms < 1 || ms > 600000)
+    return set_error(FLASH_MSA_ERR_INVALID_ARG, "wait limit %u ms outside [1, 600000]", ms);
+  set_wait_limit_ms(ms);
+  return FLASH_MSA_OK;
+}
+
+unsigned flash_msa_get_wait_limit_ms(void) { return wait_limit_ms(); }
 
 flash_msa_status flash_msa_selftest_wait_timeout(void* stream) {
   g_last_error[0] = 0;

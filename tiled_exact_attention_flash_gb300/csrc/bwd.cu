@@ -95,7 +95,9 @@ struct BwdParams {
   int B, H, N, NP;  // H: query heads
   int Hkv, G;       // key/value heads, query heads per key/value head
   int n_units;
-  int* sched;  // work counter of this launch (zeroed before it)
+  unsigned long long* sched;  // work counter of this launch (see claim_unit)
+  unsigned ticket;
+  int wait_limit_ms;          // limit of any single bounded wait
   float scale, scale_log2;
   MaskParams mask;
   ListParams list;
@@ -127,9 +129,10 @@ struct BwdLayout {
                        kRingEmpty = 10 + kStages, kUnitFull = 10 + 2 * kStages,
                        kUnitEmpty = kUnitFull + 2;
   static constexpr int kNumBars = kUnitEmpty + 2;
-  // misc: TMEM base address, abort flag, the two unit-queue slots
+  // misc: TMEM base address, abort flag, wait limit, (pad), the two
+  // unit-queue slots
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+  static constexpr int kSmemBytes = kMiscOff + 24 + 1024;
 };
 
 template <int HD>
@@ -192,7 +195,7 @@ template <int HD, bool KS>
 __device__ __forceinline__ UnitQueue unit_queue(uint8_t* smem, uint64_t* bars) {
   using L = BwdLayout<HD, KS>;
   return UnitQueue{smem_u32(bars + L::kUnitFull), smem_u32(bars + L::kUnitEmpty),
-                   reinterpret_cast<volatile int*>(smem + L::kMiscOff + 8), 0u};
+                   reinterpret_cast<volatile int*>(smem + L::kMiscOff + 16), 0u};
 }
 
 // Producer shared by both kernels.  Per unit: the stationary tiles (dkdv: K,
@@ -217,9 +220,9 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint8_t* smem, 
   bool ok = true;
   UnitQueue queue = unit_queue<HD, kKeyStationary>(smem, bars);
   // units are claimed one ahead (the dQ pass prefetches the next unit's dO)
-  int u = queue_push(queue, p.sched, p.n_units, abort_flag, p.status);
+  int u = queue_push(queue, p.sched, p.ticket, p.n_units, abort_flag, p.status);
   while (ok && u >= 0) {
-    const int u_next = queue_push(queue, p.sched, p.n_units, abort_flag, p.status);
+    const int u_next = queue_push(queue, p.sched, p.ticket, p.n_units, abort_flag, p.status);
     if (u_next == -2) {
       ok = false;
       break;
@@ -824,7 +827,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
     tmem_relinquish();
   }
   if (threadIdx.x == 0) {
-    *abort_flag = 0;
+    abort_flag[0] = 0;
+    abort_flag[1] = p.wait_limit_ms;
     init_bwd_barriers<HD, kKeyStationary>(bars);
   }
   if (warp == 0 && lane == 0) {
@@ -899,30 +903,25 @@ static flash_msa_status launch_bwd_hd(const BwdLaunch& a, cudaStream_t stream) {
   p.scale_log2 = a.scale * kLog2e;
   p.mask = a.mask;
   p.status = a.status;
-  static bool attr_set[2][2] = {{false, false}, {false, false}};
-  auto prep = [&](auto kern, int which) -> flash_msa_status {
-    if (!attr_set[HD == 128][which]) {
-      const int bytes = which == 0 ? LK::kSmemBytes : LQ::kSmemBytes;
-      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
-          cudaSuccess)
-        return set_cuda_error("cudaFuncSetAttribute(bwd)");
-      attr_set[HD == 128][which] = true;
-    }
-    return FLASH_MSA_OK;
+  p.wait_limit_ms = int(wait_limit_ms());
+  auto prep = [&](const void* kern, int which) -> flash_msa_status {
+    const int bytes = which == 0 ? LK::kSmemBytes : LQ::kSmemBytes;
+    return enable_smem(kern, bytes, 2 + 2 * which + (HD == 128 ? 1 : 0),
+                       "cudaFuncSetAttribute(bwd)");
   };
   // persistent launches: one CTA per SM (fewer for small problems), units
-  // handed out in order by a counter zeroed just before each kernel
+  // handed out in order by a counter set up just before each kernel
   const int sms = sm_count();
   if (sms <= 0) return set_cuda_error("bwd: multiprocessor count");
   auto claim_counter = [&]() -> flash_msa_status {
-    p.sched = sched_counter();
-    if (!p.sched) return set_cuda_error("bwd: work counter");
-    if (cudaMemsetAsync(p.sched, 0, sizeof(int), stream) != cudaSuccess)
-      return set_cuda_error("bwd: work counter reset");
-    return FLASH_MSA_OK;
+    SchedCounter c;
+    const flash_msa_status r = claim_sched_counter(stream, &c);
+    p.sched = c.counter;
+    p.ticket = c.ticket;
+    return r;
   };
   if (a.stages & FLASH_MSA_BWD_DKDV) {
-    if ((st = prep(bwd_main_kernel<HD, true>, 0)) != FLASH_MSA_OK) return st;
+    if ((st = prep(reinterpret_cast<const void*>(&bwd_main_kernel<HD, true>), 0)) != FLASH_MSA_OK) return st;
     if ((st = claim_counter()) != FLASH_MSA_OK) return st;
     p.list = a.cols;
     p.n_units = a.B * a.Hkv * nb;
@@ -933,7 +932,7 @@ static flash_msa_status launch_bwd_hd(const BwdLaunch& a, cudaStream_t stream) {
     if (cudaGetLastError() != cudaSuccess) return set_cuda_error("bwd_dkdv launch");
   }
   if (a.stages & FLASH_MSA_BWD_DQ) {
-    if ((st = prep(bwd_main_kernel<HD, false>, 1)) != FLASH_MSA_OK) return st;
+    if ((st = prep(reinterpret_cast<const void*>(&bwd_main_kernel<HD, false>), 1)) != FLASH_MSA_OK) return st;
     if ((st = claim_counter()) != FLASH_MSA_OK) return st;
     p.list = a.rows;
     p.n_units = a.B * a.H * nb;

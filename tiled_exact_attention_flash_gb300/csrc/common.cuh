@@ -11,7 +11,6 @@ namespace fmsa {
 
 constexpr int kTile = 128;                 // query / key tile edge (tokens)
 constexpr uint32_t kNegInfBits = 0xFF800000u;  // fp32 -inf: a dead score
-constexpr uint64_t kWaitLimitNs = 500ull * 1000ull * 1000ull;  // any single wait: 0.5 s
 constexpr uint64_t kDrainLimitNs = 50ull * 1000ull * 1000ull;  // draining copies after an abort
 constexpr int64_t kUnbounded = int64_t(1) << 40;
 
@@ -146,19 +145,24 @@ __device__ __forceinline__ void record_status(unsigned* status, unsigned code, u
   atomicCAS(status, 0u, word);
 }
 
+// CTA control words in shared memory: abort_flag[0] is the CTA-wide abort
+// flag, abort_flag[1] the limit of any single wait in milliseconds (set from
+// the launch parameters before the CTA's first barrier).
+//
 // Wait for the phase with the given parity; gives up (returns false) when the
-// CTA-wide abort flag is raised or after kWaitLimitNs, raising the flag and
+// CTA-wide abort flag is raised or after the wait limit, raising the flag and
 // recording FLASH_MSA_ERR_TIMEOUT.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                          unsigned* status, unsigned where) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
+  const uint64_t limit_ns = uint64_t(unsigned(abort_flag[1])) * 1000000ull;
   while (true) {
 #pragma unroll 1
     for (int k = 0; k < 16; ++k)
       if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (abort_flag[0]) return false;
+    if (global_timer_ns() - t0 > limit_ns) {
       *abort_flag = 1;
       record_status(status, FLASH_MSA_ERR_TIMEOUT, where);
       return false;
@@ -183,6 +187,15 @@ __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
 // producer) and an "empty" mbarrier (one arrival per consumer).  Index -1
 // means that no unit is left; it is published exactly once.  Both calls
 // return -2 when a wait was abandoned (abort).
+//
+// The counter is one 64-bit word of a small pool shared by all launches on
+// the device.  Before the kernel runs, the host sets both of its 32-bit
+// halves to the launch's ticket (a positive number below 2^31, different
+// for every launch); a claim adds 1, so the low half minus the ticket is the
+// unit index and the high half must still equal the ticket.  A launch that
+// finds another ticket there shares the counter with an overlapping launch:
+// it records FLASH_MSA_ERR_SCHEDULE and claims nothing more, so aliasing
+// counters are reported instead of silently losing work units.
 // ---------------------------------------------------------------------------
 struct UnitQueue {
   uint32_t full, empty;  // mbarriers of slot 0; slot 1's follow 8 bytes later
@@ -190,12 +203,23 @@ struct UnitQueue {
   uint32_t seq;          // number of pushes / pops done by this thread
 };
 
-__device__ __forceinline__ int queue_push(UnitQueue& q, int* counter, int n_units,
+__device__ __forceinline__ int claim_unit(unsigned long long* counter, unsigned ticket,
+                                          int n_units, unsigned* status) {
+  const unsigned long long old = atomicAdd(counter, 1ull);
+  if (unsigned(old >> 32) != ticket) {
+    record_status(status, FLASH_MSA_ERR_SCHEDULE, 0xF4);
+    return -1;
+  }
+  const unsigned u = unsigned(old) - ticket;
+  return u < unsigned(n_units) ? int(u) : -1;
+}
+
+__device__ __forceinline__ int queue_push(UnitQueue& q, unsigned long long* counter,
+                                          unsigned ticket, int n_units,
                                           volatile int* abort_flag, unsigned* status) {
   const uint32_t s = q.seq & 1;
   if (!wait_bar(q.empty + 8 * s, ((q.seq >> 1) & 1) ^ 1, abort_flag, status, 30)) return -2;
-  int u = atomicAdd(counter, 1);
-  if (u >= n_units) u = -1;
+  const int u = claim_unit(counter, ticket, n_units, status);
   q.slot[s] = u;
   mbar_arrive(q.full + 8 * s);  // release: the slot write is visible to the waiters
   ++q.seq;

@@ -35,6 +35,7 @@ struct FwdParams {
   int G;  // query heads per key/value head
   int n_units;
   float scale_log2;  // scale * log2(e)
+  int wait_limit_ms;  // limit of any single bounded wait
   MaskParams mask;
   ListParams list;
   unsigned* status;
@@ -56,6 +57,7 @@ struct FwdLayout {
                        kMmaDone = 12, kKvFull = 13, kKvEmpty = 13 + kSlots;
   static constexpr int kNumBars = 13 + 2 * kSlots;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  // misc: TMEM base address, abort flag, wait limit
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack for 1024-byte alignment
 };
 
@@ -628,7 +630,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     tmem_relinquish();
   }
   if (threadIdx.x == 0) {
-    *abort_flag = 0;
+    abort_flag[0] = 0;
+    abort_flag[1] = p.wait_limit_ms;
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(bars + L::kQFull + s), 1);
       mbar_init(smem_u32(bars + L::kQEmpty + s), 1);
@@ -703,13 +706,10 @@ static flash_msa_status launch_fwd_hd(const FwdLaunch& a, cudaStream_t stream) {
   p.list = a.list;
   p.n_units = a.B * a.H * ((a.list.n_blocks + 1) / 2);  // pairs of query blocks
   p.status = a.status;
-  static bool attr_set[2] = {false, false};
-  if (!attr_set[HD == 128]) {
-    if (cudaFuncSetAttribute(fwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L::kSmemBytes) != cudaSuccess)
-      return set_cuda_error("cudaFuncSetAttribute(fwd)");
-    attr_set[HD == 128] = true;
-  }
+  p.wait_limit_ms = int(wait_limit_ms());
+  if ((st = enable_smem(reinterpret_cast<const void*>(&fwd_kernel<HD>), L::kSmemBytes,
+                        HD == 128 ? 1 : 0, "cudaFuncSetAttribute(fwd)")) != FLASH_MSA_OK)
+    return st;
   int grid = p.n_units;
   const int sms = sm_count();
   if (sms > 0 && grid > sms) grid = sms;  // persistent: one CTA per SM

@@ -20,11 +20,23 @@ flash_msa_status set_cuda_error(const char* what);
 // (64, 128, 1, 1), 128-byte swizzle, zero fill past N.  Encoded on the host.
 flash_msa_status make_tile_map(CUtensorMap* m, const void* base, int B, int64_t N, int H, int d);
 
-// device status word (status.cu)
+// per-device state (status.cu)
 unsigned* status_word_ptr();  // device address for the current device, or null on error
 constexpr int kSchedSlots = 256;
-int* sched_counter();  // a work counter of the current device for one launch, or null on error
-int sm_count();        // multiprocessors of the current device, 0 on error
+struct SchedCounter {
+  unsigned long long* counter;  // device address of the launch's work counter
+  unsigned ticket;              // the launch's ticket (see claim_unit)
+};
+// A work counter of the current device for one launch, initialised on
+// `stream` with a fresh ticket.
+flash_msa_status claim_sched_counter(cudaStream_t stream, SchedCounter* out);
+int sm_count();  // multiprocessors of the current device, 0 on error
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per kernel (bit
+// `which`, one per kernel instantiation) and device
+flash_msa_status enable_smem(const void* kernel, int bytes, unsigned which, const char* what);
+constexpr unsigned kDefaultWaitLimitMs = 4000;
+unsigned wait_limit_ms();  // limit of any single bounded wait in the kernels
+void set_wait_limit_ms(unsigned ms);
 flash_msa_status launch_wait_timeout_probe(cudaStream_t stream);
 
 struct FwdLaunch {

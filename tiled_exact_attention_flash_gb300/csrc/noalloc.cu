@@ -14,6 +14,8 @@
 // GPU (different streams, no ordering between them) race on the array.
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "internal.h"
 
 namespace fmsa {
@@ -26,23 +28,25 @@ static __device__ __align__(256) unsigned char g_bwd_scratch[kNoAllocScratchByte
 
 // Device address of the scratch array for the current device.  Host code may
 // not pass g_bwd_scratch itself to a kernel: in host code that name is a
-// host-side stand-in, not a device address.  Looked up once per device.
+// host-side stand-in, not a device address.  Looked up once per device
+// (threads making their first calls at the same time may both look it up and
+// store the same value).
 static flash_msa_status scratch_address(void** out) {
   constexpr int kMaxDevices = 64;
-  static void* cache[kMaxDevices] = {};
+  static std::atomic<void*> cache[kMaxDevices];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return set_cuda_error("bwd_noalloc: cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices)
     return set_error(FLASH_MSA_ERR_CUDA, "bwd_noalloc: device ordinal %d out of range", dev);
-  if (!cache[dev]) {
-    void* ptr = nullptr;
+  void* ptr = cache[dev].load(std::memory_order_acquire);
+  if (!ptr) {
     const cudaError_t rc = cudaGetSymbolAddress(&ptr, g_bwd_scratch);
     if (rc != cudaSuccess || !ptr)
       return set_error(FLASH_MSA_ERR_CUDA, "bwd_noalloc: cudaGetSymbolAddress failed: %s",
                        cudaGetErrorString(rc));
-    cache[dev] = ptr;
+    cache[dev].store(ptr, std::memory_order_release);
   }
-  *out = cache[dev];
+  *out = ptr;
   return FLASH_MSA_OK;
 }
 
