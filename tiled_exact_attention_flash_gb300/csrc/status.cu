@@ -58,7 +58,7 @@ static PFN_cuMemsetD32Async_v3020 memset_d32_fn() {
   if (!f) {
     void* ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuMemsetD32Async", &ptr, 3020, cudaEnableDefault,
+    if (cudaGetDriverEntryPointByVersion("cuMemsetD32Async", &ptr, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess) {
       f = reinterpret_cast<PFN_cuMemsetD32Async_v3020>(ptr);
