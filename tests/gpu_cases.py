@@ -19,8 +19,10 @@ GRAD_REL_TOL = 3e-2
 GRAD_ABS_FLOOR = 1e-4
 
 
-def run_gpu(inp: dict, fields: dict, device="cuda", backward=True, scale=None):
-    """scale: softmax scale passed to the library (None: its default d^-1/2)."""
+def run_gpu(inp: dict, fields: dict, device="cuda", backward=True, scale=None,
+            deterministic=False):
+    """scale: softmax scale passed to the library (None: its default d^-1/2);
+    deterministic: the two-kernel backward instead of the default fused one."""
     mask = api.Mask(**fields) if fields else None
     N = inp["q"].shape[1]
     index = None
@@ -30,7 +32,8 @@ def run_gpu(inp: dict, fields: dict, device="cuda", backward=True, scale=None):
     o, lse = api.fwd(q, k, v, mask=mask, index=index, scale=scale)
     out = {"o": o, "lse": lse}
     if backward:
-        dq, dk, dv = api.bwd(q, k, v, o, lse, do, mask=mask, index=index, scale=scale)
+        dq, dk, dv = api.bwd(q, k, v, o, lse, do, mask=mask, index=index, scale=scale,
+                             deterministic=deterministic)
         out.update(dq=dq, dk=dk, dv=dv)
     st = api.get_status()
     assert st == api.OK, f"device status {st}"
@@ -97,8 +100,8 @@ def full_compare(inp, fields, res, heads=None, backward=True, scale=None):
 
 def sampled_compare(inp, fields, res, heads, rows, cols, backward=True, tail_stats=False):
     """Full-size comparison on sampled heads / query rows / key columns.
-    tail_stats (causal masks only): the row statistics the key columns need
-    are computed for rows >= min(cols) only (column j of P involves rows
+    tail_stats (causal masks only): the row statistics are computed for the
+    sampled rows and the rows >= min(cols) only (column j of P involves rows
     i >= j alone)."""
     B, N, H, d = inp["q"].shape
     spec = MaskSpec(**fields)
@@ -109,7 +112,9 @@ def sampled_compare(inp, fields, res, heads, rows, cols, backward=True, tail_sta
         check_o(res["o"][b, rows, h], o_ref)
         check_lse(res["lse"][b, h, rows], lse_ref)
         if backward:
-            need = np.arange(int(np.min(cols)), N) if (tail_stats and len(cols)) else None
+            need = None
+            if tail_stats and len(cols):
+                need = np.union1d(np.asarray(rows, dtype=np.int64), np.arange(int(np.min(cols)), N))
             stats = attention.row_stats(q, k, v, do, scale, spec, rows=need)
             dq, dk, dv = attention.backward_sampled(q, k, v, do, scale, spec, rows, cols,
                                                     stats=stats)

@@ -56,6 +56,17 @@ def test_small_cases(d, n, mname):
     gc.full_compare(inp, fields, res)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("n", [129, 517])
+@pytest.mark.parametrize("mname", sorted(SMALL_MASKS))
+def test_small_cases_deterministic_backward(d, n, mname):
+    # the two-kernel backward (no atomics) against the oracle
+    fields = SMALL_MASKS[mname]
+    inp = small_inputs(2, n, 3, d, seed=n * 5 + d)
+    res = gc.run_gpu(inp, fields, deterministic=True)
+    gc.full_compare(inp, fields, res)
+
+
 @pytest.mark.parametrize("cid", [2, 3, 4, 5, 6, 7, 9, 10])
 def test_full_size_workloads(cid):
     w = WORKLOADS[cid]
@@ -138,12 +149,23 @@ def test_smoke_shape_from_the_pages():
 
 
 def test_repeat_calls_are_deterministic():
-    w = WORKLOADS[2]
+    # O, LSE, dK, dV are bitwise reproducible on both backward paths and
+    # identical between them (same products in the same order); dQ is
+    # bitwise reproducible on the two-kernel path, while the fused path adds
+    # the tiles' dQ partial products atomically in a varying order, so its dQ
+    # is compared within the gradient tolerance
     inp = small_inputs(2, 1000, 4, 128, seed=11)
     a = gc.run_gpu(inp, {"causal": True})
     b = gc.run_gpu(inp, {"causal": True})
-    for name in ("o", "lse", "dq", "dk", "dv"):
+    da = gc.run_gpu(inp, {"causal": True}, deterministic=True)
+    db = gc.run_gpu(inp, {"causal": True}, deterministic=True)
+    for name in ("o", "lse", "dk", "dv"):
         assert np.array_equal(a[name], b[name]), name
+        assert np.array_equal(a[name], da[name]), name
+    for name in ("o", "lse", "dq", "dk", "dv"):
+        assert np.array_equal(da[name], db[name]), name
+    gc.check_grad(a["dq"], da["dq"].astype(np.float64), "dQ")
+    gc.check_grad(b["dq"], da["dq"].astype(np.float64), "dQ")
 
 
 @pytest.mark.parametrize("d", [64, 128])
@@ -227,9 +249,10 @@ def test_custom_scale(d, scale, mname):
 @pytest.mark.parametrize("order", ["dkdv_first", "dq_first"])
 @pytest.mark.parametrize("mname", ["causal", "window_strided"])
 def test_bwd_stages_match_full_backward(order, mname):
-    """flash_msa_bwd_stages: the preprocessing stage, then dK/dV and dQ in
-    either order on one workspace, gives bit-for-bit the gradients of
-    flash_msa_bwd; a stage leaves the other stage's outputs untouched."""
+    """flash_msa_bwd_stages, deterministic variant: the preprocessing stage,
+    then dK/dV and dQ in either order on one workspace, gives bit-for-bit
+    the gradients of the deterministic backward; a stage leaves the other
+    stage's outputs untouched."""
     fields = SMALL_MASKS[mname]
     inp = small_inputs(2, 517, 3, 128, seed=31)
     mask = api.Mask(**fields)
@@ -237,9 +260,10 @@ def test_bwd_stages_match_full_backward(order, mname):
     index = api.build_block_index(mask, N).to("cuda") if mask.needs_index else None
     q, k, v, do = (inp[n].to("cuda") for n in ("q", "k", "v", "do"))
     o, lse = api.fwd(q, k, v, mask=mask, index=index)
-    dq, dk, dv = api.bwd(q, k, v, o, lse, do, mask=mask, index=index)
+    dq, dk, dv = api.bwd(q, k, v, o, lse, do, mask=mask, index=index, deterministic=True)
     B, _, H, d = q.shape
-    ws = torch.empty(api.bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(api.bwd_stages_workspace_bytes(B, H, N, d, api.BWD_DETERMINISTIC),
+                     dtype=torch.uint8, device="cuda")
     sentinel = torch.tensor(7.0, dtype=torch.bfloat16)
     sq, sk, sv = (torch.full_like(t, 7.0) for t in (dq, dk, dv))
     api.bwd(q, k, v, o, lse, do, mask=mask, index=index, dq=sq, dk=sk, dv=sv, workspace=ws,
@@ -259,10 +283,42 @@ def test_bwd_stages_match_full_backward(order, mname):
         assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("mname", ["causal", "window_strided", "window_global"])
+def test_fused_bwd_stages_match_full_backward(mname):
+    """flash_msa_bwd_stages, default variant: PREPROCESS, FUSED and
+    DQ_CONVERT launched one at a time give the gradients of flash_msa_bwd
+    (dK, dV bit for bit, dQ within the gradient tolerance); FUSED writes no
+    dq and DQ_CONVERT no dk / dv; PREPROCESS zeroes an accumulator that holds
+    garbage (the workspace is filled with NaN first)."""
+    fields = SMALL_MASKS[mname]
+    inp = small_inputs(2, 517, 3, 128, seed=37)
+    mask = api.Mask(**fields)
+    N = inp["q"].shape[1]
+    index = api.build_block_index(mask, N).to("cuda") if mask.needs_index else None
+    q, k, v, do = (inp[n].to("cuda") for n in ("q", "k", "v", "do"))
+    o, lse = api.fwd(q, k, v, mask=mask, index=index)
+    dq, dk, dv = api.bwd(q, k, v, o, lse, do, mask=mask, index=index)
+    B, _, H, d = q.shape
+    ws = torch.full((api.bwd_workspace_bytes(B, H, N, d) // 4,), float("nan"), device="cuda")
+    sentinel = torch.tensor(7.0, dtype=torch.bfloat16)
+    sq, sk, sv = (torch.full_like(t, 7.0) for t in (dq, dk, dv))
+    for stage, untouched in ((api.BWD_PREPROCESS, (sq, sk, sv)), (api.BWD_FUSED, (sq,)),
+                             (api.BWD_DQ_CONVERT, ())):
+        api.bwd(q, k, v, o, lse, do, mask=mask, index=index, dq=sq, dk=sk, dv=sv, workspace=ws,
+                stages=stage)
+        torch.cuda.synchronize()
+        for t in untouched:
+            assert bool((t.cpu() == sentinel).all())
+    assert api.get_status() == api.OK
+    assert torch.equal(sk, dk) and torch.equal(sv, dv)
+    gc.check_grad(sq.float().cpu().numpy(), dq.float().cpu().numpy().astype(np.float64), "dQ")
+
+
 def test_side_streams_match_default_stream():
     """The calls run on the caller's current stream: forward and backward
-    issued on two side streams at once (each with its own work counters)
-    give bit-for-bit the results of the default stream."""
+    issued on two side streams at once (each with its own work counters and
+    workspace) give bit-for-bit the results of the default stream (dQ,
+    accumulated atomically, within the gradient tolerance)."""
     fields = {"causal": True, "window": 300, "dilation": 2, "dilation_near": 1}
     inp = small_inputs(2, 517, 3, 128, seed=77)
     mask = api.Mask(**fields)
@@ -283,5 +339,8 @@ def test_side_streams_match_default_stream():
     torch.cuda.synchronize()
     assert api.get_status() == api.OK
     for got in outs:
-        for a, b in zip(got, ref):
-            assert torch.equal(a, b)
+        for name, a, b in zip(("o", "lse", "dq", "dk", "dv"), got, ref):
+            if name == "dq":
+                gc.check_grad(a.float().cpu().numpy(), b.float().cpu().numpy().astype(np.float64), "dQ")
+            else:
+                assert torch.equal(a, b), name

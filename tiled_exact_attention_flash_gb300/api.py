@@ -392,8 +392,9 @@ def bwd_workspace_bytes(B, H, N, d) -> int:
     return int(lib().flash_msa_bwd_workspace_bytes(B, H, N, d))
 
 
-BWD_PREPROCESS, BWD_DKDV, BWD_DQ = 1, 2, 4
-BWD_DETERMINISTIC = BWD_PREPROCESS | BWD_DKDV | BWD_DQ
+BWD_PREPROCESS, BWD_DKDV, BWD_DQ, BWD_FUSED, BWD_DQ_CONVERT = 1, 2, 4, 8, 16
+BWD_DETERMINISTIC = BWD_PREPROCESS | BWD_DKDV | BWD_DQ    # seven products per tile, no atomics
+BWD_DEFAULT = BWD_PREPROCESS | BWD_FUSED | BWD_DQ_CONVERT  # what flash_msa_bwd runs
 
 
 def bwd_stages_workspace_bytes(B, H, N, d, stages) -> int:

@@ -525,18 +525,38 @@ flash_msa_status flash_msa_fwd_gqa(const void* q, const void* k, const void* v, 
   return fwd_impl(q, k, v, o, lse, B, H, Hkv, N, d, scale, mask, stream);
 }
 
+// Workspace: two fp32 vectors per (b, h) padded to whole 128-row tiles
+// (-LSE * log2(e) and D), then, for the fused backward, the fp32 dQ
+// accumulator (B, H, padded N, d).
+static size_t vectors_bytes(int B, int H, int64_t N) {
+  return 2 * size_t(B) * size_t(H) * size_t(n_blocks_of(N)) * kTile * sizeof(float);
+}
+static size_t accumulator_bytes(int B, int H, int64_t N, int d) {
+  return size_t(B) * size_t(H) * size_t(n_blocks_of(N)) * kTile * size_t(d) * sizeof(float);
+}
+static size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+static constexpr unsigned kAllStages = FLASH_MSA_BWD_PREPROCESS | FLASH_MSA_BWD_DKDV |
+                                       FLASH_MSA_BWD_DQ | FLASH_MSA_BWD_FUSED |
+                                       FLASH_MSA_BWD_DQ_CONVERT;
+static constexpr unsigned kDefaultStages =
+    FLASH_MSA_BWD_PREPROCESS | FLASH_MSA_BWD_FUSED | FLASH_MSA_BWD_DQ_CONVERT;
+
+static bool valid_stages(unsigned stages) {
+  if (stages == 0 || (stages & ~kAllStages)) return false;
+  return !((stages & FLASH_MSA_BWD_FUSED) && (stages & (FLASH_MSA_BWD_DKDV | FLASH_MSA_BWD_DQ)));
+}
+
 size_t flash_msa_bwd_workspace_bytes(int B, int H, int64_t N, int d) {
-  (void)d;
-  if (B < 1 || H < 1 || N < 1 || N > kMaxN) return 0;
-  // two fp32 vectors per (b, h) padded to whole 128-row tiles: -LSE * log2(e) and D
-  const size_t padded = size_t(n_blocks_of(N)) * kTile;
-  const size_t bytes = 2 * size_t(B) * size_t(H) * padded * sizeof(float);
-  return (bytes + 255) & ~size_t(255);
+  if (B < 1 || H < 1 || N < 1 || N > kMaxN || (d != 64 && d != 128)) return 0;
+  return round256(vectors_bytes(B, H, N) + accumulator_bytes(B, H, N, d));
 }
 
 size_t flash_msa_bwd_stages_workspace_bytes(int B, int H, int64_t N, int d, unsigned stages) {
-  if (stages == 0 || (stages & ~7u)) return 0;
-  return flash_msa_bwd_workspace_bytes(B, H, N, d);
+  if (!valid_stages(stages)) return 0;
+  if (stages & (FLASH_MSA_BWD_FUSED | FLASH_MSA_BWD_DQ_CONVERT))
+    return flash_msa_bwd_workspace_bytes(B, H, N, d);
+  if (B < 1 || H < 1 || N < 1 || N > kMaxN || (d != 64 && d != 128)) return 0;
+  return round256(vectors_bytes(B, H, N));
 }
 
 flash_msa_status flash_msa_bwd(const void* q, const void* k, const void* v, const void* o,
@@ -545,9 +565,7 @@ flash_msa_status flash_msa_bwd(const void* q, const void* k, const void* v, cons
                                const flash_msa_mask_desc* mask, void* workspace,
                                size_t workspace_bytes, void* stream) {
   return flash_msa_bwd_stages(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, mask,
-                              workspace, workspace_bytes,
-                              FLASH_MSA_BWD_PREPROCESS | FLASH_MSA_BWD_DKDV | FLASH_MSA_BWD_DQ,
-                              stream);
+                              workspace, workspace_bytes, kDefaultStages, stream);
 }
 
 static flash_msa_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
@@ -556,8 +574,10 @@ static flash_msa_status bwd_impl(const void* q, const void* k, const void* v, co
                                  const flash_msa_mask_desc* mask, void* workspace,
                                  size_t workspace_bytes, unsigned stages, void* stream) {
   g_last_error[0] = 0;
-  if (stages == 0 || (stages & ~7u))
-    return set_error(FLASH_MSA_ERR_INVALID_ARG, "bwd: stages must be a non-empty subset of 1|2|4");
+  if (!valid_stages(stages))
+    return set_error(FLASH_MSA_ERR_INVALID_ARG,
+                     "bwd: stages 0x%x: a non-empty subset of 1|2|4|8|16 without 8 together "
+                     "with 2 or 4", stages);
   flash_msa_status st = check_dims(B, H, N, d);
   if (st != FLASH_MSA_OK) return st;
   if (Hkv < 1 || H % Hkv != 0)
@@ -569,7 +589,7 @@ static flash_msa_status bwd_impl(const void* q, const void* k, const void* v, co
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
       (reinterpret_cast<uintptr_t>(lse) & 3u))
     return set_error(FLASH_MSA_ERR_INVALID_ARG, "bwd: tensors must be 16-byte aligned");
-  const size_t need_ws = flash_msa_bwd_workspace_bytes(B, H, N, d);
+  const size_t need_ws = flash_msa_bwd_stages_workspace_bytes(B, H, N, d, stages);
   if (!workspace || workspace_bytes < need_ws || !aligned16(workspace))
     return set_error(FLASH_MSA_ERR_WORKSPACE, "bwd: workspace of %zu bytes required (got %zu)",
                      need_ws, workspace_bytes);
@@ -588,6 +608,10 @@ static flash_msa_status bwd_impl(const void* q, const void* k, const void* v, co
   a.dk = dk;
   a.dv = dv;
   a.dsum = static_cast<float*>(workspace);
+  // the accumulator follows the two vectors when the workspace holds it
+  a.dqacc = workspace_bytes >= flash_msa_bwd_workspace_bytes(B, H, N, d)
+                ? reinterpret_cast<float*>(static_cast<char*>(workspace) + vectors_bytes(B, H, N))
+                : nullptr;
   a.B = B;
   a.H = H;
   a.Hkv = Hkv;
@@ -615,8 +639,7 @@ flash_msa_status flash_msa_bwd_gqa(const void* q, const void* k, const void* v, 
                                    const flash_msa_mask_desc* mask, void* workspace,
                                    size_t workspace_bytes, void* stream) {
   return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, B, H, Hkv, N, d, scale, mask, workspace,
-                  workspace_bytes,
-                  FLASH_MSA_BWD_PREPROCESS | FLASH_MSA_BWD_DKDV | FLASH_MSA_BWD_DQ, stream);
+                  workspace_bytes, kDefaultStages, stream);
 }
 
 flash_msa_status flash_msa_set_wait_limit_ms(unsigned ms) {

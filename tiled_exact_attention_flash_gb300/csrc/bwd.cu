@@ -43,6 +43,7 @@ struct PreParams {
   const float* lse;
   float* nlse2;  // (B, H, NP)
   float* dsum;  // (B, H, NP)
+  float* dqacc;  // (B, H, NP, d) fp32 dQ accumulator to zero, or null
   int B, H, N, NP;
 };
 
@@ -53,6 +54,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreParams p) {
   const int h = blockIdx.y, b = blockIdx.z;
   const int r = threadIdx.x / kTpr, c = threadIdx.x % kTpr;
   const int64_t i = int64_t(blockIdx.x) * kRows + r;  // grid covers NP exactly
+  if (p.dqacc && i < p.NP) {  // zero this thread's 8 accumulator entries of row i
+    float4* z = reinterpret_cast<float4*>(p.dqacc + ((int64_t(b) * p.H + h) * p.NP + i) * HD + c * 8);
+    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   float acc = 0.f;
   if (i < p.N) {
     const int64_t off = ((int64_t(b) * p.N + i) * p.H + h) * HD + c * 8;
@@ -95,6 +101,8 @@ struct BwdParams {
   int B, H, N, NP;  // H: query heads
   int Hkv, G;       // key/value heads, query heads per key/value head
   int n_units;
+  int head_group;             // units are handed out in groups of this many heads
+  float* dqacc;               // fused: fp32 dQ accumulator (B, H, NP, d)
   unsigned long long* sched;  // work counter of this launch (see claim_unit)
   unsigned ticket;
   int wait_limit_ms;          // limit of any single bounded wait
@@ -110,29 +118,47 @@ struct BwdParams {
 // order 0 to 6 tiles all measure within 1% (3 kept).
 constexpr int kL2PrefetchTiles = 3;
 
-template <int HD, bool KS>
+// Modes of bwd_main_kernel.
+constexpr int kModeDq = 0;     // query-stationary dQ pass (deterministic backward)
+constexpr int kModeDkdv = 1;   // key-stationary dK/dV pass (deterministic backward)
+constexpr int kModeFused = 2;  // key-stationary dK/dV plus dQ partial products added
+                               // into the fp32 accumulator (default backward)
+
+template <int HD, int kMode>
 struct BwdLayout {
+  static constexpr bool KS = kMode != kModeDq;  // key-stationary
   static constexpr int kTileBytes = kTile * HD * 2;
-  // dK/dV: even (Q and dO of a tile in consecutive stages share a vector
-  // slot); dQ: one more stage of prefetch (no vectors to stage)
+  // key-stationary: even (Q and dO of a tile in consecutive stages share a
+  // vector slot); dQ: one more stage of prefetch (no vectors to stage)
   static constexpr int kStages = KS ? (HD == 128 ? 4 : 8) : (HD == 128 ? 6 : 12);
   static constexpr int kFixOff = 0;  // dK/dV: K and V tiles; dQ: the Q tile (dO lives in TMEM)
   static constexpr int kRingOff = (KS ? 2 : 1) * kTileBytes;
   static constexpr int kVecOff = kRingOff + kStages * kTileBytes;  // (stages/2) x 1 KB
-  static constexpr int kBarOff = kVecOff + (KS ? (kStages / 2) * 1024 : 0);  // vectors: dK/dV only
-  // kSFull / kPFull: two slots each.  dK/dV: kSFull (S^T computed),
-  // kSFull + 1 (dP^T computed), kPFull (P^T written), kPFull + 1 (dS^T
-  // written); dQ: kSFull, kPFull, kDpFree and kDsEmpty (= kSFull + 1, the dS
-  // columns of TMEM may be overwritten)
+  // fused: the dS tile of the current query tile, 128 keys x 128 queries
+  // bf16, the MN-major A operand of dQ = dS K (two 16 KB chunks of 64
+  // queries, one 128-byte swizzled row per key)
+  static constexpr int kDsOff = kVecOff + (KS ? (kStages / 2) * 1024 : 0);  // vectors: KS only
+  static constexpr int kDsBytes = kMode == kModeFused ? kTile * kTile * 2 : 0;
+  static constexpr int kBarOff = kDsOff + kDsBytes;
+  // kSFull / kPFull: two slots each.  dK/dV and fused: kSFull (S^T
+  // computed), kSFull + 1 (dP^T computed), kPFull (P^T written), kPFull + 1
+  // (dS^T written); dQ: kSFull, kPFull, kDpFree and kDsEmpty (= kSFull + 1,
+  // the dS columns of TMEM may be overwritten).  Fused: kDqFull (the tile's
+  // dQ partial product computed), kDqFree (read out of TMEM).
   static constexpr int kFixFull = 0, kFixEmpty = 1, kSFull = 2, kDsEmpty = 3, kPFull = 4,
-                       kDpFree = 6, kAccFull = 7, kAccEmpty = 8, kMmaDone = 9, kRingFull = 10,
-                       kRingEmpty = 10 + kStages, kUnitFull = 10 + 2 * kStages,
-                       kUnitEmpty = kUnitFull + 2;
+                       kDpFree = 6, kAccFull = 7, kAccEmpty = 8, kMmaDone = 9, kDqFull = 10,
+                       kDqFree = 11, kRingFull = 12, kRingEmpty = 12 + kStages,
+                       kUnitFull = 12 + 2 * kStages, kUnitEmpty = kUnitFull + 2;
   static constexpr int kNumBars = kUnitEmpty + 2;
   // misc: TMEM base address, abort flag, wait limit, (pad), the two
   // unit-queue slots
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kSmemBytes = kMiscOff + 24 + 1024;
+  // The fused layout fills the 227 KB a CTA may have, so it takes no
+  // alignment slack: the kernel checks that the dynamic shared memory starts
+  // on a 1024-byte boundary (as the 128-byte swizzle needs) and reports
+  // FLASH_MSA_ERR_UNSUPPORTED otherwise.
+  static constexpr int kSmemBytes = kMiscOff + 24 + (kMode == kModeFused ? 0 : 1024);
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
 template <int HD>
@@ -148,7 +174,9 @@ __device__ __forceinline__ void load_tile_2d(const CUtensorMap* m, uint32_t dst,
 template <bool kKeyStationary>
 __device__ __forceinline__ Unit bwd_decode(int u, const BwdParams& p) {
   const int H = kKeyStationary ? p.Hkv : p.H;
-  Unit un = decode_unit(u, p.B * H, H, p.list, p.status);
+  int bh, rank;
+  unit_order_grouped(u, p.B * H, p.list.n_blocks, p.head_group, bh, rank);
+  Unit un = decode_unit_at(bh, rank, H, p.list, p.status);
   if (kKeyStationary) un.n = un.n0 * p.G;
   return un;
 }
@@ -166,9 +194,10 @@ __device__ __forceinline__ InnerTile bwd_inner(const Unit& un, int t, const BwdP
   return inner_tile(un, t - g * un.n0, p.list, p.status);
 }
 
-template <int HD, bool KS>
+template <int HD, int kMode>
 __device__ __forceinline__ void init_bwd_barriers(uint64_t* bars) {
-  using L = BwdLayout<HD, KS>;
+  using L = BwdLayout<HD, kMode>;
+  constexpr bool KS = L::KS;
   // dQ: the producer's Q tile plus every elementwise warp's rows of dO
   mbar_init(smem_u32(bars + L::kFixFull), KS ? 1 : 1 + kEwWarps);
   mbar_init(smem_u32(bars + L::kFixEmpty), 1);
@@ -180,6 +209,8 @@ __device__ __forceinline__ void init_bwd_barriers(uint64_t* bars) {
   mbar_init(smem_u32(bars + L::kAccFull), 1);
   mbar_init(smem_u32(bars + L::kAccEmpty), kEwWarps);
   mbar_init(smem_u32(bars + L::kMmaDone), 1);
+  mbar_init(smem_u32(bars + L::kDqFull), 1);
+  mbar_init(smem_u32(bars + L::kDqFree), kEwWarps);
   for (int i = 0; i < L::kStages; ++i) {
     mbar_init(smem_u32(bars + L::kRingFull + i), 1);
     mbar_init(smem_u32(bars + L::kRingEmpty + i), 1);
@@ -191,9 +222,9 @@ __device__ __forceinline__ void init_bwd_barriers(uint64_t* bars) {
   fence_mbar_init();
 }
 
-template <int HD, bool KS>
+template <int HD, int kMode>
 __device__ __forceinline__ UnitQueue unit_queue(uint8_t* smem, uint64_t* bars) {
-  using L = BwdLayout<HD, KS>;
+  using L = BwdLayout<HD, kMode>;
   return UnitQueue{smem_u32(bars + L::kUnitFull), smem_u32(bars + L::kUnitEmpty),
                    reinterpret_cast<volatile int*>(smem + L::kMiscOff + 16), 0u};
 }
@@ -201,10 +232,11 @@ __device__ __forceinline__ UnitQueue unit_queue(uint8_t* smem, uint64_t* bars) {
 // Producer shared by both kernels.  Per unit: the stationary tiles (dkdv: K,
 // V of the key block; dq: Q of the query block), then per inner tile two ring
 // stages (dkdv: Q_t + its LSE2/D vectors, dO_t; dq: K_t, V_t).
-template <int HD, bool kKeyStationary>
+template <int HD, int kMode>
 __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint8_t* smem, uint64_t* bars,
                                              volatile int* abort_flag) {
-  using L = BwdLayout<HD, kKeyStationary>;
+  using L = BwdLayout<HD, kMode>;
+  constexpr bool kKeyStationary = L::KS;
   auto bar = [&](int i) { return smem_u32(bars + i); };
   const CUtensorMap* fix_a = kKeyStationary ? &p.tm_k : &p.tm_q;
   const CUtensorMap* fix_b = kKeyStationary ? &p.tm_v : &p.tm_do;
@@ -218,7 +250,7 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint8_t* smem, 
   for (int i = 0; i < L::kStages; ++i) last[i] = -1;
   int last_fix = -1;
   bool ok = true;
-  UnitQueue queue = unit_queue<HD, kKeyStationary>(smem, bars);
+  UnitQueue queue = unit_queue<HD, kMode>(smem, bars);
   // units are claimed one ahead (the dQ pass prefetches the next unit's dO)
   int u = queue_push(queue, p.sched, p.ticket, p.n_units, abort_flag, p.status);
   while (ok && u >= 0) {
@@ -348,7 +380,7 @@ __device__ __forceinline__ void mma_tmem_a(uint32_t d, uint32_t a_tmem, uint32_t
 template <int HD>
 __device__ __forceinline__ void dq_mma(const BwdParams& p, uint8_t* smem, uint64_t* bars,
                                        uint32_t tmem, volatile int* abort_flag) {
-  using L = BwdLayout<HD, false>;
+  using L = BwdLayout<HD, kModeDq>;
   auto bar = [&](int i) { return smem_u32(bars + i); };
   constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);
   constexpr uint32_t kIdAcc = idesc_bf16_f32(128, HD, false, true);
@@ -390,7 +422,7 @@ __device__ __forceinline__ void dq_mma(const BwdParams& p, uint8_t* smem, uint64
   Pos pos{0, 0};  // ring position of the current unit's first tile
   uint32_t ff_cnt = 0, pf_cnt = 0, sdp_cnt = 0, ae_cnt = 0;
   bool ok = true, pending_sdp = false;
-  UnitQueue queue = unit_queue<HD, false>(smem, bars);
+  UnitQueue queue = unit_queue<HD, kModeDq>(smem, bars);
   int u;
   while (ok && (u = queue_pop<false>(queue, abort_flag, p.status)) >= 0) {
     const Unit un = bwd_decode<false>(u, p);
@@ -454,7 +486,7 @@ __device__ __forceinline__ void dq_mma(const BwdParams& p, uint8_t* smem, uint64
 template <int HD>
 __device__ __forceinline__ void dkdv_mma(const BwdParams& p, uint8_t* smem, uint64_t* bars,
                                          uint32_t tmem, volatile int* abort_flag) {
-  using L = BwdLayout<HD, true>;
+  using L = BwdLayout<HD, kModeDkdv>;
   auto bar = [&](int i) { return smem_u32(bars + i); };
   constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);
   constexpr uint32_t kIdAcc = idesc_bf16_f32(128, HD, false, true);
@@ -470,7 +502,7 @@ __device__ __forceinline__ void dkdv_mma(const BwdParams& p, uint8_t* smem, uint
   };
   uint32_t cnt = 0, ff_cnt = 0, pf_cnt = 0, ae_cnt = 0;
   bool ok = true;
-  UnitQueue queue = unit_queue<HD, true>(smem, bars);
+  UnitQueue queue = unit_queue<HD, kModeDkdv>(smem, bars);
   int u;
   while (ok && (u = queue_pop<false>(queue, abort_flag, p.status)) >= 0) {
     const Unit un = bwd_decode<true>(u, p);
@@ -524,6 +556,103 @@ __device__ __forceinline__ void dkdv_mma(const BwdParams& p, uint8_t* smem, uint
   drain_bar(bar(L::kMmaDone), 0);
 }
 
+// MMA issuer of the fused kernel (key-stationary, like dkdv_mma, plus the dQ
+// partial product of every tile).  TMEM: S^T at A = [0,128), dP^T at
+// B = [128,256), dV at [256, 256+d), dK at [384, 384+d); dQ(t) = dS(t) K
+// (fp32, query rows in the lanes) is written over B once dK(t) has read
+// dS^T(t) from it, and the elementwise side reads it out (dq_free) before
+// dP^T(t+1) overwrites it.  dS(t) reaches the tensor core through shared
+// memory (MN-major A operand), written by the elementwise side next to dS^T.
+// Order per tile t:
+//   [p_full(t)] dV += P^T dO_t, release dO_t, S^T(t+1) -> s_full;
+//   [ds_full(t)] dK += dS^T Q_t, dQ(t) = dS K -> dq_full, release Q_t;
+//   [dq_free(t)] dP^T(t+1) -> dp_full.
+// K is read by the unit's last dQ product, so K and V are released after it.
+template <int HD>
+__device__ __forceinline__ void fused_mma(const BwdParams& p, uint8_t* smem, uint64_t* bars,
+                                          uint32_t tmem, volatile int* abort_flag) {
+  using L = BwdLayout<HD, kModeFused>;
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+  constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);
+  constexpr uint32_t kIdAcc = idesc_bf16_f32(128, HD, false, true);
+  constexpr uint32_t kIdDq = idesc_bf16_f32(128, HD, true, true);
+  const uint32_t tA = tmem, tB = tmem + 128, tDV = tmem + 256, tDK = tmem + 384;
+  const uint32_t fk = smem_u32(smem + L::kFixOff);
+  const uint32_t fv = fk + L::kTileBytes;
+  // dQ = dS K: A = dS (MN-major: 64-query chunks 16 KB apart, 16 keys = 2 KB
+  // per k-step), B = K (MN-major, like V in the forward's P V)
+  const uint32_t dq_a = sdesc_lo(smem_u32(smem + L::kDsOff), kTile * 128);
+  const uint32_t dq_b = sdesc_lo(fk, kTile * 128);
+  auto stage_addr = [&](uint32_t c) {
+    return smem_u32(smem + L::kRingOff + (c % L::kStages) * L::kTileBytes);
+  };
+  auto ring_wait = [&](uint32_t c, unsigned where) {
+    return wait_bar(bar(L::kRingFull + c % L::kStages), (c / L::kStages) & 1, abort_flag,
+                    p.status, where);
+  };
+  uint32_t cnt = 0, ff_cnt = 0, pf_cnt = 0, ae_cnt = 0, dq_cnt = 0;
+  bool ok = true, pending_drain = false;
+  UnitQueue queue = unit_queue<HD, kModeFused>(smem, bars);
+  int u;
+  while (ok && (u = queue_pop<false>(queue, abort_flag, p.status)) >= 0) {
+    const Unit un = bwd_decode<true>(u, p);
+    if (un.n == 0) continue;
+    if (!wait_bar(bar(L::kFixFull), ff_cnt & 1, abort_flag, p.status, 10)) break;
+    ++ff_cnt;
+    if (!ring_wait(cnt, 11)) break;
+    tc_fence_after();
+    mma_kmajor<HD>(tA, fk, stage_addr(cnt), kIdS);  // S^T(0) = K Q_0^T
+    mma_commit(bar(L::kSFull));
+    if (!ring_wait(cnt + 1, 12)) break;
+    // the previous unit's last dQ product must be out of B
+    if (pending_drain && !wait_bar(bar(L::kDqFree), dq_cnt++ & 1, abort_flag, p.status, 17)) break;
+    tc_fence_after();
+    mma_kmajor<HD>(tB, fv, stage_addr(cnt + 1), kIdS);  // dP^T(0) = V dO_0^T
+    mma_commit(bar(L::kSFull + 1));
+    for (int t = 0; t < un.n && ok; ++t) {
+      const uint32_t c = cnt + 2 * t;  // Q_t at c, dO_t at c + 1
+      const bool more = t + 1 < un.n;
+      if (t == 0) {
+        if (!wait_bar(bar(L::kAccEmpty), (ae_cnt & 1) ^ 1, abort_flag, p.status, 13)) { ok = false; break; }
+        ++ae_cnt;
+      }
+      if (!wait_bar(bar(L::kPFull), pf_cnt & 1, abort_flag, p.status, 14)) { ok = false; break; }
+      tc_fence_after();
+      mma_tmem_a(tDV, tA, stage_addr(c + 1), kIdAcc, t > 0);  // dV += P^T dO_t
+      mma_commit(bar(L::kRingEmpty + (c + 1) % L::kStages));
+      if (more) {
+        if (!ring_wait(c + 2, 11)) { ok = false; break; }
+        tc_fence_after();
+        mma_kmajor<HD>(tA, fk, stage_addr(c + 2), kIdS);  // S^T(t+1) over P^T(t)
+        mma_commit(bar(L::kSFull));
+      }
+      if (!wait_bar(bar(L::kPFull + 1), pf_cnt & 1, abort_flag, p.status, 16)) { ok = false; break; }
+      ++pf_cnt;
+      tc_fence_after();
+      mma_tmem_a(tDK, tB, stage_addr(c), kIdAcc, t > 0);  // dK += dS^T Q_t
+#pragma unroll
+      for (int kk = 0; kk < kTile / 16; ++kk)  // dQ(t) = dS K over dS^T(t)
+        mma_ss(tB, dq_a + kk * (2048 >> 4), dq_b + kk * (2048 >> 4), kIdDq, kk > 0 ? 1u : 0u);
+      mma_commit(bar(L::kDqFull));
+      mma_commit(bar(L::kRingEmpty + c % L::kStages));
+      if (!more) mma_commit(bar(L::kFixEmpty));  // K and V are not read again
+      if (more) {
+        if (!wait_bar(bar(L::kDqFree), dq_cnt++ & 1, abort_flag, p.status, 17)) { ok = false; break; }
+        if (!ring_wait(c + 3, 12)) { ok = false; break; }
+        tc_fence_after();
+        mma_kmajor<HD>(tB, fv, stage_addr(c + 3), kIdS);  // dP^T(t+1) over dQ(t)
+        mma_commit(bar(L::kSFull + 1));
+      }
+    }
+    if (!ok) break;
+    cnt += 2 * un.n;
+    mma_commit(bar(L::kAccFull));
+    pending_drain = true;
+  }
+  mma_commit(bar(L::kMmaDone));
+  drain_bar(bar(L::kMmaDone), 0);
+}
+
 // Write the warpgroup's HD/2 fp32 accumulator columns of this thread's row
 // (TMEM address taddr), times `mul`, as bf16 to dst (the row's first element
 // of the piece); rows of consecutive lanes are `stride` bytes apart.
@@ -565,7 +694,7 @@ template <int HD>
 __device__ __forceinline__ void dkdv_elementwise(const BwdParams& p, uint8_t* smem,
                                                  uint64_t* bars, uint32_t tmem, int g,
                                                  volatile int* abort_flag) {
-  using L = BwdLayout<HD, true>;
+  using L = BwdLayout<HD, kModeDkdv>;
   auto bar = [&](int i) { return smem_u32(bars + i); };
   const int wq = int(warp_id()) & 3;
   const int row = wq * 32 + int(lane_id());
@@ -574,7 +703,7 @@ __device__ __forceinline__ void dkdv_elementwise(const BwdParams& p, uint8_t* sm
   const uint32_t tDV = tmem + lane_off + 256, tDK = tmem + lane_off + 384;
   const float sl2 = p.scale_log2;
   uint32_t sp_cnt = 0, af_cnt = 0, cnt = 0;
-  UnitQueue queue = unit_queue<HD, true>(smem, bars);
+  UnitQueue queue = unit_queue<HD, kModeDkdv>(smem, bars);
   while (true) {
     const int u = queue_pop<true>(queue, abort_flag, p.status);
     if (u < 0) return;
@@ -681,6 +810,183 @@ __device__ __forceinline__ void dkdv_elementwise(const BwdParams& p, uint8_t* sm
   }
 }
 
+// Elementwise warpgroups of the fused kernel.  As in dkdv_elementwise, a
+// thread owns key row j of the key tile and warpgroup g the query columns
+// [64 g, 64 g + 64) of each query tile, in two passes per tile: P^T, then
+// dS^T.  Pass 2 also writes the thread's dS values (its key row, 64 queries,
+// bf16) into the dS tile in shared memory, the A operand of dQ = dS K.  After
+// the next tile's pass 1 (or at the end of the unit) the warpgroup reads its
+// half of the tile's dQ partial product out of TMEM -- query row
+// 32 (warp % 4) + lane, columns [d/2 g, d/2 g + d/2) -- releases the columns
+// and adds it into the fp32 accumulator with vector atomics.  Order per
+// tile t: pass 2 (t), pass 1 (t + 1), drain (t).
+template <int HD>
+__device__ __forceinline__ void fused_elementwise(const BwdParams& p, uint8_t* smem,
+                                                  uint64_t* bars, uint32_t tmem, int g,
+                                                  volatile int* abort_flag) {
+  using L = BwdLayout<HD, kModeFused>;
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+  const int wq = int(warp_id()) & 3;
+  const int row = wq * 32 + int(lane_id());
+  const uint32_t lane_off = uint32_t(wq * 32) << 16;
+  const uint32_t tA = tmem + lane_off + 64 * g, tB = tA + 128;
+  const uint32_t tDV = tmem + lane_off + 256, tDK = tmem + lane_off + 384;
+  const uint32_t tDQ = tmem + lane_off + 128 + g * (HD / 2);
+  // this key row of the dS tile: chunk g, 128 bytes, 16-byte unit u stored at
+  // unit position u ^ (row % 8) (the 128-byte swizzle the descriptor names)
+  uint8_t* ds_row = smem + L::kDsOff + g * (kTile * 128) + row * 128;
+  const float sl2 = p.scale_log2;
+  uint32_t s1_cnt = 0, s2_cnt = 0, af_cnt = 0, dq_cnt = 0, cnt = 0;
+  UnitQueue queue = unit_queue<HD, kModeFused>(smem, bars);
+  auto vec_at = [&](uint32_t c) {  // -LSE log2(e) | D of the query tile at ring position c
+    return reinterpret_cast<const float*>(smem + L::kVecOff + ((c % L::kStages) / 2) * 1024);
+  };
+  uint32_t sv[64];  // P^T of the current tile (fp32), from pass 1 to pass 2
+  // pass 1: P^T = exp2(scale*log2e * S^T - LSE*log2e) on live entries, bf16
+  // to columns [64 g, 64 g + 32) of A, p_full
+  auto pass1 = [&](const Unit& un, int t, int64_t j, const float* vec) -> bool {
+    int hq;
+    const InnerTile it = bwd_inner<true>(un, t, p, hq);
+    int lo = 0, hi = kTile - 1;
+    if (it.dead) hi = -1;
+    else if (it.partial) col_live_range(j, it.blk, un.ob, p.N, p.mask, lo, hi);
+    prefetch_tile_bits(p.list, it.slot, row);
+    const bool ok = wait_bar(bar(L::kSFull), s1_cnt & 1, abort_flag, p.status, 20);
+    if (!__all_sync(0xFFFFFFFFu, ok)) return false;
+    ++s1_cnt;
+    tc_fence_after();
+    tmem_ld_x64(tA, sv);
+    if (it.partial || it.dead) {  // dead entries: S^T = -inf, so P^T = 0 below (scale > 0)
+#pragma unroll
+      for (int e = 0; e < 64; ++e)
+        if (64 * g + e < lo || 64 * g + e > hi) sv[e] = kNegInfBits;
+      if (it.slot >= 0) {  // bit-packed mask tile: this key row's bits over 64 queries
+        uint32_t bw[2];
+        load_tile_bits<2>(p.list, it.slot, row, 2 * g, bw);
+#pragma unroll
+        for (int e = 0; e < 64; ++e)
+          if (!((bw[e >> 5] >> (e & 31)) & 1u)) sv[e] = kNegInfBits;
+      }
+    }
+    uint32_t pp[32];
+    float4 l4n = *reinterpret_cast<const float4*>(vec + 64 * g);
+#pragma unroll
+    for (int x = 0; x < 64; x += 4) {
+      const float4 l4 = l4n;
+      if (x + 4 < 64)  // next group's -LSE, loaded one group ahead
+        l4n = *reinterpret_cast<const float4*>(vec + 64 * g + x + 4);
+      const float nl[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+      for (int e = 0; e < 4; e += 2) {
+        float x0, x1;
+        fma2(x0, x1, __uint_as_float(sv[x + e]), __uint_as_float(sv[x + e + 1]), sl2, sl2,
+             nl[e], nl[e + 1]);
+        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+        sv[x + e] = __float_as_uint(p0);
+        sv[x + e + 1] = __float_as_uint(p1);
+        pp[(x + e) / 2] = pack_bf16x2(p0, p1);
+      }
+    }
+    tmem_st_x32(tA, pp);
+    tmem_wait_st();
+    warp_arrive(bar(L::kPFull));
+    return true;
+  };
+  // pass 2: dS^T = P^T o (dP^T - D), bf16 to columns [64 g, 64 g + 32) of B
+  // and to this key row of the dS tile, ds_full
+  auto pass2 = [&](const float* vec) -> bool {
+    const bool ok = wait_bar(bar(L::kSFull + 1), s2_cnt & 1, abort_flag, p.status, 24);
+    if (!__all_sync(0xFFFFFFFFu, ok)) return false;
+    ++s2_cnt;
+    tc_fence_after();
+    uint32_t dpv[64];
+    tmem_ld_x64(tB, dpv);
+    uint32_t dd[32];
+    float4 d4n = *reinterpret_cast<const float4*>(vec + 128 + 64 * g);
+#pragma unroll
+    for (int x = 0; x < 64; x += 4) {
+      const float4 d4 = d4n;
+      if (x + 4 < 64) d4n = *reinterpret_cast<const float4*>(vec + 128 + 64 * g + x + 4);
+      const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+      for (int e = 0; e < 4; e += 2) {
+        float u0, u1, d0, d1;
+        sub2(u0, u1, __uint_as_float(dpv[x + e]), __uint_as_float(dpv[x + e + 1]), dv[e],
+             dv[e + 1]);
+        mul2(d0, d1, __uint_as_float(sv[x + e]), __uint_as_float(sv[x + e + 1]), u0, u1);
+        dd[(x + e) / 2] = pack_bf16x2(d0, d1);
+      }
+    }
+    tmem_st_x32(tB, dd);
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      *reinterpret_cast<uint4*>(ds_row + ((q ^ (row & 7)) << 4)) =
+          make_uint4(dd[4 * q], dd[4 * q + 1], dd[4 * q + 2], dd[4 * q + 3]);
+    fence_proxy_async_smem();  // the tensor core reads the dS tile through the async proxy
+    tmem_wait_st();
+    warp_arrive(bar(L::kPFull + 1));
+    return true;
+  };
+  // drain: the warpgroup's half of dQ(t) into the fp32 accumulator (unscaled)
+  auto drain = [&](const Unit& un, int t) -> bool {
+    int hq;
+    const InnerTile it = bwd_inner<true>(un, t, p, hq);
+    const bool ok = wait_bar(bar(L::kDqFull), dq_cnt & 1, abort_flag, p.status, 25);
+    if (!__all_sync(0xFFFFFFFFu, ok)) return false;
+    ++dq_cnt;
+    tc_fence_after();
+    const int64_t i = int64_t(it.blk) * kTile + row;  // query row of this lane
+    const bool live = !it.dead && i < p.N;
+    char* dst = reinterpret_cast<char*>(p.dqacc + ((int64_t(un.b) * p.H + hq) * p.NP + i) * HD +
+                                        g * (HD / 2));
+    constexpr int kHalves = HD / 64;  // 32 columns at a time
+#pragma unroll
+    for (int q = 0; q < kHalves; ++q) {
+      uint32_t v[32];
+      tmem_ld_x32(tDQ + 32 * q, v);
+      if (q == kHalves - 1) warp_arrive(bar(L::kDqFree));
+      uint4 c[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) c[k] = make_uint4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+      add_rows_transposed<8, 2>(c, dst + q * 128, int64_t(HD) * 4, live);
+    }
+    return true;
+  };
+  while (true) {
+    const int u = queue_pop<true>(queue, abort_flag, p.status);
+    if (u < 0) return;
+    const Unit un = bwd_decode<true>(u, p);
+    const int64_t j = int64_t(un.ob) * kTile + row;  // key token
+    const bool valid = j < p.N;
+    __nv_bfloat16* dk_row = p.out_a + ((int64_t(un.b) * p.N + j) * p.Hkv + un.h) * HD;
+    __nv_bfloat16* dv_row = p.out_b + ((int64_t(un.b) * p.N + j) * p.Hkv + un.h) * HD;
+    if (un.n == 0) {
+      if (g == 0) {
+        zero_row(dk_row, HD, valid);
+        zero_row(dv_row, HD, valid);
+      }
+      continue;
+    }
+    if (!pass1(un, 0, j, vec_at(cnt))) return;
+    for (int t = 0; t < un.n; ++t) {
+      const uint32_t c = cnt + 2 * t;
+      if (!pass2(vec_at(c))) return;
+      if (t + 1 < un.n && !pass1(un, t + 1, j, vec_at(c + 2))) return;
+      if (!drain(un, t)) return;
+    }
+    cnt += 2 * un.n;
+    const bool ok = wait_bar(bar(L::kAccFull), af_cnt & 1, abort_flag, p.status, 21);
+    if (!__all_sync(0xFFFFFFFFu, ok)) return;
+    ++af_cnt;
+    tc_fence_after();
+    // warpgroup g writes dV and dK columns [d/2 g, d/2 (g + 1))
+    const int64_t stride = int64_t(p.Hkv) * HD * 2;  // bytes between consecutive key rows
+    store_acc_piece<HD>(tDV + g * (HD / 2), 1.f, dv_row + g * (HD / 2), stride, valid);
+    store_acc_piece<HD>(tDK + g * (HD / 2), p.scale, dk_row + g * (HD / 2), stride, valid);
+    warp_arrive(bar(L::kAccEmpty));
+  }
+}
+
 // Elementwise warpgroups of bwd_dq: thread = query row i of the query tile,
 // warpgroup g = key columns [64 g, 64 g + 64).  Per unit the warpgroups first
 // write the row's dO into TMEM (warpgroup g: head-dimension half g).  Per key
@@ -691,7 +997,7 @@ __device__ __forceinline__ void dkdv_elementwise(const BwdParams& p, uint8_t* sm
 template <int HD>
 __device__ __forceinline__ void dq_elementwise(const BwdParams& p, uint8_t* smem, uint64_t* bars,
                                                uint32_t tmem, int g, volatile int* abort_flag) {
-  using L = BwdLayout<HD, false>;
+  using L = BwdLayout<HD, kModeDq>;
   auto bar = [&](int i) { return smem_u32(bars + i); };
   const int wq = int(warp_id()) & 3;
   const int row = wq * 32 + int(lane_id());
@@ -701,7 +1007,7 @@ __device__ __forceinline__ void dq_elementwise(const BwdParams& p, uint8_t* smem
   const uint32_t tDO = tmem + lane_off + 448 + (HD / 4) * g;
   const float sl2 = p.scale_log2;
   uint32_t sp_cnt = 0, af_cnt = 0, fe_cnt = 0, ds_cnt = 0;
-  UnitQueue queue = unit_queue<HD, false>(smem, bars);
+  UnitQueue queue = unit_queue<HD, kModeDq>(smem, bars);
   // next unit with live key tiles; units without any get zero dQ rows here
   auto next = [&](Unit& un) -> bool {
     while (true) {
@@ -812,10 +1118,16 @@ __device__ __forceinline__ void dq_elementwise(const BwdParams& p, uint8_t* smem
   }
 }
 
-template <int HD, bool kKeyStationary>
+template <int HD, int kMode>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_constant__ BwdParams p) {
-  using L = BwdLayout<HD, kKeyStationary>;
+  using L = BwdLayout<HD, kMode>;
   extern __shared__ uint8_t smem_raw[];
+  if (kMode == kModeFused && (smem_u32(smem_raw) & 1023u) != 0) {
+    // no room for alignment slack (see BwdLayout): refuse, uniformly, before
+    // any barrier or TMEM allocation
+    if (threadIdx.x == 0) record_status(p.status, FLASH_MSA_ERR_UNSUPPORTED, 0xF5);
+    return;
+  }
   uint8_t* smem = align_1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
@@ -829,7 +1141,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
   if (threadIdx.x == 0) {
     abort_flag[0] = 0;
     abort_flag[1] = p.wait_limit_ms;
-    init_bwd_barriers<HD, kKeyStationary>(bars);
+    init_bwd_barriers<HD, kMode>(bars);
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&p.tm_q);
@@ -843,16 +1155,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
   const uint32_t tmem = *tmem_slot;
   if (warp < 4) regs_shrink<80>();  // 384 x 168 at launch: 128 x 80 + 256 x 208
   if (warp == 0) {
-    if (lane == 0) bwd_producer<HD, kKeyStationary>(p, smem, bars, abort_flag);
+    if (lane == 0) bwd_producer<HD, kMode>(p, smem, bars, abort_flag);
   } else if (warp == 1) {
     if (lane == 0) {
-      if (kKeyStationary) dkdv_mma<HD>(p, smem, bars, tmem, abort_flag);
+      if (kMode == kModeFused) fused_mma<HD>(p, smem, bars, tmem, abort_flag);
+      else if (kMode == kModeDkdv) dkdv_mma<HD>(p, smem, bars, tmem, abort_flag);
       else dq_mma<HD>(p, smem, bars, tmem, abort_flag);
     }
   } else if (warp >= 4) {
     const int g = (warp - 4) >> 2;  // elementwise warpgroup: columns [64 g, 64 g + 64)
     regs_grow<208>();
-    if (kKeyStationary) dkdv_elementwise<HD>(p, smem, bars, tmem, g, abort_flag);
+    if (kMode == kModeFused) fused_elementwise<HD>(p, smem, bars, tmem, g, abort_flag);
+    else if (kMode == kModeDkdv) dkdv_elementwise<HD>(p, smem, bars, tmem, g, abort_flag);
     else dq_elementwise<HD>(p, smem, bars, tmem, g, abort_flag);
   }
   tc_fence_before();
@@ -863,20 +1177,54 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
   }
 }
 
+// dQ = scale * accumulator, fp32 (B, H, NP, d) -> bf16 (B, N, H, d); one
+// thread per 8 elements, consecutive threads along the output.
+template <int HD>
+__global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ acc,
+                                                         __nv_bfloat16* __restrict__ dq, int B,
+                                                         int H, int N, int NP, float scale) {
+  constexpr int kChunks = HD / 8;
+  const int64_t total = int64_t(B) * N * H * kChunks;
+  for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
+       e += int64_t(gridDim.x) * blockDim.x) {
+    const int c = int(e % kChunks);
+    const int64_t r = e / kChunks;  // output row (b, i, h)
+    const int h = int(r % H);
+    const int64_t bi = r / H;
+    const int i = int(bi % N);
+    const int b = int(bi / N);
+    const float4* src =
+        reinterpret_cast<const float4*>(acc + ((int64_t(b) * H + h) * NP + i) * HD + c * 8);
+    const float4 x = __ldg(src), y = __ldg(src + 1);
+    uint4 w;
+    w.x = pack_bf16x2(x.x * scale, x.y * scale);
+    w.y = pack_bf16x2(x.z * scale, x.w * scale);
+    w.z = pack_bf16x2(y.x * scale, y.y * scale);
+    w.w = pack_bf16x2(y.z * scale, y.w * scale);
+    *reinterpret_cast<uint4*>(dq + r * HD + c * 8) = w;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // host launcher
 // ---------------------------------------------------------------------------
+// Heads per group of the fused kernel's unit order: the CTAs running at any
+// time then add into the accumulators of about this many bytes of heads
+// (plus their streamed Q and dO tiles), which stay resident in the 129 MB L2.
+constexpr int64_t kFusedGroupBytes = int64_t(48) << 20;
+
 template <int HD>
 static flash_msa_status launch_bwd_hd(const BwdLaunch& a, cudaStream_t stream) {
-  using LK = BwdLayout<HD, true>;
-  using LQ = BwdLayout<HD, false>;
+  using LK = BwdLayout<HD, kModeDkdv>;
+  using LQ = BwdLayout<HD, kModeDq>;
+  using LF = BwdLayout<HD, kModeFused>;
   const int nb = a.rows.n_blocks;
   const int NP = nb * kTile;
-  float* nlse2 = a.dsum;                        // workspace: [nlse2 | dsum]
+  float* nlse2 = a.dsum;                        // workspace: [nlse2 | dsum | dQ accumulator]
   float* dsum = a.dsum + int64_t(a.B) * a.H * NP;
   if (a.stages & FLASH_MSA_BWD_PREPROCESS) {
     PreParams pp{reinterpret_cast<const __nv_bfloat16*>(a.o),
-                 reinterpret_cast<const __nv_bfloat16*>(a.dout), a.lse, nlse2, dsum,
+                 reinterpret_cast<const __nv_bfloat16*>(a.dout), a.lse, nlse2, dsum, a.dqacc,
                  a.B, a.H, int(a.N), NP};
     constexpr int kRows = 256 / (HD / 8);
     dim3 grid((NP + kRows - 1) / kRows, a.H, a.B);
@@ -886,12 +1234,15 @@ static flash_msa_status launch_bwd_hd(const BwdLaunch& a, cudaStream_t stream) {
   BwdParams p;
   memset(&p, 0, sizeof(p));
   flash_msa_status st;
-  if ((st = make_tile_map(&p.tm_q, a.q, a.B, a.N, a.H, HD)) != FLASH_MSA_OK) return st;
-  if ((st = make_tile_map(&p.tm_k, a.k, a.B, a.N, a.Hkv, HD)) != FLASH_MSA_OK) return st;
-  if ((st = make_tile_map(&p.tm_v, a.v, a.B, a.N, a.Hkv, HD)) != FLASH_MSA_OK) return st;
-  if ((st = make_tile_map(&p.tm_do, a.dout, a.B, a.N, a.H, HD)) != FLASH_MSA_OK) return st;
+  if (a.stages & (FLASH_MSA_BWD_DKDV | FLASH_MSA_BWD_DQ | FLASH_MSA_BWD_FUSED)) {
+    if ((st = make_tile_map(&p.tm_q, a.q, a.B, a.N, a.H, HD)) != FLASH_MSA_OK) return st;
+    if ((st = make_tile_map(&p.tm_k, a.k, a.B, a.N, a.Hkv, HD)) != FLASH_MSA_OK) return st;
+    if ((st = make_tile_map(&p.tm_v, a.v, a.B, a.N, a.Hkv, HD)) != FLASH_MSA_OK) return st;
+    if ((st = make_tile_map(&p.tm_do, a.dout, a.B, a.N, a.H, HD)) != FLASH_MSA_OK) return st;
+  }
   p.nlse2 = nlse2;
   p.dsum = dsum;
+  p.dqacc = a.dqacc;
   p.dout = reinterpret_cast<const __nv_bfloat16*>(a.dout);
   p.B = a.B;
   p.H = a.H;
@@ -904,11 +1255,6 @@ static flash_msa_status launch_bwd_hd(const BwdLaunch& a, cudaStream_t stream) {
   p.mask = a.mask;
   p.status = a.status;
   p.wait_limit_ms = int(wait_limit_ms());
-  auto prep = [&](const void* kern, int which) -> flash_msa_status {
-    const int bytes = which == 0 ? LK::kSmemBytes : LQ::kSmemBytes;
-    return enable_smem(kern, bytes, 2 + 2 * which + (HD == 128 ? 1 : 0),
-                       "cudaFuncSetAttribute(bwd)");
-  };
   // persistent launches: one CTA per SM (fewer for small problems), units
   // handed out in order by a counter set up just before each kernel
   const int sms = sm_count();
@@ -920,27 +1266,63 @@ static flash_msa_status launch_bwd_hd(const BwdLaunch& a, cudaStream_t stream) {
     p.ticket = c.ticket;
     return r;
   };
+  // which: bit of enable_smem for this kernel instantiation
+  auto launch = [&](const void* kern, int smem_bytes, unsigned which, auto kernel_fn,
+                    const char* what) -> flash_msa_status {
+    flash_msa_status r = enable_smem(kern, smem_bytes, which, "cudaFuncSetAttribute(bwd)");
+    if (r != FLASH_MSA_OK) return r;
+    if ((r = claim_counter()) != FLASH_MSA_OK) return r;
+    const int grid = p.n_units < sms ? p.n_units : sms;
+    kernel_fn<<<grid, kBwdThreads, smem_bytes, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return set_cuda_error(what);
+    return FLASH_MSA_OK;
+  };
+  const unsigned hd_bit = HD == 128 ? 1u : 0u;
   if (a.stages & FLASH_MSA_BWD_DKDV) {
-    if ((st = prep(reinterpret_cast<const void*>(&bwd_main_kernel<HD, true>), 0)) != FLASH_MSA_OK) return st;
-    if ((st = claim_counter()) != FLASH_MSA_OK) return st;
     p.list = a.cols;
     p.n_units = a.B * a.Hkv * nb;
+    p.head_group = a.B * a.Hkv;  // rank-major over all heads
     p.out_a = reinterpret_cast<__nv_bfloat16*>(a.dk);
     p.out_b = reinterpret_cast<__nv_bfloat16*>(a.dv);
-    const int grid = p.n_units < sms ? p.n_units : sms;
-    bwd_main_kernel<HD, true><<<grid, kBwdThreads, LK::kSmemBytes, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return set_cuda_error("bwd_dkdv launch");
+    if ((st = launch(reinterpret_cast<const void*>(&bwd_main_kernel<HD, kModeDkdv>),
+                     LK::kSmemBytes, 2 + hd_bit, bwd_main_kernel<HD, kModeDkdv>,
+                     "bwd_dkdv launch")) != FLASH_MSA_OK)
+      return st;
   }
   if (a.stages & FLASH_MSA_BWD_DQ) {
-    if ((st = prep(reinterpret_cast<const void*>(&bwd_main_kernel<HD, false>), 1)) != FLASH_MSA_OK) return st;
-    if ((st = claim_counter()) != FLASH_MSA_OK) return st;
     p.list = a.rows;
     p.n_units = a.B * a.H * nb;
+    p.head_group = a.B * a.H;
     p.out_a = reinterpret_cast<__nv_bfloat16*>(a.dq);
     p.out_b = nullptr;
-    const int grid = p.n_units < sms ? p.n_units : sms;
-    bwd_main_kernel<HD, false><<<grid, kBwdThreads, LQ::kSmemBytes, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return set_cuda_error("bwd_dq launch");
+    if ((st = launch(reinterpret_cast<const void*>(&bwd_main_kernel<HD, kModeDq>),
+                     LQ::kSmemBytes, 4 + hd_bit, bwd_main_kernel<HD, kModeDq>,
+                     "bwd_dq launch")) != FLASH_MSA_OK)
+      return st;
+  }
+  if (a.stages & FLASH_MSA_BWD_FUSED) {
+    p.list = a.cols;
+    p.n_units = a.B * a.Hkv * nb;
+    // key/value heads per group: accumulator (G query heads) plus Q and dO
+    const int64_t per_head = int64_t(NP) * HD * (4 + 2 + 2) * p.G;
+    int grp = int(kFusedGroupBytes / (per_head > 0 ? per_head : 1));
+    if (grp < 1) grp = 1;
+    if (grp > a.B * a.Hkv) grp = a.B * a.Hkv;
+    p.head_group = grp;
+    p.out_a = reinterpret_cast<__nv_bfloat16*>(a.dk);
+    p.out_b = reinterpret_cast<__nv_bfloat16*>(a.dv);
+    if ((st = launch(reinterpret_cast<const void*>(&bwd_main_kernel<HD, kModeFused>),
+                     LF::kSmemBytes, 6 + hd_bit, bwd_main_kernel<HD, kModeFused>,
+                     "bwd_fused launch")) != FLASH_MSA_OK)
+      return st;
+  }
+  if (a.stages & FLASH_MSA_BWD_DQ_CONVERT) {
+    const int64_t chunks = int64_t(a.B) * a.N * a.H * (HD / 8);
+    int64_t blocks = (chunks + 255) / 256;
+    if (blocks > int64_t(sms) * 16) blocks = int64_t(sms) * 16;
+    dq_convert_kernel<HD><<<int(blocks), 256, 0, stream>>>(
+        a.dqacc, reinterpret_cast<__nv_bfloat16*>(a.dq), a.B, a.H, int(a.N), NP, a.scale);
+    if (cudaGetLastError() != cudaSuccess) return set_cuda_error("dq_convert launch");
   }
   return FLASH_MSA_OK;
 }

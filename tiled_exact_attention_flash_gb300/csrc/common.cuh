@@ -281,6 +281,28 @@ __device__ __forceinline__ void unit_order(int u, int BH, int& bh, int& rank) {
   bh = u - rank * BH;
 }
 
+// Launch order in groups of heads: the units of heads [G g, G g + G) come
+// before those of the next group, rank-major inside the group (the last group
+// may be smaller).  G = BH is the plain rank-major order of unit_order.  With
+// a small G the CTAs running at any time work on a few heads only, whose
+// streamed tiles and accumulators then stay in L2.
+__device__ __forceinline__ void unit_order_grouped(int u, int BH, int n_blocks, int G, int& bh,
+                                                   int& rank) {
+  const int per_group = G * n_blocks;
+  const int full = BH / G;
+  const int gi = u / per_group;
+  if (gi < full) {
+    const int rem = u - gi * per_group;
+    rank = rem / G;
+    bh = gi * G + (rem - rank * G);
+  } else {
+    const int gl = BH - full * G;
+    const int rem = u - full * per_group;
+    rank = rem / gl;
+    bh = full * G + (rem - rank * gl);
+  }
+}
+
 // Unit at (bh, rank) of a launch over heads of H (b = bh / H).
 __device__ __forceinline__ Unit decode_unit_at(int bh, int rank, int H, const ListParams& L,
                                                unsigned* status) {
@@ -377,12 +399,10 @@ __device__ __forceinline__ InnerTile inner_tile(const Unit& un, int t, const Lis
 // for every row of the lane group), so that every store instruction writes
 // kG * 16 contiguous bytes of each of 32 / kG rows.  row_ok: whether this
 // lane's row exists.
-template <int kC, int kG = kC>
-__device__ __forceinline__ void store_rows_transposed(uint4 (&c)[kC], char* dst, int64_t stride,
-                                                      bool row_ok) {
+template <int kC, int kG>
+__device__ __forceinline__ void transpose_chunks(uint4 (&c)[kC]) {
   static_assert(kC % kG == 0 && (kG & (kG - 1)) == 0, "kG: a power of two dividing kC");
-  const int lane = int(threadIdx.x & 31);
-  const int i = lane & (kG - 1);
+  const int i = int(threadIdx.x & 31) & (kG - 1);
 #pragma unroll
   for (int q = 0; q < kC; q += kG) {
 #pragma unroll
@@ -403,6 +423,14 @@ __device__ __forceinline__ void store_rows_transposed(uint4 (&c)[kC], char* dst,
       }
     }
   }
+}
+
+template <int kC, int kG = kC>
+__device__ __forceinline__ void store_rows_transposed(uint4 (&c)[kC], char* dst, int64_t stride,
+                                                      bool row_ok) {
+  transpose_chunks<kC, kG>(c);
+  const int lane = int(threadIdx.x & 31);
+  const int i = lane & (kG - 1);
   const uint32_t ok = __ballot_sync(0xFFFFFFFFu, row_ok);
   const int base = lane - i;
 #pragma unroll
@@ -411,6 +439,30 @@ __device__ __forceinline__ void store_rows_transposed(uint4 (&c)[kC], char* dst,
     for (int k = 0; k < kG; ++k)
       if ((ok >> (base + k)) & 1u)
         *reinterpret_cast<uint4*>(dst + int64_t(k - i) * stride + (q + i) * 16) = c[q + k];
+}
+
+// The same pattern for fp32 accumulation: chunk c[k] holds four fp32 values
+// to be ADDED (vector atomics, performed in L2) to the lane's row at
+// dst + 16 k bytes; after the transpose every atomic instruction of the warp
+// covers kG * 16 contiguous bytes of each of 32 / kG rows.
+template <int kC, int kG>
+__device__ __forceinline__ void add_rows_transposed(uint4 (&c)[kC], char* dst, int64_t stride,
+                                                    bool row_ok) {
+  transpose_chunks<kC, kG>(c);
+  const int lane = int(threadIdx.x & 31);
+  const int i = lane & (kG - 1);
+  const uint32_t ok = __ballot_sync(0xFFFFFFFFu, row_ok);
+  const int base = lane - i;
+#pragma unroll
+  for (int q = 0; q < kC; q += kG)
+#pragma unroll
+    for (int k = 0; k < kG; ++k)
+      if ((ok >> (base + k)) & 1u) {
+        const uint4 v = c[q + k];
+        atomicAdd(reinterpret_cast<float4*>(dst + int64_t(k - i) * stride + (q + i) * 16),
+                  make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
+                              __uint_as_float(v.w)));
+      }
 }
 
 // Bits of one row of a bit tile (bit-packed masks): kWords 32-bit words

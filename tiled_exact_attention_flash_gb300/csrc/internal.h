@@ -57,7 +57,8 @@ struct BwdLaunch {
   const void *q, *k, *v, *o, *dout;
   const float* lse;
   void *dq, *dk, *dv;
-  float* dsum;  // workspace: [-LSE * log2(e) | D], fp32 (B, H, padded N) each
+  float* dsum;   // workspace: [-LSE * log2(e) | D], fp32 (B, H, padded N) each
+  float* dqacc;  // workspace: fp32 dQ accumulator (B, H, padded N, d), or null
   int B, H, d;
   int Hkv;      // key/value heads
   int64_t N;
