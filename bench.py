@@ -415,14 +415,21 @@ def run_ours(args):
     kernel_flops = {"fwd": fwd_flops}
     kernel_flops.update({name: f * fwd_flops for name, _, f in BWD_LAUNCHES if f > 0})
     dominant = max(kernel_flops, key=lambda n: per_kernel[n])
+    # the kernels are timed inside a long loop of back-to-back steps (about a
+    # second and a half at the default workload), under the power cap: the
+    # sustained bf16 figure is their roofline; the burst figure is reported
+    # beside it (the *_pct_peak keys)
     peak = peaks["bf16_tflops"]
+    peak_sus = peaks.get("bf16_tflops_sustained", peak)
     achieved = kernel_flops[dominant] / (per_kernel[dominant] * 1e-3) / 1e12
     roofline = {"kernel": dominant, "bound": "tensor", "achieved": round(achieved, 1),
-                "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                "peak_source": f"{peak_src} bf16_tflops (burst)",
+                "peak": peak_sus, "unit": "TFLOP/s", "frac": round(achieved / peak_sus, 4),
+                "peak_source": f"{peak_src} bf16_tflops_sustained (kernels timed inside a "
+                               f"long loop of steps); frac of the burst {peak}: "
+                               f"{achieved / peak:.4f}",
                 "traffic": traffic_per_launch(dominant, w.name),
                 "per_kernel_ms": {n: round(t, 4) for n, t in per_kernel.items()},
-                "per_kernel_frac": {n: round(kernel_flops[n] / (per_kernel[n] * 1e-3) / 1e12 / peak, 4)
+                "per_kernel_frac": {n: round(kernel_flops[n] / (per_kernel[n] * 1e-3) / 1e12 / peak_sus, 4)
                                     for n in kernel_flops}}
 
     # end to end through the same C-ABI with pinned host buffers: every step
@@ -528,6 +535,9 @@ def run_ours(args):
             "fwd_pct_peak": round(100 * fwd_tflops / peak, 2),
             "bwd_pct_peak": round(100 * bwd_tflops / peak, 2),
             "step_pct_peak": round(100 * value / world / peak, 2),
+            "pct_of": f"burst bf16 peak {peak} TF/s; against the sustained {peak_sus}: "
+                      f"fwd {100 * fwd_tflops / peak_sus:.2f}%, bwd {100 * bwd_tflops / peak_sus:.2f}%, "
+                      f"step {100 * value / world / peak_sus:.2f}%",
             "roofline": roofline, "cpu_baseline": cpu_baseline, "e2e": e2e,
             "sparse_scaling": scaling,
             "gpu_launches": (1 + len(BWD_LAUNCHES)) * args.steps, "clocks": clock_rec,

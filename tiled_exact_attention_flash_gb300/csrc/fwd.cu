@@ -34,6 +34,7 @@ struct FwdParams {
   int B, H, N;
   int G;  // query heads per key/value head
   int n_units;
+  int head_group;    // pair units are numbered in groups of this many heads
   float scale_log2;  // scale * log2(e)
   int wait_limit_ms;  // limit of any single bounded wait
   MaskParams mask;
@@ -88,7 +89,7 @@ __device__ __forceinline__ int fwd_unit(int k) {
 __device__ __forceinline__ PairUnit decode_pair(int u, const FwdParams& p) {
   const ListParams& L = p.list;
   int bh, r;
-  unit_order(u, p.B * p.H, bh, r);
+  unit_order_grouped(u, p.B * p.H, (L.n_blocks + 1) / 2, p.head_group, bh, r);
   PairUnit pu;
   pu.b = bh / p.H;
   pu.h = bh - pu.b * p.H;
@@ -686,6 +687,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
 // ---------------------------------------------------------------------------
 // host launcher
 // ---------------------------------------------------------------------------
+// Heads per group of the forward's unit order, in bytes of streamed K and V
+// (0: no grouping).
+constexpr int64_t kFwdGroupBytes = 0;
+
 template <int HD>
 static flash_msa_status launch_fwd_hd(const FwdLaunch& a, cudaStream_t stream) {
   using L = FwdLayout<HD>;
@@ -705,6 +710,15 @@ static flash_msa_status launch_fwd_hd(const FwdLaunch& a, cudaStream_t stream) {
   p.mask = a.mask;
   p.list = a.list;
   p.n_units = a.B * a.H * ((a.list.n_blocks + 1) / 2);  // pairs of query blocks
+  // heads per group of the unit order: K and V of about kFwdGroupBytes of
+  // heads are streamed at any time (0: one group of all heads, rank-major)
+  {
+    const int64_t per_head = int64_t(a.list.n_blocks) * kTile * HD * 2 * 2 / (a.H / a.Hkv);
+    int64_t grp = kFwdGroupBytes > 0 ? kFwdGroupBytes / (per_head > 0 ? per_head : 1) : a.B * a.H;
+    if (grp < 1) grp = 1;
+    if (grp > int64_t(a.B) * a.H) grp = int64_t(a.B) * a.H;
+    p.head_group = int(grp);
+  }
   p.status = a.status;
   p.wait_limit_ms = int(wait_limit_ms());
   if ((st = enable_smem(reinterpret_cast<const void*>(&fwd_kernel<HD>), L::kSmemBytes,
