@@ -58,6 +58,22 @@ flash_msa_status make_tile_map(CUtensorMap* m, const void* base, int B, int64_t 
   return FLASH_MSA_OK;
 }
 
+flash_msa_status make_acc_map(CUtensorMap* m, float* base, int B, int H, int64_t NP, int d) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return set_error(FLASH_MSA_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  const cuuint64_t dims[4] = {cuuint64_t(d), cuuint64_t(NP), cuuint64_t(H), cuuint64_t(B)};
+  const cuuint64_t strides[3] = {cuuint64_t(d) * 4, cuuint64_t(NP) * d * 4,
+                                 cuuint64_t(H) * NP * d * 4};
+  const cuuint32_t box[4] = {32, 128, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return set_error(FLASH_MSA_ERR_CUDA, "cuTensorMapEncodeTiled(acc) failed (CUresult %d)", int(r));
+  return FLASH_MSA_OK;
+}
+
 // ---------------------------------------------------------------------------
 // validation helpers
 // ---------------------------------------------------------------------------

@@ -93,6 +93,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreParams p) {
 // ---------------------------------------------------------------------------
 struct BwdParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;
+  CUtensorMap tm_dqacc;  // fused: the fp32 dQ accumulator (target of bulk reductions)
   __nv_bfloat16* out_a;  // dkdv: dK, dq: dQ
   __nv_bfloat16* out_b;  // dkdv: dV
   const float* nlse2;
@@ -147,8 +148,8 @@ struct BwdLayout {
   // dQ partial product computed), kDqFree (read out of TMEM).
   static constexpr int kFixFull = 0, kFixEmpty = 1, kSFull = 2, kDsEmpty = 3, kPFull = 4,
                        kDpFree = 6, kAccFull = 7, kAccEmpty = 8, kMmaDone = 9, kDqFull = 10,
-                       kDqFree = 11, kRingFull = 12, kRingEmpty = 12 + kStages,
-                       kUnitFull = 12 + 2 * kStages, kUnitEmpty = kUnitFull + 2;
+                       kDqFree = 11, kWgSync = 12, kRingFull = 14, kRingEmpty = 14 + kStages,
+                       kUnitFull = 14 + 2 * kStages, kUnitEmpty = kUnitFull + 2;
   static constexpr int kNumBars = kUnitEmpty + 2;
   // misc: TMEM base address, abort flag, wait limit, (pad), the two
   // unit-queue slots
@@ -211,6 +212,7 @@ __device__ __forceinline__ void init_bwd_barriers(uint64_t* bars) {
   mbar_init(smem_u32(bars + L::kMmaDone), 1);
   mbar_init(smem_u32(bars + L::kDqFull), 1);
   mbar_init(smem_u32(bars + L::kDqFree), kEwWarps);
+  for (int i = 0; i < 2; ++i) mbar_init(smem_u32(bars + L::kWgSync + i), 4);
   for (int i = 0; i < L::kStages; ++i) {
     mbar_init(smem_u32(bars + L::kRingFull + i), 1);
     mbar_init(smem_u32(bars + L::kRingEmpty + i), 1);
@@ -835,8 +837,18 @@ __device__ __forceinline__ void fused_elementwise(const BwdParams& p, uint8_t* s
   // this key row of the dS tile: chunk g, 128 bytes, 16-byte unit u stored at
   // unit position u ^ (row % 8) (the 128-byte swizzle the descriptor names)
   uint8_t* ds_row = smem + L::kDsOff + g * (kTile * 128) + row * 128;
+  // the same 16 KB half of the dS tile stages the warpgroup's dQ rows
+  const uint32_t stage = smem_u32(smem + L::kDsOff + g * (kTile * 128));
+  const bool wg_leader = (threadIdx.x & 127) == 0;  // issues the warpgroup's bulk reductions
   const float sl2 = p.scale_log2;
-  uint32_t s1_cnt = 0, s2_cnt = 0, af_cnt = 0, dq_cnt = 0, cnt = 0;
+  uint32_t s1_cnt = 0, s2_cnt = 0, af_cnt = 0, dq_cnt = 0, cnt = 0, ws_cnt = 0;
+  // the four warps of this warpgroup meet (a bounded wait, like every other)
+  auto wg_sync = [&]() -> bool {
+    warp_arrive(bar(L::kWgSync + g));
+    const bool ok = wait_bar(bar(L::kWgSync + g), ws_cnt & 1, abort_flag, p.status, 26);
+    ++ws_cnt;
+    return __all_sync(0xFFFFFFFFu, ok);
+  };
   UnitQueue queue = unit_queue<HD, kModeFused>(smem, bars);
   auto vec_at = [&](uint32_t c) {  // -LSE log2(e) | D of the query tile at ring position c
     return reinterpret_cast<const float*>(smem + L::kVecOff + ((c % L::kStages) / 2) * 1024);
@@ -918,6 +930,9 @@ __device__ __forceinline__ void fused_elementwise(const BwdParams& p, uint8_t* s
       }
     }
     tmem_st_x32(tB, dd);
+    // the previous drain's bulk reductions must have read the buffer
+    if (wg_leader) bulk_wait_read_all();
+    if (!wg_sync()) return false;
 #pragma unroll
     for (int q = 0; q < 8; ++q)
       *reinterpret_cast<uint4*>(ds_row + ((q ^ (row & 7)) << 4)) =
@@ -927,7 +942,11 @@ __device__ __forceinline__ void fused_elementwise(const BwdParams& p, uint8_t* s
     warp_arrive(bar(L::kPFull + 1));
     return true;
   };
-  // drain: the warpgroup's half of dQ(t) into the fp32 accumulator (unscaled)
+  // drain: the warpgroup's half of dQ(t) into the fp32 accumulator
+  // (unscaled), in rounds of 32 columns staged through the warpgroup's 16 KB
+  // half of the dS tile (free once dQ(t) has read it): each thread writes its
+  // query row (128 bytes, 128-byte swizzled), and the warpgroup's first
+  // thread has the TMA engine add the 128 x 32 tile into the accumulator
   auto drain = [&](const Unit& un, int t) -> bool {
     int hq;
     const InnerTile it = bwd_inner<true>(un, t, p, hq);
@@ -935,20 +954,26 @@ __device__ __forceinline__ void fused_elementwise(const BwdParams& p, uint8_t* s
     if (!__all_sync(0xFFFFFFFFu, ok)) return false;
     ++dq_cnt;
     tc_fence_after();
-    const int64_t i = int64_t(it.blk) * kTile + row;  // query row of this lane
-    const bool live = !it.dead && i < p.N;
-    char* dst = reinterpret_cast<char*>(p.dqacc + ((int64_t(un.b) * p.H + hq) * p.NP + i) * HD +
-                                        g * (HD / 2));
-    constexpr int kHalves = HD / 64;  // 32 columns at a time
+    constexpr int kRounds = HD / 64;
 #pragma unroll
-    for (int q = 0; q < kHalves; ++q) {
+    for (int q = 0; q < kRounds; ++q) {
       uint32_t v[32];
       tmem_ld_x32(tDQ + 32 * q, v);
-      if (q == kHalves - 1) warp_arrive(bar(L::kDqFree));
-      uint4 c[8];
+      if (q == kRounds - 1) warp_arrive(bar(L::kDqFree));
+      if (q > 0) {  // the previous round's copy must have left the staging buffer
+        if (wg_leader) bulk_wait_read_all();
+        if (!wg_sync()) return false;
+      }
 #pragma unroll
-      for (int k = 0; k < 8; ++k) c[k] = make_uint4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
-      add_rows_transposed<8, 2>(c, dst + q * 128, int64_t(HD) * 4, live);
+      for (int k = 0; k < 8; ++k)
+        *reinterpret_cast<uint4*>(ds_row + ((k ^ (row & 7)) << 4)) =
+            make_uint4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+      fence_proxy_async_smem();  // the TMA engine reads the tile through the async proxy
+      if (!wg_sync()) return false;
+      if (wg_leader && !it.dead) {
+        tma_reduce_add_4d(&p.tm_dqacc, stage, g * (HD / 2) + 32 * q, it.blk * kTile, hq, un.b);
+        bulk_commit_group();
+      }
     }
     return true;
   };
@@ -1148,6 +1173,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
     tma_prefetch_desc(&p.tm_k);
     tma_prefetch_desc(&p.tm_v);
     tma_prefetch_desc(&p.tm_do);
+    if (kMode == kModeFused) tma_prefetch_desc(&p.tm_dqacc);
   }
   tc_fence_before();
   __syncthreads();
@@ -1165,9 +1191,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
   } else if (warp >= 4) {
     const int g = (warp - 4) >> 2;  // elementwise warpgroup: columns [64 g, 64 g + 64)
     regs_grow<208>();
-    if (kMode == kModeFused) fused_elementwise<HD>(p, smem, bars, tmem, g, abort_flag);
-    else if (kMode == kModeDkdv) dkdv_elementwise<HD>(p, smem, bars, tmem, g, abort_flag);
-    else dq_elementwise<HD>(p, smem, bars, tmem, g, abort_flag);
+    if (kMode == kModeFused) {
+      fused_elementwise<HD>(p, smem, bars, tmem, g, abort_flag);
+      // bulk reductions still in flight read shared memory: finish them
+      // before the CTA releases it
+      if ((threadIdx.x & 127) == 0) bulk_wait_all();
+    } else if (kMode == kModeDkdv) {
+      dkdv_elementwise<HD>(p, smem, bars, tmem, g, abort_flag);
+    } else {
+      dq_elementwise<HD>(p, smem, bars, tmem, g, abort_flag);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -1301,6 +1334,8 @@ static flash_msa_status launch_bwd_hd(const BwdLaunch& a, cudaStream_t stream) {
       return st;
   }
   if (a.stages & FLASH_MSA_BWD_FUSED) {
+    if (!a.dqacc) return set_error(FLASH_MSA_ERR_WORKSPACE, "bwd: no dQ accumulator");
+    if ((st = make_acc_map(&p.tm_dqacc, a.dqacc, a.B, a.H, NP, HD)) != FLASH_MSA_OK) return st;
     p.list = a.cols;
     p.n_units = a.B * a.Hkv * nb;
     // key/value heads per group: accumulator (G query heads) plus Q and dO

@@ -19,6 +19,9 @@ flash_msa_status set_cuda_error(const char* what);
 // 4-D TMA map over a bf16 (B, N, H, d) tensor: dims (d, N, H, B), box
 // (64, 128, 1, 1), 128-byte swizzle, zero fill past N.  Encoded on the host.
 flash_msa_status make_tile_map(CUtensorMap* m, const void* base, int B, int64_t N, int H, int d);
+// 4-D TMA map over an fp32 (B, H, NP, d) accumulator: dims (d, NP, H, B), box
+// (32, 128, 1, 1), 128-byte swizzle (the target of bulk tensor reductions).
+flash_msa_status make_acc_map(CUtensorMap* m, float* base, int B, int H, int64_t NP, int d);
 
 // per-device state (status.cu)
 unsigned* status_word_ptr();  // device address for the current device, or null on error
