@@ -3,9 +3,8 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl ours|reference]
 
 One step = the whole hot path over one batch of synthetic input: the forward
-kernel (O, LSE) and the three backward launches (D and zeroing of the dQ
-accumulator; dK, dV and dQ partial products; dQ conversion), called through
-the C-ABI library.  FLOPs are counted on live 128 x 128 tiles only:
+kernel (O, LSE) and the three backward launches of flash_msa_bwd (D, dK/dV,
+dQ), called through the C-ABI library.  FLOPs are counted on live 128 x 128 tiles only:
 fwd = B * H * nnz * 4 * 128 * 128 * d, bwd = 2.5 x fwd (five products per
 tile), step = 3.5 x fwd.  The default workload is B=1, H=32, N=16384,
 d=128, causal (a 7B-style layer at long context); ``--config`` picks another
@@ -248,8 +247,8 @@ def traffic_per_launch(kernel, workload_name):
 # tensor-core FLOPs it issues per live tile in units of the forward's 4 x
 # 128 x 128 x d, for the per-kernel roofline).
 BWD_LAUNCHES = (("bwd_pre", "BWD_PREPROCESS", 0.0),
-                ("bwd_fused", "BWD_FUSED", 2.5),
-                ("bwd_convert", "BWD_DQ_CONVERT", 0.0))
+                ("bwd_dkdv", "BWD_DKDV", 2.0),
+                ("bwd_dq", "BWD_DQ", 1.5))
 
 
 class Problem:

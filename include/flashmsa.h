@@ -207,8 +207,7 @@ flash_msa_status flash_msa_fwd(const void* q, const void* k, const void* v, void
 
 /* Bytes of device workspace flash_msa_bwd() needs: two fp32 vectors per
  * (b, h), each padded to whole 128-row tiles -- -LSE_i * log2(e) and
- * D_i = sum_c dO_ic * O_ic -- and the fp32 dQ accumulator (B, H, padded N, d),
- * rounded up to 256 bytes.  0 for invalid sizes. */
+ * D_i = sum_c dO_ic * O_ic -- rounded up to 256 bytes.  0 for invalid sizes. */
 size_t flash_msa_bwd_workspace_bytes(int B, int H, int64_t N, int d);
 
 /* Backward: given the forward's o and lse and the upstream gradient dO,
@@ -219,15 +218,10 @@ size_t flash_msa_bwd_workspace_bytes(int B, int H, int64_t N, int d);
  * and dK by the chain rule).  `workspace` is a DEVICE buffer of at least
  * flash_msa_bwd_workspace_bytes() bytes owned by the caller (contents are
  * overwritten); else FLASH_MSA_ERR_WORKSPACE.  Three kernel launches on
- * `stream`: D (and zeroing of the dQ accumulator); one key-stationary kernel
- * that computes the five products of every live tile, accumulating dK and dV
- * on chip and adding each tile's dQ partial product into the fp32
- * accumulator with atomics (the "accumulated atomically" option for dQ);
- * and the conversion of the accumulator to bf16 dq.  dK, dV are bitwise
- * deterministic; dQ is within rounding of a fixed-order sum but its low bits
- * may differ between calls (the order of the fp32 additions varies).
- * flash_msa_bwd_stages() with FLASH_MSA_BWD_DETERMINISTIC gives a bitwise
- * deterministic backward. */
+ * `stream` (D, then a key-stationary dK/dV kernel, then a query-stationary dQ
+ * kernel: the "reduced separately" option for dQ, which recomputes S and dP,
+ * seven tensor-core products per live tile); no atomics, every output is
+ * bitwise reproducible. */
 flash_msa_status flash_msa_bwd(const void* q, const void* k, const void* v, const void* o,
                                const float* lse, const void* dO, void* dq, void* dk, void* dv,
                                int B, int H, int64_t N, int d, float scale,
@@ -235,29 +229,40 @@ flash_msa_status flash_msa_bwd(const void* q, const void* k, const void* v, cons
                                size_t workspace_bytes, void* stream);
 
 /* The backward's launches one at a time (same arguments plus a bit set), in
- * two variants.  Default (flash_msa_bwd() is stages = PREPROCESS | FUSED |
- * DQ_CONVERT, run in that order):
- *   PREPROCESS  D and the scaled LSE into the workspace; also zeroes the dQ
- *               accumulator when workspace_bytes >= flash_msa_bwd_workspace_bytes()
- *   FUSED       dK, dV, and dQ partial products added into the accumulator
+ * two variants.
+ * Two-kernel (flash_msa_bwd() is FLASH_MSA_BWD_DETERMINISTIC = PREPROCESS |
+ * DKDV | DQ):
+ *   PREPROCESS  D and the scaled LSE into the workspace (must run first); run
+ *               together with FUSED, or on its own with a workspace large
+ *               enough for the accumulated variant, it also zeroes the dQ
+ *               accumulator
+ *   DKDV        dK and dV (key-stationary, four products per live tile)
+ *   DQ          dQ (query-stationary, recomputes S and dP: three products)
+ *   DKDV and DQ read the workspace written by PREPROCESS, in either order.
+ * Accumulated dQ (FLASH_MSA_BWD_ACCUMULATED = PREPROCESS | FUSED |
+ * DQ_CONVERT, run in that order; the "dQ accumulated atomically" option):
+ *   FUSED       one key-stationary kernel issuing the five products of every
+ *               live tile: dK and dV accumulate on chip, and each tile's dQ
+ *               partial product dS K is added into an fp32 accumulator in the
+ *               workspace by TMA bulk tensor reductions
  *   DQ_CONVERT  dq = scale * accumulator, rounded to bf16
- * Deterministic (FLASH_MSA_BWD_DETERMINISTIC = PREPROCESS | DKDV | DQ): a
- * key-stationary dK/dV kernel and a query-stationary dQ kernel that
- * recomputes S and dP (seven products per live tile instead of five, no
- * atomics, every output bitwise reproducible, no dQ accumulator: the
- * workspace is only the two vectors).  DKDV and DQ read the workspace
- * written by PREPROCESS and may run in either order.  FUSED may not be
- * combined with DKDV or DQ (FLASH_MSA_ERR_INVALID_ARG).  The workspace
- * needed is flash_msa_bwd_stages_workspace_bytes(). */
+ *   dK and dV are bitwise equal to the two-kernel variant's; dQ is within
+ *   rounding of it, and its low bits may differ between calls (the order of
+ *   the fp32 additions varies).  On GB300 this variant is the slower one
+ *   (the reductions, 64 KB of fp32 per live tile, cost more than the two
+ *   recomputed products); it needs the larger workspace of
+ *   flash_msa_bwd_stages_workspace_bytes().
+ * FUSED may not be combined with DKDV or DQ (FLASH_MSA_ERR_INVALID_ARG). */
 #define FLASH_MSA_BWD_PREPROCESS 1u
 #define FLASH_MSA_BWD_DKDV 2u
 #define FLASH_MSA_BWD_DQ 4u
 #define FLASH_MSA_BWD_FUSED 8u
 #define FLASH_MSA_BWD_DQ_CONVERT 16u
 #define FLASH_MSA_BWD_DETERMINISTIC 7u
+#define FLASH_MSA_BWD_ACCUMULATED 25u
 /* Workspace bytes flash_msa_bwd_stages() needs for this set of stages: the
- * two vectors, plus the dQ accumulator when FUSED or DQ_CONVERT is set (0 for
- * invalid sizes or stage bits). */
+ * two vectors, plus the fp32 dQ accumulator (B, H, padded N, d) when FUSED or
+ * DQ_CONVERT is set (0 for invalid sizes or stage bits). */
 size_t flash_msa_bwd_stages_workspace_bytes(int B, int H, int64_t N, int d, unsigned stages);
 flash_msa_status flash_msa_bwd_stages(const void* q, const void* k, const void* v, const void* o,
                                       const float* lse, const void* dO, void* dq, void* dk,
@@ -282,18 +287,24 @@ flash_msa_status flash_msa_bwd_gqa(const void* q, const void* k, const void* v, 
                                    int B, int H, int Hkv, int64_t N, int d, float scale,
                                    const flash_msa_mask_desc* mask, void* workspace,
                                    size_t workspace_bytes, void* stream);
+/* flash_msa_bwd_stages() for grouped-query attention (arguments as in
+ * flash_msa_bwd_gqa() plus the stage bits). */
+flash_msa_status flash_msa_bwd_gqa_stages(const void* q, const void* k, const void* v,
+                                          const void* o, const float* lse, const void* dO,
+                                          void* dq, void* dk, void* dv, int B, int H, int Hkv,
+                                          int64_t N, int d, float scale,
+                                          const flash_msa_mask_desc* mask, void* workspace,
+                                          size_t workspace_bytes, unsigned stages, void* stream);
 
 /* Backward for callers that may not allocate device memory at call time (a
  * host framework that owns the whole device memory pool, or a latency-bound
  * loop where cudaMalloc/cudaFree are banned because they can synchronise the
  * device).  No counterpart on the pages: it exists only because such callers
  * cannot hand flash_msa_bwd() a workspace.  Same arguments, kernels and
- * results as the deterministic backward (flash_msa_bwd_stages() with
- * FLASH_MSA_BWD_DETERMINISTIC) minus the workspace: the scratch is a fixed
+ * results as flash_msa_bwd() minus the workspace: the scratch is a fixed
  * 16 MiB array inside the library, held on every device that loads the
  * library until the process exits.  Limit: B * H * ceil(N/128) * 128 <= 2^21
- * (flash_msa_bwd_stages_workspace_bytes() of FLASH_MSA_BWD_DETERMINISTIC
- * <= 16 MiB); larger calls return
+ * (flash_msa_bwd_workspace_bytes() <= 16 MiB); larger calls return
  * FLASH_MSA_ERR_WORKSPACE without launching anything.  Allocates nothing and
  * calls no allocating routine.  The first call on a device looks the array's
  * device address up (cudaGetSymbolAddress); make that first call before any

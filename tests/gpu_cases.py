@@ -20,9 +20,10 @@ GRAD_ABS_FLOOR = 1e-4
 
 
 def run_gpu(inp: dict, fields: dict, device="cuda", backward=True, scale=None,
-            deterministic=False):
+            accumulated=False):
     """scale: softmax scale passed to the library (None: its default d^-1/2);
-    deterministic: the two-kernel backward instead of the default fused one."""
+    accumulated: the fused backward with dQ added into an fp32 accumulator
+    instead of the default two-kernel backward."""
     mask = api.Mask(**fields) if fields else None
     N = inp["q"].shape[1]
     index = None
@@ -33,7 +34,7 @@ def run_gpu(inp: dict, fields: dict, device="cuda", backward=True, scale=None,
     out = {"o": o, "lse": lse}
     if backward:
         dq, dk, dv = api.bwd(q, k, v, o, lse, do, mask=mask, index=index, scale=scale,
-                             deterministic=deterministic)
+                             accumulated=accumulated)
         out.update(dq=dq, dk=dk, dv=dv)
     st = api.get_status()
     assert st == api.OK, f"device status {st}"
@@ -158,13 +159,13 @@ def gqa_reference(q, k, v, do, scale, spec, backward=True):
     return o, lse, dq, dk, dv
 
 
-def run_gpu_gqa(inp, fields, device="cuda"):
+def run_gpu_gqa(inp, fields, device="cuda", accumulated=False):
     mask = api.Mask(**fields) if fields else None
     N = inp["q"].shape[1]
     index = api.build_block_index(mask, N).to(device) if (mask and mask.needs_index) else None
     q, k, v, do = (inp[n].to(device) for n in ("q", "k", "v", "do"))
     o, lse = api.fwd(q, k, v, mask=mask, index=index)
-    dq, dk, dv = api.bwd(q, k, v, o, lse, do, mask=mask, index=index)
+    dq, dk, dv = api.bwd(q, k, v, o, lse, do, mask=mask, index=index, accumulated=accumulated)
     assert api.get_status() == api.OK
     f = lambda t: t.float().cpu().numpy()
     return {"o": f(o), "lse": lse.cpu().numpy(), "dq": f(dq), "dk": f(dk), "dv": f(dv)}

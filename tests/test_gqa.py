@@ -70,3 +70,18 @@ def test_gqa_parity(H, Hkv, d, fields):
     inp = _inputs(2, 389, H, Hkv, d, seed=H * 10 + Hkv + d)
     res = gc.run_gpu_gqa(inp, fields)
     gc.gqa_full_compare(inp, fields, res)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("H,Hkv", [(4, 2), (4, 1)])
+@pytest.mark.parametrize("fields", [{"causal": True}, {"causal": True, "window": 150, "stride": 2, "stride_phase": 1}])
+def test_gqa_parity_accumulated_backward(H, Hkv, fields):
+    # the fused backward walks each key/value head's group of query heads and
+    # adds every query head's dQ partial products into its own accumulator rows
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from tests.libbuild import ensure_built
+    ensure_built()
+    inp = _inputs(2, 389, H, Hkv, 128, seed=H * 7 + Hkv)
+    res = gc.run_gpu_gqa(inp, fields, accumulated=True)
+    gc.gqa_full_compare(inp, fields, res)

@@ -86,18 +86,18 @@ def test_index_for_another_n_is_rejected(L):
 
 def test_bwd_workspace_errors(L):
     need = L.flash_msa_bwd_workspace_bytes(2, 3, 300, 128)
-    # two fp32 vectors and the fp32 dQ accumulator per (b, h), padded rows
-    assert need == 2 * 2 * 3 * 384 * 4 + 2 * 3 * 384 * 128 * 4
+    assert need == 2 * 2 * 3 * 384 * 4  # two fp32 vectors per (b, h), padded rows
     assert L.flash_msa_bwd_workspace_bytes(0, 3, 300, 128) == 0
     ws = L.flash_msa_bwd_stages_workspace_bytes
-    assert ws(2, 3, 300, 128, api.BWD_DETERMINISTIC) == 2 * 2 * 3 * 384 * 4
-    assert ws(2, 3, 300, 128, api.BWD_DEFAULT) == need
+    assert ws(2, 3, 300, 128, api.BWD_DETERMINISTIC) == need
+    big = ws(2, 3, 300, 128, api.BWD_ACCUMULATED)
+    assert big == need + 2 * 3 * 384 * 128 * 4  # plus the fp32 dQ accumulator
+    assert ws(2, 3, 300, 128, api.BWD_DQ_CONVERT) == big
     assert ws(2, 3, 300, 128, api.BWD_FUSED | api.BWD_DKDV) == 0
     assert ws(2, 3, 300, 128, 32) == 0
-    stage_args = [FAKE] * 9 + [2, 3, 300, 128, 0.0, None, FAKE, need]
+    stage_args = [FAKE] * 9 + [2, 3, 300, 128, 0.0, None, FAKE, big]
     assert L.flash_msa_bwd_stages(*stage_args, api.BWD_FUSED | api.BWD_DQ, None) == api.ERR_INVALID_ARG
-    small = ws(2, 3, 300, 128, api.BWD_DETERMINISTIC)
-    assert L.flash_msa_bwd_stages(*stage_args[:-1], small, api.BWD_FUSED, None) == api.ERR_WORKSPACE
+    assert L.flash_msa_bwd_stages(*stage_args[:-1], need, api.BWD_FUSED, None) == api.ERR_WORKSPACE
     args = [FAKE] * 9 + [2, 3, 300, 128, 0.0, None]
     assert L.flash_msa_bwd(*args, None, need, None) == api.ERR_WORKSPACE
     assert L.flash_msa_bwd(*args, FAKE, need - 4, None) == api.ERR_WORKSPACE

@@ -37,6 +37,7 @@ SYMBOLS = (
     "flash_msa_bwd_stages_workspace_bytes",
     "flash_msa_fwd_gqa",
     "flash_msa_bwd_gqa",
+    "flash_msa_bwd_gqa_stages",
     "flash_msa_bwd_noalloc",
     "flash_msa_selftest_wait_timeout",
     "flash_msa_set_wait_limit_ms",
@@ -119,6 +120,9 @@ def lib() -> ctypes.CDLL:
                                     ctypes.POINTER(MaskDescStruct), vp]
     L.flash_msa_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i64, i32,
                                     f32, ctypes.POINTER(MaskDescStruct), vp, ctypes.c_size_t, vp]
+    L.flash_msa_bwd_gqa_stages.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i64,
+                                           i32, f32, ctypes.POINTER(MaskDescStruct), vp,
+                                           ctypes.c_size_t, ctypes.c_uint, vp]
     L.flash_msa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i64, i32,
                                         f32, ctypes.POINTER(MaskDescStruct), vp]
     L.flash_msa_get_status.argtypes = [vp]
@@ -129,7 +133,7 @@ def lib() -> ctypes.CDLL:
     L.flash_msa_version.restype = ctypes.c_char_p
     for name in ("flash_msa_build_block_index", "flash_msa_check_block_index", "flash_msa_fwd",
                  "flash_msa_bwd", "flash_msa_bwd_stages", "flash_msa_bwd_noalloc",
-                 "flash_msa_fwd_gqa", "flash_msa_bwd_gqa", "flash_msa_get_status",
+                 "flash_msa_fwd_gqa", "flash_msa_bwd_gqa", "flash_msa_bwd_gqa_stages", "flash_msa_get_status",
                  "flash_msa_selftest_wait_timeout", "flash_msa_set_wait_limit_ms"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -393,8 +397,8 @@ def bwd_workspace_bytes(B, H, N, d) -> int:
 
 
 BWD_PREPROCESS, BWD_DKDV, BWD_DQ, BWD_FUSED, BWD_DQ_CONVERT = 1, 2, 4, 8, 16
-BWD_DETERMINISTIC = BWD_PREPROCESS | BWD_DKDV | BWD_DQ    # seven products per tile, no atomics
-BWD_DEFAULT = BWD_PREPROCESS | BWD_FUSED | BWD_DQ_CONVERT  # what flash_msa_bwd runs
+BWD_DETERMINISTIC = BWD_PREPROCESS | BWD_DKDV | BWD_DQ      # flash_msa_bwd: two kernels
+BWD_ACCUMULATED = BWD_PREPROCESS | BWD_FUSED | BWD_DQ_CONVERT  # dQ accumulated in fp32
 
 
 def bwd_stages_workspace_bytes(B, H, N, d, stages) -> int:
@@ -404,10 +408,11 @@ def bwd_stages_workspace_bytes(B, H, N, d, stages) -> int:
 
 def bwd(q, k, v, o, lse, do, mask: Optional[Mask] = None, index: Optional[BlockIndex] = None,
         scale: Optional[float] = None, dq=None, dk=None, dv=None, workspace=None, stream=None,
-        stages: Optional[int] = None, deterministic: bool = False):
+        stages: Optional[int] = None, accumulated: bool = False):
     """dQ, dK, dV (bf16, like q).  ``stages`` (bits BWD_*) runs a subset of the
-    launches through flash_msa_bwd_stages; ``deterministic`` runs the
-    two-kernel backward (stages BWD_DETERMINISTIC); default: flash_msa_bwd."""
+    launches through flash_msa_bwd_stages; ``accumulated`` runs the fused
+    kernel with dQ added into an fp32 accumulator (stages BWD_ACCUMULATED);
+    default: flash_msa_bwd (two kernels, bitwise deterministic)."""
     _check_qkv("q", q)
     B, N, H, d = q.shape
     kv_shape = _kv_shape(q, k)
@@ -417,12 +422,10 @@ def bwd(q, k, v, o, lse, do, mask: Optional[Mask] = None, index: Optional[BlockI
         _check_qkv(name, t, q.shape)
     if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (B, H, N):
         raise ValueError("lse must be contiguous float32 (B, H, N)")
-    if deterministic:
+    if accumulated:
         if stages is not None:
-            raise ValueError("pass either stages or deterministic")
-        stages = BWD_DETERMINISTIC
-    if Hkv != H and stages is not None:
-        raise ValueError("stages are available for equal query / key-value head counts only")
+            raise ValueError("pass either stages or accumulated")
+        stages = BWD_ACCUMULATED
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
@@ -435,8 +438,11 @@ def bwd(q, k, v, o, lse, do, mask: Optional[Mask] = None, index: Optional[BlockI
             do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d,
             float(scale or 0.0), ctypes.byref(desc) if desc is not None else None,
             workspace.data_ptr(), workspace.numel() * workspace.element_size())
-    if Hkv != H:
+    if Hkv != H and stages is None:
         code = lib().flash_msa_bwd_gqa(*args[:11], Hkv, *args[11:], _stream_ptr(stream))  # after H
+    elif Hkv != H:
+        code = lib().flash_msa_bwd_gqa_stages(*args[:11], Hkv, *args[11:], stages,
+                                              _stream_ptr(stream))
     elif stages is None:
         code = lib().flash_msa_bwd(*args, _stream_ptr(stream))
     else:

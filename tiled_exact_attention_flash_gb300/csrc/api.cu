@@ -554,25 +554,24 @@ static size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 static constexpr unsigned kAllStages = FLASH_MSA_BWD_PREPROCESS | FLASH_MSA_BWD_DKDV |
                                        FLASH_MSA_BWD_DQ | FLASH_MSA_BWD_FUSED |
                                        FLASH_MSA_BWD_DQ_CONVERT;
-static constexpr unsigned kDefaultStages =
-    FLASH_MSA_BWD_PREPROCESS | FLASH_MSA_BWD_FUSED | FLASH_MSA_BWD_DQ_CONVERT;
+static constexpr unsigned kDefaultStages = FLASH_MSA_BWD_DETERMINISTIC;
+static constexpr unsigned kAccumulatorStages = FLASH_MSA_BWD_FUSED | FLASH_MSA_BWD_DQ_CONVERT;
 
 static bool valid_stages(unsigned stages) {
   if (stages == 0 || (stages & ~kAllStages)) return false;
   return !((stages & FLASH_MSA_BWD_FUSED) && (stages & (FLASH_MSA_BWD_DKDV | FLASH_MSA_BWD_DQ)));
 }
 
-size_t flash_msa_bwd_workspace_bytes(int B, int H, int64_t N, int d) {
-  if (B < 1 || H < 1 || N < 1 || N > kMaxN || (d != 64 && d != 128)) return 0;
-  return round256(vectors_bytes(B, H, N) + accumulator_bytes(B, H, N, d));
-}
-
 size_t flash_msa_bwd_stages_workspace_bytes(int B, int H, int64_t N, int d, unsigned stages) {
   if (!valid_stages(stages)) return 0;
-  if (stages & (FLASH_MSA_BWD_FUSED | FLASH_MSA_BWD_DQ_CONVERT))
-    return flash_msa_bwd_workspace_bytes(B, H, N, d);
   if (B < 1 || H < 1 || N < 1 || N > kMaxN || (d != 64 && d != 128)) return 0;
-  return round256(vectors_bytes(B, H, N));
+  size_t bytes = vectors_bytes(B, H, N);
+  if (stages & kAccumulatorStages) bytes += accumulator_bytes(B, H, N, d);
+  return round256(bytes);
+}
+
+size_t flash_msa_bwd_workspace_bytes(int B, int H, int64_t N, int d) {
+  return flash_msa_bwd_stages_workspace_bytes(B, H, N, d, kDefaultStages);
 }
 
 flash_msa_status flash_msa_bwd(const void* q, const void* k, const void* v, const void* o,
@@ -624,8 +623,14 @@ static flash_msa_status bwd_impl(const void* q, const void* k, const void* v, co
   a.dk = dk;
   a.dv = dv;
   a.dsum = static_cast<float*>(workspace);
-  // the accumulator follows the two vectors when the workspace holds it
-  a.dqacc = workspace_bytes >= flash_msa_bwd_workspace_bytes(B, H, N, d)
+  // the accumulator follows the two vectors; it is used (and PREPROCESS
+  // zeroes it) by the accumulated-dQ stages, and by PREPROCESS run on its own
+  // when the workspace holds it (a stage-by-stage accumulated backward)
+  const bool acc_call = (stages & kAccumulatorStages) ||
+                        (stages == FLASH_MSA_BWD_PREPROCESS &&
+                         workspace_bytes >= flash_msa_bwd_stages_workspace_bytes(
+                                                B, H, N, d, FLASH_MSA_BWD_ACCUMULATED));
+  a.dqacc = acc_call
                 ? reinterpret_cast<float*>(static_cast<char*>(workspace) + vectors_bytes(B, H, N))
                 : nullptr;
   a.B = B;
@@ -656,6 +661,16 @@ flash_msa_status flash_msa_bwd_gqa(const void* q, const void* k, const void* v, 
                                    size_t workspace_bytes, void* stream) {
   return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, B, H, Hkv, N, d, scale, mask, workspace,
                   workspace_bytes, kDefaultStages, stream);
+}
+
+flash_msa_status flash_msa_bwd_gqa_stages(const void* q, const void* k, const void* v,
+                                          const void* o, const float* lse, const void* dO,
+                                          void* dq, void* dk, void* dv, int B, int H, int Hkv,
+                                          int64_t N, int d, float scale,
+                                          const flash_msa_mask_desc* mask, void* workspace,
+                                          size_t workspace_bytes, unsigned stages, void* stream) {
+  return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, B, H, Hkv, N, d, scale, mask, workspace,
+                  workspace_bytes, stages, stream);
 }
 
 flash_msa_status flash_msa_set_wait_limit_ms(unsigned ms) {

@@ -441,30 +441,6 @@ __device__ __forceinline__ void store_rows_transposed(uint4 (&c)[kC], char* dst,
         *reinterpret_cast<uint4*>(dst + int64_t(k - i) * stride + (q + i) * 16) = c[q + k];
 }
 
-// The same pattern for fp32 accumulation: chunk c[k] holds four fp32 values
-// to be ADDED (vector atomics, performed in L2) to the lane's row at
-// dst + 16 k bytes; after the transpose every atomic instruction of the warp
-// covers kG * 16 contiguous bytes of each of 32 / kG rows.
-template <int kC, int kG>
-__device__ __forceinline__ void add_rows_transposed(uint4 (&c)[kC], char* dst, int64_t stride,
-                                                    bool row_ok) {
-  transpose_chunks<kC, kG>(c);
-  const int lane = int(threadIdx.x & 31);
-  const int i = lane & (kG - 1);
-  const uint32_t ok = __ballot_sync(0xFFFFFFFFu, row_ok);
-  const int base = lane - i;
-#pragma unroll
-  for (int q = 0; q < kC; q += kG)
-#pragma unroll
-    for (int k = 0; k < kG; ++k)
-      if ((ok >> (base + k)) & 1u) {
-        const uint4 v = c[q + k];
-        atomicAdd(reinterpret_cast<float4*>(dst + int64_t(k - i) * stride + (q + i) * 16),
-                  make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
-                              __uint_as_float(v.w)));
-      }
-}
-
 // Bits of one row of a bit tile (bit-packed masks): kWords 32-bit words
 // starting at word w0 of tile-local row r.  prefetch_tile_bits pulls the row
 // into L1 before the tile's barrier wait without holding registers across

@@ -20,8 +20,7 @@
 
 namespace fmsa {
 
-// 16 MiB: the deterministic backward's two fp32 vectors of
-// B * H * ceil(N/128) * 128 entries, i.e.
+// 16 MiB: two fp32 vectors of B * H * ceil(N/128) * 128 entries, i.e.
 // B * H * ceil(N/128) * 128 <= 2^21 (for example B*H = 32 heads at N = 65536).
 constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
 
@@ -60,7 +59,7 @@ extern "C" flash_msa_status flash_msa_bwd_noalloc(const void* q, const void* k, 
                                                   void* dq, void* dk, void* dv, int B, int H,
                                                   int64_t N, int d, float scale,
                                                   const flash_msa_mask_desc* mask, void* stream) {
-  const size_t need = flash_msa_bwd_stages_workspace_bytes(B, H, N, d, FLASH_MSA_BWD_DETERMINISTIC);
+  const size_t need = flash_msa_bwd_workspace_bytes(B, H, N, d);
   if (need > kNoAllocScratchBytes)
     return set_error(FLASH_MSA_ERR_WORKSPACE,
                      "bwd_noalloc: B=%d H=%d N=%lld needs %zu bytes of scratch, more than the "
@@ -69,9 +68,8 @@ extern "C" flash_msa_status flash_msa_bwd_noalloc(const void* q, const void* k, 
   void* scratch = nullptr;
   const flash_msa_status st = scratch_address(&scratch);
   if (st != FLASH_MSA_OK) return st;
-  // Same kernels and launches as the deterministic backward (its workspace
-  // is two vectors, no dQ accumulator); only the workspace differs.  need == 0
-  // means invalid sizes, which flash_msa_bwd_stages() reports.
-  return flash_msa_bwd_stages(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, mask, scratch,
-                              kNoAllocScratchBytes, FLASH_MSA_BWD_DETERMINISTIC, stream);
+  // Same kernels and launches as flash_msa_bwd(); only the workspace differs.
+  // need == 0 means invalid sizes, which flash_msa_bwd() reports.
+  return flash_msa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, mask, scratch,
+                       kNoAllocScratchBytes, stream);
 }
