@@ -24,6 +24,17 @@ slots are numbered in CSR order; bits[slot] holds 128 rows (query) of four
 transpose (128 key rows of four words over the queries); bit_slot /
 bit_slot_t give each CSR / CSC entry its slot or -1.
 
+Packed sequences (variable-length batches) whose other mask parts depend
+only on i - j (causal, local window) and that carry no bit-packed mask are
+tiled per sequence instead: sequence [s0, s1) gets its own tiles starting at
+s0, s0 + 128, ..., so no tile holds tokens of two sequences (the way P1's
+request batching keeps each request's attention to itself), and only tile
+pairs of one sequence exist.  Tiles are numbered sequence by sequence; for
+tile t, tile_start[t] is its first token, tile_seq0[t] and tile_seq_len[t]
+its sequence's first token and length.  Entries of a tile past its
+sequence's end count as dead, and each tile pair is classified by evaluating
+the predicate on all of its entries, as above.
+
 For masks with a local window and no strided part, key blocks farther than
 the window from the query block are skipped without evaluation: by the window
 definition none of their entries is live (with global tokens, the key
@@ -73,8 +84,44 @@ def _pack_rows(live: np.ndarray) -> np.ndarray:
     return (live.reshape(live.shape[0], 4, 32).astype(np.uint32) * weights).sum(axis=2).astype(np.uint32)
 
 
+def sequence_tiled(spec: MaskSpec) -> bool:
+    """Whether a mask is tiled per sequence (see the module docstring)."""
+    return (spec.doc_starts is not None and spec.bitmask is None and spec.dilation is None
+            and spec.stride is None and spec.global_tokens is None)
+
+
+def sequence_tiles(spec: MaskSpec, tile: int = 128):
+    """(tile_start, tile_seq0, tile_seq_len) of the per-sequence tiling."""
+    start, seq0, seq_len = [], [], []
+    for s0, s1 in zip(spec.doc_starts[:-1], spec.doc_starts[1:]):
+        for m in range((s1 - s0 + tile - 1) // tile):
+            start.append(s0 + m * tile)
+            seq0.append(s0)
+            seq_len.append(s1 - s0)
+    return (np.array(start, dtype=np.int32), np.array(seq0, dtype=np.int32),
+            np.array(seq_len, dtype=np.int32))
+
+
+def classify_sequence_tiles(n: int, spec: MaskSpec, tile: int = 128) -> np.ndarray:
+    """kinds[qt, kt] over the per-sequence tiles; pairs of two sequences are dead."""
+    start, seq0, seq_len = sequence_tiles(spec, tile)
+    nt = len(start)
+    kinds = np.full((nt, nt), DEAD, dtype=np.int8)
+    for qt in range(nt):
+        end = int(seq0[qt]) + int(seq_len[qt])
+        rows = np.arange(start[qt], start[qt] + tile)
+        for kt in np.nonzero(seq0 == seq0[qt])[0]:
+            cols = np.arange(start[kt], start[kt] + tile)
+            live = live_matrix(rows, cols, n, spec) & (rows < end)[:, None] & (cols < end)[None, :]
+            cnt = int(live.sum())
+            if cnt:
+                kinds[qt, kt] = FULL if cnt == tile * tile else PARTIAL
+    return kinds
+
+
 def build(n: int, spec: MaskSpec, tile: int = 128, prune: bool = True) -> dict:
-    kinds = classify(n, spec, tile, prune)
+    seq = sequence_tiled(spec)
+    kinds = classify_sequence_tiles(n, spec, tile) if seq else classify(n, spec, tile, prune)
     nb = kinds.shape[0]
     row_ptr = np.zeros(nb + 1, dtype=np.int32)
     col_idx, kind = [], []
@@ -93,7 +140,7 @@ def build(n: int, spec: MaskSpec, tile: int = 128, prune: bool = True) -> dict:
     # bit tiles (bit-packed masks only)
     bit_slot = np.full(len(col_idx), -1, dtype=np.int32)
     bits, bits_t = [], []
-    if spec.bitmask is not None or spec.doc_starts is not None:
+    if (spec.bitmask is not None or spec.doc_starts is not None) and not seq:
         plain = dataclasses.replace(spec, bitmask=None, doc_starts=None)
         for qb in range(nb):
             rows = np.arange(qb * tile, qb * tile + tile)
@@ -115,7 +162,12 @@ def build(n: int, spec: MaskSpec, tile: int = 128, prune: bool = True) -> dict:
     col_len = np.diff(col_ptr)
     q_order = np.array(sorted(range(nb), key=lambda b: (-row_len[b], b)), dtype=np.int32)
     k_order = np.array(sorted(range(nb), key=lambda b: (-col_len[b], b)), dtype=np.int32)
+    empty = np.zeros(0, dtype=np.int32)
+    tile_start, tile_seq0, tile_seq_len = sequence_tiles(spec, tile) if seq else (empty,) * 3
     return {
+        "tile_start": tile_start,
+        "tile_seq0": tile_seq0,
+        "tile_seq_len": tile_seq_len,
         "n_blocks": nb,
         "nnz": int(row_ptr[-1]),
         "row_ptr": row_ptr,

@@ -592,3 +592,56 @@ def test_documents_index_equals_bitmask_index():
     b = block_index.build(n, MaskSpec(causal=True, bitmask=document_bitmask(n, lens)))
     for key in a:
         assert np.array_equal(np.asarray(a[key]), np.asarray(b[key])), key
+
+
+def test_sequence_tiles_hand_example():
+    # sequences [0,1) [1,201) [201,208) [208,337) [337,401): tiles start at
+    # each sequence's first token, 128 tokens apart, causal pairs only inside
+    # a sequence (1 + 3 + 1 + 3 + 1 = 9), every one cut by the diagonal or a
+    # sequence end
+    spec = MaskSpec(causal=True, doc_starts=(0, 1, 201, 208, 337, 401))
+    r = block_index.build(401, spec)
+    assert r["tile_start"].tolist() == [0, 1, 129, 201, 208, 336, 337]
+    assert r["tile_seq0"].tolist() == [0, 1, 1, 201, 208, 208, 337]
+    assert r["tile_seq_len"].tolist() == [1, 200, 200, 7, 129, 129, 64]
+    assert r["nnz"] == 9 and (r["kind"] == block_index.PARTIAL).all()
+    assert r["row_ptr"].tolist() == [0, 1, 2, 4, 5, 6, 8, 9]
+    assert r["col_idx"].tolist() == [0, 1, 1, 2, 3, 4, 4, 5, 6]
+    assert r["n_bit_tiles"] == 0
+
+
+@pytest.mark.parametrize("causal,window", [(True, None), (False, None), (True, 150), (False, 70)])
+def test_sequence_tiles_are_the_sequences_own_tiles(causal, window):
+    # the per-sequence index is the block-diagonal concatenation of every
+    # sequence's index built on its own (the plain single-sequence builder)
+    lens = [1, 300, 128, 129, 7, 511]
+    starts = tuple(int(x) for x in np.cumsum([0] + lens))
+    spec = MaskSpec(causal=causal, window=window, doc_starts=starts)
+    got = block_index.build(starts[-1], spec)
+    base, nnz = 0, 0
+    for s0, ln in zip(starts[:-1], lens):
+        own = block_index.build(ln, MaskSpec(causal=causal, window=window))
+        nb = own["n_blocks"]
+        rows = slice(base, base + nb)
+        assert (got["tile_start"][rows] == s0 + 128 * np.arange(nb)).all()
+        assert (got["tile_seq_len"][rows] == ln).all() and (got["tile_seq0"][rows] == s0).all()
+        for qb in range(nb):
+            a, e = got["row_ptr"][base + qb], got["row_ptr"][base + qb + 1]
+            oa, oe = own["row_ptr"][qb], own["row_ptr"][qb + 1]
+            assert (got["col_idx"][a:e] == base + own["col_idx"][oa:oe]).all()
+            assert (got["kind"][a:e] == own["kind"][oa:oe]).all()
+        base += nb
+        nnz += own["nnz"]
+    assert got["n_blocks"] == base and got["nnz"] == nnz
+
+
+def test_documents_with_block_patterns_keep_packed_tiles():
+    # block-level parts (dilation, strides, global tokens) and bit-packed
+    # masks are defined on the packed axis's 128-token blocks: those masks
+    # keep the packed tiling with bit tiles
+    starts = (0, 100, 300)
+    for spec in (MaskSpec(causal=True, stride=2, doc_starts=starts),
+                 MaskSpec(causal=True, window=50, global_tokens=128, doc_starts=starts)):
+        r = block_index.build(300, spec)
+        assert not block_index.sequence_tiled(spec) and r["tile_start"].size == 0
+        assert r["n_blocks"] == 3
