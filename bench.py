@@ -276,7 +276,8 @@ class Problem:
         self.o = torch.empty_like(self.q)
         self.lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
         self.dq, self.dk, self.dv = (torch.empty_like(self.q) for _ in range(3))
-        self.ws = torch.empty(api.bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
+        self.ws = torch.empty(api.bwd_workspace_bytes(B, H, N, d, self.index), dtype=torch.uint8,
+                              device=dev)
 
     def step(self, api, stream, ev=None):
         """fwd, then the backward's launches one by one; ev: events recorded

@@ -143,6 +143,21 @@ typedef struct flash_msa_block_index {
   uint32_t* bits;      /* [512 n_bit_tiles] */
   uint32_t* bits_t;    /* [512 n_bit_tiles] */
   int64_t live_elements; /* live (i, j) pairs of the mask over N x N; set by both build calls */
+  /* Per-sequence tiles (set by both build calls: 1 or 0).  A DOCUMENTS mask
+   * without BITMASK whose other flags are only CAUSAL and WINDOW is tiled per
+   * sequence: sequence [s0, s1) gets its own tiles starting at s0, s0 + 128,
+   * ..., so no tile holds tokens of two sequences and tile pairs of two
+   * sequences do not exist.  Tiles are numbered sequence by sequence;
+   * n_q_blocks = n_k_blocks = the number of tiles, and the lists above index
+   * tiles.  tile_start[t] is the first token of tile t, tile_seq0[t] and
+   * tile_seq_len[t] the first token and length of its sequence ([n_q_blocks]
+   * int32 each; NULL when sequence_tiles is 0).  Entries of a tile past its
+   * sequence's end are dead.  (Other DOCUMENTS masks are tiled on the packed
+   * axis, with bit tiles.) */
+  int32_t sequence_tiles;
+  int32_t* tile_start;
+  int32_t* tile_seq0;
+  int32_t* tile_seq_len;
 } flash_msa_block_index;
 
 /* Mask description (host memory).  A NULL mask, or flags == 0, is dense
@@ -182,8 +197,9 @@ typedef struct {
  * allocate every
  * array with those sizes (row_ptr/col_ptr n+1 int32, col_idx/row_idx nnz
  * int32, kind/kind_t nnz uint8, q_order/k_order n int32; with BITMASK also
- * bit_slot/bit_slot_t nnz int32 and bits/bits_t 512 n_bit_tiles uint32) and
- * call again to fill them.  mask->index is ignored.  Errors: INVALID_ARG
+ * bit_slot/bit_slot_t nnz int32 and bits/bits_t 512 n_bit_tiles uint32; with
+ * sequence_tiles also tile_start/tile_seq0/tile_seq_len n int32) and call
+ * again to fill them.  mask->index is ignored.  Errors: INVALID_ARG
  * (null, N < 1, bad field, BITMASK without mask->bitmask, DOCUMENTS without
  * offsets rising strictly from 0 to N), UNSUPPORTED (block != 128). */
 flash_msa_status flash_msa_build_block_index(const flash_msa_mask_desc* mask, int64_t N,
@@ -207,7 +223,9 @@ flash_msa_status flash_msa_fwd(const void* q, const void* k, const void* v, void
 
 /* Bytes of device workspace flash_msa_bwd() needs: two fp32 vectors per
  * (b, h), each padded to whole 128-row tiles -- -LSE_i * log2(e) and
- * D_i = sum_c dO_ic * O_ic -- rounded up to 256 bytes.  0 for invalid sizes. */
+ * D_i = sum_c dO_ic * O_ic -- rounded up to 256 bytes.  0 for invalid sizes.
+ * With a per-sequence tiled index the vectors hold 128 rows per tile: pass
+ * N = 128 * index->n_q_blocks. */
 size_t flash_msa_bwd_workspace_bytes(int B, int H, int64_t N, int d);
 
 /* Backward: given the forward's o and lse and the upstream gradient dO,

@@ -24,6 +24,9 @@ def compare(n, fields):
     if fields.get("bitmask") is not None:
         assert got.header.n_bit_tiles == ref["n_bit_tiles"]
         names = ARRAYS + ("bit_slot", "bit_slot_t", "bits", "bits_t")
+    assert got.sequence_tiles == (ref["tile_start"].size > 0)
+    if got.sequence_tiles:
+        names = names + ("tile_start", "tile_seq0", "tile_seq_len")
     for name in names:
         a, b = got.host[name], ref[name]
         assert a.dtype == b.dtype, name
@@ -119,6 +122,17 @@ def test_pattern_indices_match_hand_counts():
         assert (idx.nnz, int((kind == 0).sum()), int((kind == 1).sum())) == \
             (g["nnz"], g["full"], g["partial"]), key
         assert api.check_block_index(idx) == api.OK
+
+
+@pytest.mark.parametrize("lens", [(1, 300, 128, 129, 7, 511), (5000,), (127, 1, 1, 2, 256)])
+@pytest.mark.parametrize("fields", [{"causal": True}, {}, {"causal": True, "window": 150},
+                                    {"window": 70}])
+def test_sequence_tile_indices_bit_exact(lens, fields):
+    # packed sequences with a causal / window mask are tiled per sequence,
+    # bit-exact with the oracle's per-sequence build
+    starts = tuple(int(x) for x in np.cumsum((0,) + lens))
+    got = compare(starts[-1], dict(fields, doc_starts=starts))
+    assert got.sequence_tiles and got.n_tiles == sum((n + 127) // 128 for n in lens)
 
 
 def test_checker_rejects_corruption():

@@ -346,3 +346,22 @@ def test_side_streams_match_default_stream():
     for got in outs:
         for name, a, b in zip(("o", "lse", "dq", "dk", "dv"), got, ref):
             assert torch.equal(a, b), name
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("lens", [(1, 300, 128, 129, 7, 211), (517,), (90, 1, 2, 300, 130)])
+@pytest.mark.parametrize("extra", [{"causal": True}, {}, {"causal": True, "window": 150},
+                                   {"window": 70}, {"causal": True, "stride": 2}])
+def test_packed_sequences(d, lens, extra):
+    """Sequences packed on one axis (the DOCUMENTS mask): with causal / window
+    parts the index tiles every sequence from its own first token (no tile
+    spans two sequences); with a block-level part (strides) it keeps the
+    packed 128-token tiles with bit tiles.  Both against the oracle, element
+    by element."""
+    starts = tuple(int(x) for x in np.cumsum((0,) + lens))
+    fields = dict(extra, doc_starts=starts)
+    inp = small_inputs(2, starts[-1], 3, d, seed=sum(lens) + 3 * d + len(extra))
+    mask = api.Mask(**fields)
+    assert api.build_block_index(mask, starts[-1]).sequence_tiles == ("stride" not in extra)
+    res = gc.run_gpu(inp, fields)
+    gc.full_compare(inp, fields, res)

@@ -69,6 +69,10 @@ class BlockIndexStruct(ctypes.Structure):
         ("bits", ctypes.c_void_p),
         ("bits_t", ctypes.c_void_p),
         ("live_elements", ctypes.c_int64),
+        ("sequence_tiles", ctypes.c_int32),
+        ("tile_start", ctypes.c_void_p),
+        ("tile_seq0", ctypes.c_void_p),
+        ("tile_seq_len", ctypes.c_void_p),
     ]
 
 
@@ -214,7 +218,9 @@ _INDEX_ARRAYS = (("row_ptr", np.int32, "nq1"), ("col_idx", np.int32, "nnz"),
                  ("row_idx", np.int32, "nnz"), ("kind_t", np.uint8, "nnz"),
                  ("q_order", np.int32, "nq"), ("k_order", np.int32, "nk"),
                  ("bit_slot", np.int32, "nnz"), ("bit_slot_t", np.int32, "nnz"),
-                 ("bits", np.uint32, "nbits"), ("bits_t", np.uint32, "nbits"))
+                 ("bits", np.uint32, "nbits"), ("bits_t", np.uint32, "nbits"),
+                 ("tile_start", np.int32, "ntiles"), ("tile_seq0", np.int32, "ntiles"),
+                 ("tile_seq_len", np.int32, "ntiles"))
 
 
 class BlockIndex:
@@ -234,12 +240,27 @@ class BlockIndex:
         """Live (i, j) pairs of the mask over the N x N score matrix."""
         return int(self.header.live_elements)
 
+    @property
+    def sequence_tiles(self) -> bool:
+        """Tiled per sequence (packed sequences with a causal / window mask)."""
+        return bool(self.header.sequence_tiles)
+
+    @property
+    def n_tiles(self) -> int:
+        return int(self.header.n_q_blocks)
+
+    def _copy_header(self, s: BlockIndexStruct):
+        s.n_bit_tiles = self.header.n_bit_tiles
+        s.live_elements = self.header.live_elements
+        s.sequence_tiles = self.header.sequence_tiles
+
     def host_struct(self) -> BlockIndexStruct:
         s = BlockIndexStruct(self.header.seq_len, self.header.n_q_blocks, self.header.n_k_blocks,
                              self.header.block, self.header.nnz)
-        s.n_bit_tiles = self.header.n_bit_tiles
-        s.live_elements = self.header.live_elements
-        for name, _, _ in _INDEX_ARRAYS:
+        self._copy_header(s)
+        for name, _, kind in _INDEX_ARRAYS:
+            if kind == "ntiles" and not self.sequence_tiles:
+                continue  # null: packed tiling
             setattr(s, name, self.host[name].ctypes.data)
         return s
 
@@ -249,11 +270,11 @@ class BlockIndex:
                        for name, arr in self.host.items()}
         s = BlockIndexStruct(self.header.seq_len, self.header.n_q_blocks, self.header.n_k_blocks,
                              self.header.block, self.header.nnz)
-        s.n_bit_tiles = self.header.n_bit_tiles
-        s.live_elements = self.header.live_elements
-        for name, _, _ in _INDEX_ARRAYS:
-            t = self.device[name]
-            setattr(s, name, t.data_ptr())
+        self._copy_header(s)
+        for name, _, kind in _INDEX_ARRAYS:
+            if kind == "ntiles" and not self.sequence_tiles:
+                continue
+            setattr(s, name, self.device[name].data_ptr())
         self.device_struct = s
         return self
 
@@ -266,11 +287,14 @@ def build_block_index(mask: Mask, n: int) -> BlockIndex:
     _check(L.flash_msa_build_block_index(ctypes.byref(desc), n, ctypes.byref(hdr)),
            "build_block_index(count)")
     sizes = {"nq1": hdr.n_q_blocks + 1, "nk1": hdr.n_k_blocks + 1, "nnz": hdr.nnz,
-             "nq": hdr.n_q_blocks, "nk": hdr.n_k_blocks, "nbits": 512 * hdr.n_bit_tiles}
+             "nq": hdr.n_q_blocks, "nk": hdr.n_k_blocks, "nbits": 512 * hdr.n_bit_tiles,
+             "ntiles": hdr.n_q_blocks if hdr.sequence_tiles else 0}
     host = {name: np.zeros(max(1, sizes[kind]), dtype=dt) for name, dt, kind in _INDEX_ARRAYS}
     out = BlockIndexStruct(hdr.seq_len, hdr.n_q_blocks, hdr.n_k_blocks, hdr.block, hdr.nnz)
     out.n_bit_tiles = hdr.n_bit_tiles
-    for name, _, _ in _INDEX_ARRAYS:
+    for name, _, kind in _INDEX_ARRAYS:
+        if kind == "ntiles" and not hdr.sequence_tiles:
+            continue
         setattr(out, name, host[name].ctypes.data)
     _check(L.flash_msa_build_block_index(ctypes.byref(desc), n, ctypes.byref(out)),
            "build_block_index(fill)")
@@ -392,7 +416,11 @@ def fwd(q, k, v, mask: Optional[Mask] = None, index: Optional[BlockIndex] = None
     return o, l
 
 
-def bwd_workspace_bytes(B, H, N, d) -> int:
+def bwd_workspace_bytes(B, H, N, d, index: Optional["BlockIndex"] = None) -> int:
+    """Workspace of flash_msa_bwd; with a per-sequence tiled index the vectors
+    hold 128 rows per tile."""
+    if index is not None and index.sequence_tiles:
+        N = 128 * index.n_tiles
     return int(lib().flash_msa_bwd_workspace_bytes(B, H, N, d))
 
 
@@ -401,8 +429,10 @@ BWD_DETERMINISTIC = BWD_PREPROCESS | BWD_DKDV | BWD_DQ      # flash_msa_bwd: two
 BWD_ACCUMULATED = BWD_PREPROCESS | BWD_FUSED | BWD_DQ_CONVERT  # dQ accumulated in fp32
 
 
-def bwd_stages_workspace_bytes(B, H, N, d, stages) -> int:
+def bwd_stages_workspace_bytes(B, H, N, d, stages, index: Optional["BlockIndex"] = None) -> int:
     """Workspace of flash_msa_bwd_stages for this set of stages."""
+    if index is not None and index.sequence_tiles:
+        N = 128 * index.n_tiles
     return int(lib().flash_msa_bwd_stages_workspace_bytes(B, H, N, d, stages))
 
 
@@ -429,8 +459,8 @@ def bwd(q, k, v, o, lse, do, mask: Optional[Mask] = None, index: Optional[BlockI
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    ws_bytes = (bwd_workspace_bytes(B, H, N, d) if stages is None
-                else bwd_stages_workspace_bytes(B, H, N, d, stages))
+    ws_bytes = (bwd_workspace_bytes(B, H, N, d, index) if stages is None
+                else bwd_stages_workspace_bytes(B, H, N, d, stages, index))
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
     desc, _keep = _mask_desc(mask, index, N)

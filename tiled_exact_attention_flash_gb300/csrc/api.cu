@@ -161,12 +161,21 @@ static flash_msa_status make_lists(const flash_msa_mask_desc* m, int64_t N, bool
       return set_error(FLASH_MSA_ERR_INDEX, "mask has window/dilation/stride flags but no index");
     return FLASH_MSA_OK;
   }
-  if (ix->seq_len != N || ix->block != kTile || ix->n_q_blocks != nb || ix->n_k_blocks != nb ||
-      ix->nnz < 0)
+  const int nt = ix->sequence_tiles ? ix->n_q_blocks : nb;  // tiles along each axis
+  if (ix->seq_len != N || ix->block != kTile || ix->n_q_blocks != nt || ix->n_k_blocks != nt ||
+      ix->nnz < 0 || nt < 1)
     return set_error(FLASH_MSA_ERR_INDEX,
                      "index built for N=%lld block=%d blocks=%dx%d, call has N=%lld",
                      static_cast<long long>(ix->seq_len), ix->block, ix->n_q_blocks,
                      ix->n_k_blocks, static_cast<long long>(N));
+  if (ix->sequence_tiles) {
+    if (!ix->tile_start || !ix->tile_seq0 || !ix->tile_seq_len)
+      return set_error(FLASH_MSA_ERR_INDEX, "index: per-sequence tile arrays missing");
+    rows.n_blocks = cols.n_blocks = nt;
+    rows.t_start = cols.t_start = ix->tile_start;
+    rows.t_seq0 = cols.t_seq0 = ix->tile_seq0;
+    rows.t_len = cols.t_len = ix->tile_seq_len;
+  }
   if (!ix->row_ptr || !ix->col_idx || !ix->kind || !ix->q_order)
     return set_error(FLASH_MSA_ERR_INDEX, "index: CSR arrays or q_order missing");
   const bool bits = (m->flags & (FLASH_MSA_BITMASK | FLASH_MSA_DOCUMENTS)) && ix->n_bit_tiles > 0;
@@ -214,6 +223,129 @@ const char* flash_msa_last_error_string(void) { return g_last_error; }
 
 const char* flash_msa_version(void) { return "libflashmsa 0.1 (sm_103a, tcgen05)"; }
 
+// CSC (by counting sort: query blocks come out ascending within each
+// column) and the longest-first orders, from a filled CSR.
+static void finish_lists(flash_msa_block_index* out, int64_t nb,
+                         const std::vector<int32_t>& col_count, bool with_bits) {
+  out->col_ptr[0] = 0;
+  for (int64_t kb = 0; kb < nb; ++kb) out->col_ptr[kb + 1] = out->col_ptr[kb] + col_count[size_t(kb)];
+  std::vector<int32_t> fill(out->col_ptr, out->col_ptr + nb);
+  for (int64_t qb = 0; qb < nb; ++qb)
+    for (int32_t e = out->row_ptr[qb]; e < out->row_ptr[qb + 1]; ++e) {
+      const int32_t kb = out->col_idx[e];
+      const int32_t dst = fill[size_t(kb)]++;
+      out->row_idx[dst] = int32_t(qb);
+      out->kind_t[dst] = out->kind[e];
+      if (with_bits) out->bit_slot_t[dst] = out->bit_slot[e];
+    }
+  // longest-first orders (stable)
+  for (int64_t b = 0; b < nb; ++b) out->q_order[b] = out->k_order[b] = int32_t(b);
+  std::stable_sort(out->q_order, out->q_order + nb, [&](int32_t a, int32_t b) {
+    return out->row_ptr[a + 1] - out->row_ptr[a] > out->row_ptr[b + 1] - out->row_ptr[b];
+  });
+  std::stable_sort(out->k_order, out->k_order + nb, [&](int32_t a, int32_t b) {
+    return out->col_ptr[a + 1] - out->col_ptr[a] > out->col_ptr[b + 1] - out->col_ptr[b];
+  });
+}
+
+// Live (i, j) pairs of a live tile (qb, kb) of class k (0 full) of one
+// sequence of n tokens: all valid entries of a full tile, one interval of
+// columns per row of a partial one (the kernels' row_live_range).
+static int64_t tile_live_count(int qb, int kb, int k, int64_t n, const MaskParams& mp) {
+  const int64_t i0 = int64_t(qb) * kTile, j0 = int64_t(kb) * kTile;
+  const int64_t rows = std::min<int64_t>(kTile, n - i0), cols = std::min<int64_t>(kTile, n - j0);
+  if (k == 0) return rows * cols;
+  const DeltaRange r = tile_delta_range(qb, kb, mp);
+  if (r.none) return 0;
+  int64_t live = 0;
+  for (int64_t row = 0; row < rows; ++row) {
+    const int64_t i = i0 + row;
+    const int64_t clo = std::max<int64_t>(i - r.hi - j0, 0);
+    const int64_t chi = std::min<int64_t>({i - r.lo - j0, n - 1 - j0, int64_t(kTile - 1)});
+    if (chi >= clo) live += chi - clo + 1;
+  }
+  return live;
+}
+
+// Per-sequence tiles of packed sequences (flash_msa_block_index,
+// sequence_tiles): every sequence is tiled from its own first token and its
+// tile pairs are classified with the in-sequence mask parts (causal, window)
+// and the sequence's own length; tiles are numbered sequence by sequence.
+// Both build phases (counts only when out->row_ptr is null).
+static flash_msa_status build_sequence_tiles(const flash_msa_mask_desc* mask,
+                                             const MaskParams& mask_params, int64_t N,
+                                             flash_msa_block_index* out) {
+  MaskParams mp = mask_params;
+  mp.flags &= FLASH_MSA_CAUSAL | FLASH_MSA_WINDOW;
+  const int64_t* ds = mask->doc_starts;
+  const bool window = (mp.flags & FLASH_MSA_WINDOW) != 0;
+  const int64_t span = window ? mp.window / kTile + 2 : int64_t(1) << 40;
+  // key tiles of query tile m in a sequence of nb tiles that may be live
+  auto key_range = [&](int64_t m, int64_t nb, int64_t& k0, int64_t& k1) {
+    k0 = std::max<int64_t>(0, m - span);
+    k1 = std::min<int64_t>(nb - 1, m + span);
+    if (mp.flags & FLASH_MSA_CAUSAL) k1 = std::min(k1, m);
+  };
+  int64_t nt = 0, nnz = 0, live = 0;
+  for (int64_t d = 0; d < mask->n_docs; ++d) {
+    const int64_t len = ds[d + 1] - ds[d], nb = (len + kTile - 1) / kTile;
+    nt += nb;
+    for (int64_t m = 0; m < nb; ++m) {
+      int64_t k0, k1;
+      key_range(m, nb, k0, k1);
+      for (int64_t k = k0; k <= k1; ++k) {
+        const int c = classify_tile(int(m), int(k), len, mp);
+        if (c < 0) continue;
+        ++nnz;
+        live += tile_live_count(int(m), int(k), c, len, mp);
+      }
+    }
+  }
+  if (nt > INT32_MAX || nnz > INT32_MAX)
+    return set_error(FLASH_MSA_ERR_INVALID_ARG, "build_block_index: more than 2^31 tiles");
+  out->seq_len = N;
+  out->block = kTile;
+  out->n_q_blocks = out->n_k_blocks = int32_t(nt);
+  out->n_bit_tiles = 0;
+  out->live_elements = live;
+  out->sequence_tiles = 1;
+  if (!out->row_ptr) {
+    out->nnz = nnz;
+    return FLASH_MSA_OK;
+  }
+  if (out->nnz != nnz)
+    return set_error(FLASH_MSA_ERR_INVALID_ARG, "build_block_index: nnz %lld, the mask has %lld",
+                     static_cast<long long>(out->nnz), static_cast<long long>(nnz));
+  if (!out->col_idx || !out->kind || !out->col_ptr || !out->row_idx || !out->kind_t ||
+      !out->q_order || !out->k_order || !out->tile_start || !out->tile_seq0 || !out->tile_seq_len)
+    return set_error(FLASH_MSA_ERR_INVALID_ARG, "build_block_index: some output arrays are null");
+  std::vector<int32_t> col_count(size_t(nt), 0);
+  int64_t pos = 0, base = 0;
+  out->row_ptr[0] = 0;
+  for (int64_t d = 0; d < mask->n_docs; ++d) {
+    const int64_t len = ds[d + 1] - ds[d], nb = (len + kTile - 1) / kTile;
+    for (int64_t m = 0; m < nb; ++m) {
+      out->tile_start[base + m] = int32_t(ds[d] + m * kTile);
+      out->tile_seq0[base + m] = int32_t(ds[d]);
+      out->tile_seq_len[base + m] = int32_t(len);
+      int64_t k0, k1;
+      key_range(m, nb, k0, k1);
+      for (int64_t k = k0; k <= k1; ++k) {
+        const int c = classify_tile(int(m), int(k), len, mp);
+        if (c < 0) continue;
+        out->col_idx[pos] = int32_t(base + k);
+        out->kind[pos] = uint8_t(c);
+        ++col_count[size_t(base + k)];
+        ++pos;
+      }
+      out->row_ptr[base + m + 1] = int32_t(pos);
+    }
+    base += nb;
+  }
+  finish_lists(out, nt, col_count, false);
+  return FLASH_MSA_OK;
+}
+
 flash_msa_status flash_msa_build_block_index(const flash_msa_mask_desc* mask, int64_t N,
                                              flash_msa_block_index* out) {
   g_last_error[0] = 0;
@@ -251,6 +383,11 @@ flash_msa_status flash_msa_build_block_index(const flash_msa_mask_desc* mask, in
       }
     }
   }
+  // packed sequences with in-sequence (delta-only) parts: one tiling per sequence
+  const uint32_t in_sequence = FLASH_MSA_CAUSAL | FLASH_MSA_WINDOW | FLASH_MSA_DOCUMENTS;
+  if (with_docs && !with_bitmask && (mask->flags & ~in_sequence) == 0)
+    return build_sequence_tiles(mask, mp, N, out);
+  out->sequence_tiles = 0;
   const int64_t nb = n_blocks_of(N);
   const int64_t words_per_row = (N + 31) / 32;
   // Tile class with the bits: live entries of row r = interval of the other
@@ -410,36 +547,35 @@ flash_msa_status flash_msa_build_block_index(const flash_msa_mask_desc* mask, in
                      static_cast<long long>(pos), static_cast<long long>(slot));
   if (!with_bits) out->n_bit_tiles = 0;
   out->live_elements = live;
-  // CSC by counting sort: query blocks come out ascending within each column
-  out->col_ptr[0] = 0;
-  for (int64_t kb = 0; kb < nb; ++kb) out->col_ptr[kb + 1] = out->col_ptr[kb] + col_count[size_t(kb)];
-  std::vector<int32_t> fill(out->col_ptr, out->col_ptr + nb);
-  for (int64_t qb = 0; qb < nb; ++qb)
-    for (int32_t e = out->row_ptr[qb]; e < out->row_ptr[qb + 1]; ++e) {
-      const int32_t kb = out->col_idx[e];
-      const int32_t dst = fill[size_t(kb)]++;
-      out->row_idx[dst] = int32_t(qb);
-      out->kind_t[dst] = out->kind[e];
-      if (with_bits) out->bit_slot_t[dst] = out->bit_slot[e];
-    }
-  // longest-first orders (stable)
-  for (int64_t b = 0; b < nb; ++b) out->q_order[b] = out->k_order[b] = int32_t(b);
-  std::stable_sort(out->q_order, out->q_order + nb, [&](int32_t a, int32_t b) {
-    return out->row_ptr[a + 1] - out->row_ptr[a] > out->row_ptr[b + 1] - out->row_ptr[b];
-  });
-  std::stable_sort(out->k_order, out->k_order + nb, [&](int32_t a, int32_t b) {
-    return out->col_ptr[a + 1] - out->col_ptr[a] > out->col_ptr[b + 1] - out->col_ptr[b];
-  });
+  finish_lists(out, nb, col_count, with_bits);
   return FLASH_MSA_OK;
+}
+
+// Per-sequence tiles cover [0, N) sequence by sequence, 128 tokens apart
+// inside each sequence.
+static bool tile_geometry_ok(const flash_msa_block_index* ix, int64_t N) {
+  if (!ix->tile_start || !ix->tile_seq0 || !ix->tile_seq_len) return false;
+  int64_t expect = 0;  // first token of the next tile
+  for (int64_t t = 0; t < ix->n_q_blocks; ++t) {
+    const int64_t st = ix->tile_start[t], s0 = ix->tile_seq0[t], len = ix->tile_seq_len[t];
+    if (len < 1 || s0 < 0 || s0 + len > N || st != expect || (st - s0) % kTile != 0 || st < s0 ||
+        st >= s0 + len)
+      return false;
+    expect = st + kTile < s0 + len ? st + kTile : s0 + len;
+  }
+  return expect == N;
 }
 
 flash_msa_status flash_msa_check_block_index(const flash_msa_block_index* ix, int64_t N) {
   g_last_error[0] = 0;
   if (!ix) return set_error(FLASH_MSA_ERR_INVALID_ARG, "check_block_index: null index");
-  const int64_t nb = n_blocks_of(N);
-  if (ix->seq_len != N || ix->block != kTile || ix->n_q_blocks != nb || ix->n_k_blocks != nb)
+  const int64_t nb = ix->sequence_tiles ? int64_t(ix->n_q_blocks) : n_blocks_of(N);
+  if (ix->seq_len != N || ix->block != kTile || ix->n_q_blocks != nb || ix->n_k_blocks != nb ||
+      nb < 1)
     return set_error(FLASH_MSA_ERR_INDEX, "index: header does not match N=%lld",
                      static_cast<long long>(N));
+  if (ix->sequence_tiles && !tile_geometry_ok(ix, N))
+    return set_error(FLASH_MSA_ERR_INDEX, "index: per-sequence tile geometry is inconsistent");
   if (!ix->row_ptr || !ix->col_idx || !ix->kind || !ix->col_ptr || !ix->row_idx || !ix->kind_t ||
       !ix->q_order || !ix->k_order)
     return set_error(FLASH_MSA_ERR_INDEX, "index: missing array");
@@ -458,6 +594,11 @@ flash_msa_status flash_msa_check_block_index(const flash_msa_block_index* ix, in
   };
   if (!check_lists(ix->row_ptr, ix->col_idx, ix->kind, "CSR"))
     return set_error(FLASH_MSA_ERR_INDEX, "index: CSR arrays are inconsistent");
+  if (ix->sequence_tiles)
+    for (int64_t qb = 0; qb < nb; ++qb)
+      for (int32_t e = ix->row_ptr[qb]; e < ix->row_ptr[qb + 1]; ++e)
+        if (ix->tile_seq0[ix->col_idx[e]] != ix->tile_seq0[qb])
+          return set_error(FLASH_MSA_ERR_INDEX, "index: a tile pair spans two sequences");
   if (ix->n_bit_tiles < 0)
     return set_error(FLASH_MSA_ERR_INDEX, "index: negative bit tile count");
   if (ix->n_bit_tiles > 0) {
@@ -604,15 +745,25 @@ static flash_msa_status bwd_impl(const void* q, const void* k, const void* v, co
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
       (reinterpret_cast<uintptr_t>(lse) & 3u))
     return set_error(FLASH_MSA_ERR_INVALID_ARG, "bwd: tensors must be 16-byte aligned");
-  const size_t need_ws = flash_msa_bwd_stages_workspace_bytes(B, H, N, d, stages);
-  if (!workspace || workspace_bytes < need_ws || !aligned16(workspace))
-    return set_error(FLASH_MSA_ERR_WORKSPACE, "bwd: workspace of %zu bytes required (got %zu)",
-                     need_ws, workspace_bytes);
   BwdLaunch a;
   memset(&a, 0, sizeof(a));
   bool need = false;
   if ((st = check_mask(mask, a.mask, need)) != FLASH_MSA_OK) return st;
   if ((st = make_lists(mask, N, need, true, a.rows, a.cols)) != FLASH_MSA_OK) return st;
+  // the vectors hold 128 rows per tile: per-sequence tiles may outnumber
+  // ceil(N / 128)
+  const int64_t n_rows = int64_t(a.rows.n_blocks) * kTile;
+  const bool seq_tiles = a.rows.t_start != nullptr;
+  if (seq_tiles && (stages & kAccumulatorStages))
+    return set_error(FLASH_MSA_ERR_UNSUPPORTED,
+                     "bwd: the accumulated-dQ stages do not take per-sequence tiles");
+  const size_t need_ws = flash_msa_bwd_stages_workspace_bytes(B, H, n_rows, d, stages);
+  if (need_ws == 0)
+    return set_error(FLASH_MSA_ERR_INVALID_ARG, "bwd: %lld tile rows are too many",
+                     static_cast<long long>(n_rows));
+  if (!workspace || workspace_bytes < need_ws || !aligned16(workspace))
+    return set_error(FLASH_MSA_ERR_WORKSPACE, "bwd: workspace of %zu bytes required (got %zu)",
+                     need_ws, workspace_bytes);
   a.q = q;
   a.k = k;
   a.v = v;
@@ -627,7 +778,7 @@ static flash_msa_status bwd_impl(const void* q, const void* k, const void* v, co
   // zeroes it) by the accumulated-dQ stages, and by PREPROCESS run on its own
   // when the workspace holds it (a stage-by-stage accumulated backward)
   const bool acc_call = (stages & kAccumulatorStages) ||
-                        (stages == FLASH_MSA_BWD_PREPROCESS &&
+                        (stages == FLASH_MSA_BWD_PREPROCESS && !seq_tiles &&
                          workspace_bytes >= flash_msa_bwd_stages_workspace_bytes(
                                                 B, H, N, d, FLASH_MSA_BWD_ACCUMULATED));
   a.dqacc = acc_call

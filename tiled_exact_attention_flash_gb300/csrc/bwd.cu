@@ -45,6 +45,7 @@ struct PreParams {
   float* dsum;  // (B, H, NP)
   float* dqacc;  // (B, H, NP, d) fp32 dQ accumulator to zero, or null
   int B, H, N, NP;
+  ListParams geo;  // tiles of the rows: row i of the vectors is entry i % 128 of tile i / 128
 };
 
 template <int HD>
@@ -59,9 +60,14 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreParams p) {
     z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
     z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  // the token of vector row i: entry i % 128 of tile i / 128
+  const TileGeo tg = tile_geo(p.geo, int(i / kTile), p.N);
+  const int64_t loc = int64_t(tg.lb) * kTile + i % kTile;  // token within its sequence
+  const int64_t tok = tg.row0 + i % kTile;                 // token on the sequence axis
+  const bool live_row = i < p.NP && loc < tg.n;
   float acc = 0.f;
-  if (i < p.N) {
-    const int64_t off = ((int64_t(b) * p.N + i) * p.H + h) * HD + c * 8;
+  if (live_row) {
+    const int64_t off = ((int64_t(b) * p.N + tok) * p.H + h) * HD + c * 8;
     const uint4 ov = *reinterpret_cast<const uint4*>(p.o + off);
     const uint4 gv = *reinterpret_cast<const uint4*>(p.dout + off);
     const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
@@ -79,8 +85,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreParams p) {
   if (c == 0 && i < p.NP) {
     const int64_t at = (int64_t(b) * p.H + h) * p.NP + i;
     float nl2 = -INFINITY;  // a row without live keys has P = 0, like padding
-    if (i < p.N) {
-      const float l = p.lse[(int64_t(b) * p.H + h) * p.N + i];
+    if (live_row) {
+      const float l = p.lse[(int64_t(b) * p.H + h) * p.N + tok];
       nl2 = (l == -INFINITY) ? -INFINITY : -l * kLog2e;
     }
     p.nlse2[at] = nl2;
@@ -269,11 +275,11 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint8_t* smem, 
       break;
     }
     mbar_arrive_expect_tx(bar(L::kFixFull), (kKeyStationary ? 2 : 1) * L::kTileBytes);
-    load_tile_2d<HD>(fix_a, smem_u32(smem + L::kFixOff), bar(L::kFixFull), un.ob * kTile, un.h,
-                     un.b);
+    const int fix_row = int(tile_geo(p.list, un.ob, p.N).row0);
+    load_tile_2d<HD>(fix_a, smem_u32(smem + L::kFixOff), bar(L::kFixFull), fix_row, un.h, un.b);
     if (kKeyStationary) {
       load_tile_2d<HD>(fix_b, smem_u32(smem + L::kFixOff + L::kTileBytes), bar(L::kFixFull),
-                       un.ob * kTile, un.h, un.b);
+                       fix_row, un.h, un.b);
     } else {
       // the elementwise warps read the next unit's dO rows with plain loads:
       // start pulling them into L2 now
@@ -281,7 +287,7 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint8_t* smem, 
         const Unit nx = bwd_decode<false>(u_next, p);
 #pragma unroll
         for (int c = 0; c < HD / 64; ++c)
-          tma_prefetch_l2_4d(fix_b, c * 64, nx.ob * kTile, nx.h, nx.b);
+          tma_prefetch_l2_4d(fix_b, c * 64, int(tile_geo(p.list, nx.ob, p.N).row0), nx.h, nx.b);
       }
     }
     last_fix = int(fe_cnt);
@@ -291,6 +297,7 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint8_t* smem, 
       int hq;
       const InnerTile it = bwd_inner<kKeyStationary>(un, t, p, hq);
       const int hr = kKeyStationary ? hq : hkv;  // head of the streamed tiles
+      const int ring_row = int(tile_geo(p.list, it.blk, p.N).row0);
       for (int half = 0; half < 2; ++half) {
         if (!wait_bar(bar(L::kRingEmpty + stage), phase ^ 1, abort_flag, p.status, 2)) {
           ok = false;
@@ -300,7 +307,7 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint8_t* smem, 
         if (half == 0) {
           const bool vec = kKeyStationary;
           mbar_arrive_expect_tx(bar(L::kRingFull + stage), L::kTileBytes + (vec ? 1024 : 0));
-          load_tile_2d<HD>(ring_a, dst, bar(L::kRingFull + stage), it.blk * kTile, hr, un.b);
+          load_tile_2d<HD>(ring_a, dst, bar(L::kRingFull + stage), ring_row, hr, un.b);
           if (vec) {
             const int64_t row0 = (int64_t(un.b) * p.H + hq) * p.NP + int64_t(it.blk) * kTile;
             const uint32_t vdst = smem_u32(smem + L::kVecOff + (stage / 2) * 1024);
@@ -309,7 +316,7 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint8_t* smem, 
           }
         } else {
           mbar_arrive_expect_tx(bar(L::kRingFull + stage), L::kTileBytes);
-          load_tile_2d<HD>(ring_b, dst, bar(L::kRingFull + stage), it.blk * kTile, hr, un.b);
+          load_tile_2d<HD>(ring_b, dst, bar(L::kRingFull + stage), ring_row, hr, un.b);
         }
         last[stage] = int(phase);
         if (++stage == L::kStages) {
@@ -322,9 +329,10 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint8_t* smem, 
         const InnerTile ft = bwd_inner<kKeyStationary>(un, t + kL2PrefetchTiles, p, fq);
         const int fr = kKeyStationary ? fq : hkv;
 #pragma unroll
+        const int pf_row = int(tile_geo(p.list, ft.blk, p.N).row0);
         for (int c = 0; c < HD / 64; ++c) {
-          tma_prefetch_l2_4d(ring_a, c * 64, ft.blk * kTile, fr, un.b);
-          tma_prefetch_l2_4d(ring_b, c * 64, ft.blk * kTile, fr, un.b);
+          tma_prefetch_l2_4d(ring_a, c * 64, pf_row, fr, un.b);
+          tma_prefetch_l2_4d(ring_b, c * 64, pf_row, fr, un.b);
         }
       }
     }
@@ -710,10 +718,13 @@ __device__ __forceinline__ void dkdv_elementwise(const BwdParams& p, uint8_t* sm
     const int u = queue_pop<true>(queue, abort_flag, p.status);
     if (u < 0) return;
     const Unit un = bwd_decode<true>(u, p);
-    const int64_t j = int64_t(un.ob) * kTile + row;  // key token
-    const bool valid = j < p.N;
-    __nv_bfloat16* dk_row = p.out_a + ((int64_t(un.b) * p.N + j) * p.Hkv + un.h) * HD;
-    __nv_bfloat16* dv_row = p.out_b + ((int64_t(un.b) * p.N + j) * p.Hkv + un.h) * HD;
+    // this key row: token j of its sequence (kg.n tokens), token kg.row0 + row of the axis
+    const TileGeo kg = tile_geo(p.list, un.ob, p.N);
+    const int64_t j = int64_t(kg.lb) * kTile + row;
+    const bool valid = j < kg.n;
+    const int64_t ktok = kg.row0 + row;
+    __nv_bfloat16* dk_row = p.out_a + ((int64_t(un.b) * p.N + ktok) * p.Hkv + un.h) * HD;
+    __nv_bfloat16* dv_row = p.out_b + ((int64_t(un.b) * p.N + ktok) * p.Hkv + un.h) * HD;
     if (un.n == 0) {
       if (g == 0) {
         zero_row(dk_row, HD, valid);
@@ -726,7 +737,8 @@ __device__ __forceinline__ void dkdv_elementwise(const BwdParams& p, uint8_t* sm
       const InnerTile it = bwd_inner<true>(un, t, p, hq);
       int lo = 0, hi = kTile - 1;
       if (it.dead) hi = -1;
-      else if (it.partial) col_live_range(j, it.blk, un.ob, p.N, p.mask, lo, hi);
+      else if (it.partial)
+        col_live_range(j, tile_geo(p.list, it.blk, p.N).lb, kg.lb, kg.n, p.mask, lo, hi);
       prefetch_tile_bits(p.list, it.slot, row);
       const float* vec =
           reinterpret_cast<const float*>(smem + L::kVecOff + ((cnt % L::kStages) / 2) * 1024);
@@ -856,12 +868,13 @@ __device__ __forceinline__ void fused_elementwise(const BwdParams& p, uint8_t* s
   uint32_t sv[64];  // P^T of the current tile (fp32), from pass 1 to pass 2
   // pass 1: P^T = exp2(scale*log2e * S^T - LSE*log2e) on live entries, bf16
   // to columns [64 g, 64 g + 32) of A, p_full
-  auto pass1 = [&](const Unit& un, int t, int64_t j, const float* vec) -> bool {
+  auto pass1 = [&](const Unit& un, int t, int64_t j, const TileGeo& kg, const float* vec) -> bool {
     int hq;
     const InnerTile it = bwd_inner<true>(un, t, p, hq);
     int lo = 0, hi = kTile - 1;
     if (it.dead) hi = -1;
-    else if (it.partial) col_live_range(j, it.blk, un.ob, p.N, p.mask, lo, hi);
+    else if (it.partial)
+      col_live_range(j, tile_geo(p.list, it.blk, p.N).lb, kg.lb, kg.n, p.mask, lo, hi);
     prefetch_tile_bits(p.list, it.slot, row);
     const bool ok = wait_bar(bar(L::kSFull), s1_cnt & 1, abort_flag, p.status, 20);
     if (!__all_sync(0xFFFFFFFFu, ok)) return false;
@@ -981,10 +994,13 @@ __device__ __forceinline__ void fused_elementwise(const BwdParams& p, uint8_t* s
     const int u = queue_pop<true>(queue, abort_flag, p.status);
     if (u < 0) return;
     const Unit un = bwd_decode<true>(u, p);
-    const int64_t j = int64_t(un.ob) * kTile + row;  // key token
-    const bool valid = j < p.N;
-    __nv_bfloat16* dk_row = p.out_a + ((int64_t(un.b) * p.N + j) * p.Hkv + un.h) * HD;
-    __nv_bfloat16* dv_row = p.out_b + ((int64_t(un.b) * p.N + j) * p.Hkv + un.h) * HD;
+    // this key row: token j of its sequence (kg.n tokens), token kg.row0 + row of the axis
+    const TileGeo kg = tile_geo(p.list, un.ob, p.N);
+    const int64_t j = int64_t(kg.lb) * kTile + row;
+    const bool valid = j < kg.n;
+    const int64_t ktok = kg.row0 + row;
+    __nv_bfloat16* dk_row = p.out_a + ((int64_t(un.b) * p.N + ktok) * p.Hkv + un.h) * HD;
+    __nv_bfloat16* dv_row = p.out_b + ((int64_t(un.b) * p.N + ktok) * p.Hkv + un.h) * HD;
     if (un.n == 0) {
       if (g == 0) {
         zero_row(dk_row, HD, valid);
@@ -992,11 +1008,11 @@ __device__ __forceinline__ void fused_elementwise(const BwdParams& p, uint8_t* s
       }
       continue;
     }
-    if (!pass1(un, 0, j, vec_at(cnt))) return;
+    if (!pass1(un, 0, j, kg, vec_at(cnt))) return;
     for (int t = 0; t < un.n; ++t) {
       const uint32_t c = cnt + 2 * t;
       if (!pass2(vec_at(c))) return;
-      if (t + 1 < un.n && !pass1(un, t + 1, j, vec_at(c + 2))) return;
+      if (t + 1 < un.n && !pass1(un, t + 1, j, kg, vec_at(c + 2))) return;
       if (!drain(un, t)) return;
     }
     cnt += 2 * un.n;
@@ -1040,18 +1056,20 @@ __device__ __forceinline__ void dq_elementwise(const BwdParams& p, uint8_t* smem
       if (u < 0) return false;
       un = bwd_decode<false>(u, p);
       if (un.n > 0) return true;
-      const int64_t i = int64_t(un.ob) * kTile + row;
+      const TileGeo qg = tile_geo(p.list, un.ob, p.N);
       if (g == 0)
-        zero_row(p.out_a + ((int64_t(un.b) * p.N + i) * p.H + un.h) * HD, HD, i < p.N);
+        zero_row(p.out_a + ((int64_t(un.b) * p.N + qg.row0 + row) * p.H + un.h) * HD, HD,
+                 int64_t(qg.lb) * kTile + row < qg.n);
     }
   };
   // this row's dO half into TMEM (after the previous unit's last dP has
   // been computed), its -LSE * log2(e) and D into nl2 / di
   auto stage_unit = [&](const Unit& un, float& nl2, float& di) -> bool {
-    const int64_t i = int64_t(un.ob) * kTile + row;
-    const bool valid = i < p.N;
+    const TileGeo qg = tile_geo(p.list, un.ob, p.N);
+    const bool valid = int64_t(qg.lb) * kTile + row < qg.n;
+    const int64_t i = int64_t(un.ob) * kTile + row;  // row of the (tile-layout) vectors
     const uint4* src = reinterpret_cast<const uint4*>(
-        p.dout + ((int64_t(un.b) * p.N + i) * p.H + un.h) * HD + (HD / 2) * g);
+        p.dout + ((int64_t(un.b) * p.N + qg.row0 + row) * p.H + un.h) * HD + (HD / 2) * g);
     uint32_t rw[HD / 4];
 #pragma unroll
     for (int j = 0; j < HD / 16; ++j) {
@@ -1079,12 +1097,15 @@ __device__ __forceinline__ void dq_elementwise(const BwdParams& p, uint8_t* smem
   float nl2 = 0.f, di = 0.f;
   if (has && !stage_unit(cur, nl2, di)) return;
   while (has) {
-    const int64_t i = int64_t(cur.ob) * kTile + row;
+    // this query row: token i of its sequence (qg.n tokens), token qg.row0 + row of the axis
+    const TileGeo qg = tile_geo(p.list, cur.ob, p.N);
+    const int64_t i = int64_t(qg.lb) * kTile + row;
     for (int t = 0; t < cur.n; ++t) {
       const InnerTile it = inner_tile(cur, t, p.list, p.status);
       int lo = 0, hi = kTile - 1;
       if (it.dead) hi = -1;
-      else if (it.partial) row_live_range(i, cur.ob, it.blk, p.N, p.mask, lo, hi);
+      else if (it.partial)
+        row_live_range(i, qg.lb, tile_geo(p.list, it.blk, p.N).lb, qg.n, p.mask, lo, hi);
       prefetch_tile_bits(p.list, it.slot, row);
       bool ok = wait_bar(bar(L::kSFull), sp_cnt & 1, abort_flag, p.status, 20);
       if (!__all_sync(0xFFFFFFFFu, ok)) return;
@@ -1132,9 +1153,10 @@ __device__ __forceinline__ void dq_elementwise(const BwdParams& p, uint8_t* smem
     if (!__all_sync(0xFFFFFFFFu, ok)) return;
     ++af_cnt;
     tc_fence_after();
-    __nv_bfloat16* dq_row = p.out_a + ((int64_t(cur.b) * p.N + i) * p.H + cur.h) * HD;
+    __nv_bfloat16* dq_row =
+        p.out_a + ((int64_t(cur.b) * p.N + qg.row0 + row) * p.H + cur.h) * HD;
     store_acc_piece<HD>(tDQ + g * (HD / 2), p.scale, dq_row + g * (HD / 2),
-                        int64_t(p.H) * HD * 2, i < p.N);
+                        int64_t(p.H) * HD * 2, i < qg.n);
     warp_arrive(bar(L::kAccEmpty));
     cur = nxt;
     has = has_next;
@@ -1258,7 +1280,7 @@ static flash_msa_status launch_bwd_hd(const BwdLaunch& a, cudaStream_t stream) {
   if (a.stages & FLASH_MSA_BWD_PREPROCESS) {
     PreParams pp{reinterpret_cast<const __nv_bfloat16*>(a.o),
                  reinterpret_cast<const __nv_bfloat16*>(a.dout), a.lse, nlse2, dsum, a.dqacc,
-                 a.B, a.H, int(a.N), NP};
+                 a.B, a.H, int(a.N), NP, a.rows};
     constexpr int kRows = 256 / (HD / 8);
     dim3 grid((NP + kRows - 1) / kRows, a.H, a.B);
     bwd_pre_kernel<HD><<<grid, 256, 0, stream>>>(pp);

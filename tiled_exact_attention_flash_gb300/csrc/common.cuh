@@ -260,7 +260,29 @@ struct ListParams {
   int causal;            // arithmetic mode: causal mask
   int tail;              // N % 128 != 0
   int transposed;        // 0: outer = query block (CSR); 1: outer = key block (CSC)
+  // per-sequence tiles (null otherwise): first token of each tile, first
+  // token and length of its sequence
+  const int32_t* t_start;
+  const int32_t* t_seq0;
+  const int32_t* t_len;
 };
+
+// Where a tile lies: row0 = its first token on the (packed) sequence axis,
+// lb = its block index inside its own sequence and n = that sequence's
+// length.  Without per-sequence tiles, tile blk of a length-N sequence is the
+// 128-token block blk.  Masks are evaluated in the sequence's own coordinates
+// (token lb * 128 + r of a sequence of n tokens), outputs go to token row0 + r.
+struct TileGeo {
+  int64_t row0;
+  int lb;
+  int64_t n;
+};
+
+__device__ __forceinline__ TileGeo tile_geo(const ListParams& L, int blk, int64_t N) {
+  if (!L.t_start) return TileGeo{int64_t(blk) * kTile, blk, N};
+  const int start = __ldg(L.t_start + blk), s0 = __ldg(L.t_seq0 + blk);
+  return TileGeo{start, (start - s0) / kTile, __ldg(L.t_len + blk)};
+}
 
 struct Unit {
   int b, h, ob;  // batch, head, outer block

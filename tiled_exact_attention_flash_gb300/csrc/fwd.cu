@@ -183,7 +183,7 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, uint8_t* smem, 
       }
       mbar_arrive_expect_tx(bar(L::kQFull + s), L::kTileBytes);
       load_tile<HD>(&p.tm_q, smem_u32(smem + L::kQOff + s * L::kTileBytes), bar(L::kQFull + s),
-                    pu.q[s] * kTile, pu.h, pu.b);
+                    int(tile_geo(p.list, pu.q[s], p.N).row0), pu.h, pu.b);
       last_q[s] = int(qe_cnt[s]);
       ++qe_cnt[s];
     }
@@ -198,9 +198,11 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, uint8_t* smem, 
         return false;
       mbar_arrive_expect_tx(bar(L::kKvFull + slot), (kb_b >= 0 ? 2 : 1) * L::kTileBytes);
       const uint32_t dst = smem_u32(smem + L::kRingOff + 2 * slot * L::kTileBytes);
-      load_tile<HD>(ma, dst, bar(L::kKvFull + slot), kb_a * kTile, hkv, pu.b);
+      load_tile<HD>(ma, dst, bar(L::kKvFull + slot), int(tile_geo(p.list, kb_a, p.N).row0), hkv,
+                    pu.b);
       if (kb_b >= 0)
-        load_tile<HD>(&p.tm_k, dst + L::kTileBytes, bar(L::kKvFull + slot), kb_b * kTile, hkv, pu.b);
+        load_tile<HD>(&p.tm_k, dst + L::kTileBytes, bar(L::kKvFull + slot),
+                      int(tile_geo(p.list, kb_b, p.N).row0), hkv, pu.b);
       last_g[slot] = int(g_cnt);
       ++g_cnt;
       return true;
@@ -480,7 +482,10 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint64_t* bars, 
     un.ob = pu.q[slot];
     un.begin = pu.beg[slot];
     un.n = pu.n[slot];
-    const int64_t i = int64_t(un.ob) * kTile + row;
+    // this row: token i of its sequence (qg.n tokens), token tok of the axis
+    const TileGeo qg = tile_geo(p.list, un.ob, p.N);
+    const int64_t i = int64_t(qg.lb) * kTile + row;
+    const int64_t tok = qg.row0 + row;
     float m_run = -INFINITY, l_run = 0.f;
     for (int t = 0; t < un.n; ++t) {
       const InnerTile it = inner_tile(un, t, p.list, p.status);
@@ -488,7 +493,7 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint64_t* bars, 
       if (it.dead) {
         hi = -1;
       } else if (it.partial) {
-        row_live_range(i, un.ob, it.blk, p.N, p.mask, lo, hi);
+        row_live_range(i, qg.lb, tile_geo(p.list, it.blk, p.N).lb, qg.n, p.mask, lo, hi);
       }
       prefetch_tile_bits(p.list, it.slot, row);
       const bool ok = wait_bar(bar(L::kSFull + slot), sf_cnt & 1, abort_flag, p.status, 20);
@@ -582,7 +587,7 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint64_t* bars, 
     }
     const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
     __nv_bfloat16* orow =
-        p.o + ((int64_t(un.b) * p.N + i) * p.H + un.h) * int64_t(HD);
+        p.o + ((int64_t(un.b) * p.N + tok) * p.H + un.h) * int64_t(HD);
 #pragma unroll
     for (int c = 0; c < HD / 32; ++c) {
       uint32_t o[32];
@@ -602,14 +607,14 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint64_t* bars, 
 #pragma unroll
       for (int j = 0; j < 4; ++j) cc[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
       store_rows_transposed<4, 2>(cc, reinterpret_cast<char*>(orow + c * 32),
-                                  int64_t(p.H) * HD * 2, i < p.N);
+                                  int64_t(p.H) * HD * 2, i < qg.n);
     }
     if (un.n > 0) {
       tc_fence_before();
       mbar_arrive(bar(L::kOEmpty + slot));
     }
-    if (i < p.N) {
-      p.lse[(int64_t(un.b) * p.H + un.h) * p.N + i] =
+    if (i < qg.n) {
+      p.lse[(int64_t(un.b) * p.H + un.h) * p.N + tok] =
           l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
     }
   }
