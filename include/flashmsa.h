@@ -114,7 +114,12 @@ enum {
  *   CSR by query block: row_ptr[n_q_blocks+1], col_idx[nnz] (ascending), kind[nnz]
  *   CSC by key block:   col_ptr[n_k_blocks+1], row_idx[nnz] (ascending), kind_t[nnz]
  *   q_order[n_q_blocks] / k_order[n_k_blocks]: blocks by descending live-tile
- *   count, ties by ascending index (longest work is scheduled first).
+ *   count, ties by ascending index (longest work is scheduled first); with
+ *   per-sequence tiles (below) q_order instead holds each sequence's tiles in
+ *   neighbouring pairs counted from its last tile, pairs by descending count
+ *   of their first tile (ties: ascending id), then the single first tiles of
+ *   sequences with an odd tile count (the forward runs positions 2r, 2r + 1
+ *   together and shares their key tiles).
  * With a BITMASK or DOCUMENTS mask, a partial tile whose live entries are not all given
  * by the other mask parts carries them as bits, in a slot numbered in CSR
  * order: bits[512 slot + 4 r + c / 32] bit c % 32 = live(128 qb + r,

@@ -31,7 +31,8 @@ s0, s0 + 128, ..., so no tile holds tokens of two sequences (the way P1's
 request batching keeps each request's attention to itself), and only tile
 pairs of one sequence exist.  Tiles are numbered sequence by sequence; for
 tile t, tile_start[t] is its first token, tile_seq0[t] and tile_seq_len[t]
-its sequence's first token and length.  Entries of a tile past its
+its sequence's first token and length.  q_order then keeps neighbouring
+tiles of one sequence together in pairs (see _pair_order).  Entries of a tile past its
 sequence's end count as dead, and each tile pair is classified by evaluating
 the predicate on all of its entries, as above.
 
@@ -102,6 +103,29 @@ def sequence_tiles(spec: MaskSpec, tile: int = 128):
             np.array(seq_len, dtype=np.int32))
 
 
+def _pair_order(spec: MaskSpec, row_len, tile: int) -> np.ndarray:
+    """q_order of per-sequence tiles: every sequence's tiles in neighbouring
+    pairs counted from its last tile ((t, t - 1), (t - 2, t - 3), ...; a
+    sequence with an odd tile count leaves its first tile single).  Pairs come
+    first, by descending live-tile count of their first tile, ties by
+    ascending tile id, each pair's tiles in that order; then the single
+    tiles, by descending count, ties by ascending id.  Positions 2r and
+    2r + 1 thus hold two neighbouring tiles of one sequence (or two singles)."""
+    starts = spec.doc_starts
+    pairs, singles, base = [], [], 0
+    for s0, s1 in zip(starts[:-1], starts[1:]):
+        nt = (s1 - s0 + tile - 1) // tile
+        last = base + nt - 1
+        for t in range(last, base, -2):
+            pairs.append((t, t - 1))
+        if nt % 2:
+            singles.append(base)
+        base += nt
+    pairs.sort(key=lambda pr: (-row_len[pr[0]], pr[0]))
+    singles.sort(key=lambda t: (-row_len[t], t))
+    return np.array([t for pr in pairs for t in pr] + singles, dtype=np.int32)
+
+
 def classify_sequence_tiles(n: int, spec: MaskSpec, tile: int = 128) -> np.ndarray:
     """kinds[qt, kt] over the per-sequence tiles; pairs of two sequences are dead."""
     start, seq0, seq_len = sequence_tiles(spec, tile)
@@ -160,7 +184,10 @@ def build(n: int, spec: MaskSpec, tile: int = 128, prune: bool = True) -> dict:
                            for qb in row_idx[col_ptr[kb]:col_ptr[kb + 1]]], dtype=np.int32)
     row_len = np.diff(row_ptr)
     col_len = np.diff(col_ptr)
-    q_order = np.array(sorted(range(nb), key=lambda b: (-row_len[b], b)), dtype=np.int32)
+    if seq:
+        q_order = _pair_order(spec, row_len, tile)
+    else:
+        q_order = np.array(sorted(range(nb), key=lambda b: (-row_len[b], b)), dtype=np.int32)
     k_order = np.array(sorted(range(nb), key=lambda b: (-col_len[b], b)), dtype=np.int32)
     empty = np.zeros(0, dtype=np.int32)
     tile_start, tile_seq0, tile_seq_len = sequence_tiles(spec, tile) if seq else (empty,) * 3

@@ -611,6 +611,9 @@ def test_sequence_tiles_hand_example():
     assert r["row_ptr"].tolist() == [0, 1, 2, 4, 5, 6, 8, 9]
     assert r["col_idx"].tolist() == [0, 1, 1, 2, 3, 4, 4, 5, 6]
     assert r["n_bit_tiles"] == 0
+    # pairs of neighbouring tiles from each sequence's end: (2, 1) and (5, 4),
+    # longest first (counts 2 and 2, tie by id), then the single tiles 0, 3, 6
+    assert r["q_order"].tolist() == [2, 1, 5, 4, 0, 3, 6]
 
 
 @pytest.mark.parametrize("causal,window", [(True, None), (False, None), (True, 150), (False, 70)])

@@ -343,6 +343,31 @@ static flash_msa_status build_sequence_tiles(const flash_msa_mask_desc* mask,
     base += nb;
   }
   finish_lists(out, nt, col_count, false);
+  // q_order: each sequence's tiles in neighbouring pairs counted from its last
+  // tile, so that the forward's pair units (positions 2r, 2r + 1) hold two
+  // tiles of one sequence with nearly the same key tiles; pairs by descending
+  // live-tile count of their first tile (ties: ascending id), then the single
+  // first tiles of sequences with an odd tile count, likewise
+  auto count = [&](int32_t t) { return out->row_ptr[t + 1] - out->row_ptr[t]; };
+  auto longer = [&](int32_t a, int32_t b) {
+    return count(a) != count(b) ? count(a) > count(b) : a < b;
+  };
+  std::vector<int32_t> firsts, singles;
+  base = 0;
+  for (int64_t d = 0; d < mask->n_docs; ++d) {
+    const int64_t nb = (ds[d + 1] - ds[d] + kTile - 1) / kTile;
+    for (int64_t t = base + nb - 1; t > base; t -= 2) firsts.push_back(int32_t(t));
+    if (nb % 2) singles.push_back(int32_t(base));
+    base += nb;
+  }
+  std::sort(firsts.begin(), firsts.end(), longer);
+  std::sort(singles.begin(), singles.end(), longer);
+  int64_t at = 0;
+  for (int32_t t : firsts) {
+    out->q_order[at++] = t;
+    out->q_order[at++] = t - 1;
+  }
+  for (int32_t t : singles) out->q_order[at++] = t;
   return FLASH_MSA_OK;
 }
 

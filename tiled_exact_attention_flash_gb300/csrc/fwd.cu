@@ -35,6 +35,7 @@ struct FwdParams {
   int G;  // query heads per key/value head
   int n_units;
   int head_group;    // pair units are numbered in groups of this many heads
+  int slot_issuers;  // one MMA-issuing thread per query slot (else one for both)
   float scale_log2;  // scale * log2(e)
   int wait_limit_ms;  // limit of any single bounded wait
   MaskParams mask;
@@ -347,8 +348,9 @@ __device__ __forceinline__ void fwd_mma(const FwdParams& p, uint8_t* smem, uint6
 template <int HD>
 __device__ __forceinline__ void fwd_mma_slot(const FwdParams& p, uint8_t* smem, uint64_t* bars,
                                              uint32_t tmem, int s, volatile int* abort_flag) {
-  // MMA issuer of query slot s, used for lists from a block index: one
-  // thread per slot, both walking the same union of key tiles (so both see
+  // MMA issuer of query slot s, used for lists from a block index (other than
+  // per-sequence tiles): one thread per slot, both walking the same union of
+  // key tiles (so both see
   // the same ring groups) and both releasing every group (kKvEmpty then
   // counts two commits).  Where the two slots' lists differ, neither slot
   // waits for the other's softmax; with identical dense / causal lists the
@@ -646,7 +648,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       mbar_init(smem_u32(bars + L::kOFull + s), 1);
       mbar_init(smem_u32(bars + L::kOEmpty + s), 128);
     }
-    const uint32_t issuers = p.list.ptr ? 2 : 1;  // MMA threads (see fwd_mma_slot)
+    const uint32_t issuers = p.slot_issuers ? 2 : 1;  // MMA threads (see fwd_mma_slot)
     mbar_init(smem_u32(bars + L::kMmaDone), issuers);
     for (int i = 0; i < L::kSlots; ++i) {
       mbar_init(smem_u32(bars + L::kKvFull + i), 1);
@@ -670,7 +672,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     regs_shrink<80>();
     if (warp == 0) {
       if (lane == 0) fwd_producer<HD>(p, smem, bars, abort_flag);
-    } else if (p.list.ptr) {  // index lists: one MMA issuer per slot (warps 1 and 3)
+    } else if (p.slot_issuers) {  // one MMA issuer per slot (warps 1 and 3)
       if ((warp == 1 || warp == 3) && lane == 0)
         fwd_mma_slot<HD>(p, smem, bars, tmem, warp == 1 ? 0 : 1, abort_flag);
     } else if (warp == 1) {
@@ -715,6 +717,10 @@ static flash_msa_status launch_fwd_hd(const FwdLaunch& a, cudaStream_t stream) {
   p.mask = a.mask;
   p.list = a.list;
   p.n_units = a.B * a.H * ((a.list.n_blocks + 1) / 2);  // pairs of query blocks
+  // lists from a block index differ between the two slots of a pair, except
+  // for per-sequence tiles, whose pairs are neighbours in one sequence: those
+  // (like dense / causal lists) take the single issuer that staggers the slots
+  p.slot_issuers = (a.list.ptr && !a.list.t_start) ? 1 : 0;
   // heads per group of the unit order: K and V of about kFwdGroupBytes of
   // heads are streamed at any time (0: one group of all heads, rank-major)
   {
