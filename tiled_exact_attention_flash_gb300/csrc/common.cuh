@@ -291,23 +291,18 @@ struct Unit {
 };
 
 // Launch order of the work units: unit u -> (bh = b * H + h, rank), rank =
-// position in one head's longest-first block order.  Rank-major: rank 0 of
-// every (b, h), then rank 1 of every (b, h), and so on, so the whole launch
-// runs longest list first and its last units are short.  In (b, h)-major
-// order the last heads' longest units started at the very end and left most
-// SMs idle (measured: 15% of the forward's span at N = 4096); chunks of 4 to
-// 16 ranks per head, which keep more of a head's units running together for
-// L2 reuse, recovered less than half of the gain.
-__device__ __forceinline__ void unit_order(int u, int BH, int& bh, int& rank) {
-  rank = u / BH;
-  bh = u - rank * BH;
-}
-
-// Launch order in groups of heads: the units of heads [G g, G g + G) come
-// before those of the next group, rank-major inside the group (the last group
-// may be smaller).  G = BH is the plain rank-major order of unit_order.  With
-// a small G the CTAs running at any time work on a few heads only, whose
-// streamed tiles and accumulators then stay in L2.
+// position in one head's longest-first block order, in groups of G heads: the
+// units of heads [G g, G g + G) come before those of the next group,
+// rank-major inside the group (rank 0 of every head of the group, then rank
+// 1, ...; the last group may be smaller).  G = BH is plain rank-major order:
+// the whole launch runs longest lists first and its last units are short.
+// In (b, h)-major order the last heads' longest units started at the very
+// end and left most SMs idle (measured: 15% of the forward's span at
+// N = 4096); chunks of 4 to 16 ranks per head, which keep more of a head's
+// units running together for L2 reuse, recovered less than half of the gain.
+// With a small G the CTAs running at any time work on a few heads only, whose
+// streamed tiles and accumulators then stay in L2 (the accumulated-dQ
+// backward uses that).
 __device__ __forceinline__ void unit_order_grouped(int u, int BH, int n_blocks, int G, int& bh,
                                                    int& rank) {
   const int per_group = G * n_blocks;
@@ -361,14 +356,6 @@ __device__ __forceinline__ Unit decode_unit_at(int bh, int rank, int H, const Li
   }
   un.n0 = un.n;
   return un;
-}
-
-// Unit u of a launch over BH = B * H heads, in the order of unit_order.
-__device__ __forceinline__ Unit decode_unit(int u, int BH, int H, const ListParams& L,
-                                            unsigned* status) {
-  int bh, rank;
-  unit_order(u, BH, bh, rank);
-  return decode_unit_at(bh, rank, H, L, status);
 }
 
 // Inner block t of a unit: block id, whether the element mask must be

@@ -70,7 +70,8 @@ constexpr int kFwdThreads = 384;
 // blocks whose key-tile lists nearly coincide).  Slot 0 takes rank 2r, slot
 // 1 rank 2r + 1.  The producer loads each key/value tile of the UNION of the
 // two lists once; the MMA issuer runs Q K^T and P V for whichever slots the
-// tile belongs to.  Pair units are numbered rank-major (unit_order: pair r
+// tile belongs to.  Pair units are numbered rank-major (unit_order_grouped
+// with one group of all heads: pair r
 // of every (b, h) before pair r + 1), so the launch runs its longest units
 // first; each CTA takes its units in the order of fwd_unit.
 struct PairUnit {
@@ -694,10 +695,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
 // ---------------------------------------------------------------------------
 // host launcher
 // ---------------------------------------------------------------------------
-// Heads per group of the forward's unit order, in bytes of streamed K and V
-// (0: no grouping).
-constexpr int64_t kFwdGroupBytes = 0;
-
 template <int HD>
 static flash_msa_status launch_fwd_hd(const FwdLaunch& a, cudaStream_t stream) {
   using L = FwdLayout<HD>;
@@ -721,15 +718,10 @@ static flash_msa_status launch_fwd_hd(const FwdLaunch& a, cudaStream_t stream) {
   // for per-sequence tiles, whose pairs are neighbours in one sequence: those
   // (like dense / causal lists) take the single issuer that staggers the slots
   p.slot_issuers = (a.list.ptr && !a.list.t_start) ? 1 : 0;
-  // heads per group of the unit order: K and V of about kFwdGroupBytes of
-  // heads are streamed at any time (0: one group of all heads, rank-major)
-  {
-    const int64_t per_head = int64_t(a.list.n_blocks) * kTile * HD * 2 * 2 / (a.H / a.Hkv);
-    int64_t grp = kFwdGroupBytes > 0 ? kFwdGroupBytes / (per_head > 0 ? per_head : 1) : a.B * a.H;
-    if (grp < 1) grp = 1;
-    if (grp > int64_t(a.B) * a.H) grp = int64_t(a.B) * a.H;
-    p.head_group = int(grp);
-  }
+  // one group of all heads: plain rank-major order (groups of a few heads,
+  // whose K and V would stay in L2, measured slower: the static deal then
+  // leaves CTAs idle at the group boundaries)
+  p.head_group = a.B * a.H;
   p.status = a.status;
   p.wait_limit_ms = int(wait_limit_ms());
   if ((st = enable_smem(reinterpret_cast<const void*>(&fwd_kernel<HD>), L::kSmemBytes,
