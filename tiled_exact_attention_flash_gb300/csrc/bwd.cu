@@ -207,28 +207,25 @@ __device__ __forceinline__ void init_bwd_barriers(uint64_t* bars) {
   constexpr bool KS = L::KS;
   // dQ: the producer's Q tile plus every elementwise warp's rows of dO
   mbar_init(smem_u32(bars + L::kFixFull), KS ? 1 : 1 + kEwWarps);
-  // the dK/dV kernel issues its products from two threads (dkdv_mma_role),
-  // each releasing the shared resources once
-  constexpr uint32_t kIssuers = kMode == kModeDkdv ? 2 : 1;
-  mbar_init(smem_u32(bars + L::kFixEmpty), kIssuers);
+  mbar_init(smem_u32(bars + L::kFixEmpty), 1);
   for (int i = 0; i < 2; ++i) {
     mbar_init(smem_u32(bars + L::kSFull + i), 1);
     mbar_init(smem_u32(bars + L::kPFull + i), kEwWarps);
   }
   mbar_init(smem_u32(bars + L::kDpFree), kEwWarps);
-  mbar_init(smem_u32(bars + L::kAccFull), kIssuers);
+  mbar_init(smem_u32(bars + L::kAccFull), 1);
   mbar_init(smem_u32(bars + L::kAccEmpty), kEwWarps);
-  mbar_init(smem_u32(bars + L::kMmaDone), kIssuers);
+  mbar_init(smem_u32(bars + L::kMmaDone), 1);
   mbar_init(smem_u32(bars + L::kDqFull), 1);
   mbar_init(smem_u32(bars + L::kDqFree), kEwWarps);
   for (int i = 0; i < 2; ++i) mbar_init(smem_u32(bars + L::kWgSync + i), 4);
   for (int i = 0; i < L::kStages; ++i) {
     mbar_init(smem_u32(bars + L::kRingFull + i), 1);
-    mbar_init(smem_u32(bars + L::kRingEmpty + i), kIssuers);
+    mbar_init(smem_u32(bars + L::kRingEmpty + i), 1);
   }
   for (int i = 0; i < 2; ++i) {
     mbar_init(smem_u32(bars + L::kUnitFull + i), 1);               // the producer
-    mbar_init(smem_u32(bars + L::kUnitEmpty + i), kIssuers + kEwWarps);  // MMA threads, EW warps
+    mbar_init(smem_u32(bars + L::kUnitEmpty + i), 1 + kEwWarps);  // MMA thread, EW warps
   }
   fence_mbar_init();
 }
@@ -487,38 +484,25 @@ __device__ __forceinline__ void dq_mma(const BwdParams& p, uint8_t* smem, uint64
   drain_bar(bar(L::kMmaDone), 0);
 }
 
-// The two MMA issuers of bwd_dkdv (key-stationary; fixed tiles K, V; ring
-// Q_t, dO_t).  One thread issuing every product cannot keep the tensor core
-// busy: back-to-back M128 N128 K16 products from a single thread run at 64%
-// (both operands in shared memory) and 46% (A in TMEM) of the clock's peak,
-// two threads issuing to independent accumulators at 87-91% (measured).  So
-// the four products of a tile are issued from two threads on independent
-// chains that share no TMEM region:
-//   role 0 (P path):  S^T = K Q_t^T into A, dV += P^T dO_t (P^T over A)
-//   role 1 (dS path): dP^T = V dO_t^T into B, dK += dS^T Q_t (dS^T over B)
-// TMEM: A = [0,128), B = [128,256), dV at [256, 256+d), dK at [384, 384+d).
-// The elementwise side reads S^T, writes P^T (bf16) over it and signals
-// p_full; then reads dP^T, writes dS^T (bf16) over it and signals ds_full.
-// Each region is refilled by its own thread right after the product that
-// reads it.  Every shared resource is released once by each role: a ring
-// stage of Q_t (S^T; dK) or dO_t (dP^T; dV), K (role 0) and V (role 1) with
-// the fixed-tile barrier, the accumulators (acc_full counts both roles).
-// Order per tile t, role 0: [p_full(t)] dV += P^T dO_t, release dO_t,
-// S^T(t+1) -> s_full, release Q_{t+1}; role 1: [ds_full(t)] dK += dS^T Q_t,
-// release Q_t, dP^T(t+1) -> dp_full, release dO_{t+1}.
+// MMA issuer of bwd_dkdv (key-stationary; fixed tiles K, V; ring Q_t, dO_t).
+// TMEM: S^T at A = [0,128), dP^T at B = [128,256), dV at [256, 256+d), dK at
+// [384, 384+d).  The elementwise side reads S^T, writes P^T (bf16) over it
+// and signals p_full; then reads dP^T, writes dS^T (bf16) over it and
+// signals ds_full.  Each region is refilled for the next tile as soon as
+// the product reading it has been issued, so the next tile's S^T is ready
+// while dS^T is still being computed.  Order per tile t:
+//   [p_full(t)] dV += P^T dO_t, release dO_t, S^T(t+1) -> s_full;
+//   [ds_full(t)] dK += dS^T Q_t, release Q_t, dP^T(t+1) -> dp_full.
 template <int HD>
-__device__ __forceinline__ void dkdv_mma_role(const BwdParams& p, uint8_t* smem, uint64_t* bars,
-                                              uint32_t tmem, int role, volatile int* abort_flag) {
+__device__ __forceinline__ void dkdv_mma(const BwdParams& p, uint8_t* smem, uint64_t* bars,
+                                         uint32_t tmem, volatile int* abort_flag) {
   using L = BwdLayout<HD, kModeDkdv>;
   auto bar = [&](int i) { return smem_u32(bars + i); };
   constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);
   constexpr uint32_t kIdAcc = idesc_bf16_f32(128, HD, false, true);
-  // role 0: region A, fixed tile K, ring operand Q (first stage of a tile),
-  // accumulator dV fed by dO (second stage); role 1: B, V, dO, dK fed by Q
-  const uint32_t tR = tmem + (role ? 128u : 0u);
-  const uint32_t tAcc = tmem + (role ? 384u : 256u);
-  const uint32_t fixed = smem_u32(smem + L::kFixOff) + (role ? L::kTileBytes : 0u);
-  const int s_bar = L::kSFull + role, p_bar = L::kPFull + role;
+  const uint32_t tA = tmem, tB = tmem + 128, tDV = tmem + 256, tDK = tmem + 384;
+  const uint32_t fk = smem_u32(smem + L::kFixOff);
+  const uint32_t fv = fk + L::kTileBytes;
   auto stage_addr = [&](uint32_t c) {
     return smem_u32(smem + L::kRingOff + (c % L::kStages) * L::kTileBytes);
   };
@@ -535,36 +519,42 @@ __device__ __forceinline__ void dkdv_mma_role(const BwdParams& p, uint8_t* smem,
     if (un.n == 0) continue;
     if (!wait_bar(bar(L::kFixFull), ff_cnt & 1, abort_flag, p.status, 10)) break;
     ++ff_cnt;
-    // the region's first product: S^T(0) = K Q_0^T or dP^T(0) = V dO_0^T
-    const uint32_t own = cnt + uint32_t(role);  // this role's ring operand of tile 0
-    if (!ring_wait(own, 11)) break;
+    if (!ring_wait(cnt, 11)) break;
     tc_fence_after();
-    mma_kmajor<HD>(tR, fixed, stage_addr(own), kIdS);
-    mma_commit(bar(s_bar));
-    mma_commit(bar(L::kRingEmpty + own % L::kStages));
-    if (un.n == 1) mma_commit(bar(L::kFixEmpty));  // K (V) is not read again
+    mma_kmajor<HD>(tA, fk, stage_addr(cnt), kIdS);  // S^T(0) = K Q_0^T
+    mma_commit(bar(L::kSFull));
+    if (!ring_wait(cnt + 1, 12)) break;
+    tc_fence_after();
+    mma_kmajor<HD>(tB, fv, stage_addr(cnt + 1), kIdS);  // dP^T(0) = V dO_0^T
+    mma_commit(bar(L::kSFull + 1));
+    if (un.n == 1) mma_commit(bar(L::kFixEmpty));  // K and V are not read again
     for (int t = 0; t < un.n && ok; ++t) {
       const uint32_t c = cnt + 2 * t;  // Q_t at c, dO_t at c + 1
-      // the accumulator's operand: dO_t (role 0) or Q_t (role 1)
-      const uint32_t acc_op = c + (role ? 0u : 1u);
       const bool more = t + 1 < un.n;
       if (t == 0) {
         if (!wait_bar(bar(L::kAccEmpty), (ae_cnt & 1) ^ 1, abort_flag, p.status, 13)) { ok = false; break; }
         ++ae_cnt;
       }
-      if (!wait_bar(bar(p_bar), pf_cnt & 1, abort_flag, p.status, 14 + 2 * role)) { ok = false; break; }
-      ++pf_cnt;
-      if (!ring_wait(acc_op, 12)) { ok = false; break; }
+      if (!wait_bar(bar(L::kPFull), pf_cnt & 1, abort_flag, p.status, 14)) { ok = false; break; }
       tc_fence_after();
-      mma_tmem_a(tAcc, tR, stage_addr(acc_op), kIdAcc, t > 0);  // dV += P^T dO_t; dK += dS^T Q_t
-      mma_commit(bar(L::kRingEmpty + acc_op % L::kStages));
+      mma_tmem_a(tDV, tA, stage_addr(c + 1), kIdAcc, t > 0);  // dV += P^T dO_t
+      mma_commit(bar(L::kRingEmpty + (c + 1) % L::kStages));
       if (more) {
-        const uint32_t nxt = c + 2 + uint32_t(role);  // Q_{t+1} or dO_{t+1}
-        if (!ring_wait(nxt, 11)) { ok = false; break; }
+        if (!ring_wait(c + 2, 11)) { ok = false; break; }
         tc_fence_after();
-        mma_kmajor<HD>(tR, fixed, stage_addr(nxt), kIdS);  // over P^T(t) / dS^T(t)
-        mma_commit(bar(s_bar));
-        mma_commit(bar(L::kRingEmpty + nxt % L::kStages));
+        mma_kmajor<HD>(tA, fk, stage_addr(c + 2), kIdS);  // S^T(t+1) over P^T(t)
+        mma_commit(bar(L::kSFull));
+      }
+      if (!wait_bar(bar(L::kPFull + 1), pf_cnt & 1, abort_flag, p.status, 16)) { ok = false; break; }
+      ++pf_cnt;
+      tc_fence_after();
+      mma_tmem_a(tDK, tB, stage_addr(c), kIdAcc, t > 0);  // dK += dS^T Q_t
+      mma_commit(bar(L::kRingEmpty + c % L::kStages));
+      if (more) {
+        if (!ring_wait(c + 3, 12)) { ok = false; break; }
+        tc_fence_after();
+        mma_kmajor<HD>(tB, fv, stage_addr(c + 3), kIdS);  // dP^T(t+1) over dS^T(t)
+        mma_commit(bar(L::kSFull + 1));
         if (t + 2 == un.n) mma_commit(bar(L::kFixEmpty));
       }
     }
@@ -576,7 +566,7 @@ __device__ __forceinline__ void dkdv_mma_role(const BwdParams& p, uint8_t* smem,
   drain_bar(bar(L::kMmaDone), 0);
 }
 
-// MMA issuer of the fused kernel (key-stationary, like dkdv_mma_role, plus the dQ
+// MMA issuer of the fused kernel (key-stationary, like dkdv_mma, plus the dQ
 // partial product of every tile).  TMEM: S^T at A = [0,128), dP^T at
 // B = [128,256), dV at [256, 256+d), dK at [384, 384+d); dQ(t) = dS(t) K
 // (fp32, query rows in the lanes) is written over B once dK(t) has read
@@ -1214,11 +1204,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
   if (warp < 4) regs_shrink<80>();  // 384 x 168 at launch: 128 x 80 + 256 x 208
   if (warp == 0) {
     if (lane == 0) bwd_producer<HD, kMode>(p, smem, bars, abort_flag);
-  } else if (warp == 1 || warp == 3) {
+  } else if (warp == 1) {
     if (lane == 0) {
-      if (kMode == kModeDkdv) dkdv_mma_role<HD>(p, smem, bars, tmem, warp == 3, abort_flag);
-      else if (warp == 1 && kMode == kModeFused) fused_mma<HD>(p, smem, bars, tmem, abort_flag);
-      else if (warp == 1) dq_mma<HD>(p, smem, bars, tmem, abort_flag);
+      if (kMode == kModeFused) fused_mma<HD>(p, smem, bars, tmem, abort_flag);
+      else if (kMode == kModeDkdv) dkdv_mma<HD>(p, smem, bars, tmem, abort_flag);
+      else dq_mma<HD>(p, smem, bars, tmem, abort_flag);
     }
   } else if (warp >= 4) {
     const int g = (warp - 4) >> 2;  // elementwise warpgroup: columns [64 g, 64 g + 64)
