@@ -27,13 +27,16 @@ What it computes (one attention head at a time, float64 throughout):
 * ``block_index`` -- classification of every 128 x 128 tile as dead / full /
   partial by evaluating the element predicate on all of its entries, and the
   CSR / CSC / longest-row-first orders built from it ("How Does Flash-MSA
-  Sparse Attention Work", the precomputed per-block index list).
+  Sparse Attention Work", the precomputed per-block index list); packed
+  variable-length sequences with causal / window masks are tiled per
+  sequence (``sequence_tiles``), each from its own first token.
 
 Pins (``tests/test_oracle_pins.py``, run with ``-m "not gpu"``): uniform
 attention for Q = 0, causal row 0, one-hot dominant rows, constant V, row sums
 of P, gradient-sum invariants, permutation invariance, central finite
 differences, agreement with the scalar loops and with the tiled online-softmax
-restatement, closed-form live-tile counts for the benchmark masks, and
+restatement, closed-form live-tile counts for the benchmark masks, the
+per-sequence tiling equal to every sequence's own index, and
 negative controls (mistakes planted in copies of these functions must fail a
 pin).  Every function here is pinned; none is "parity unpinned".
 """

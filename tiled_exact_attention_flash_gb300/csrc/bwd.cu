@@ -831,9 +831,10 @@ __device__ __forceinline__ void dkdv_elementwise(const BwdParams& p, uint8_t* sm
 // bf16) into the dS tile in shared memory, the A operand of dQ = dS K.  After
 // the next tile's pass 1 (or at the end of the unit) the warpgroup reads its
 // half of the tile's dQ partial product out of TMEM -- query row
-// 32 (warp % 4) + lane, columns [d/2 g, d/2 g + d/2) -- releases the columns
-// and adds it into the fp32 accumulator with vector atomics.  Order per
-// tile t: pass 2 (t), pass 1 (t + 1), drain (t).
+// 32 (warp % 4) + lane, columns [d/2 g, d/2 g + d/2) -- releases the columns,
+// stages it in shared memory and adds it into the fp32 accumulator with TMA
+// bulk tensor reductions.  Order per tile t: pass 2 (t), pass 1 (t + 1),
+// drain (t).
 template <int HD>
 __device__ __forceinline__ void fused_elementwise(const BwdParams& p, uint8_t* smem,
                                                   uint64_t* bars, uint32_t tmem, int g,
