@@ -414,7 +414,7 @@ __device__ __forceinline__ void dq_mma(const BwdParams& p, uint8_t* smem, uint64
   };
   auto stage_addr = [&](int s) { return ring + uint32_t(s) * L::kTileBytes; };
   auto ring_wait = [&](int s, uint32_t ph, unsigned where) {
-    return wait_bar(bar(L::kRingFull + s), ph, abort_flag, p.status, where);
+    return wait_bar_warp(bar(L::kRingFull + s), ph, abort_flag, p.status, where);
   };
   // S = Q K^T (both operands in shared memory), dP = dO[tmem] V^T, for the
   // tile at ring position r
@@ -434,16 +434,16 @@ __device__ __forceinline__ void dq_mma(const BwdParams& p, uint8_t* smem, uint64
   bool ok = true, pending_sdp = false;
   UnitQueue queue = unit_queue<HD, kModeDq>(smem, bars);
   int u;
-  while (ok && (u = queue_pop<false>(queue, abort_flag, p.status)) >= 0) {
+  while (ok && (u = queue_pop<true>(queue, abort_flag, p.status)) >= 0) {
     const Unit un = bwd_decode<false>(u, p);
     if (un.n == 0) continue;
-    if (!wait_bar(bar(L::kFixFull), ff_cnt & 1, abort_flag, p.status, 10)) break;
+    if (!wait_bar_warp(bar(L::kFixFull), ff_cnt & 1, abort_flag, p.status, 10)) break;
     ++ff_cnt;
     if (!ring_wait(pos.s, pos.ph, 11) || !ring_wait(pos.s + 1, pos.ph, 12)) break;
     // the previous unit's last S / dP must be in registers before S(0) and
     // dP(0) overwrite them
     if (pending_sdp) {
-      if (!wait_bar(bar(L::kDpFree), sdp_cnt & 1, abort_flag, p.status, 15)) break;
+      if (!wait_bar_warp(bar(L::kDpFree), sdp_cnt & 1, abort_flag, p.status, 15)) break;
       ++sdp_cnt;
     }
     tc_fence_after();
@@ -453,17 +453,17 @@ __device__ __forceinline__ void dq_mma(const BwdParams& p, uint8_t* smem, uint64
       const Pos nxt = advance(pos);  // pos: tile t, nxt: tile t + 1
       if (t + 1 < un.n) {
         if (!ring_wait(nxt.s, nxt.ph, 11) || !ring_wait(nxt.s + 1, nxt.ph, 12)) { ok = false; break; }
-        if (!wait_bar(bar(L::kDpFree), sdp_cnt & 1, abort_flag, p.status, 15)) { ok = false; break; }
+        if (!wait_bar_warp(bar(L::kDpFree), sdp_cnt & 1, abort_flag, p.status, 15)) { ok = false; break; }
         ++sdp_cnt;
         tc_fence_after();
         issue_sdp(nxt);
         if (t + 2 == un.n) mma_commit(bar(L::kFixEmpty));
       }
       if (t == 0) {
-        if (!wait_bar(bar(L::kAccEmpty), (ae_cnt & 1) ^ 1, abort_flag, p.status, 13)) { ok = false; break; }
+        if (!wait_bar_warp(bar(L::kAccEmpty), (ae_cnt & 1) ^ 1, abort_flag, p.status, 13)) { ok = false; break; }
         ++ae_cnt;
       }
-      if (!wait_bar(bar(L::kPFull), pf_cnt & 1, abort_flag, p.status, 14)) { ok = false; break; }
+      if (!wait_bar_warp(bar(L::kPFull), pf_cnt & 1, abort_flag, p.status, 14)) { ok = false; break; }
       ++pf_cnt;
       tc_fence_after();
       // dQ (+)= dS K_t: dS from TMEM (k-step kk = keys [16 kk, 16 kk + 16) =
@@ -507,17 +507,17 @@ __device__ __forceinline__ void dkdv_mma(const BwdParams& p, uint8_t* smem, uint
     return smem_u32(smem + L::kRingOff + (c % L::kStages) * L::kTileBytes);
   };
   auto ring_wait = [&](uint32_t c, unsigned where) {
-    return wait_bar(bar(L::kRingFull + c % L::kStages), (c / L::kStages) & 1, abort_flag,
+    return wait_bar_warp(bar(L::kRingFull + c % L::kStages), (c / L::kStages) & 1, abort_flag,
                     p.status, where);
   };
   uint32_t cnt = 0, ff_cnt = 0, pf_cnt = 0, ae_cnt = 0;
   bool ok = true;
   UnitQueue queue = unit_queue<HD, kModeDkdv>(smem, bars);
   int u;
-  while (ok && (u = queue_pop<false>(queue, abort_flag, p.status)) >= 0) {
+  while (ok && (u = queue_pop<true>(queue, abort_flag, p.status)) >= 0) {
     const Unit un = bwd_decode<true>(u, p);
     if (un.n == 0) continue;
-    if (!wait_bar(bar(L::kFixFull), ff_cnt & 1, abort_flag, p.status, 10)) break;
+    if (!wait_bar_warp(bar(L::kFixFull), ff_cnt & 1, abort_flag, p.status, 10)) break;
     ++ff_cnt;
     if (!ring_wait(cnt, 11)) break;
     tc_fence_after();
@@ -532,10 +532,10 @@ __device__ __forceinline__ void dkdv_mma(const BwdParams& p, uint8_t* smem, uint
       const uint32_t c = cnt + 2 * t;  // Q_t at c, dO_t at c + 1
       const bool more = t + 1 < un.n;
       if (t == 0) {
-        if (!wait_bar(bar(L::kAccEmpty), (ae_cnt & 1) ^ 1, abort_flag, p.status, 13)) { ok = false; break; }
+        if (!wait_bar_warp(bar(L::kAccEmpty), (ae_cnt & 1) ^ 1, abort_flag, p.status, 13)) { ok = false; break; }
         ++ae_cnt;
       }
-      if (!wait_bar(bar(L::kPFull), pf_cnt & 1, abort_flag, p.status, 14)) { ok = false; break; }
+      if (!wait_bar_warp(bar(L::kPFull), pf_cnt & 1, abort_flag, p.status, 14)) { ok = false; break; }
       tc_fence_after();
       mma_tmem_a(tDV, tA, stage_addr(c + 1), kIdAcc, t > 0);  // dV += P^T dO_t
       mma_commit(bar(L::kRingEmpty + (c + 1) % L::kStages));
@@ -545,7 +545,7 @@ __device__ __forceinline__ void dkdv_mma(const BwdParams& p, uint8_t* smem, uint
         mma_kmajor<HD>(tA, fk, stage_addr(c + 2), kIdS);  // S^T(t+1) over P^T(t)
         mma_commit(bar(L::kSFull));
       }
-      if (!wait_bar(bar(L::kPFull + 1), pf_cnt & 1, abort_flag, p.status, 16)) { ok = false; break; }
+      if (!wait_bar_warp(bar(L::kPFull + 1), pf_cnt & 1, abort_flag, p.status, 16)) { ok = false; break; }
       ++pf_cnt;
       tc_fence_after();
       mma_tmem_a(tDK, tB, stage_addr(c), kIdAcc, t > 0);  // dK += dS^T Q_t
@@ -597,17 +597,17 @@ __device__ __forceinline__ void fused_mma(const BwdParams& p, uint8_t* smem, uin
     return smem_u32(smem + L::kRingOff + (c % L::kStages) * L::kTileBytes);
   };
   auto ring_wait = [&](uint32_t c, unsigned where) {
-    return wait_bar(bar(L::kRingFull + c % L::kStages), (c / L::kStages) & 1, abort_flag,
+    return wait_bar_warp(bar(L::kRingFull + c % L::kStages), (c / L::kStages) & 1, abort_flag,
                     p.status, where);
   };
   uint32_t cnt = 0, ff_cnt = 0, pf_cnt = 0, ae_cnt = 0, dq_cnt = 0;
   bool ok = true, pending_drain = false;
   UnitQueue queue = unit_queue<HD, kModeFused>(smem, bars);
   int u;
-  while (ok && (u = queue_pop<false>(queue, abort_flag, p.status)) >= 0) {
+  while (ok && (u = queue_pop<true>(queue, abort_flag, p.status)) >= 0) {
     const Unit un = bwd_decode<true>(u, p);
     if (un.n == 0) continue;
-    if (!wait_bar(bar(L::kFixFull), ff_cnt & 1, abort_flag, p.status, 10)) break;
+    if (!wait_bar_warp(bar(L::kFixFull), ff_cnt & 1, abort_flag, p.status, 10)) break;
     ++ff_cnt;
     if (!ring_wait(cnt, 11)) break;
     tc_fence_after();
@@ -615,7 +615,7 @@ __device__ __forceinline__ void fused_mma(const BwdParams& p, uint8_t* smem, uin
     mma_commit(bar(L::kSFull));
     if (!ring_wait(cnt + 1, 12)) break;
     // the previous unit's last dQ product must be out of B
-    if (pending_drain && !wait_bar(bar(L::kDqFree), dq_cnt++ & 1, abort_flag, p.status, 17)) break;
+    if (pending_drain && !wait_bar_warp(bar(L::kDqFree), dq_cnt++ & 1, abort_flag, p.status, 17)) break;
     tc_fence_after();
     mma_kmajor<HD>(tB, fv, stage_addr(cnt + 1), kIdS);  // dP^T(0) = V dO_0^T
     mma_commit(bar(L::kSFull + 1));
@@ -623,10 +623,10 @@ __device__ __forceinline__ void fused_mma(const BwdParams& p, uint8_t* smem, uin
       const uint32_t c = cnt + 2 * t;  // Q_t at c, dO_t at c + 1
       const bool more = t + 1 < un.n;
       if (t == 0) {
-        if (!wait_bar(bar(L::kAccEmpty), (ae_cnt & 1) ^ 1, abort_flag, p.status, 13)) { ok = false; break; }
+        if (!wait_bar_warp(bar(L::kAccEmpty), (ae_cnt & 1) ^ 1, abort_flag, p.status, 13)) { ok = false; break; }
         ++ae_cnt;
       }
-      if (!wait_bar(bar(L::kPFull), pf_cnt & 1, abort_flag, p.status, 14)) { ok = false; break; }
+      if (!wait_bar_warp(bar(L::kPFull), pf_cnt & 1, abort_flag, p.status, 14)) { ok = false; break; }
       tc_fence_after();
       mma_tmem_a(tDV, tA, stage_addr(c + 1), kIdAcc, t > 0);  // dV += P^T dO_t
       mma_commit(bar(L::kRingEmpty + (c + 1) % L::kStages));
@@ -636,7 +636,7 @@ __device__ __forceinline__ void fused_mma(const BwdParams& p, uint8_t* smem, uin
         mma_kmajor<HD>(tA, fk, stage_addr(c + 2), kIdS);  // S^T(t+1) over P^T(t)
         mma_commit(bar(L::kSFull));
       }
-      if (!wait_bar(bar(L::kPFull + 1), pf_cnt & 1, abort_flag, p.status, 16)) { ok = false; break; }
+      if (!wait_bar_warp(bar(L::kPFull + 1), pf_cnt & 1, abort_flag, p.status, 16)) { ok = false; break; }
       ++pf_cnt;
       tc_fence_after();
       mma_tmem_a(tDK, tB, stage_addr(c), kIdAcc, t > 0);  // dK += dS^T Q_t
@@ -647,7 +647,7 @@ __device__ __forceinline__ void fused_mma(const BwdParams& p, uint8_t* smem, uin
       mma_commit(bar(L::kRingEmpty + c % L::kStages));
       if (!more) mma_commit(bar(L::kFixEmpty));  // K and V are not read again
       if (more) {
-        if (!wait_bar(bar(L::kDqFree), dq_cnt++ & 1, abort_flag, p.status, 17)) { ok = false; break; }
+        if (!wait_bar_warp(bar(L::kDqFree), dq_cnt++ & 1, abort_flag, p.status, 17)) { ok = false; break; }
         if (!ring_wait(c + 3, 12)) { ok = false; break; }
         tc_fence_after();
         mma_kmajor<HD>(tB, fv, stage_addr(c + 3), kIdS);  // dP^T(t+1) over dQ(t)
@@ -1205,12 +1205,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
   if (warp < 4) regs_shrink<80>();  // 384 x 168 at launch: 128 x 80 + 256 x 208
   if (warp == 0) {
     if (lane == 0) bwd_producer<HD, kMode>(p, smem, bars, abort_flag);
-  } else if (warp == 1) {
-    if (lane == 0) {
-      if (kMode == kModeFused) fused_mma<HD>(p, smem, bars, tmem, abort_flag);
-      else if (kMode == kModeDkdv) dkdv_mma<HD>(p, smem, bars, tmem, abort_flag);
-      else dq_mma<HD>(p, smem, bars, tmem, abort_flag);
-    }
+  } else if (warp == 1) {  // the whole warp: the MMA wrappers elect one lane
+    if (kMode == kModeFused) fused_mma<HD>(p, smem, bars, tmem, abort_flag);
+    else if (kMode == kModeDkdv) dkdv_mma<HD>(p, smem, bars, tmem, abort_flag);
+    else dq_mma<HD>(p, smem, bars, tmem, abort_flag);
   } else if (warp >= 4) {
     const int g = (warp - 4) >> 2;  // elementwise warpgroup: columns [64 g, 64 g + 64)
     regs_grow<208>();

@@ -170,6 +170,15 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   }
 }
 
+// wait_bar for all 32 lanes of a warp (the MMA-issuing warps): every lane
+// gets the same answer and the warp is converged afterwards, as the
+// warp-elected MMA and commit wrappers require.
+__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity,
+                                              volatile int* abort_flag, unsigned* status,
+                                              unsigned where) {
+  return __all_sync(0xFFFFFFFFu, wait_bar(bar, parity, abort_flag, status, where));
+}
+
 // Used only on the abort path: wait for copies already in flight, ignoring
 // the abort flag, with a short limit.
 __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {

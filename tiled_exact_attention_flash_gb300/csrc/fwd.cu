@@ -241,7 +241,7 @@ __device__ __forceinline__ void fwd_mma(const FwdParams& p, uint8_t* smem, uint6
   // buffer h of the slot holding group g
   auto buf = [&](uint32_t g, int h) { return ring + (2 * (g % L::kSlots) + h) * L::kTileBytes; };
   auto wait_group = [&](uint32_t g, unsigned where) {
-    return wait_bar(bar(L::kKvFull + g % L::kSlots), (g / L::kSlots) & 1, abort_flag, p.status,
+    return wait_bar_warp(bar(L::kKvFull + g % L::kSlots), (g / L::kSlots) & 1, abort_flag, p.status,
                     where);
   };
   bool ok = true;
@@ -272,7 +272,7 @@ __device__ __forceinline__ void fwd_mma(const FwdParams& p, uint8_t* smem, uint6
     // prologue: Q K^T of the first tile (the unit's first ring group: its K)
     {
       for (int s = 0; s < 2 && ok; ++s)
-        if (cur.in[s] && !wait_bar(bar(L::kQFull + s), qf_cnt[s] & 1, abort_flag, p.status, 13))
+        if (cur.in[s] && !wait_bar_warp(bar(L::kQFull + s), qf_cnt[s] & 1, abort_flag, p.status, 13))
           ok = false;
       if (ok && !wait_group(g_cnt, 14)) ok = false;
       if (!ok) break;
@@ -296,7 +296,7 @@ __device__ __forceinline__ void fwd_mma(const FwdParams& p, uint8_t* smem, uint6
       if (more) {
         for (int s = 0; s < 2 && ok; ++s)
           if (nxt.in[s] && issued[s] == 0 &&
-              !wait_bar(bar(L::kQFull + s), qf_cnt[s] & 1, abort_flag, p.status, 13))
+              !wait_bar_warp(bar(L::kQFull + s), qf_cnt[s] & 1, abort_flag, p.status, 13))
             ok = false;
         if (!ok) break;
       }
@@ -304,13 +304,13 @@ __device__ __forceinline__ void fwd_mma(const FwdParams& p, uint8_t* smem, uint6
       for (int s = 0; s < 2 && ok; ++s) {
         const uint32_t tS = tmem + uint32_t(s * 256);
         if (cur.in[s]) {  // O_s (+)= P_s V
-          if (!wait_bar(bar(L::kPFull + s), pf_cnt[s] & 1, abort_flag, p.status, 10)) {
+          if (!wait_bar_warp(bar(L::kPFull + s), pf_cnt[s] & 1, abort_flag, p.status, 10)) {
             ok = false;
             break;
           }
           ++pf_cnt[s];
           if (seen[s] == 0) {
-            if (!wait_bar(bar(L::kOEmpty + s), (oe_cnt[s] & 1) ^ 1, abort_flag, p.status, 11)) {
+            if (!wait_bar_warp(bar(L::kOEmpty + s), (oe_cnt[s] & 1) ^ 1, abort_flag, p.status, 11)) {
               ok = false;
               break;
             }
@@ -367,7 +367,7 @@ __device__ __forceinline__ void fwd_mma_slot(const FwdParams& p, uint8_t* smem, 
   // that skipped the wait could release a later use of the slot before the
   // other thread released this one (arrivals are not tagged)
   auto wait_group = [&](uint32_t g, unsigned where) {
-    return wait_bar(bar(L::kKvFull + g % L::kSlots), (g / L::kSlots) & 1, abort_flag, p.status,
+    return wait_bar_warp(bar(L::kKvFull + g % L::kSlots), (g / L::kSlots) & 1, abort_flag, p.status,
                     where);
   };
   const uint32_t tS = tmem + uint32_t(s * 256);
@@ -398,7 +398,7 @@ __device__ __forceinline__ void fwd_mma_slot(const FwdParams& p, uint8_t* smem, 
     walk_next(w, p.list, cur);  // the union is non-empty
     // prologue: Q K^T of the first tile (the unit's first ring group: its K)
     {
-      if (cur.in[s] && !wait_bar(bar(L::kQFull + s), qf_cnt & 1, abort_flag, p.status, 13))
+      if (cur.in[s] && !wait_bar_warp(bar(L::kQFull + s), qf_cnt & 1, abort_flag, p.status, 13))
         ok = false;
       if (ok && !wait_group(g_cnt, 14)) ok = false;
       if (!ok) break;
@@ -418,13 +418,13 @@ __device__ __forceinline__ void fwd_mma_slot(const FwdParams& p, uint8_t* smem, 
         break;
       }
       if (cur.in[s]) {  // O_s (+)= P_s V
-        if (!wait_bar(bar(L::kPFull + s), pf_cnt & 1, abort_flag, p.status, 10)) {
+        if (!wait_bar_warp(bar(L::kPFull + s), pf_cnt & 1, abort_flag, p.status, 10)) {
           ok = false;
           break;
         }
         ++pf_cnt;
         if (seen == 0) {
-          if (!wait_bar(bar(L::kOEmpty + s), (oe_cnt & 1) ^ 1, abort_flag, p.status, 11)) {
+          if (!wait_bar_warp(bar(L::kOEmpty + s), (oe_cnt & 1) ^ 1, abort_flag, p.status, 11)) {
             ok = false;
             break;
           }
@@ -442,7 +442,7 @@ __device__ __forceinline__ void fwd_mma_slot(const FwdParams& p, uint8_t* smem, 
         if (seen == pu.n[s]) mma_commit(bar(L::kOFull + s));
       }
       if (more && nxt.in[s]) {
-        if (issued == 0 && !wait_bar(bar(L::kQFull + s), qf_cnt & 1, abort_flag, p.status, 13)) {
+        if (issued == 0 && !wait_bar_warp(bar(L::kQFull + s), qf_cnt & 1, abort_flag, p.status, 13)) {
           ok = false;
           break;
         }
@@ -673,11 +673,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     regs_shrink<80>();
     if (warp == 0) {
       if (lane == 0) fwd_producer<HD>(p, smem, bars, abort_flag);
-    } else if (p.slot_issuers) {  // one MMA issuer per slot (warps 1 and 3)
-      if ((warp == 1 || warp == 3) && lane == 0)
+    } else if (p.slot_issuers) {  // one MMA-issuing warp per slot (warps 1 and 3)
+      if (warp == 1 || warp == 3)
         fwd_mma_slot<HD>(p, smem, bars, tmem, warp == 1 ? 0 : 1, abort_flag);
-    } else if (warp == 1) {
-      if (lane == 0) fwd_mma<HD>(p, smem, bars, tmem, abort_flag);
+    } else if (warp == 1) {  // the whole warp: the MMA wrappers elect one lane
+      fwd_mma<HD>(p, smem, bars, tmem, abort_flag);
     }
   } else {
     regs_grow<208>();
