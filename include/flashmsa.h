@@ -163,6 +163,15 @@ typedef struct flash_msa_block_index {
   int32_t* tile_start;
   int32_t* tile_seq0;
   int32_t* tile_seq_len;
+  /* Of the key tiles listed by the two query blocks at q_order positions 2r
+   * and 2r + 1 (the blocks the forward runs together), the fraction that
+   * both of them list: sum over the pairs of |common tiles| / sum of |tiles
+   * of either| (0 with fewer than two blocks).  Set by the filling build
+   * call (0 after the counting call).  A scheduling hint only: the forward
+   * issues the pair's products from one thread, interleaved, when it is at
+   * least 1/2, else from one thread per block; 0 (a struct filled by other
+   * means) keeps the latter. */
+  float pair_overlap;
 } flash_msa_block_index;
 
 /* Mask description (host memory).  A NULL mask, or flags == 0, is dense

@@ -221,3 +221,34 @@ def test_live_element_counts_with_bits(n, fields, seed):
                   {"doc_starts": tuple(int(x) for x in np.cumsum([0] + document_lengths(n, seed, 90)))}):
         f = dict(fields, **extra)
         assert api.build_block_index(api.Mask(**f), n).live_elements == _oracle_live_count(n, f)
+
+
+def _pair_overlap(host):
+    """Sum over q_order pairs of the common key tiles / sum of the tiles of
+    either block, from the lists as sets."""
+    rp, ci, qo = host["row_ptr"], host["col_idx"], host["q_order"]
+    common = either = 0
+    for r in range(0, len(qo) - 1, 2):
+        a = set(ci[rp[qo[r]]:rp[qo[r] + 1]].tolist())
+        b = set(ci[rp[qo[r + 1]]:rp[qo[r + 1] + 1]].tolist())
+        common += len(a & b)
+        either += len(a | b)
+    return common / either if either else 0.0
+
+
+@pytest.mark.parametrize("cid,shared", [(2, True), (4, True), (5, False), (6, True), (7, False),
+                                        (8, False), (9, False), (10, True)])
+def test_pair_overlap(cid, shared):
+    """pair_overlap (the forward's choice between one interleaving MMA warp and
+    one per query slot) is the overlap of the paired blocks' key-tile lists;
+    the counting call leaves it 0."""
+    import ctypes
+    w = WORKLOADS[cid]
+    m = api.Mask(**w.mask_fields())
+    got = api.build_block_index(m, w.N)
+    assert got.header.pair_overlap == pytest.approx(_pair_overlap(got.host), rel=1e-6)
+    assert (got.header.pair_overlap >= 0.5) == shared
+    hdr = api.BlockIndexStruct()
+    assert api.lib().flash_msa_build_block_index(ctypes.byref(m.desc()), w.N,
+                                                 ctypes.byref(hdr)) == api.OK
+    assert hdr.pair_overlap == 0.0

@@ -73,6 +73,7 @@ class BlockIndexStruct(ctypes.Structure):
         ("tile_start", ctypes.c_void_p),
         ("tile_seq0", ctypes.c_void_p),
         ("tile_seq_len", ctypes.c_void_p),
+        ("pair_overlap", ctypes.c_float),
     ]
 
 
@@ -253,6 +254,7 @@ class BlockIndex:
         s.n_bit_tiles = self.header.n_bit_tiles
         s.live_elements = self.header.live_elements
         s.sequence_tiles = self.header.sequence_tiles
+        s.pair_overlap = self.header.pair_overlap
 
     def host_struct(self) -> BlockIndexStruct:
         s = BlockIndexStruct(self.header.seq_len, self.header.n_q_blocks, self.header.n_k_blocks,

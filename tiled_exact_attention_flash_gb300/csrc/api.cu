@@ -248,6 +248,31 @@ static void finish_lists(flash_msa_block_index* out, int64_t nb,
   });
 }
 
+// flash_msa_block_index::pair_overlap from the filled CSR lists (ascending
+// within a row) and the final q_order.
+static float pair_overlap(const flash_msa_block_index* ix, int64_t nb) {
+  int64_t common = 0, either = 0;
+  for (int64_t r = 0; r + 1 < nb; r += 2) {
+    const int32_t a = ix->q_order[r], b = ix->q_order[r + 1];
+    int32_t i = ix->row_ptr[a], j = ix->row_ptr[b];
+    const int32_t ie = ix->row_ptr[a + 1], je = ix->row_ptr[b + 1];
+    either += (ie - i) + (je - j);
+    while (i < ie && j < je) {
+      if (ix->col_idx[i] == ix->col_idx[j]) {
+        ++common;
+        ++i;
+        ++j;
+      } else if (ix->col_idx[i] < ix->col_idx[j]) {
+        ++i;
+      } else {
+        ++j;
+      }
+    }
+  }
+  either -= common;
+  return either > 0 ? float(double(common) / double(either)) : 0.f;
+}
+
 // Live (i, j) pairs of a live tile (qb, kb) of class k (0 full) of one
 // sequence of n tokens: all valid entries of a full tile, one interval of
 // columns per row of a partial one (the kernels' row_live_range).
@@ -368,6 +393,7 @@ static flash_msa_status build_sequence_tiles(const flash_msa_mask_desc* mask,
     out->q_order[at++] = t - 1;
   }
   for (int32_t t : singles) out->q_order[at++] = t;
+  out->pair_overlap = pair_overlap(out, nt);
   return FLASH_MSA_OK;
 }
 
@@ -382,6 +408,7 @@ flash_msa_status flash_msa_build_block_index(const flash_msa_mask_desc* mask, in
   bool need = false;
   flash_msa_status st = check_mask(mask, mp, need);
   if (st != FLASH_MSA_OK) return st;
+  out->pair_overlap = 0.f;  // set at the end of the filling call
   const bool with_bitmask = (mask->flags & FLASH_MSA_BITMASK) != 0;
   const bool with_docs = (mask->flags & FLASH_MSA_DOCUMENTS) != 0;
   const bool with_bits = with_bitmask || with_docs;
@@ -573,6 +600,7 @@ flash_msa_status flash_msa_build_block_index(const flash_msa_mask_desc* mask, in
   if (!with_bits) out->n_bit_tiles = 0;
   out->live_elements = live;
   finish_lists(out, nb, col_count, with_bits);
+  out->pair_overlap = pair_overlap(out, nb);
   return FLASH_MSA_OK;
 }
 
@@ -679,6 +707,7 @@ static flash_msa_status fwd_impl(const void* q, const void* k, const void* v, vo
   if ((st = check_mask(mask, a.mask, need)) != FLASH_MSA_OK) return st;
   ListParams unused;
   if ((st = make_lists(mask, N, need, false, a.list, unused)) != FLASH_MSA_OK) return st;
+  a.pair_overlap = (mask && mask->index) ? mask->index->pair_overlap : 0.f;
   a.q = q;
   a.k = k;
   a.v = v;

@@ -19,7 +19,8 @@
 // outputs are deterministic.
 //
 // CTA layout of the two main kernels (384 threads, one CTA per SM):
-//   warp 0 TMA producer (one lane), warp 1 MMA issuer (one lane), warp 2
+//   warp 0 TMA producer (one lane), warp 1 MMA issuer (the whole warp runs
+//   the loop, one elected lane issues), warp 2
 //   TMEM allocator, warps 4-11 elementwise work in two warpgroups: thread =
 //   row of the stationary tile (key row in bwd_dkdv, query row in bwd_dq),
 //   warpgroup g = columns [64 g, 64 g + 64) of the moving tile.
@@ -225,7 +226,7 @@ __device__ __forceinline__ void init_bwd_barriers(uint64_t* bars) {
   }
   for (int i = 0; i < 2; ++i) {
     mbar_init(smem_u32(bars + L::kUnitFull + i), 1);               // the producer
-    mbar_init(smem_u32(bars + L::kUnitEmpty + i), 1 + kEwWarps);  // MMA thread, EW warps
+    mbar_init(smem_u32(bars + L::kUnitEmpty + i), 1 + kEwWarps);  // MMA warp, EW warps
   }
   fence_mbar_init();
 }

@@ -8,8 +8,10 @@
 //
 // CTA layout (384 threads, one CTA per SM, each working through pair units):
 //   warp 0      TMA producer: Q tiles and the K/V ring, one elected lane
-//   warp 1      MMA issuer: tcgen05.mma for S = Q K^T and O += P V, one lane
-//               (with an index: slot 0 only, warp 3 issuing for slot 1)
+//   warp 1      MMA issuer: tcgen05.mma for S = Q K^T and O += P V (the
+//               whole warp runs the loop, one elected lane issues; for
+//               index lists whose pairs mostly differ: slot 0 only, warp 3
+//               issuing for slot 1)
 //   warp 2      TMEM allocator
 //   warps 4-7   softmax + epilogue for query slot 0 (thread = query row)
 //   warps 8-11  softmax + epilogue for query slot 1
@@ -35,7 +37,7 @@ struct FwdParams {
   int G;  // query heads per key/value head
   int n_units;
   int head_group;    // pair units are numbered in groups of this many heads
-  int slot_issuers;  // one MMA-issuing thread per query slot (else one for both)
+  int slot_issuers;  // one MMA-issuing warp per query slot (else one for both)
   float scale_log2;  // scale * log2(e)
   int wait_limit_ms;  // limit of any single bounded wait
   MaskParams mask;
@@ -349,13 +351,13 @@ __device__ __forceinline__ void fwd_mma(const FwdParams& p, uint8_t* smem, uint6
 template <int HD>
 __device__ __forceinline__ void fwd_mma_slot(const FwdParams& p, uint8_t* smem, uint64_t* bars,
                                              uint32_t tmem, int s, volatile int* abort_flag) {
-  // MMA issuer of query slot s, used for lists from a block index (other than
-  // per-sequence tiles): one thread per slot, both walking the same union of
-  // key tiles (so both see
-  // the same ring groups) and both releasing every group (kKvEmpty then
-  // counts two commits).  Where the two slots' lists differ, neither slot
-  // waits for the other's softmax; with identical dense / causal lists the
-  // single issuer (fwd_mma), whose order staggers the slots, is faster.
+  // MMA issuer of query slot s, used for lists from a block index whose
+  // pairs mostly differ (pair_overlap below 1/2): one warp per slot, both
+  // walking the same union of key tiles (so both see the same ring groups)
+  // and both releasing every group (kKvEmpty then counts two commits).
+  // Where the two slots' lists differ, neither slot waits for the other's
+  // softmax; where they mostly coincide the single issuer (fwd_mma), whose
+  // order staggers the slots, is faster.
   using L = FwdLayout<HD>;
   auto bar = [&](int i) { return smem_u32(bars + i); };
   constexpr uint32_t kIdQK = idesc_bf16_f32(128, 128, false, false);
@@ -649,7 +651,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       mbar_init(smem_u32(bars + L::kOFull + s), 1);
       mbar_init(smem_u32(bars + L::kOEmpty + s), 128);
     }
-    const uint32_t issuers = p.slot_issuers ? 2 : 1;  // MMA threads (see fwd_mma_slot)
+    const uint32_t issuers = p.slot_issuers ? 2 : 1;  // MMA warps (see fwd_mma_slot)
     mbar_init(smem_u32(bars + L::kMmaDone), issuers);
     for (int i = 0; i < L::kSlots; ++i) {
       mbar_init(smem_u32(bars + L::kKvFull + i), 1);
@@ -717,7 +719,11 @@ static flash_msa_status launch_fwd_hd(const FwdLaunch& a, cudaStream_t stream) {
   // lists from a block index differ between the two slots of a pair, except
   // for per-sequence tiles, whose pairs are neighbours in one sequence: those
   // (like dense / causal lists) take the single issuer that staggers the slots
-  p.slot_issuers = (a.list.ptr && !a.list.t_start) ? 1 : 0;
+  // one MMA-issuing warp per slot where the pairs' lists mostly differ (the
+  // fixed interleave of a single issuer would make each slot wait on the
+  // other's tiles); one warp interleaving both slots where they mostly
+  // coincide, as for arithmetic lists and per-sequence tiles
+  p.slot_issuers = (a.list.ptr && !a.list.t_start && a.pair_overlap < 0.5f) ? 1 : 0;
   // one group of all heads: plain rank-major order (groups of a few heads,
   // whose K and V would stay in L2, measured slower: the static deal then
   // leaves CTAs idle at the group boundaries)

@@ -51,7 +51,8 @@ struct FwdLaunch {
   int64_t N;
   float scale;
   MaskParams mask;
-  ListParams list;  // CSR by query block (or arithmetic)
+  ListParams list;     // CSR by query block (or arithmetic)
+  float pair_overlap;  // the index's pair_overlap (0 without an index)
   unsigned* status;
 };
 flash_msa_status launch_fwd(const FwdLaunch& a, cudaStream_t stream);
