@@ -220,8 +220,14 @@ __device__ __forceinline__ void init_bwd_barriers(uint64_t* bars) {
   mbar_init(smem_u32(bars + L::kDqFull), 1);
   mbar_init(smem_u32(bars + L::kDqFree), kEwWarps);
   for (int i = 0; i < 2; ++i) mbar_init(smem_u32(bars + L::kWgSync + i), 4);
+  // dQ pass: K_t and V_t (ring stages 2i, 2i + 1) are loaded together and
+  // read by the same first products, so both arrive on the full barrier of
+  // stage 2i (count 2) and the MMA warp waits once per key tile; the
+  // key-stationary kernels keep one full barrier per stage (S^T(t+1) needs
+  // only Q_t+1)
+  static_assert(L::kStages % 2 == 0, "ring stages come in pairs");
   for (int i = 0; i < L::kStages; ++i) {
-    mbar_init(smem_u32(bars + L::kRingFull + i), 1);
+    mbar_init(smem_u32(bars + L::kRingFull + i), (kMode == kModeDq && i % 2 == 0) ? 2 : 1);
     mbar_init(smem_u32(bars + L::kRingEmpty + i), 1);
   }
   for (int i = 0; i < 2; ++i) {
@@ -305,19 +311,21 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint8_t* smem, 
           break;
         }
         const uint32_t dst = smem_u32(smem + L::kRingOff + stage * L::kTileBytes);
+        // the stage's full barrier, or in the dQ pass the pair's (see the init)
+        const uint32_t full = bar(L::kRingFull + (kKeyStationary ? stage : (stage & ~1)));
         if (half == 0) {
           const bool vec = kKeyStationary;
-          mbar_arrive_expect_tx(bar(L::kRingFull + stage), L::kTileBytes + (vec ? 1024 : 0));
-          load_tile_2d<HD>(ring_a, dst, bar(L::kRingFull + stage), ring_row, hr, un.b);
+          mbar_arrive_expect_tx(full, L::kTileBytes + (vec ? 1024 : 0));
+          load_tile_2d<HD>(ring_a, dst, full, ring_row, hr, un.b);
           if (vec) {
             const int64_t row0 = (int64_t(un.b) * p.H + hq) * p.NP + int64_t(it.blk) * kTile;
             const uint32_t vdst = smem_u32(smem + L::kVecOff + (stage / 2) * 1024);
-            bulk_load(vdst, p.nlse2 + row0, 512, bar(L::kRingFull + stage));
-            bulk_load(vdst + 512, p.dsum + row0, 512, bar(L::kRingFull + stage));
+            bulk_load(vdst, p.nlse2 + row0, 512, full);
+            bulk_load(vdst + 512, p.dsum + row0, 512, full);
           }
         } else {
-          mbar_arrive_expect_tx(bar(L::kRingFull + stage), L::kTileBytes);
-          load_tile_2d<HD>(ring_b, dst, bar(L::kRingFull + stage), ring_row, hr, un.b);
+          mbar_arrive_expect_tx(full, L::kTileBytes);
+          load_tile_2d<HD>(ring_b, dst, full, ring_row, hr, un.b);
         }
         last[stage] = int(phase);
         if (++stage == L::kStages) {
@@ -338,9 +346,10 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint8_t* smem, 
       }
     }
   }
-  if (!ok) {
+  if (!ok) {  // (in the dQ pass a pair whose V was never issued waits out the drain limit)
     for (int i = 0; i < L::kStages; ++i)
-      if (last[i] >= 0) drain_bar(bar(L::kRingFull + i), uint32_t(last[i]));
+      if (last[i] >= 0)
+        drain_bar(bar(L::kRingFull + (kKeyStationary ? i : (i & ~1))), uint32_t(last[i]));
     if (last_fix >= 0) drain_bar(bar(L::kFixFull), last_fix & 1);
   }
 }
@@ -440,7 +449,7 @@ __device__ __forceinline__ void dq_mma(const BwdParams& p, uint8_t* smem, uint64
     if (un.n == 0) continue;
     if (!wait_bar_warp(bar(L::kFixFull), ff_cnt & 1, abort_flag, p.status, 10)) break;
     ++ff_cnt;
-    if (!ring_wait(pos.s, pos.ph, 11) || !ring_wait(pos.s + 1, pos.ph, 12)) break;
+    if (!ring_wait(pos.s, pos.ph, 11)) break;  // K_t and V_t: one barrier per pair
     // the previous unit's last S / dP must be in registers before S(0) and
     // dP(0) overwrite them
     if (pending_sdp) {
@@ -453,7 +462,7 @@ __device__ __forceinline__ void dq_mma(const BwdParams& p, uint8_t* smem, uint64
     for (int t = 0; t < un.n && ok; ++t) {
       const Pos nxt = advance(pos);  // pos: tile t, nxt: tile t + 1
       if (t + 1 < un.n) {
-        if (!ring_wait(nxt.s, nxt.ph, 11) || !ring_wait(nxt.s + 1, nxt.ph, 12)) { ok = false; break; }
+        if (!ring_wait(nxt.s, nxt.ph, 11)) { ok = false; break; }
         if (!wait_bar_warp(bar(L::kDpFree), sdp_cnt & 1, abort_flag, p.status, 15)) { ok = false; break; }
         ++sdp_cnt;
         tc_fence_after();
