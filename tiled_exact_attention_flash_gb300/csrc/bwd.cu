@@ -220,14 +220,15 @@ __device__ __forceinline__ void init_bwd_barriers(uint64_t* bars) {
   mbar_init(smem_u32(bars + L::kDqFull), 1);
   mbar_init(smem_u32(bars + L::kDqFree), kEwWarps);
   for (int i = 0; i < 2; ++i) mbar_init(smem_u32(bars + L::kWgSync + i), 4);
-  // dQ pass: K_t and V_t (ring stages 2i, 2i + 1) are loaded together and
-  // read by the same first products, so both arrive on the full barrier of
-  // stage 2i (count 2) and the MMA warp waits once per key tile; the
-  // key-stationary kernels keep one full barrier per stage (S^T(t+1) needs
-  // only Q_t+1)
+  // The ring holds pairs loaded together: (K_t, V_t) in the dQ pass, (Q_t,
+  // dO_t) in the key-stationary kernels, in stages 2i and 2i + 1.  Both
+  // copies of a pair arrive on the full barrier of stage 2i (count 2; the
+  // odd stages' full barriers are unused), so the MMA warp waits once per
+  // inner tile; the empty barriers stay per stage (the halves are released
+  // apart).
   static_assert(L::kStages % 2 == 0, "ring stages come in pairs");
   for (int i = 0; i < L::kStages; ++i) {
-    mbar_init(smem_u32(bars + L::kRingFull + i), (kMode == kModeDq && i % 2 == 0) ? 2 : 1);
+    mbar_init(smem_u32(bars + L::kRingFull + i), (i % 2 == 0) ? 2 : 1);
     mbar_init(smem_u32(bars + L::kRingEmpty + i), 1);
   }
   for (int i = 0; i < 2; ++i) {
@@ -305,15 +306,22 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint8_t* smem, 
       const InnerTile it = bwd_inner<kKeyStationary>(un, t, p, hq);
       const int hr = kKeyStationary ? hq : hkv;  // head of the streamed tiles
       const int ring_row = int(tile_geo(p.list, it.blk, p.N).row0);
+      // the pair: ring_a's tile (Q or K) into stage `stage` (even), ring_b's
+      // (dO or V) into stage + 1, both completing the full barrier of
+      // `stage`.  The key-stationary kernels copy dO first: its stage is
+      // released earlier (after dV) than Q's (after dK), so Q, which the
+      // pair's first product S^T needs, is the later copy and waiting for
+      // the whole pair costs nothing
+      const uint32_t full = bar(L::kRingFull + stage);
       for (int half = 0; half < 2; ++half) {
-        if (!wait_bar(bar(L::kRingEmpty + stage), phase ^ 1, abort_flag, p.status, 2)) {
+        const bool is_a = kKeyStationary ? (half == 1) : (half == 0);
+        const int st = stage + (is_a ? 0 : 1);
+        if (!wait_bar(bar(L::kRingEmpty + st), phase ^ 1, abort_flag, p.status, 2)) {
           ok = false;
           break;
         }
-        const uint32_t dst = smem_u32(smem + L::kRingOff + stage * L::kTileBytes);
-        // the stage's full barrier, or in the dQ pass the pair's (see the init)
-        const uint32_t full = bar(L::kRingFull + (kKeyStationary ? stage : (stage & ~1)));
-        if (half == 0) {
+        const uint32_t dst = smem_u32(smem + L::kRingOff + st * L::kTileBytes);
+        if (is_a) {
           const bool vec = kKeyStationary;
           mbar_arrive_expect_tx(full, L::kTileBytes + (vec ? 1024 : 0));
           load_tile_2d<HD>(ring_a, dst, full, ring_row, hr, un.b);
@@ -327,11 +335,13 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint8_t* smem, 
           mbar_arrive_expect_tx(full, L::kTileBytes);
           load_tile_2d<HD>(ring_b, dst, full, ring_row, hr, un.b);
         }
-        last[stage] = int(phase);
-        if (++stage == L::kStages) {
-          stage = 0;
-          phase ^= 1;
-        }
+        last[st] = int(phase);
+      }
+      if (!ok) break;
+      stage += 2;
+      if (stage == L::kStages) {
+        stage = 0;
+        phase ^= 1;
       }
       if (t + kL2PrefetchTiles < un.n) {
         int fq;
@@ -346,10 +356,9 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint8_t* smem, 
       }
     }
   }
-  if (!ok) {  // (in the dQ pass a pair whose V was never issued waits out the drain limit)
+  if (!ok) {  // (a pair whose second copy was never issued waits out the drain limit)
     for (int i = 0; i < L::kStages; ++i)
-      if (last[i] >= 0)
-        drain_bar(bar(L::kRingFull + (kKeyStationary ? i : (i & ~1))), uint32_t(last[i]));
+      if (last[i] >= 0) drain_bar(bar(L::kRingFull + (i & ~1)), uint32_t(last[i]));
     if (last_fix >= 0) drain_bar(bar(L::kFixFull), last_fix & 1);
   }
 }
@@ -529,12 +538,10 @@ __device__ __forceinline__ void dkdv_mma(const BwdParams& p, uint8_t* smem, uint
     if (un.n == 0) continue;
     if (!wait_bar_warp(bar(L::kFixFull), ff_cnt & 1, abort_flag, p.status, 10)) break;
     ++ff_cnt;
-    if (!ring_wait(cnt, 11)) break;
+    if (!ring_wait(cnt, 11)) break;  // Q_0 and dO_0 (one barrier per ring pair)
     tc_fence_after();
     mma_kmajor<HD>(tA, fk, stage_addr(cnt), kIdS);  // S^T(0) = K Q_0^T
     mma_commit(bar(L::kSFull));
-    if (!ring_wait(cnt + 1, 12)) break;
-    tc_fence_after();
     mma_kmajor<HD>(tB, fv, stage_addr(cnt + 1), kIdS);  // dP^T(0) = V dO_0^T
     mma_commit(bar(L::kSFull + 1));
     if (un.n == 1) mma_commit(bar(L::kFixEmpty));  // K and V are not read again
@@ -560,9 +567,7 @@ __device__ __forceinline__ void dkdv_mma(const BwdParams& p, uint8_t* smem, uint
       tc_fence_after();
       mma_tmem_a(tDK, tB, stage_addr(c), kIdAcc, t > 0);  // dK += dS^T Q_t
       mma_commit(bar(L::kRingEmpty + c % L::kStages));
-      if (more) {
-        if (!ring_wait(c + 3, 12)) { ok = false; break; }
-        tc_fence_after();
+      if (more) {  // dO_t+1 arrived with Q_t+1 (waited for before S^T(t+1))
         mma_kmajor<HD>(tB, fv, stage_addr(c + 3), kIdS);  // dP^T(t+1) over dS^T(t)
         mma_commit(bar(L::kSFull + 1));
         if (t + 2 == un.n) mma_commit(bar(L::kFixEmpty));
@@ -619,11 +624,10 @@ __device__ __forceinline__ void fused_mma(const BwdParams& p, uint8_t* smem, uin
     if (un.n == 0) continue;
     if (!wait_bar_warp(bar(L::kFixFull), ff_cnt & 1, abort_flag, p.status, 10)) break;
     ++ff_cnt;
-    if (!ring_wait(cnt, 11)) break;
+    if (!ring_wait(cnt, 11)) break;  // Q_0 and dO_0 (one barrier per ring pair)
     tc_fence_after();
     mma_kmajor<HD>(tA, fk, stage_addr(cnt), kIdS);  // S^T(0) = K Q_0^T
     mma_commit(bar(L::kSFull));
-    if (!ring_wait(cnt + 1, 12)) break;
     // the previous unit's last dQ product must be out of B
     if (pending_drain && !wait_bar_warp(bar(L::kDqFree), dq_cnt++ & 1, abort_flag, p.status, 17)) break;
     tc_fence_after();
@@ -658,7 +662,6 @@ __device__ __forceinline__ void fused_mma(const BwdParams& p, uint8_t* smem, uin
       if (!more) mma_commit(bar(L::kFixEmpty));  // K and V are not read again
       if (more) {
         if (!wait_bar_warp(bar(L::kDqFree), dq_cnt++ & 1, abort_flag, p.status, 17)) { ok = false; break; }
-        if (!ring_wait(c + 3, 12)) { ok = false; break; }
         tc_fence_after();
         mma_kmajor<HD>(tB, fv, stage_addr(c + 3), kIdS);  // dP^T(t+1) over dQ(t)
         mma_commit(bar(L::kSFull + 1));
