@@ -365,3 +365,29 @@ def test_packed_sequences(d, lens, extra):
     assert api.build_block_index(mask, starts[-1]).sequence_tiles == ("stride" not in extra)
     res = gc.run_gpu(inp, fields)
     gc.full_compare(inp, fields, res)
+
+
+@pytest.mark.parametrize("mname", ["window_strided", "window_dilated", "window_global", "relstride"])
+def test_forward_issuer_modes_agree(mname):
+    """The forward issues a query-block pair's products from one interleaving
+    MMA warp or from one warp per block, chosen by the index's pair_overlap.
+    Each block's products run in the same order either way, so forcing
+    either mode (through the hint) gives bitwise the same O and LSE, and
+    both match the oracle."""
+    n = 1500
+    inp = small_inputs(2, n, 3, 128, seed=23)
+    fields = SMALL_MASKS[mname]
+    mask = api.Mask(**fields)
+    index = api.build_block_index(mask, n).to("cuda")
+    q, k, v = (inp[t].to("cuda") for t in ("q", "k", "v"))
+    outs = []
+    for overlap in (0.0, 1.0):
+        index.device_struct.pair_overlap = overlap
+        o, lse = api.fwd(q, k, v, mask=mask, index=index)
+        torch.cuda.synchronize()
+        assert api.get_status() == api.OK
+        outs.append((o.clone(), lse.clone()))
+    assert torch.equal(outs[0][0], outs[1][0])
+    assert torch.equal(outs[0][1], outs[1][1])
+    res = {"o": outs[0][0].float().cpu().numpy(), "lse": outs[0][1].cpu().numpy()}
+    gc.full_compare(inp, fields, res, backward=False)
