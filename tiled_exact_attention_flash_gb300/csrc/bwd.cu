@@ -1280,6 +1280,17 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
 // (plus their streamed Q and dO tiles), which stay resident in the 129 MB L2.
 constexpr int64_t kFusedGroupBytes = int64_t(48) << 20;
 
+// Units of the two-kernel backward are numbered rank-major within groups of
+// heads whose streamed tiles (per_head_bytes each) fit kBwdGroupBytes, so
+// the CTAs working at the same time re-read the same heads' tiles from L2
+// (129 MB) instead of DRAM.  When fewer than two heads fit, one group of all
+// heads keeps plain rank-major order (longest units first over the launch).
+constexpr int64_t kBwdGroupBytes = int64_t(64) << 20;
+static int bwd_head_group(int64_t per_head_bytes, int heads) {
+  const int64_t g = kBwdGroupBytes / (per_head_bytes > 0 ? per_head_bytes : 1);
+  return (g < 2 || g >= heads) ? heads : int(g);
+}
+
 template <int HD>
 static flash_msa_status launch_bwd_hd(const BwdLaunch& a, cudaStream_t stream) {
   using LK = BwdLayout<HD, kModeDkdv>;
@@ -1348,7 +1359,8 @@ static flash_msa_status launch_bwd_hd(const BwdLaunch& a, cudaStream_t stream) {
   if (a.stages & FLASH_MSA_BWD_DKDV) {
     p.list = a.cols;
     p.n_units = a.B * a.Hkv * nb;
-    p.head_group = a.B * a.Hkv;  // rank-major over all heads
+    // a key/value head's units stream the Q and dO tiles of its H / Hkv query heads
+    p.head_group = bwd_head_group(int64_t(a.H / a.Hkv) * 2 * a.N * a.d * 2, a.B * a.Hkv);
     p.out_a = reinterpret_cast<__nv_bfloat16*>(a.dk);
     p.out_b = reinterpret_cast<__nv_bfloat16*>(a.dv);
     if ((st = launch(reinterpret_cast<const void*>(&bwd_main_kernel<HD, kModeDkdv>),
@@ -1359,7 +1371,7 @@ static flash_msa_status launch_bwd_hd(const BwdLaunch& a, cudaStream_t stream) {
   if (a.stages & FLASH_MSA_BWD_DQ) {
     p.list = a.rows;
     p.n_units = a.B * a.H * nb;
-    p.head_group = a.B * a.H;
+    p.head_group = bwd_head_group(int64_t(2) * a.N * a.d * 2, a.B * a.H);  // K and V tiles
     p.out_a = reinterpret_cast<__nv_bfloat16*>(a.dq);
     p.out_b = nullptr;
     if ((st = launch(reinterpret_cast<const void*>(&bwd_main_kernel<HD, kModeDq>),
