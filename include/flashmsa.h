@@ -113,13 +113,20 @@ enum {
  * count as dead entries, so tail tiles are never full.
  *   CSR by query block: row_ptr[n_q_blocks+1], col_idx[nnz] (ascending), kind[nnz]
  *   CSC by key block:   col_ptr[n_k_blocks+1], row_idx[nnz] (ascending), kind_t[nnz]
- *   q_order[n_q_blocks] / k_order[n_k_blocks]: blocks by descending live-tile
- *   count, ties by ascending index (longest work is scheduled first); with
- *   per-sequence tiles (below) q_order instead holds each sequence's tiles in
- *   neighbouring pairs counted from its last tile, pairs by descending count
- *   of their first tile (ties: ascending id), then the single first tiles of
- *   sequences with an odd tile count (the forward runs positions 2r, 2r + 1
- *   together and shares their key tiles).
+ *   k_order[n_k_blocks]: key blocks by descending live-tile count, ties by
+ *   ascending index (longest work is scheduled first).
+ *   q_order[n_q_blocks]: query blocks in pairs (the forward runs positions
+ *   2r and 2r + 1 together and loads their key tiles once) that share key
+ *   tiles: blocks are visited by descending live-tile count (ties: ascending
+ *   index); an unpaired block takes, among the unpaired blocks 1, 2, 4 or 8
+ *   away (tried as +1, -1, +2, -2, +4, -4, +8, -8), the one with the most key
+ *   tiles in common (the first tried on ties), if any is in common; blocks
+ *   left over are paired in visiting order; pairs come by descending count
+ *   of their first block (ties: ascending index), an odd block out last.
+ *   With per-sequence tiles (below) q_order instead holds each sequence's
+ *   tiles in neighbouring pairs counted from its last tile, pairs by
+ *   descending count of their first tile (ties: ascending id), then the
+ *   single first tiles of sequences with an odd tile count.
  * With a BITMASK or DOCUMENTS mask, a partial tile whose live entries are not all given
  * by the other mask parts carries them as bits, in a slot numbered in CSR
  * order: bits[512 slot + 4 r + c / 32] bit c % 32 = live(128 qb + r,
@@ -168,8 +175,8 @@ typedef struct flash_msa_block_index {
    * both of them list: sum over the pairs of |common tiles| / sum of |tiles
    * of either| (0 with fewer than two blocks).  Set by the filling build
    * call (0 after the counting call).  A scheduling hint only: the forward
-   * issues the pair's products from one thread, interleaved, when it is at
-   * least 1/2, else from one thread per block; 0 (a struct filled by other
+   * issues the pair's products from one warp, interleaved, when it is at
+   * least 1/2, else from one warp per block; 0 (a struct filled by other
    * means) keeps the latter. */
   float pair_overlap;
 } flash_msa_block_index;

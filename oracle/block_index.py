@@ -13,8 +13,10 @@ and the lists are built from that classification:
 
     CSR  by query block: row_ptr, col_idx (ascending kb), kind (0 full, 1 partial)
     CSC  by key block:   col_ptr, row_idx (ascending qb), kind_t
-    q_order / k_order:   query / key blocks sorted by descending live-tile
-                         count, ties by ascending index (longest work first)
+    k_order:             key blocks sorted by descending live-tile count,
+                         ties by ascending index (longest work first)
+    q_order:             query blocks in pairs that share key tiles, pairs
+                         longest first (see _shared_pairs_order)
 
 With a bit-packed mask (or packed documents), a partial tile whose live set
 differs from the live set of the same mask without the bits (and without
@@ -126,6 +128,49 @@ def _pair_order(spec: MaskSpec, row_len, tile: int) -> np.ndarray:
     return np.array([t for pr in pairs for t in pr] + singles, dtype=np.int32)
 
 
+# Candidate partners of a query block, in the order they are tried.
+PAIR_OFFSETS = (1, -1, 2, -2, 4, -4, 8, -8)
+
+
+def _shared_pairs_order(row_ptr, col_idx) -> np.ndarray:
+    """q_order of a packed-axis index: the query blocks in pairs (positions
+    2r and 2r + 1, which the forward runs together, loading their key tiles
+    once) chosen to share key tiles.  Blocks are visited longest first
+    (descending live-tile count, ties by ascending index); an unpaired block
+    takes, among the unpaired blocks PAIR_OFFSETS away, the one whose list
+    has the most key tiles in common with its own (the first one tried on
+    ties), provided they have any in common.  The blocks left over are paired
+    in visiting order.  The pairs are then ordered by the live-tile count of
+    their first block (descending, ties by its ascending index); a last
+    unpaired block, if any, comes at the end."""
+    nb = len(row_ptr) - 1
+    lens = np.diff(row_ptr)
+    lists = [set(col_idx[row_ptr[b]:row_ptr[b + 1]].tolist()) for b in range(nb)]
+    visit = sorted(range(nb), key=lambda b: (-lens[b], b))
+    paired = [False] * nb
+    pairs = []
+    for a in visit:
+        if paired[a]:
+            continue
+        best, best_common = -1, 0
+        for off in PAIR_OFFSETS:
+            c = a + off
+            if 0 <= c < nb and not paired[c]:
+                common = len(lists[a] & lists[c])
+                if common > best_common:
+                    best, best_common = c, common
+        if best >= 0:
+            paired[a] = paired[best] = True
+            pairs.append((a, best))
+    rest = [a for a in visit if not paired[a]]
+    pairs += [(rest[i], rest[i + 1]) for i in range(0, len(rest) - 1, 2)]
+    pairs.sort(key=lambda pr: (-lens[pr[0]], pr[0]))
+    order = [b for pr in pairs for b in pr]
+    if len(rest) % 2:
+        order.append(rest[-1])
+    return np.array(order, dtype=np.int32)
+
+
 def classify_sequence_tiles(n: int, spec: MaskSpec, tile: int = 128) -> np.ndarray:
     """kinds[qt, kt] over the per-sequence tiles; pairs of two sequences are dead."""
     start, seq0, seq_len = sequence_tiles(spec, tile)
@@ -187,7 +232,7 @@ def build(n: int, spec: MaskSpec, tile: int = 128, prune: bool = True) -> dict:
     if seq:
         q_order = _pair_order(spec, row_len, tile)
     else:
-        q_order = np.array(sorted(range(nb), key=lambda b: (-row_len[b], b)), dtype=np.int32)
+        q_order = _shared_pairs_order(row_ptr, np.array(col_idx, dtype=np.int32))
     k_order = np.array(sorted(range(nb), key=lambda b: (-col_len[b], b)), dtype=np.int32)
     empty = np.zeros(0, dtype=np.int32)
     tile_start, tile_seq0, tile_seq_len = sequence_tiles(spec, tile) if seq else (empty,) * 3

@@ -236,19 +236,52 @@ def _pair_overlap(host):
     return common / either if either else 0.0
 
 
-@pytest.mark.parametrize("cid,shared", [(2, True), (4, True), (5, False), (6, True), (7, False),
-                                        (8, False), (9, False), (10, True)])
-def test_pair_overlap(cid, shared):
+def _random_block_mask(nb, density, seed):
+    """Block-sparse bit-packed mask: each 128 x 128 tile live or dead at random."""
+    from tiled_exact_attention_flash_gb300.inputs import pack_bitmask
+    blocks = np.random.default_rng(seed).random((nb, nb)) < density
+    return pack_bitmask(np.kron(blocks, np.ones((128, 128), dtype=bool)))
+
+
+@pytest.mark.parametrize("cid,low", [(2, 0.9), (4, 0.75), (5, 0.75), (6, 0.9), (7, 0.5), (8, 0.9),
+                                     (9, 0.85), (10, 0.9), (None, None)])
+def test_pair_overlap(cid, low):
     """pair_overlap (the forward's choice between one interleaving MMA warp and
     one per query slot) is the overlap of the paired blocks' key-tile lists;
-    the counting call leaves it 0."""
+    with q_order pairing blocks that share key tiles it is high for every
+    workload mask, and low for tiles live at random; the counting call leaves
+    it 0."""
     import ctypes
-    w = WORKLOADS[cid]
-    m = api.Mask(**w.mask_fields())
-    got = api.build_block_index(m, w.N)
+    if cid is None:
+        n = 40 * 128
+        m = api.Mask(bitmask=_random_block_mask(40, 0.08, 3))
+    else:
+        w = WORKLOADS[cid]
+        n = w.N
+        m = api.Mask(**w.mask_fields())
+    got = api.build_block_index(m, n)
     assert got.header.pair_overlap == pytest.approx(_pair_overlap(got.host), rel=1e-6)
-    assert (got.header.pair_overlap >= 0.5) == shared
+    if low is None:
+        assert got.header.pair_overlap < 0.5
+    else:
+        assert got.header.pair_overlap >= low
     hdr = api.BlockIndexStruct()
-    assert api.lib().flash_msa_build_block_index(ctypes.byref(m.desc()), w.N,
+    assert api.lib().flash_msa_build_block_index(ctypes.byref(m.desc()), n,
                                                  ctypes.byref(hdr)) == api.OK
     assert hdr.pair_overlap == 0.0
+
+
+@pytest.mark.parametrize("density,seed", [(0.08, 3), (0.3, 4), (0.7, 5)])
+def test_random_block_masks_bit_exact(density, seed):
+    """Block-sparse random masks: the shared-pairs q_order (and the rest of
+    the index) of the C++ builder equals the oracle's."""
+    n = 40 * 128 - 57
+    compare(n, {"bitmask": _random_block_mask_n(n, density, seed)})
+
+
+def _random_block_mask_n(n, density, seed):
+    """As _random_block_mask, cut to n tokens (a ragged tail)."""
+    from tiled_exact_attention_flash_gb300.inputs import pack_bitmask
+    nb = (n + 127) // 128
+    blocks = np.random.default_rng(seed).random((nb, nb)) < density
+    return pack_bitmask(np.kron(blocks, np.ones((128, 128), dtype=bool))[:n, :n])

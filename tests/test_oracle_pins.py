@@ -328,7 +328,9 @@ def test_tail_tiles_are_partial_and_structure_consistent(n):
     assert csr == csc
     lens = np.diff(idx["row_ptr"])
     assert sorted(idx["q_order"].tolist()) == list(range(nb))
-    assert all(lens[a] >= lens[b] for a, b in zip(idx["q_order"], idx["q_order"][1:]))
+    # pairs (positions 2r, 2r + 1) come by descending count of their first block
+    firsts = idx["q_order"][0:nb - nb % 2:2]
+    assert all(lens[a] >= lens[b] for a, b in zip(firsts, firsts[1:]))
 
 
 def test_smoke_golden_shape():
@@ -651,3 +653,27 @@ def test_documents_with_block_patterns_keep_packed_tiles():
         r = block_index.build(300, spec)
         assert not block_index.sequence_tiled(spec) and r["tile_start"].size == 0
         assert r["n_blocks"] == 3
+
+
+def test_shared_pairs_hand_example():
+    # six 128-token blocks; blocks of the same parity attend to each other's
+    # keys only: 0, 2, 4 list key blocks {0, 2, 4}, and 1, 3, 5 list {1, 3, 5}.
+    # Visited in id order (equal counts): 0 pairs with 2 (3 common tiles; 1
+    # shares none), 1 with 3, then 4 and 5 share nothing with any unpaired
+    # block within reach and are paired as leftovers.  Longest-first order
+    # alone would have paired 0 with 1 and 2 with 3, which share nothing.
+    from tiled_exact_attention_flash_gb300.inputs import pack_bitmask
+    par = np.arange(768) // 128 % 2
+    spec = MaskSpec(bitmask=pack_bitmask(par[:, None] == par[None, :]))
+    r = block_index.build(768, spec)
+    assert np.diff(r["row_ptr"]).tolist() == [3] * 6
+    assert r["q_order"].tolist() == [0, 2, 1, 3, 4, 5]
+
+
+@pytest.mark.parametrize("n", [129, 1000, 1024, 2100])
+def test_shared_pairs_of_causal_masks_are_longest_first(n):
+    # causal block qb lists qb + 1 tiles: its best partner is qb - 1, so the
+    # pairs are (nb-1, nb-2), (nb-3, nb-4), ... -- plain longest-first order
+    r = block_index.build(n, MaskSpec(causal=True, window=n))
+    lens = np.diff(r["row_ptr"])
+    assert r["q_order"].tolist() == sorted(range(len(lens)), key=lambda b: (-lens[b], b))

@@ -224,7 +224,7 @@ const char* flash_msa_last_error_string(void) { return g_last_error; }
 const char* flash_msa_version(void) { return "libflashmsa 0.1 (sm_103a, tcgen05)"; }
 
 // CSC (by counting sort: query blocks come out ascending within each
-// column) and the longest-first orders, from a filled CSR.
+// column) and the longest-first key-block order, from a filled CSR.
 static void finish_lists(flash_msa_block_index* out, int64_t nb,
                          const std::vector<int32_t>& col_count, bool with_bits) {
   out->col_ptr[0] = 0;
@@ -238,14 +238,86 @@ static void finish_lists(flash_msa_block_index* out, int64_t nb,
       out->kind_t[dst] = out->kind[e];
       if (with_bits) out->bit_slot_t[dst] = out->bit_slot[e];
     }
-  // longest-first orders (stable)
-  for (int64_t b = 0; b < nb; ++b) out->q_order[b] = out->k_order[b] = int32_t(b);
-  std::stable_sort(out->q_order, out->q_order + nb, [&](int32_t a, int32_t b) {
-    return out->row_ptr[a + 1] - out->row_ptr[a] > out->row_ptr[b + 1] - out->row_ptr[b];
-  });
+  // k_order: longest first (stable); q_order is filled by the caller
+  for (int64_t b = 0; b < nb; ++b) out->k_order[b] = int32_t(b);
   std::stable_sort(out->k_order, out->k_order + nb, [&](int32_t a, int32_t b) {
     return out->col_ptr[a + 1] - out->col_ptr[a] > out->col_ptr[b + 1] - out->col_ptr[b];
   });
+}
+
+// Key tiles listed by both query blocks a and b (CSR rows ascend).
+static int64_t common_tiles(const flash_msa_block_index* ix, int32_t a, int32_t b) {
+  int32_t i = ix->row_ptr[a], j = ix->row_ptr[b];
+  const int32_t ie = ix->row_ptr[a + 1], je = ix->row_ptr[b + 1];
+  int64_t n = 0;
+  while (i < ie && j < je) {
+    if (ix->col_idx[i] == ix->col_idx[j]) {
+      ++n;
+      ++i;
+      ++j;
+    } else if (ix->col_idx[i] < ix->col_idx[j]) {
+      ++i;
+    } else {
+      ++j;
+    }
+  }
+  return n;
+}
+
+// q_order of a packed-axis index: the query blocks in pairs (positions 2r
+// and 2r + 1, which the forward runs together, loading their key tiles once)
+// chosen to share key tiles.  Blocks are visited longest first (descending
+// live-tile count, ties by ascending index); an unpaired block takes, among
+// the unpaired blocks 1, 2, 4 or 8 away (tried in the order +1, -1, +2, -2,
+// +4, -4, +8, -8), the one with the most key tiles in common with it (the
+// first one tried on ties), provided they have any in common.  The blocks
+// left over are paired in visiting order.  Pairs are ordered by the live-tile
+// count of their first block (descending, ties by its ascending index); a
+// last unpaired block, if any, comes at the end.  For causal masks this is
+// plain longest-first order; for block dilation it pairs blocks of the same
+// parity, for packed documents neighbours of one document.
+static void shared_pairs_order(flash_msa_block_index* out, int64_t nb) {
+  static const int kOffsets[8] = {1, -1, 2, -2, 4, -4, 8, -8};
+  auto len = [&](int32_t b) { return out->row_ptr[b + 1] - out->row_ptr[b]; };
+  std::vector<int32_t> visit(static_cast<size_t>(nb));
+  for (int64_t b = 0; b < nb; ++b) visit[size_t(b)] = int32_t(b);
+  std::stable_sort(visit.begin(), visit.end(),
+                   [&](int32_t a, int32_t b) { return len(a) > len(b); });
+  std::vector<char> paired(static_cast<size_t>(nb), 0);
+  std::vector<std::pair<int32_t, int32_t>> pairs;
+  for (const int32_t a : visit) {
+    if (paired[size_t(a)]) continue;
+    int32_t best = -1;
+    int64_t best_common = 0;
+    for (const int off : kOffsets) {
+      const int64_t c = int64_t(a) + off;
+      if (c < 0 || c >= nb || paired[size_t(c)]) continue;
+      const int64_t common = common_tiles(out, a, int32_t(c));
+      if (common > best_common) {
+        best_common = common;
+        best = int32_t(c);
+      }
+    }
+    if (best >= 0) {
+      paired[size_t(a)] = paired[size_t(best)] = 1;
+      pairs.emplace_back(a, best);
+    }
+  }
+  std::vector<int32_t> rest;
+  for (const int32_t a : visit)
+    if (!paired[size_t(a)]) rest.push_back(a);
+  for (size_t i = 0; i + 1 < rest.size(); i += 2) pairs.emplace_back(rest[i], rest[i + 1]);
+  std::stable_sort(pairs.begin(), pairs.end(), [&](const std::pair<int32_t, int32_t>& x,
+                                                   const std::pair<int32_t, int32_t>& y) {
+    const int32_t lx = len(x.first), ly = len(y.first);
+    return lx != ly ? lx > ly : x.first < y.first;
+  });
+  int64_t at = 0;
+  for (const auto& pr : pairs) {
+    out->q_order[at++] = pr.first;
+    out->q_order[at++] = pr.second;
+  }
+  if (rest.size() % 2) out->q_order[at++] = rest.back();
 }
 
 // flash_msa_block_index::pair_overlap from the filled CSR lists (ascending
@@ -254,20 +326,8 @@ static float pair_overlap(const flash_msa_block_index* ix, int64_t nb) {
   int64_t common = 0, either = 0;
   for (int64_t r = 0; r + 1 < nb; r += 2) {
     const int32_t a = ix->q_order[r], b = ix->q_order[r + 1];
-    int32_t i = ix->row_ptr[a], j = ix->row_ptr[b];
-    const int32_t ie = ix->row_ptr[a + 1], je = ix->row_ptr[b + 1];
-    either += (ie - i) + (je - j);
-    while (i < ie && j < je) {
-      if (ix->col_idx[i] == ix->col_idx[j]) {
-        ++common;
-        ++i;
-        ++j;
-      } else if (ix->col_idx[i] < ix->col_idx[j]) {
-        ++i;
-      } else {
-        ++j;
-      }
-    }
+    either += (ix->row_ptr[a + 1] - ix->row_ptr[a]) + (ix->row_ptr[b + 1] - ix->row_ptr[b]);
+    common += common_tiles(ix, a, b);
   }
   either -= common;
   return either > 0 ? float(double(common) / double(either)) : 0.f;
@@ -600,6 +660,7 @@ flash_msa_status flash_msa_build_block_index(const flash_msa_mask_desc* mask, in
   if (!with_bits) out->n_bit_tiles = 0;
   out->live_elements = live;
   finish_lists(out, nb, col_count, with_bits);
+  shared_pairs_order(out, nb);
   out->pair_overlap = pair_overlap(out, nb);
   return FLASH_MSA_OK;
 }
