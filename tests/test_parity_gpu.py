@@ -391,3 +391,18 @@ def test_forward_issuer_modes_agree(mname):
     assert torch.equal(outs[0][1], outs[1][1])
     res = {"o": outs[0][0].float().cpu().numpy(), "lse": outs[0][1].cpu().numpy()}
     gc.full_compare(inp, fields, res, backward=False)
+
+
+def test_backward_head_groups_with_a_remainder():
+    """The backward numbers its units within groups of heads whose streamed
+    tiles fit 64 MB of L2: at N = 32768, d = 128 a head streams 16 MB, so six
+    heads form groups of 4 and 2.  Every head -- the last group's included --
+    matches the oracle on sampled rows and columns."""
+    B, N, H, d = 1, 32768, 6, 128
+    inp = small_inputs(B, N, H, d, seed=29)
+    fields = {"causal": True}
+    res = gc.run_gpu(inp, fields)
+    rng = np.random.default_rng(29)
+    rows = gc.sample_positions(N, rng, k=48)
+    cols = gc.sample_positions(N, rng, k=48)
+    gc.sampled_compare(inp, fields, res, [(0, 0), (0, 4), (0, 5)], rows, cols)
