@@ -519,48 +519,37 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint64_t* bars, 
             if (!((bw[c >> 5] >> (c & 31)) & 1u)) sr[c] = kNegInfBits;
         }
       }
-      // Optimistic pass: exponentials against the current reference max while
-      // the tile's row max is formed alongside.  Only if some row's max
-      // exceeds the reference by more than 8 (log2 units) -- always on a
-      // unit's first live tile -- is the pass redone with the raised reference.
+      // The tile's row max first (four max3 chains), then one pass of
+      // exponentials against the row's reference max.  The reference is
+      // raised to the tile's max only when that exceeds it by more than 8
+      // (log2 units) -- always on a unit's first live tile -- so P <= 2^8 and
+      // O is rescaled rarely.  (An optimistic pass against the old reference
+      // with the max formed alongside, redone when a row's max grew, kept two
+      // copies of this loop in the kernel and measured slower.)
       float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 64; c += 2) {
+        float& m = (c & 2) ? mx1 : mx0;
+        float& n = (c & 2) ? mx3 : mx2;
+        m = max3(m, __uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1]));
+        n = max3(n, __uint_as_float(sr[2 * c + 2]), __uint_as_float(sr[2 * c + 3]));
+      }
+      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      const float m_new = (mx > m_run + 8.f) ? mx : m_run;
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
       float sa[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       uint32_t pk[64];
-      const float m_opt = (m_run == -INFINITY) ? 0.f : m_run;
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
-        const float s0 = __uint_as_float(sr[2 * c]), s1 = __uint_as_float(sr[2 * c + 1]);
-        if (c & 1) mx1 = max3(mx1, s0, s1); else mx0 = max3(mx0, s0, s1);
         float x0, x1;
-        fma2(x0, x1, s0, s1, sl2, sl2, -m_opt, -m_opt);
+        fma2(x0, x1, __uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1]), sl2, sl2, -m_use,
+             -m_use);
         const float p0 = ex2_approx(x0);
         const float p1 = ex2_approx(x1);
         const int a = 2 * (c & 3);
         add2(sa[a], sa[a + 1], sa[a], sa[a + 1], p0, p1);
         pk[c] = pack_bf16x2(p0, p1);
         if (c == 31) tmem_st_x32(tS, *reinterpret_cast<uint32_t(*)[32]>(pk));
-      }
-      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
-      const bool grow = mx > m_run + 8.f;
-      float m_new = m_run, m_use = m_opt;
-      if (__any_sync(0xFFFFFFFFu, grow)) {
-        m_new = grow ? mx : m_run;
-        m_use = (m_new == -INFINITY) ? 0.f : m_new;
-#pragma unroll
-        for (int a = 0; a < 8; ++a) sa[a] = 0.f;
-        tmem_wait_st();  // the first half of P is rewritten
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          float x0, x1;
-          fma2(x0, x1, __uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1]), sl2, sl2,
-               -m_use, -m_use);
-          const float p0 = ex2_approx(x0);
-          const float p1 = ex2_approx(x1);
-          const int a = 2 * (c & 3);
-          add2(sa[a], sa[a + 1], sa[a], sa[a + 1], p0, p1);
-          pk[c] = pack_bf16x2(p0, p1);
-        }
-        tmem_st_x32(tS, *reinterpret_cast<uint32_t(*)[32]>(pk));
       }
       tmem_st_x32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
       const float alpha = ex2_approx(m_run - m_use);
