@@ -582,19 +582,31 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint64_t* bars, 
     const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
     __nv_bfloat16* orow =
         p.o + ((int64_t(un.b) * p.N + tok) * p.H + un.h) * int64_t(HD);
+    // O into registers with one TMEM load, and its columns released at once:
+    // the next unit's first P V may overwrite them while this row is stored
+    uint32_t o[HD];
+    if (un.n > 0) {
+      if constexpr (HD == 128) {
+        tmem_ld_x128(tO, o);
+      } else {
+        tmem_ld_x64(tO, o);
+      }
+      tc_fence_before();
+      mbar_arrive(bar(L::kOEmpty + slot));
+    } else {
+#pragma unroll
+      for (int j = 0; j < HD; ++j) o[j] = 0u;
+    }
 #pragma unroll
     for (int c = 0; c < HD / 32; ++c) {
-      uint32_t o[32];
-      if (un.n > 0) {
-        tmem_ld_x32(tO + c * 32, o);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) o[j] = 0u;
-      }
       uint32_t w[16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        w[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv_l, __uint_as_float(o[2 * j + 1]) * inv_l);
+      for (int j = 0; j < 16; ++j) {
+        float a0, a1;
+        mul2(a0, a1, __uint_as_float(o[c * 32 + 2 * j]), __uint_as_float(o[c * 32 + 2 * j + 1]),
+             inv_l, inv_l);
+        w[j] = pack_bf16x2(a0, a1);
+      }
       // pairs of lanes swap 16-byte chunks, so each store writes 32 contiguous
       // bytes (a whole sector) of 16 rows instead of 16 bytes of 32 rows
       uint4 cc[4];
@@ -602,10 +614,6 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint64_t* bars, 
       for (int j = 0; j < 4; ++j) cc[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
       store_rows_transposed<4, 2>(cc, reinterpret_cast<char*>(orow + c * 32),
                                   int64_t(p.H) * HD * 2, i < qg.n);
-    }
-    if (un.n > 0) {
-      tc_fence_before();
-      mbar_arrive(bar(L::kOEmpty + slot));
     }
     if (i < qg.n) {
       p.lse[(int64_t(un.b) * p.H + un.h) * p.N + tok] =
