@@ -36,7 +36,7 @@ struct FwdParams {
   int B, H, N;
   int G;  // query heads per key/value head
   int n_units;
-  int head_group;    // pair units are numbered in groups of this many heads
+  UnitOrder order;   // pair units: rank-major over all heads
   int slot_issuers;  // one MMA-issuing warp per query slot (else one for both)
   float scale_log2;  // scale * log2(e)
   int wait_limit_ms;  // limit of any single bounded wait
@@ -92,19 +92,18 @@ __device__ __forceinline__ int fwd_unit(int k) {
 
 __device__ __forceinline__ PairUnit decode_pair(int u, const FwdParams& p) {
   const ListParams& L = p.list;
-  int bh, r;
-  unit_order_grouped(u, p.B * p.H, (L.n_blocks + 1) / 2, p.head_group, bh, r);
   PairUnit pu;
-  pu.b = bh / p.H;
-  pu.h = bh - pu.b * p.H;
+  int r;
+  unit_order_grouped(u, (L.n_blocks + 1) / 2, p.order, pu.b, pu.h, r);
   for (int s = 0; s < 2; ++s) {
     const int rank = 2 * r + s;
     pu.q[s] = -1;
     pu.beg[s] = 0;
     pu.n[s] = 0;
     if (rank >= L.n_blocks) continue;
-    // reuse the single-unit decoder for the block id and its list bounds
-    const Unit un = decode_unit_at(bh, rank, p.H, L, p.status);
+    // the single-unit decoder gives the block id and its list bounds
+    Unit un;
+    decode_block_at(un, rank, L, p.status);
     pu.q[s] = un.ob;
     pu.beg[s] = un.begin;
     pu.n[s] = un.n;
@@ -724,7 +723,7 @@ static flash_msa_status launch_fwd_hd(const FwdLaunch& a, cudaStream_t stream) {
   // one group of all heads: plain rank-major order (groups of a few heads,
   // whose K and V would stay in L2, measured slower: the static deal then
   // leaves CTAs idle at the group boundaries)
-  p.head_group = a.B * a.H;
+  p.order = make_unit_order(a.B, a.H, (a.list.n_blocks + 1) / 2, a.B * a.H);
   p.status = a.status;
   p.wait_limit_ms = int(wait_limit_ms());
   if ((st = enable_smem(reinterpret_cast<const void*>(&fwd_kernel<HD>), L::kSmemBytes,
