@@ -406,3 +406,40 @@ def test_backward_head_groups_with_a_remainder():
     rows = gc.sample_positions(N, rng, k=48)
     cols = gc.sample_positions(N, rng, k=48)
     gc.sampled_compare(inp, fields, res, [(0, 0), (0, 4), (0, 5)], rows, cols)
+
+
+@pytest.mark.parametrize("cid", [3, 4, 9, 10])
+def test_full_size_constant_values_every_row(cid):
+    """Every output row of every head at full size.  With all value rows of a
+    head equal (V[b, j, h] = c[b, h] for every key j) each softmax row sums to
+    one, so O[b, i, h] = c[b, h] for every query row with a live key (every
+    row here: each attends to itself).  The kernel rounds P to bf16 before
+    P V (bf16 keeps 8 significant bits: unit roundoff u = 2^-8 per entry, so
+    the weights sum to within u of the fp32 row sum that divides them) and
+    rounds O to bf16 (within u |O|): |O - c| <= (2u + u^2) |c| up to fp32
+    accumulation.  O and LSE start as NaN, so a row that no work unit wrote
+    fails the check."""
+    w = WORKLOADS[cid]
+    inp = workload_inputs(w)
+    B, N, H, d = inp["q"].shape
+    rng = np.random.default_rng(1000 + cid)
+    c = torch.from_numpy(rng.standard_normal((B, 1, H, d)).astype(np.float32)).to(torch.bfloat16)
+    fields = w.mask_fields()
+    mask = api.Mask(**fields) if fields else None
+    index = api.build_block_index(mask, N).to("cuda") if (mask and mask.needs_index) else None
+    q, k = inp["q"].to("cuda"), inp["k"].to("cuda")
+    v = c.expand(B, N, H, d).contiguous().to("cuda")
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((B, H, N), float("nan"), dtype=torch.float32, device="cuda")
+    api.fwd(q, k, v, mask=mask, index=index, out=o, lse=lse)
+    assert api.get_status() == api.OK
+    got = o.float().cpu().numpy()
+    cc = c.float().numpy()
+    assert np.isfinite(got).all(), "an output row was not written"
+    assert np.isfinite(lse.cpu().numpy()).all(), "an LSE entry was not written"
+    err = np.abs(got - cc)
+    u = 2.0 ** -8
+    bound = (2 * u + u * u) * np.abs(cc) + 1e-6
+    bad = err > bound
+    assert not bad.any(), (f"{int(bad.sum())} entries off; worst {err.max():.3e} at "
+                           f"{np.unravel_index(np.argmax(err - bound), err.shape)}")
