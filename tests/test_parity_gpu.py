@@ -443,3 +443,25 @@ def test_full_size_constant_values_every_row(cid):
     bad = err > bound
     assert not bad.any(), (f"{int(bad.sum())} entries off; worst {err.max():.3e} at "
                            f"{np.unravel_index(np.argmax(err - bound), err.shape)}")
+
+
+@pytest.mark.parametrize("cid", [3, 4, 9, 10])
+def test_full_size_zero_output_gradient_every_row(cid):
+    """Every gradient row of every head at full size.  With dO = 0, D = 0 and
+    dP = 0, so dS = P (dP - D) = 0 and dQ, dK, dV are exactly zero.  The
+    gradients start as NaN, so a row that no backward work unit wrote fails
+    the check (their values are covered by the sampled oracle comparisons)."""
+    w = WORKLOADS[cid]
+    inp = workload_inputs(w)
+    B, N, H, d = inp["q"].shape
+    fields = w.mask_fields()
+    mask = api.Mask(**fields) if fields else None
+    index = api.build_block_index(mask, N).to("cuda") if (mask and mask.needs_index) else None
+    q, k, v = (inp[n].to("cuda") for n in ("q", "k", "v"))
+    o, lse = api.fwd(q, k, v, mask=mask, index=index)
+    do = torch.zeros_like(q)
+    grads = [torch.full_like(t, float("nan")) for t in (q, k, v)]
+    api.bwd(q, k, v, o, lse, do, mask=mask, index=index, dq=grads[0], dk=grads[1], dv=grads[2])
+    assert api.get_status() == api.OK
+    for name, g in zip(("dq", "dk", "dv"), grads):
+        assert bool((g == 0).all()), f"{name}: {int((g != 0).sum())} entries not exactly zero"
